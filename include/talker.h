@@ -1,0 +1,169 @@
+/*
+ * talker.h — C-ABI of the GB300 KV-cached Qwen3 "Talker" decoder forward.
+ *
+ * The operation is the KV-cached forward of a Qwen3-style causal decoder stack
+ * as defined on "qwentts.cpp/src/talker-forward.h": per layer a pre-norm
+ * RMSNorm, bias-free Q/K/V projections, per-head QK-RMSNorm, 1-D NEOX RoPE
+ * (the multimodal axes collapsed to one position), K/V appended to a causal
+ * cache, GQA scaled-dot-product attention over [0, pos], o_proj + residual,
+ * a post-attention RMSNorm, a SwiGLU MLP + residual; after the last layer a
+ * final RMSNorm and the codec_head projection (talker_layer_forward,
+ * talker_forward_core). The entry points follow that page's statement of the
+ * problem (talker_forward_prefill, talker_forward_decode, the KV cache reset)
+ * and the batched cache of "transcribe.cpp/src/causal_lm/causal_lm.cpp"
+ * (kv_init_batched).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are CUDA DEVICE pointers on the device that was
+ *     current at talker_create, unless a comment says "host".
+ *   - Matrices are row-major. Linear weights are [out, in] (in contiguous),
+ *     as ggml_mul_mat(W, x) reads them. Activations are [rows, features].
+ *   - Work is enqueued on the stream given to talker_create and runs
+ *     asynchronously; outputs are ready once that stream reaches the point
+ *     after the call. Inputs must stay valid until then.
+ *   - The caller owns every pointer it passes. The library owns its weight
+ *     store, KV cache, workspaces and CUDA graphs, and frees them in
+ *     talker_destroy.
+ *   - Errors are returned as talker_status; nothing aborts or throws. All
+ *     argument and capacity checks run before any work is enqueued, and a call
+ *     that fails changes no state (per-stream lengths advance only on success,
+ *     as cur_len does on the page).
+ *   - A handle is not thread-safe: calls on one handle must be serialised.
+ */
+#ifndef TALKER_H
+#define TALKER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct talker talker_t; /* opaque, library-owned */
+
+typedef enum {
+    TALKER_OK = 0,
+    TALKER_EINVAL = 1,    /* bad argument: null pointer, size out of range, unsupported geometry */
+    TALKER_EOVERFLOW = 2, /* the call would write cache rows at or past max_seq_len */
+    TALKER_ENOMEM = 3,    /* a device allocation failed */
+    TALKER_ECUDA = 4,     /* a CUDA runtime call failed */
+    TALKER_ESTATE = 5,    /* call out of order (e.g. prefill before talker_kv_init_batched) */
+    TALKER_EDEVICE = 6    /* a kernel reported an error through the device status word */
+} talker_status;
+
+typedef enum { TALKER_DTYPE_F32 = 0, TALKER_DTYPE_BF16 = 1 } talker_dtype;
+
+/* Geometry and storage formats (names as in the rightkit-qts TtsTransformerConfig).
+ * Supported: head_dim in {32, 64, 128}; n_q_heads a multiple of n_kv_heads with
+ * n_q_heads / n_kv_heads <= 8; hidden, n_q_heads*head_dim and intermediate
+ * multiples of 64; vocab a multiple of 8. */
+typedef struct {
+    int32_t n_layers;
+    int32_t hidden;
+    int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t intermediate;
+    int32_t vocab;
+    float rms_eps;        /* inside the square root of every RMSNorm, QK-norm included */
+    float rope_theta;     /* NEOX RoPE frequency base */
+    int32_t weight_dtype; /* talker_dtype of the linear weights (norm gains are always f32) */
+    int32_t kv_dtype;     /* talker_dtype of the KV cache */
+} talker_config;
+
+/* Device pointers to one layer's weights. Linear weights are [out, in] in
+ * weight_dtype: q_proj [nq*hd, H], k_proj/v_proj [nkv*hd, H], o_proj [H, nq*hd],
+ * gate_proj/up_proj [I, H], down_proj [H, I]. Norm gains are f32: input_norm and
+ * post_norm [H], q_norm and k_norm [hd]. */
+typedef struct {
+    const void *input_norm, *q_proj, *k_proj, *v_proj, *q_norm, *k_norm, *o_proj;
+    const void *post_norm, *gate_proj, *up_proj, *down_proj;
+} talker_layer_ptrs;
+
+typedef struct {
+    const talker_layer_ptrs *layers; /* HOST array of n_layers entries */
+    const void *final_norm;          /* f32 [H] */
+    const void *codec_head;          /* weight_dtype [vocab, H] */
+} talker_weight_ptrs;
+
+/* Create a handle: validates the geometry, copies and repacks the weights into
+ * the library's store (packed [Wq;Wk;Wv] and row-interleaved [Wg;Wu]), so the
+ * caller may free its copies once the stream has passed this call.
+ * cuda_stream is a cudaStream_t (NULL = the legacy default stream).
+ * Errors: EINVAL (null/unsupported), ENOMEM, ECUDA. On error *out is NULL. */
+talker_status talker_create(const talker_config *cfg, const talker_weight_ptrs *weights,
+                            void *cuda_stream, talker_t **out);
+
+/* Synchronises the stream and frees everything the handle owns. NULL is a no-op. */
+void talker_destroy(talker_t *t);
+
+/* Allocate (or re-allocate) the KV cache for n_streams independent streams of
+ * up to max_seq_len rows each ("causal_lm.cpp", kv_init_batched). The cache is
+ * bf16 or f32 (kv_dtype), laid out per stream in pages of 64 positions; each
+ * page holds [layer][kv_head][64][head_dim] for K and likewise for V. Pages are
+ * zeroed and every stream's length is set to 0.
+ * Errors: EINVAL (n_streams < 1, max_seq_len < 1), ENOMEM, ECUDA. */
+talker_status talker_kv_init_batched(talker_t *t, int n_streams, int max_seq_len);
+
+/* Set stream's length to new_len (0 <= new_len <= current length). Rows past
+ * new_len become stale and are never read again. Errors: EINVAL, ESTATE. */
+talker_status talker_kv_rewind(talker_t *t, int stream, int new_len);
+
+/* Current length of a stream (host int). Errors: EINVAL, ESTATE. */
+talker_status talker_cur_len(const talker_t *t, int stream, int *out_len);
+
+/* Prefill ("talker-forward.h", talker_forward_prefill): rewind `stream` to 0 and
+ * run T rows emb [T, H] f32 at positions 0..T-1, writing their K/V at rows
+ * 0..T-1; afterwards the stream's length is T.
+ * Outputs for the last row only: hidden_last [H] f32 (after the final norm;
+ * may be NULL), logits_last [vocab] f32 (required), argmax_last [1] int32
+ * (greedy token, lowest index on ties; may be NULL).
+ * Errors: EINVAL (T < 1, null emb/logits, bad stream), EOVERFLOW (T >
+ * max_seq_len), ESTATE (no cache), ECUDA. */
+talker_status talker_prefill(talker_t *t, int stream, const float *emb, int T,
+                             float *hidden_last, float *logits_last, int32_t *argmax_last);
+
+/* Decode ("talker-forward.h", talker_forward_decode): one row per stream for
+ * streams 0..B-1. Row b of emb [B, H] f32 runs at position cur_len[b], its K/V
+ * are appended at that row, it attends to [0, cur_len[b]], and afterwards
+ * cur_len[b] += 1. Outputs: logits [B, vocab] f32 (required), hidden [B, H] f32
+ * after the final norm (may be NULL), argmax [B] int32 (may be NULL).
+ * The step runs as one replayed CUDA graph per (B, pointer set).
+ * Errors: EINVAL (B < 1 or > n_streams, null pointers), EOVERFLOW (some
+ * cur_len[b] + 1 > max_seq_len), ESTATE, ECUDA. */
+talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits, float *hidden,
+                            int32_t *argmax);
+
+/* Test support: the prefill above, but writing every row's outputs:
+ * hidden [T, H] (may be NULL) and logits [T, vocab] (required). */
+talker_status talker_prefill_all_rows(talker_t *t, int stream, const float *emb, int T,
+                                      float *hidden, float *logits);
+
+/* Test support, modelled on the state import/export of
+ * "audio.cpp/src/models/vibevoice/decoder.cpp" (TransformerKVState):
+ * copy `len` rows of a stream's cache in or out. k and v are device buffers
+ * [n_layers][n_kv_heads][len][head_dim] in kv_dtype. Import sets the stream's
+ * length to len. Errors: EINVAL, EOVERFLOW (len > max_seq_len), ESTATE, ECUDA. */
+talker_status talker_kv_import(talker_t *t, int stream, const void *k, const void *v, int len);
+talker_status talker_kv_export(const talker_t *t, int stream, void *k, void *v, int len);
+
+/* Synchronise the handle's stream and read the device status word, which a
+ * kernel sets (and never traps) when it meets an impossible condition (a
+ * position past the cache, a wait that gave up, a NaN logit in argmax).
+ * Returns OK, EDEVICE (status word non-zero; *code gets its bits, then the
+ * word is cleared) or ECUDA. code may be NULL. */
+talker_status talker_sync_status(talker_t *t, int32_t *code);
+
+/* Human-readable name of a status code (static string). */
+const char *talker_status_str(talker_status s);
+
+/* Test support: count of kernel launches the library enqueued since creation
+ * (a graph replay counts each of its kernels). */
+int64_t talker_kernel_launches(const talker_t *t);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TALKER_H */

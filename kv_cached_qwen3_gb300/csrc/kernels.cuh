@@ -1,0 +1,106 @@
+// Parameter blocks and host launchers of the Talker kernels. Included by the
+// kernel translation units and by the host runtime (talker_runtime.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace talker_k {
+
+enum Epilogue : int {
+    EPI_QKV = 0,     // raw q|k|v rows; the CTA that completes a head applies QK-norm, RoPE, KV append
+    EPI_RESID = 1,   // out[r][f] += acc (residual stream)
+    EPI_SWIGLU = 2,  // rows 2j (gate) and 2j+1 (up): out[r][j] = silu(gate) * up
+    EPI_HEAD = 3     // logits, final hidden, argmax (last CTA), decode length bump
+};
+
+// Which stream and position each activation row belongs to.
+//   mode 0 (decode):  row r is stream r at position cur_len[r]
+//   mode 1 (prefill): row r is stream `stream0` at position pos0 + r
+struct RowMap {
+    int mode;
+    int stream0;
+    int pos0;
+    const int *cur_len;
+};
+
+// The paged KV cache. Page = [n_layers][n_kv][kPage][head_dim] elements; the
+// position p of stream s lives in page page_table[s * pages_per_stream + p / kPage].
+struct CacheView {
+    void *k;
+    void *v;
+    const int *page_table;
+    int pages_per_stream;
+    int max_seq;
+    int n_layers;
+    int n_kv;
+    int head_dim;
+    int kv_bf16;        // 1: bf16 cache, 0: f32
+    size_t page_elems;
+};
+
+struct GemvParams {
+    const void *W;       // [rows_w, K] weight_dtype (rows_w = n_out, or 2*n_out for SWIGLU)
+    const float *act;    // [rows, act_ld] f32 input activations
+    int act_ld;
+    const float *norm_w; // RMSNorm gain [K] for the fused prologue (QKV, SWIGLU, HEAD)
+    float eps;
+    int K;
+    int n_out;
+    int rows;
+    float *out;          // epilogue destination, row stride out_ld
+    int out_ld;
+    float *copy_x;       // optional: CTA column 0 copies the raw input rows here (residual init)
+    // EPI_QKV
+    int layer, n_q, n_kv, head_dim;
+    const float *q_norm, *k_norm;
+    const float2 *rope;  // [max_seq][head_dim/2] (cos, sin)
+    float *q_out;        // [rows, n_q*head_dim]
+    CacheView cache;
+    RowMap rowmap;
+    int *cnt;            // per (row block, head) completion counters, zero between launches
+    // EPI_HEAD
+    float *hidden_out;   // [rows, K] final hidden (may be null)
+    int *argmax_out;     // [rows] (may be null)
+    float *part_val;     // per (row block, CTA, row) partial maxima
+    int *part_idx;
+    int *head_cnt;       // per row block counter
+    int inc_len;         // decode: last CTA does cur_len[r] += 1
+    int *cur_len_rw;
+    int *status;
+};
+
+struct AttnParams {
+    const float *q;      // [rows, n_q*hd] after QK-norm and RoPE
+    void *out;           // [rows, n_q*hd] f32, or bf16 when out_bf16
+    int out_bf16;
+    CacheView cache;
+    RowMap rowmap;
+    int layer;
+    int n_q, n_kv, group;
+    int splits;          // CTAs per (row, kv head) along the sequence
+    float scale;         // 1/sqrt(head_dim)
+    float *ws;           // partials [rows][n_q][splits][hd + 4]
+    int *cnt;            // [rows][n_kv] completion counters, zero between launches
+    int *status;
+};
+
+constexpr int kGemvWarps = 8;
+constexpr int kGemvThreads = 256;
+constexpr int kAttnThreads = 256;
+
+// Row-block heights the GEMV family is built for.
+int gemv_rows_for(int rows);
+size_t gemv_smem_bytes(int rows_tmpl, int K);
+size_t attn_smem_bytes(int kv_bf16, int head_dim, int group);
+
+cudaError_t launch_gemv(int epi, int w_bf16, int rows_tmpl, const GemvParams &p, cudaStream_t st, bool pdl);
+cudaError_t launch_attn(int kv_bf16, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl);
+cudaError_t launch_set_len(int *cur_len, int stream, int value, cudaStream_t st);
+// Copy len rows of a stream between a dense [n_layers][n_kv][len][hd] buffer and the cache.
+cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *dense_v, int len, int to_cache,
+                           cudaStream_t st);
+cudaError_t prepare_kernels();  // raise dynamic shared-memory limits once per process
+
+}  // namespace talker_k
