@@ -1,0 +1,291 @@
+// Split-K flash-decode GQA attention over the paged KV cache.
+//
+// Computes, for each query row r (stream s, position p) and q head h,
+//   o_h = softmax_j(q_h . k_{g,j} / sqrt(hd)) v_{g,j},  j in [0, p],  g = h / (n_q / n_kv)
+// ("qwentts.cpp/src/talker-forward.h", talker_layer_forward: flash_attn_ext
+// with F32 precision over the causal window; GQA by repeat_interleave of the KV
+// heads as in "causal_lm.cpp"). The window is bounded by the row's length, not
+// by a mask, so cache rows past p are never read into the arithmetic.
+//
+// Grid (splits, n_kv, rows). CTA (split, g, r) walks a contiguous range of
+// 64-position pages of (s, layer, g); each K and V page tile is one contiguous
+// block moved into shared memory by a bulk (TMA) copy, double buffered. All
+// q heads of the group share each tile. Running max / sum / output are fp32
+// (online softmax). Each CTA writes its partial (m, l, o); the CTA that
+// finishes last for (r, g) (atomic counter, no waiting) combines the partials
+// in split order, so the result is deterministic.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace talker_dev;
+
+namespace talker_k {
+
+constexpr int kMaxGroup = 8;
+
+__device__ __forceinline__ int attn_row_stream(const RowMap &m, int r) { return m.mode == 0 ? r : m.stream0; }
+__device__ __forceinline__ int attn_row_pos(const RowMap &m, int r) {
+    return m.mode == 0 ? m.cur_len[r] : m.pos0 + r;
+}
+
+size_t attn_smem_bytes(int kv_bf16, int head_dim, int group) {
+    const size_t esz = kv_bf16 ? 2 : 4;
+    return 4 * (size_t)kPage * head_dim * esz + (size_t)group * head_dim * 4 + (size_t)group * kPage * 4;
+}
+
+template <typename KT, int HD>
+__global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p) {
+    constexpr int E = HD / 32;                       // elements of a key row per lane
+    constexpr int NO = (kMaxGroup * HD + kAttnThreads - 1) / kAttnThreads;
+    constexpr uint32_t kTileBytes = kPage * HD * sizeof(KT);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    KT *kbuf = reinterpret_cast<KT *>(smem_raw);                       // [2][kPage*HD]
+    KT *vbuf = kbuf + 2 * kPage * HD;                                   // [2][kPage*HD]
+    float *q_s = reinterpret_cast<float *>(vbuf + 2 * kPage * HD);      // [G][HD]
+    float *sc = q_s + p.group * HD;                                     // [G][kPage]
+    __shared__ float m_s[kMaxGroup], l_s[kMaxGroup], al_s[kMaxGroup];
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int flag_s;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sidx = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+    const int G = p.group;
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    const int s = attn_row_stream(p.rowmap, r);
+    const int pos = attn_row_pos(p.rowmap, r);
+    if (pos < 0 || pos >= p.cache.max_seq) {
+        if (tid == 0 && sidx == 0) atomicOr(p.status, ST_BAD_POSITION);
+        return;
+    }
+    const int nvis = pos + 1;
+    const int npages = (nvis + kPage - 1) / kPage;
+    const int per = (npages + p.splits - 1) / p.splits;
+    const int pb = sidx * per;
+    const int pe = min(pb + per, npages);
+    const int nact = (npages + per - 1) / per;
+    if (pb >= pe) return;
+
+    const int *ptab = p.cache.page_table + (size_t)s * p.cache.pages_per_stream;
+    const size_t head_off = (size_t)(p.layer * p.cache.n_kv + g) * kPage * HD;
+    const KT *kpool = static_cast<const KT *>(p.cache.k);
+    const KT *vpool = static_cast<const KT *>(p.cache.v);
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const size_t off = (size_t)ptab[pb] * p.cache.page_elems + head_off;
+        mbar_arrive_expect_tx(&bars[0], 2 * kTileBytes);
+        bulk_g2s(kbuf, kpool + off, kTileBytes, &bars[0]);
+        bulk_g2s(vbuf, vpool + off, kTileBytes, &bars[0]);
+    }
+    const float *qsrc = p.q + (size_t)r * p.n_q * HD + (size_t)g * G * HD;
+    for (int i = tid; i < G * HD; i += kAttnThreads) q_s[i] = qsrc[i] * p.scale;
+    if (tid < G) {
+        m_s[tid] = -INFINITY;
+        l_s[tid] = 0.f;
+    }
+    float o_acc[NO];
+#pragma unroll
+    for (int o = 0; o < NO; ++o) o_acc[o] = 0.f;
+    __syncthreads();
+
+    bool failed = false;
+    int fail_it = 0;
+    for (int pg = pb, it = 0; pg < pe; ++pg, ++it) {
+        const int buf = it & 1;
+        const uint32_t parity = (it >> 1) & 1;
+        if (tid == 0 && pg + 1 < pe) {
+            // The other buffer was released by the barrier that ended the previous iteration.
+            fence_proxy_async();
+            const size_t off = (size_t)ptab[pg + 1] * p.cache.page_elems + head_off;
+            mbar_arrive_expect_tx(&bars[buf ^ 1], 2 * kTileBytes);
+            bulk_g2s(kbuf + (buf ^ 1) * kPage * HD, kpool + off, kTileBytes, &bars[buf ^ 1]);
+            bulk_g2s(vbuf + (buf ^ 1) * kPage * HD, vpool + off, kTileBytes, &bars[buf ^ 1]);
+        }
+        const bool ok = mbar_wait(&bars[buf], parity, p.status);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            fail_it = it;
+            break;
+        }
+        const KT *Ks = kbuf + buf * kPage * HD;
+        const KT *Vs = vbuf + buf * kPage * HD;
+        const int valid = min(kPage, nvis - pg * kPage);
+
+        // scores: one warp per key row, lanes split the head dimension
+        for (int j = warp; j < kPage; j += kAttnThreads / 32) {
+            float kv[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) kv[e] = Elem<KT>::load(Ks, (size_t)j * HD + lane * E + e);
+            for (int gi = 0; gi < G; ++gi) {
+                float d = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) d = fmaf(q_s[gi * HD + lane * E + e], kv[e], d);
+                d = warp_sum(d);
+                if (lane == 0) sc[gi * kPage + j] = (j < valid) ? d : -INFINITY;
+            }
+        }
+        __syncthreads();
+        // online softmax update, one warp per q head of the group
+        if (warp < G) {
+            const int gi = warp;
+            const float v0 = sc[gi * kPage + lane], v1 = sc[gi * kPage + lane + 32];
+            const float mp = warp_max(fmaxf(v0, v1));
+            const float m_old = m_s[gi];
+            const float m_new = fmaxf(m_old, mp);
+            const float alpha = expf(m_old - m_new);
+            const float p0 = (lane < valid) ? expf(v0 - m_new) : 0.f;
+            const float p1 = (lane + 32 < valid) ? expf(v1 - m_new) : 0.f;
+            sc[gi * kPage + lane] = p0;
+            sc[gi * kPage + lane + 32] = p1;
+            const float ls = warp_sum(p0 + p1);
+            if (lane == 0) {
+                l_s[gi] = l_s[gi] * alpha + ls;
+                m_s[gi] = m_new;
+                al_s[gi] = alpha;
+            }
+        }
+        __syncthreads();
+        // o = o * alpha + sum_j p_j v_j over the valid rows only
+#pragma unroll
+        for (int o = 0; o < NO; ++o) {
+            const int idx = tid + o * kAttnThreads;
+            if (idx < G * HD) {
+                const int gi = idx / HD, d = idx - gi * HD;
+                float a = o_acc[o] * al_s[gi];
+                const float *pj = sc + gi * kPage;
+                for (int j = 0; j < valid; ++j) a = fmaf(pj[j], Elem<KT>::load(Vs, (size_t)j * HD + d), a);
+                o_acc[o] = a;
+            }
+        }
+        __syncthreads();
+    }
+    if (failed) {
+        // Give the copies still in flight (this page's, and the next page's if it
+        // was prefetched) a bounded chance to land before the CTA exits.
+        if (tid == 0) {
+            mbar_wait(&bars[fail_it & 1], (fail_it >> 1) & 1, p.status);
+            if (pb + fail_it + 1 < pe) mbar_wait(&bars[(fail_it + 1) & 1], ((fail_it + 1) >> 1) & 1, p.status);
+        }
+        __syncthreads();
+        return;
+    }
+
+    const int hq0 = g * G;
+    const size_t out_row = (size_t)r * p.n_q * HD;
+    if (nact == 1) {
+#pragma unroll
+        for (int o = 0; o < NO; ++o) {
+            const int idx = tid + o * kAttnThreads;
+            if (idx < G * HD) {
+                const int gi = idx / HD, d = idx - gi * HD;
+                const float v = o_acc[o] / l_s[gi];
+                const size_t oi = out_row + (size_t)(hq0 + gi) * HD + d;
+                if (p.out_bf16) static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(v);
+                else static_cast<float *>(p.out)[oi] = v;
+            }
+        }
+        return;
+    }
+
+    // partial (m, l, o) of this split
+    constexpr int WS = HD + 4;
+#pragma unroll
+    for (int o = 0; o < NO; ++o) {
+        const int idx = tid + o * kAttnThreads;
+        if (idx < G * HD) {
+            const int gi = idx / HD, d = idx - gi * HD;
+            float *w = p.ws + (((size_t)r * p.n_q + hq0 + gi) * p.splits + sidx) * WS;
+            w[4 + d] = o_acc[o];
+            if (d == 0) {
+                w[0] = m_s[gi];
+                w[1] = l_s[gi];
+            }
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    int *cnt = p.cnt + (size_t)r * p.n_kv + g;
+    if (tid == 0) {
+        const int old = atomicAdd(cnt, 1);
+        flag_s = (old == nact - 1);
+    }
+    __syncthreads();
+    if (!flag_s) return;
+    __threadfence();
+    for (int idx = tid; idx < G * HD; idx += kAttnThreads) {
+        const int gi = idx / HD, d = idx - gi * HD;
+        const float *w0 = p.ws + (((size_t)r * p.n_q + hq0 + gi) * p.splits) * WS;
+        float M = -INFINITY;
+        for (int c = 0; c < nact; ++c) M = fmaxf(M, __ldcg(w0 + (size_t)c * WS));
+        float L = 0.f, O = 0.f;
+        for (int c = 0; c < nact; ++c) {
+            const float sc_c = expf(__ldcg(w0 + (size_t)c * WS) - M);
+            L = fmaf(__ldcg(w0 + (size_t)c * WS + 1), sc_c, L);
+            O = fmaf(__ldcg(w0 + (size_t)c * WS + 4 + d), sc_c, O);
+        }
+        const float v = O / L;
+        const size_t oi = out_row + (size_t)(hq0 + gi) * HD + d;
+        if (p.out_bf16) static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(v);
+        else static_cast<float *>(p.out)[oi] = v;
+    }
+    if (tid == 0) *cnt = 0;
+}
+
+template <typename KT, int HD>
+static cudaError_t launch_attn_t(const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.splits, p.n_kv, rows);
+    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.dynamicSmemBytes = attn_smem_bytes(sizeof(KT) == 2, HD, p.group);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_attn_decode<KT, HD>, p);
+}
+
+cudaError_t launch_attn(int kv_bf16, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
+    if (kv_bf16) {
+        switch (head_dim) {
+            case 32: return launch_attn_t<__nv_bfloat16, 32>(p, rows, st, pdl);
+            case 64: return launch_attn_t<__nv_bfloat16, 64>(p, rows, st, pdl);
+            case 128: return launch_attn_t<__nv_bfloat16, 128>(p, rows, st, pdl);
+        }
+    } else {
+        switch (head_dim) {
+            case 32: return launch_attn_t<float, 32>(p, rows, st, pdl);
+            case 64: return launch_attn_t<float, 64>(p, rows, st, pdl);
+            case 128: return launch_attn_t<float, 128>(p, rows, st, pdl);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t prepare_attn() {
+    const int bytes = 200 * 1024;
+    cudaError_t e = cudaSuccess;
+    e = e ? e : cudaFuncSetAttribute(k_attn_decode<float, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_decode<float, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_decode<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_decode<__nv_bfloat16, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_decode<__nv_bfloat16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_decode<__nv_bfloat16, 128>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e;
+}
+
+}  // namespace talker_k

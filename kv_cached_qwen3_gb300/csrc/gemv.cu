@@ -1,0 +1,393 @@
+// Fused GEMV family for decode and small row counts (SIMT, f32 activations).
+//
+// One warp computes one output feature (or one gate/up pair) for up to ROWS
+// activation rows; a CTA is 8 warps = 8 consecutive features; blockIdx.y is
+// the row block. Each warp streams its weight row(s) with 128-bit loads issued
+// before the activations are staged, so under programmatic dependent launch
+// the weight fetch of this kernel overlaps the tail of the previous one.
+//
+// Prologue (QKV, SWIGLU, HEAD): RMSNorm of each activation row with the gain,
+// x / sqrt(mean(x^2) + eps) * w ("qwentts.cpp/src/talker-forward.h",
+// talker_layer_forward "Pre-norm" and the MLP pre-norm; talker_forward_core
+// final norm). Epilogues: see talker_k::Epilogue.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace talker_dev;
+
+namespace talker_k {
+
+// Index of element k of row r in the staged activation tile. For bf16
+// weights a 16-byte weight vector covers 8 elements; its two halves are kept
+// in two planes so that lane-consecutive vectors read contiguous float4s.
+template <int EPV>
+__device__ __forceinline__ int act_index(int r, int k, int K) {
+    if (EPV == 8) return r * K + ((k >> 2) & 1) * (K >> 1) + (k >> 3) * 4 + (k & 3);
+    return r * K + k;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ size_t cache_offset(const CacheView &c, int stream, int layer, int head, int pos) {
+    const int page = c.page_table[stream * c.pages_per_stream + pos / kPage];
+    return (size_t)page * c.page_elems + ((size_t)(layer * c.n_kv + head) * kPage + (pos % kPage)) * c.head_dim;
+}
+
+__device__ __forceinline__ int row_stream(const RowMap &m, int r) { return m.mode == 0 ? r : m.stream0; }
+__device__ __forceinline__ int row_pos(const RowMap &m, int r) { return m.mode == 0 ? m.cur_len[r] : m.pos0 + r; }
+
+// QK-norm + NEOX RoPE + KV append for one completed head over the rows of a
+// row block ("talker-forward.h", talker_layer_forward: per-head QK-norm, RoPE
+// NEOX (half-split), set_rows into the cache at the fresh positions).
+__device__ void finish_head(const GemvParams &p, int hidx, int row0, int nrows) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hd = p.head_dim, half = hd >> 1;
+    const bool is_q = hidx < p.n_q;
+    const bool is_k = !is_q && hidx < p.n_q + p.n_kv;
+    const float *gain = is_q ? p.q_norm : p.k_norm;
+    for (int r = warp; r < nrows; r += kGemvWarps) {
+        const int row = row0 + r;
+        const float *src = p.out + (size_t)row * p.out_ld + (size_t)hidx * hd;
+        float a[2], b[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = lane + 32 * j;
+            a[j] = (i < half) ? __ldcg(src + i) : 0.f;
+            b[j] = (i < half) ? __ldcg(src + i + half) : 0.f;
+        }
+        const int pos = row_pos(p.rowmap, row);
+        if (pos < 0 || pos >= p.cache.max_seq) {
+            if (lane == 0) atomicOr(p.status, ST_BAD_POSITION);
+            continue;
+        }
+        if (is_q || is_k) {
+            float ss = a[0] * a[0] + b[0] * b[0] + a[1] * a[1] + b[1] * b[1];
+            ss = warp_sum(ss);
+            const float inv = 1.0f / sqrtf(ss / (float)hd + p.eps);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = lane + 32 * j;
+                if (i < half) {
+                    const float x0 = a[j] * inv * gain[i];
+                    const float x1 = b[j] * inv * gain[i + half];
+                    const float2 cs = p.rope[(size_t)pos * half + i];
+                    a[j] = x0 * cs.x - x1 * cs.y;
+                    b[j] = x1 * cs.x + x0 * cs.y;
+                }
+            }
+        }
+        if (is_q) {
+            float *dst = p.q_out + (size_t)row * p.n_q * hd + (size_t)hidx * hd;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = lane + 32 * j;
+                if (i < half) {
+                    dst[i] = a[j];
+                    dst[i + half] = b[j];
+                }
+            }
+        } else {
+            const int kvh = is_k ? hidx - p.n_q : hidx - p.n_q - p.n_kv;
+            const int stream = row_stream(p.rowmap, row);
+            const size_t off = cache_offset(p.cache, stream, p.layer, kvh, pos);
+            void *base = is_k ? p.cache.k : p.cache.v;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = lane + 32 * j;
+                if (i < half) {
+                    if (p.cache.kv_bf16) {
+                        __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(base) + off;
+                        d[i] = __float2bfloat16_rn(a[j]);
+                        d[i + half] = __float2bfloat16_rn(b[j]);
+                    } else {
+                        float *d = static_cast<float *>(base) + off;
+                        d[i] = a[j];
+                        d[i + half] = b[j];
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <typename WT, int ROWS, int EPI>
+__global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
+    constexpr int EPV = Elem<WT>::kPerVec;
+    constexpr int NW = (EPI == EPI_SWIGLU) ? 2 : 1;
+    constexpr int MAXC = (NW == 2) ? 8 : 16;
+    constexpr bool NORM = (EPI != EPI_RESID);
+    extern __shared__ __align__(16) float act_s[];
+    __shared__ float inv_s[ROWS];
+    __shared__ float hv_s[kGemvWarps][ROWS];
+    __shared__ int hi_s[kGemvWarps][ROWS];
+    __shared__ int flag_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rb = blockIdx.y;
+    const int row0 = rb * ROWS;
+    const int nrows = min(ROWS, p.rows - row0);
+    const int f = blockIdx.x * kGemvWarps + warp;
+    const bool fvalid = f < p.n_out;
+    const int K = p.K;
+    const int nvec = K / EPV;
+    const WT *wrow = static_cast<const WT *>(p.W) + (size_t)(NW * (fvalid ? f : 0)) * K;
+
+    pdl_launch_dependents();
+
+    float acc[NW][ROWS];
+#pragma unroll
+    for (int n = 0; n < NW; ++n)
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) acc[n][r] = 0.f;
+
+    for (int base = 0; base < nvec; base += 32 * MAXC) {
+        uint4 w[NW][MAXC];
+#pragma unroll
+        for (int n = 0; n < NW; ++n)
+#pragma unroll
+            for (int i = 0; i < MAXC; ++i) {
+                const int c = base + i * 32 + lane;
+                w[n][i] = (fvalid && c < nvec) ? ldg_stream(wrow + (size_t)n * K + (size_t)c * EPV)
+                                               : make_uint4(0u, 0u, 0u, 0u);
+            }
+        if (base == 0) {
+            // Activations are produced by the previous kernel: wait for it only now.
+            pdl_wait();
+            if (NORM) {
+                for (int r = warp; r < nrows; r += kGemvWarps) {
+                    const float *a = p.act + (size_t)(row0 + r) * p.act_ld;
+                    float ss = 0.f;
+                    for (int k = lane; k < K; k += 32) {
+                        const float v = a[k];
+                        ss += v * v;
+                    }
+                    ss = warp_sum(ss);
+                    if (lane == 0) inv_s[r] = 1.0f / sqrtf(ss / (float)K + p.eps);
+                }
+                __syncthreads();
+            }
+            const int K4 = K >> 2;
+            const bool do_copy = (p.copy_x != nullptr) && blockIdx.x == 0;
+            for (int idx = threadIdx.x; idx < nrows * K4; idx += kGemvThreads) {
+                const int r = idx / K4, k = (idx - r * K4) * 4;
+                const float4 v = *reinterpret_cast<const float4 *>(p.act + (size_t)(row0 + r) * p.act_ld + k);
+                if (do_copy) *reinterpret_cast<float4 *>(p.copy_x + (size_t)(row0 + r) * K + k) = v;
+                float e[4] = {v.x, v.y, v.z, v.w};
+                if (NORM) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) e[t] = e[t] * inv_s[r] * p.norm_w[k + t];
+                }
+                *reinterpret_cast<float4 *>(act_s + act_index<EPV>(r, k, K)) = make_float4(e[0], e[1], e[2], e[3]);
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int i = 0; i < MAXC; ++i) {
+            const int c = base + i * 32 + lane;
+            if (c < nvec) {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    if (r < nrows) {
+                        if (EPV == 8) {
+                            const float4 a0 = *reinterpret_cast<const float4 *>(act_s + r * K + c * 4);
+                            const float4 a1 = *reinterpret_cast<const float4 *>(act_s + r * K + (K >> 1) + c * 4);
+#pragma unroll
+                            for (int n = 0; n < NW; ++n) {
+                                const uint4 u = w[n][i];
+                                float s = acc[n][r];
+                                s = fmaf(bf16lo(u.x), a0.x, s);
+                                s = fmaf(bf16hi(u.x), a0.y, s);
+                                s = fmaf(bf16lo(u.y), a0.z, s);
+                                s = fmaf(bf16hi(u.y), a0.w, s);
+                                s = fmaf(bf16lo(u.z), a1.x, s);
+                                s = fmaf(bf16hi(u.z), a1.y, s);
+                                s = fmaf(bf16lo(u.w), a1.z, s);
+                                s = fmaf(bf16hi(u.w), a1.w, s);
+                                acc[n][r] = s;
+                            }
+                        } else {
+                            const float4 a0 = *reinterpret_cast<const float4 *>(act_s + r * K + c * 4);
+#pragma unroll
+                            for (int n = 0; n < NW; ++n) {
+                                const uint4 u = w[n][i];
+                                float s = acc[n][r];
+                                s = fmaf(__uint_as_float(u.x), a0.x, s);
+                                s = fmaf(__uint_as_float(u.y), a0.y, s);
+                                s = fmaf(__uint_as_float(u.z), a0.z, s);
+                                s = fmaf(__uint_as_float(u.w), a0.w, s);
+                                acc[n][r] = s;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- epilogue
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        const float v0 = warp_sum(acc[0][r]);
+        const float v1 = (NW == 2) ? warp_sum(acc[NW - 1][r]) : 0.f;
+        if (EPI == EPI_HEAD && lane == r) {
+            hv_s[warp][r] = (fvalid && r < nrows) ? v0 : -INFINITY;
+            hi_s[warp][r] = f;
+        }
+        if (lane == r && r < nrows && fvalid) {
+            float *o = p.out + (size_t)(row0 + r) * p.out_ld + f;
+            if (EPI == EPI_RESID) *o += v0;
+            else if (EPI == EPI_SWIGLU) *o = silu_f(v0) * v1;
+            else *o = v0;
+        }
+    }
+
+    if (EPI == EPI_QKV) {
+        __threadfence();
+        __syncthreads();
+        const int hidx = (blockIdx.x * kGemvWarps) / p.head_dim;
+        const int n_heads = p.n_q + 2 * p.n_kv;
+        int *cnt = p.cnt + (size_t)rb * n_heads + hidx;
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const int old = atomicAdd(cnt, 1);
+            flag_s = (old == p.head_dim / kGemvWarps - 1);
+        }
+        __syncthreads();
+        if (flag_s) {
+            __threadfence();
+            finish_head(p, hidx, row0, nrows);
+            if (threadIdx.x == 0) *cnt = 0;
+        }
+    }
+
+    if (EPI == EPI_HEAD) {
+        __syncthreads();
+        if (p.hidden_out != nullptr && blockIdx.x == 0) {
+            for (int idx = threadIdx.x; idx < nrows * K; idx += kGemvThreads) {
+                const int r = idx / K, k = idx - r * K;
+                p.hidden_out[(size_t)(row0 + r) * K + k] = act_s[act_index<EPV>(r, k, K)];
+            }
+        }
+        if (threadIdx.x < nrows) {
+            const int r = threadIdx.x;
+            float best = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int w = 0; w < kGemvWarps; ++w) {
+                const float v = hv_s[w][r];
+                const int i = hi_s[w][r];
+                if (isnan(v)) {
+                    atomicOr(p.status, ST_NAN_LOGIT);
+                    continue;
+                }
+                if (v > best || (v == best && i < bi)) {
+                    best = v;
+                    bi = i;
+                }
+            }
+            const size_t slot = ((size_t)rb * gridDim.x + blockIdx.x) * ROWS + r;
+            p.part_val[slot] = best;
+            p.part_idx[slot] = bi;
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const int old = atomicAdd(p.head_cnt + rb, 1);
+            flag_s = (old == (int)gridDim.x - 1);
+        }
+        __syncthreads();
+        if (flag_s) {
+            __threadfence();
+            if (threadIdx.x < nrows) {
+                const int r = threadIdx.x;
+                float best = -INFINITY;
+                int bi = 0x7fffffff;
+                for (int b = 0; b < (int)gridDim.x; ++b) {
+                    const size_t slot = ((size_t)rb * gridDim.x + b) * ROWS + r;
+                    const float v = __ldcg(p.part_val + slot);
+                    const int i = __ldcg(p.part_idx + slot);
+                    if (v > best || (v == best && i < bi)) {
+                        best = v;
+                        bi = i;
+                    }
+                }
+                if (p.argmax_out != nullptr) p.argmax_out[row0 + r] = bi;
+                if (p.inc_len) p.cur_len_rw[row0 + r] += 1;
+            }
+            if (threadIdx.x == 0) p.head_cnt[rb] = 0;
+        }
+    }
+}
+
+int gemv_rows_for(int rows) { return rows <= 1 ? 1 : (rows <= 4 ? 4 : 16); }
+
+size_t gemv_smem_bytes(int rows_tmpl, int K) { return (size_t)rows_tmpl * K * sizeof(float); }
+
+template <typename WT, int ROWS, int EPI>
+static cudaError_t launch_one(const GemvParams &p, cudaStream_t st, bool pdl) {
+    const int nfeat = p.n_out;
+    dim3 grid((nfeat + kGemvWarps - 1) / kGemvWarps, (p.rows + ROWS - 1) / ROWS, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = gemv_smem_bytes(ROWS, p.K);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_gemv<WT, ROWS, EPI>, p);
+}
+
+template <typename WT, int ROWS>
+static cudaError_t launch_rows(int epi, const GemvParams &p, cudaStream_t st, bool pdl) {
+    switch (epi) {
+        case EPI_QKV: return launch_one<WT, ROWS, EPI_QKV>(p, st, pdl);
+        case EPI_RESID: return launch_one<WT, ROWS, EPI_RESID>(p, st, pdl);
+        case EPI_SWIGLU: return launch_one<WT, ROWS, EPI_SWIGLU>(p, st, pdl);
+        case EPI_HEAD: return launch_one<WT, ROWS, EPI_HEAD>(p, st, pdl);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename WT>
+static cudaError_t launch_wt(int epi, int rows_tmpl, const GemvParams &p, cudaStream_t st, bool pdl) {
+    switch (rows_tmpl) {
+        case 1: return launch_rows<WT, 1>(epi, p, st, pdl);
+        case 4: return launch_rows<WT, 4>(epi, p, st, pdl);
+        case 16: return launch_rows<WT, 16>(epi, p, st, pdl);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemv(int epi, int w_bf16, int rows_tmpl, const GemvParams &p, cudaStream_t st, bool pdl) {
+    if (w_bf16) return launch_wt<__nv_bfloat16>(epi, rows_tmpl, p, st, pdl);
+    return launch_wt<float>(epi, rows_tmpl, p, st, pdl);
+}
+
+template <typename WT, int ROWS>
+static cudaError_t raise_rows() {
+    const int bytes = 200 * 1024;
+    cudaError_t e = cudaSuccess;
+    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e;
+}
+
+cudaError_t prepare_gemv() {
+    cudaError_t e = cudaSuccess;
+    e = e ? e : raise_rows<float, 1>();
+    e = e ? e : raise_rows<float, 4>();
+    e = e ? e : raise_rows<float, 16>();
+    e = e ? e : raise_rows<__nv_bfloat16, 1>();
+    e = e ? e : raise_rows<__nv_bfloat16, 4>();
+    e = e ? e : raise_rows<__nv_bfloat16, 16>();
+    return e;
+}
+
+}  // namespace talker_k
