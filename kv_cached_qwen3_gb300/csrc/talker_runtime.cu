@@ -1,0 +1,667 @@
+// Host runtime of the C-ABI declared in include/talker.h: weight store,
+// paged KV cache, workspaces, per-stream length bookkeeping, kernel sequencing
+// and the replayed CUDA graph of a decode step.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "kernels.cuh"
+#include "talker.h"
+
+using namespace talker_k;
+
+namespace {
+
+constexpr int kPageRows = 64;     // positions per KV page (kernels use the same constant)
+constexpr int kMaxGraphs = 8;     // cached decode graphs per handle
+
+struct LayerDev {
+    const float *in_norm, *post_norm, *q_norm, *k_norm;
+    const void *qkv, *o, *gu, *down;
+};
+
+struct GraphEntry {
+    int B;
+    const float *emb;
+    float *logits, *hidden;
+    int32_t *argmax;
+    cudaGraphExec_t exec;
+    int n_kernels;
+};
+
+talker_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return TALKER_OK;
+    cudaGetLastError();  // clear a non-sticky error so the handle stays usable
+    return e == cudaErrorMemoryAllocation ? TALKER_ENOMEM : TALKER_ECUDA;
+}
+
+#define TRY_CUDA(expr)                                     \
+    do {                                                   \
+        cudaError_t e_ = (expr);                           \
+        if (e_ != cudaSuccess) return from_cuda(e_);       \
+    } while (0)
+
+#define TRY(expr)                                          \
+    do {                                                   \
+        talker_status s_ = (expr);                         \
+        if (s_ != TALKER_OK) return s_;                    \
+    } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct talker {
+    talker_config c{};
+    cudaStream_t st = nullptr;
+    int dev = 0, n_sm = 0;
+    int H = 0, nq = 0, nkv = 0, hd = 0, qd = 0, kvd = 0, qkv_n = 0, I = 0, V = 0, G = 0;
+    int w_bf16 = 0, kv_bf16 = 0;
+    size_t wsz = 0, kvsz = 0;
+    char *wstore = nullptr;
+    std::vector<LayerDev> L;
+    const float *fnorm = nullptr;
+    const void *head = nullptr;
+    // KV cache
+    int n_streams = 0, max_seq = 0, pps = 0;
+    size_t page_elems = 0;
+    void *kpool = nullptr, *vpool = nullptr;
+    int *d_pt = nullptr, *d_len = nullptr;
+    float2 *d_rope = nullptr;
+    std::vector<int> len;
+    // activations, sized for cap_rows rows
+    int cap_rows = 0;
+    float *x = nullptr, *raw = nullptr, *q = nullptr, *attn = nullptr, *act = nullptr;
+    // workspaces
+    size_t cap_attn_ws = 0, cap_head_part = 0;
+    float *attn_ws = nullptr, *head_val = nullptr;
+    int *head_idx = nullptr;
+    int cap_cnt_rows = 0;
+    int *qkv_cnt = nullptr, *attn_cnt = nullptr, *head_cnt = nullptr;
+    int *d_status = nullptr;
+    int64_t launches = 0;
+    std::vector<GraphEntry> graphs;
+};
+
+namespace {
+
+void drop_graphs(talker *t) {
+    for (auto &g : t->graphs) cudaGraphExecDestroy(g.exec);
+    t->graphs.clear();
+}
+
+void free_ptr(void *p) {
+    if (p) cudaFree(p);
+}
+
+void free_workspaces(talker *t) {
+    float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->attn_ws, &t->head_val};
+    for (auto pp : fl) {
+        free_ptr(*pp);
+        *pp = nullptr;
+    }
+    int **il[] = {&t->head_idx, &t->qkv_cnt, &t->attn_cnt, &t->head_cnt};
+    for (auto pp : il) {
+        free_ptr(*pp);
+        *pp = nullptr;
+    }
+    t->cap_rows = 0;
+    t->cap_attn_ws = t->cap_head_part = 0;
+    t->cap_cnt_rows = 0;
+}
+
+void free_cache(talker *t) {
+    free_ptr(t->kpool);
+    free_ptr(t->vpool);
+    free_ptr(t->d_pt);
+    free_ptr(t->d_len);
+    free_ptr(t->d_rope);
+    t->kpool = t->vpool = nullptr;
+    t->d_pt = t->d_len = nullptr;
+    t->d_rope = nullptr;
+    t->n_streams = t->max_seq = t->pps = 0;
+    t->len.clear();
+}
+
+// Row-block height of the GEMV family for `rows` rows and input width K
+// (the staged activation tile must fit in shared memory).
+int pick_rows(int rows, int K) {
+    int r = gemv_rows_for(rows);
+    while (r > 1 && gemv_smem_bytes(r, K) > 200 * 1024) r = (r == 16) ? 4 : 1;
+    return r;
+}
+
+int decode_splits(const talker *t, int B) {
+    const int want = (2 * t->n_sm + B * t->nkv - 1) / (B * t->nkv);
+    return std::max(1, std::min(64, want));
+}
+
+// Grow activation buffers and workspaces to cover `rows` rows with `splits`
+// attention splits. Growing invalidates captured graphs (their pointers move).
+talker_status ensure_capacity(talker *t, int rows, int splits) {
+    const size_t need_ws = (size_t)rows * t->nq * splits * (t->hd + 4);
+    const int head_grid = (t->V + kGemvWarps - 1) / kGemvWarps;
+    const size_t need_head = ((size_t)rows + 16) * head_grid;   // row blocks * grid * ROWS <= (rows + 15) * grid
+    const bool grow_rows = rows > t->cap_rows;
+    const bool grow_ws = need_ws > t->cap_attn_ws;
+    const bool grow_head = need_head > t->cap_head_part;
+    if (!grow_rows && !grow_ws && !grow_head) return TALKER_OK;
+    TRY_CUDA(cudaStreamSynchronize(t->st));
+    drop_graphs(t);
+    if (grow_rows) {
+        const int cap = std::max(rows, 16);
+        float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act};
+        const int widths[] = {t->H, t->qkv_n, t->qd, t->qd, t->I};
+        for (int i = 0; i < 5; ++i) {
+            free_ptr(*fl[i]);
+            *fl[i] = nullptr;
+            TRY_CUDA(cudaMalloc(fl[i], (size_t)cap * widths[i] * sizeof(float)));
+        }
+        // counters: QKV per (row block of up to 16 rows, head); attention per (row, kv head); head per row block
+        int **il[] = {&t->qkv_cnt, &t->attn_cnt, &t->head_cnt};
+        const size_t n_heads = (size_t)t->nq + 2 * t->nkv;
+        const size_t counts[] = {(size_t)cap * n_heads, (size_t)cap * t->nkv, (size_t)cap};
+        for (int i = 0; i < 3; ++i) {
+            free_ptr(*il[i]);
+            *il[i] = nullptr;
+            TRY_CUDA(cudaMalloc(il[i], counts[i] * sizeof(int)));
+            TRY_CUDA(cudaMemsetAsync(*il[i], 0, counts[i] * sizeof(int), t->st));
+        }
+        t->cap_rows = cap;
+        t->cap_cnt_rows = cap;
+    }
+    if (grow_ws) {
+        free_ptr(t->attn_ws);
+        t->attn_ws = nullptr;
+        TRY_CUDA(cudaMalloc(&t->attn_ws, need_ws * sizeof(float)));
+        t->cap_attn_ws = need_ws;
+    }
+    if (grow_head) {
+        free_ptr(t->head_val);
+        free_ptr(t->head_idx);
+        t->head_val = nullptr;
+        t->head_idx = nullptr;
+        TRY_CUDA(cudaMalloc(&t->head_val, need_head * sizeof(float)));
+        TRY_CUDA(cudaMalloc(&t->head_idx, need_head * sizeof(int)));
+        t->cap_head_part = need_head;
+    }
+    return TALKER_OK;
+}
+
+talker_status validate_config(const talker_config *c) {
+    if (!c) return TALKER_EINVAL;
+    if (c->n_layers < 1 || c->hidden < 64 || c->hidden % 64 || c->n_q_heads < 1 || c->n_kv_heads < 1) return TALKER_EINVAL;
+    if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128) return TALKER_EINVAL;
+    if (c->n_q_heads % c->n_kv_heads || c->n_q_heads / c->n_kv_heads > 8) return TALKER_EINVAL;
+    if ((c->n_q_heads * c->head_dim) % 64 || c->intermediate < 64 || c->intermediate % 64) return TALKER_EINVAL;
+    if (c->vocab < 8 || c->vocab % 8) return TALKER_EINVAL;
+    if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return TALKER_EINVAL;
+    if ((c->weight_dtype != TALKER_DTYPE_F32 && c->weight_dtype != TALKER_DTYPE_BF16) ||
+        (c->kv_dtype != TALKER_DTYPE_F32 && c->kv_dtype != TALKER_DTYPE_BF16))
+        return TALKER_EINVAL;
+    // the widest GEMV input must fit one staged row in shared memory
+    const int kmax = std::max(std::max(c->hidden, c->n_q_heads * c->head_dim), c->intermediate);
+    if (gemv_smem_bytes(1, kmax) > 200 * 1024) return TALKER_EINVAL;
+    return TALKER_OK;
+}
+
+talker_status build_store(talker *t, const talker_weight_ptrs *w) {
+    const int H = t->H, I = t->I;
+    const size_t wsz = t->wsz;
+    const size_t sz_qkv = (size_t)t->qkv_n * H * wsz, sz_o = (size_t)H * t->qd * wsz;
+    const size_t sz_gu = (size_t)2 * I * H * wsz, sz_d = (size_t)H * I * wsz;
+    const size_t sz_norms = (2 * (size_t)H + 2 * (size_t)t->hd) * sizeof(float);
+    size_t per_layer = align_up(sz_qkv, 256) + align_up(sz_o, 256) + align_up(sz_gu, 256) + align_up(sz_d, 256) +
+                       align_up(sz_norms, 256);
+    size_t total = per_layer * t->c.n_layers + align_up((size_t)t->V * H * wsz, 256) + align_up(H * sizeof(float), 256);
+    TRY_CUDA(cudaMalloc(&t->wstore, total));
+    char *p = t->wstore;
+    auto take = [&](size_t bytes) {
+        char *r = p;
+        p += align_up(bytes, 256);
+        return r;
+    };
+    const cudaMemcpyKind D2D = cudaMemcpyDeviceToDevice;
+    t->L.resize(t->c.n_layers);
+    for (int l = 0; l < t->c.n_layers; ++l) {
+        const talker_layer_ptrs &src = w->layers[l];
+        const void *need[] = {src.input_norm, src.q_proj, src.k_proj, src.v_proj, src.q_norm, src.k_norm,
+                              src.o_proj, src.post_norm, src.gate_proj, src.up_proj, src.down_proj};
+        for (const void *n : need)
+            if (!n) return TALKER_EINVAL;
+        LayerDev &d = t->L[l];
+        char *qkv = take(sz_qkv);
+        const size_t qbytes = (size_t)t->qd * H * wsz, kbytes = (size_t)t->kvd * H * wsz;
+        TRY_CUDA(cudaMemcpyAsync(qkv, src.q_proj, qbytes, D2D, t->st));
+        TRY_CUDA(cudaMemcpyAsync(qkv + qbytes, src.k_proj, kbytes, D2D, t->st));
+        TRY_CUDA(cudaMemcpyAsync(qkv + qbytes + kbytes, src.v_proj, kbytes, D2D, t->st));
+        d.qkv = qkv;
+        char *o = take(sz_o);
+        TRY_CUDA(cudaMemcpyAsync(o, src.o_proj, sz_o, D2D, t->st));
+        d.o = o;
+        // gate row j -> row 2j, up row j -> row 2j+1 (one GEMV warp or GEMM column pair per output j)
+        char *gu = take(sz_gu);
+        const size_t row = (size_t)H * wsz;
+        TRY_CUDA(cudaMemcpy2DAsync(gu, 2 * row, src.gate_proj, row, row, I, D2D, t->st));
+        TRY_CUDA(cudaMemcpy2DAsync(gu + row, 2 * row, src.up_proj, row, row, I, D2D, t->st));
+        d.gu = gu;
+        char *dn = take(sz_d);
+        TRY_CUDA(cudaMemcpyAsync(dn, src.down_proj, sz_d, D2D, t->st));
+        d.down = dn;
+        float *nrm = reinterpret_cast<float *>(take(sz_norms));
+        TRY_CUDA(cudaMemcpyAsync(nrm, src.input_norm, H * sizeof(float), D2D, t->st));
+        TRY_CUDA(cudaMemcpyAsync(nrm + H, src.post_norm, H * sizeof(float), D2D, t->st));
+        TRY_CUDA(cudaMemcpyAsync(nrm + 2 * H, src.q_norm, t->hd * sizeof(float), D2D, t->st));
+        TRY_CUDA(cudaMemcpyAsync(nrm + 2 * H + t->hd, src.k_norm, t->hd * sizeof(float), D2D, t->st));
+        d.in_norm = nrm;
+        d.post_norm = nrm + H;
+        d.q_norm = nrm + 2 * H;
+        d.k_norm = nrm + 2 * H + t->hd;
+    }
+    if (!w->codec_head || !w->final_norm) return TALKER_EINVAL;
+    char *hw = take((size_t)t->V * H * wsz);
+    TRY_CUDA(cudaMemcpyAsync(hw, w->codec_head, (size_t)t->V * H * wsz, D2D, t->st));
+    t->head = hw;
+    float *fn = reinterpret_cast<float *>(take(H * sizeof(float)));
+    TRY_CUDA(cudaMemcpyAsync(fn, w->final_norm, H * sizeof(float), D2D, t->st));
+    t->fnorm = fn;
+    return TALKER_OK;
+}
+
+}  // namespace
+
+namespace {
+
+CacheView cache_view(const talker *t) {
+    CacheView c{};
+    c.k = t->kpool;
+    c.v = t->vpool;
+    c.page_table = t->d_pt;
+    c.pages_per_stream = t->pps;
+    c.max_seq = t->max_seq;
+    c.n_layers = t->c.n_layers;
+    c.n_kv = t->nkv;
+    c.head_dim = t->hd;
+    c.kv_bf16 = t->kv_bf16;
+    c.page_elems = t->page_elems;
+    return c;
+}
+
+struct ForwardOut {
+    float *logits;
+    float *hidden;
+    int32_t *argmax;
+    bool head_all_rows;  // logits/hidden for every row, else the last row only
+    int inc_len;         // decode: bump cur_len[r] for every row after the step
+};
+
+// Enqueue the whole forward for `rows` rows: per layer QKV (+QK-norm, RoPE, KV
+// append), attention, o_proj + residual, gate/up SwiGLU, down + residual; then
+// the final norm + codec_head (+argmax). Returns the number of kernels enqueued
+// through *n_kernels.
+talker_status enqueue_forward(talker *t, int rows, const RowMap &rm, const float *emb, int splits,
+                              const ForwardOut &out, int *n_kernels) {
+    const CacheView cv = cache_view(t);
+    const int nh = t->c.n_layers;
+    int nk = 0;
+    bool pdl = false;  // the first kernel waits on everything before it in the stream
+    for (int l = 0; l < nh; ++l) {
+        const LayerDev &d = t->L[l];
+        GemvParams p{};
+        p.eps = t->c.rms_eps;
+        p.rows = rows;
+        p.status = t->d_status;
+        // 1) RMSNorm -> [Wq;Wk;Wv] -> QK-norm, RoPE, KV append
+        p.W = d.qkv;
+        p.act = (l == 0) ? emb : t->x;
+        p.act_ld = t->H;
+        p.norm_w = d.in_norm;
+        p.K = t->H;
+        p.n_out = t->qkv_n;
+        p.out = t->raw;
+        p.out_ld = t->qkv_n;
+        p.copy_x = (l == 0) ? t->x : nullptr;
+        p.layer = l;
+        p.n_q = t->nq;
+        p.n_kv = t->nkv;
+        p.head_dim = t->hd;
+        p.q_norm = d.q_norm;
+        p.k_norm = d.k_norm;
+        p.rope = t->d_rope;
+        p.q_out = t->q;
+        p.cache = cv;
+        p.rowmap = rm;
+        p.cnt = t->qkv_cnt;
+        TRY_CUDA(launch_gemv(EPI_QKV, t->w_bf16, pick_rows(rows, t->H), p, t->st, pdl));
+        pdl = true;
+        ++nk;
+        // 2) attention over [0, pos]
+        AttnParams a{};
+        a.q = t->q;
+        a.out = t->attn;
+        a.out_bf16 = 0;
+        a.cache = cv;
+        a.rowmap = rm;
+        a.layer = l;
+        a.n_q = t->nq;
+        a.n_kv = t->nkv;
+        a.group = t->G;
+        a.splits = splits;
+        a.scale = 1.0f / sqrtf((float)t->hd);
+        a.ws = t->attn_ws;
+        a.cnt = t->attn_cnt;
+        a.status = t->d_status;
+        TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, rows, t->st, pdl));
+        ++nk;
+        // 3) o_proj + residual
+        GemvParams o{};
+        o.rows = rows;
+        o.status = t->d_status;
+        o.W = d.o;
+        o.act = t->attn;
+        o.act_ld = t->qd;
+        o.K = t->qd;
+        o.n_out = t->H;
+        o.out = t->x;
+        o.out_ld = t->H;
+        TRY_CUDA(launch_gemv(EPI_RESID, t->w_bf16, pick_rows(rows, t->qd), o, t->st, pdl));
+        ++nk;
+        // 4) post-norm -> [Wg;Wu] -> silu(gate) * up
+        GemvParams m{};
+        m.rows = rows;
+        m.status = t->d_status;
+        m.eps = t->c.rms_eps;
+        m.W = d.gu;
+        m.act = t->x;
+        m.act_ld = t->H;
+        m.norm_w = d.post_norm;
+        m.K = t->H;
+        m.n_out = t->I;
+        m.out = t->act;
+        m.out_ld = t->I;
+        TRY_CUDA(launch_gemv(EPI_SWIGLU, t->w_bf16, pick_rows(rows, t->H), m, t->st, pdl));
+        ++nk;
+        // 5) down + residual
+        GemvParams dn{};
+        dn.rows = rows;
+        dn.status = t->d_status;
+        dn.W = d.down;
+        dn.act = t->act;
+        dn.act_ld = t->I;
+        dn.K = t->I;
+        dn.n_out = t->H;
+        dn.out = t->x;
+        dn.out_ld = t->H;
+        TRY_CUDA(launch_gemv(EPI_RESID, t->w_bf16, pick_rows(rows, t->I), dn, t->st, pdl));
+        ++nk;
+    }
+    // final norm -> codec_head -> logits, hidden, argmax
+    const int hrows = out.head_all_rows ? rows : 1;
+    GemvParams h{};
+    h.eps = t->c.rms_eps;
+    h.rows = hrows;
+    h.status = t->d_status;
+    h.W = t->head;
+    h.act = out.head_all_rows ? t->x : t->x + (size_t)(rows - 1) * t->H;
+    h.act_ld = t->H;
+    h.norm_w = t->fnorm;
+    h.K = t->H;
+    h.n_out = t->V;
+    h.out = out.logits;
+    h.out_ld = t->V;
+    h.hidden_out = out.hidden;
+    h.argmax_out = out.argmax;
+    h.part_val = t->head_val;
+    h.part_idx = t->head_idx;
+    h.head_cnt = t->head_cnt;
+    h.inc_len = out.inc_len;
+    h.cur_len_rw = t->d_len;
+    TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, t->st, pdl));
+    ++nk;
+    *n_kernels = nk;
+    return TALKER_OK;
+}
+
+talker_status check_stream(const talker *t, int stream) {
+    if (!t) return TALKER_EINVAL;
+    if (t->n_streams == 0) return TALKER_ESTATE;
+    if (stream < 0 || stream >= t->n_streams) return TALKER_EINVAL;
+    return TALKER_OK;
+}
+
+talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float *hidden, float *logits,
+                           int32_t *argmax, bool all_rows) {
+    TRY(check_stream(t, stream));
+    if (!emb || !logits || T < 1) return TALKER_EINVAL;
+    if (T > t->max_seq) return TALKER_EOVERFLOW;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    TRY(ensure_capacity(t, T, 1));
+    RowMap rm{1, stream, 0, t->d_len};
+    ForwardOut out{logits, hidden, all_rows ? nullptr : argmax, all_rows, 0};
+    int nk = 0;
+    TRY(enqueue_forward(t, T, rm, emb, 1, out, &nk));
+    TRY_CUDA(launch_set_len(t->d_len, stream, T, t->st));
+    t->launches += nk + 1;
+    t->len[stream] = T;
+    return TALKER_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *talker_status_str(talker_status s) {
+    switch (s) {
+        case TALKER_OK: return "ok";
+        case TALKER_EINVAL: return "invalid argument";
+        case TALKER_EOVERFLOW: return "KV cache overflow";
+        case TALKER_ENOMEM: return "out of device memory";
+        case TALKER_ECUDA: return "CUDA error";
+        case TALKER_ESTATE: return "call out of order";
+        case TALKER_EDEVICE: return "device status word set";
+    }
+    return "unknown status";
+}
+
+talker_status talker_create(const talker_config *cfg, const talker_weight_ptrs *weights, void *cuda_stream,
+                            talker_t **out) {
+    if (!out) return TALKER_EINVAL;
+    *out = nullptr;
+    TRY(validate_config(cfg));
+    if (!weights || !weights->layers) return TALKER_EINVAL;
+    talker *t = new talker();
+    t->c = *cfg;
+    t->st = static_cast<cudaStream_t>(cuda_stream);
+    t->H = cfg->hidden;
+    t->nq = cfg->n_q_heads;
+    t->nkv = cfg->n_kv_heads;
+    t->hd = cfg->head_dim;
+    t->qd = t->nq * t->hd;
+    t->kvd = t->nkv * t->hd;
+    t->qkv_n = t->qd + 2 * t->kvd;
+    t->I = cfg->intermediate;
+    t->V = cfg->vocab;
+    t->G = t->nq / t->nkv;
+    t->w_bf16 = cfg->weight_dtype == TALKER_DTYPE_BF16;
+    t->kv_bf16 = cfg->kv_dtype == TALKER_DTYPE_BF16;
+    t->wsz = t->w_bf16 ? 2 : 4;
+    t->kvsz = t->kv_bf16 ? 2 : 4;
+    talker_status s = from_cuda(cudaGetDevice(&t->dev));
+    if (s == TALKER_OK) s = from_cuda(cudaDeviceGetAttribute(&t->n_sm, cudaDevAttrMultiProcessorCount, t->dev));
+    if (s == TALKER_OK) s = from_cuda(prepare_kernels());
+    if (s == TALKER_OK) s = from_cuda(cudaMalloc(&t->d_status, sizeof(int)));
+    if (s == TALKER_OK) s = from_cuda(cudaMemsetAsync(t->d_status, 0, sizeof(int), t->st));
+    if (s == TALKER_OK) s = build_store(t, weights);
+    if (s == TALKER_OK) s = from_cuda(cudaStreamSynchronize(t->st));
+    if (s != TALKER_OK) {
+        talker_destroy(t);
+        return s;
+    }
+    *out = t;
+    return TALKER_OK;
+}
+
+void talker_destroy(talker_t *t) {
+    if (!t) return;
+    cudaSetDevice(t->dev);
+    cudaStreamSynchronize(t->st);
+    drop_graphs(t);
+    free_workspaces(t);
+    free_cache(t);
+    free_ptr(t->wstore);
+    free_ptr(t->d_status);
+    delete t;
+}
+
+talker_status talker_kv_init_batched(talker_t *t, int n_streams, int max_seq_len) {
+    if (!t || n_streams < 1 || max_seq_len < 1) return TALKER_EINVAL;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    TRY_CUDA(cudaStreamSynchronize(t->st));
+    drop_graphs(t);
+    free_cache(t);
+    const int pps = (max_seq_len + kPageRows - 1) / kPageRows;
+    const size_t page_elems = (size_t)t->c.n_layers * t->nkv * kPageRows * t->hd;
+    const size_t n_pages = (size_t)n_streams * pps;
+    const size_t pool_bytes = n_pages * page_elems * t->kvsz;
+    TRY_CUDA(cudaMalloc(&t->kpool, pool_bytes));
+    TRY_CUDA(cudaMalloc(&t->vpool, pool_bytes));
+    TRY_CUDA(cudaMemsetAsync(t->kpool, 0, pool_bytes, t->st));
+    TRY_CUDA(cudaMemsetAsync(t->vpool, 0, pool_bytes, t->st));
+    std::vector<int> pt(n_pages);
+    for (size_t i = 0; i < n_pages; ++i) pt[i] = (int)i;  // stream s owns pages [s*pps, (s+1)*pps)
+    TRY_CUDA(cudaMalloc(&t->d_pt, n_pages * sizeof(int)));
+    TRY_CUDA(cudaMemcpy(t->d_pt, pt.data(), n_pages * sizeof(int), cudaMemcpyHostToDevice));
+    TRY_CUDA(cudaMalloc(&t->d_len, n_streams * sizeof(int)));
+    TRY_CUDA(cudaMemsetAsync(t->d_len, 0, n_streams * sizeof(int), t->st));
+    // RoPE table: angle p * theta^(-2i/hd) evaluated in double on the host, stored as f32 (cos, sin)
+    const int half = t->hd / 2;
+    std::vector<float2> rope((size_t)max_seq_len * half);
+    for (int i = 0; i < half; ++i) {
+        const double inv = std::pow((double)t->c.rope_theta, -2.0 * i / t->hd);
+        for (int pos = 0; pos < max_seq_len; ++pos) {
+            const double ang = pos * inv;
+            rope[(size_t)pos * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    }
+    TRY_CUDA(cudaMalloc(&t->d_rope, rope.size() * sizeof(float2)));
+    TRY_CUDA(cudaMemcpy(t->d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    TRY_CUDA(cudaStreamSynchronize(t->st));
+    t->n_streams = n_streams;
+    t->max_seq = max_seq_len;
+    t->pps = pps;
+    t->page_elems = page_elems;
+    t->len.assign(n_streams, 0);
+    return TALKER_OK;
+}
+
+talker_status talker_kv_rewind(talker_t *t, int stream, int new_len) {
+    TRY(check_stream(t, stream));
+    if (new_len < 0 || new_len > t->len[stream]) return TALKER_EINVAL;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    TRY_CUDA(launch_set_len(t->d_len, stream, new_len, t->st));
+    t->launches += 1;
+    t->len[stream] = new_len;
+    return TALKER_OK;
+}
+
+talker_status talker_cur_len(const talker_t *t, int stream, int *out_len) {
+    TRY(check_stream(t, stream));
+    if (!out_len) return TALKER_EINVAL;
+    *out_len = t->len[stream];
+    return TALKER_OK;
+}
+
+talker_status talker_prefill(talker_t *t, int stream, const float *emb, int T, float *hidden_last,
+                             float *logits_last, int32_t *argmax_last) {
+    return prefill_impl(t, stream, emb, T, hidden_last, logits_last, argmax_last, false);
+}
+
+talker_status talker_prefill_all_rows(talker_t *t, int stream, const float *emb, int T, float *hidden,
+                                      float *logits) {
+    return prefill_impl(t, stream, emb, T, hidden, logits, nullptr, true);
+}
+
+talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits, float *hidden, int32_t *argmax) {
+    if (!t) return TALKER_EINVAL;
+    if (t->n_streams == 0) return TALKER_ESTATE;
+    if (!emb || !logits || B < 1 || B > t->n_streams) return TALKER_EINVAL;
+    for (int b = 0; b < B; ++b)
+        if (t->len[b] + 1 > t->max_seq) return TALKER_EOVERFLOW;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    const int splits = decode_splits(t, B);
+    TRY(ensure_capacity(t, B, splits));
+    GraphEntry *ge = nullptr;
+    for (auto &g : t->graphs)
+        if (g.B == B && g.emb == emb && g.logits == logits && g.hidden == hidden && g.argmax == argmax) ge = &g;
+    if (!ge) {
+        if ((int)t->graphs.size() >= kMaxGraphs) {
+            cudaGraphExecDestroy(t->graphs.front().exec);
+            t->graphs.erase(t->graphs.begin());
+        }
+        RowMap rm{0, 0, 0, t->d_len};
+        ForwardOut out{logits, hidden, argmax, true, 1};
+        int nk = 0;
+        cudaGraph_t graph = nullptr;
+        TRY_CUDA(cudaStreamBeginCapture(t->st, cudaStreamCaptureModeThreadLocal));
+        talker_status s = enqueue_forward(t, B, rm, emb, splits, out, &nk);
+        cudaError_t e = cudaStreamEndCapture(t->st, &graph);
+        if (s != TALKER_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return s;
+        }
+        if (e != cudaSuccess) return from_cuda(e);
+        cudaGraphExec_t exec = nullptr;
+        e = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return from_cuda(e);
+        t->graphs.push_back(GraphEntry{B, emb, logits, hidden, argmax, exec, nk});
+        ge = &t->graphs.back();
+    }
+    TRY_CUDA(cudaGraphLaunch(ge->exec, t->st));
+    t->launches += ge->n_kernels;
+    for (int b = 0; b < B; ++b) t->len[b] += 1;
+    return TALKER_OK;
+}
+
+talker_status talker_kv_import(talker_t *t, int stream, const void *k, const void *v, int len) {
+    TRY(check_stream(t, stream));
+    if (!k || !v || len < 0) return TALKER_EINVAL;
+    if (len > t->max_seq) return TALKER_EOVERFLOW;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    TRY_CUDA(launch_kv_copy(cache_view(t), stream, const_cast<void *>(k), const_cast<void *>(v), len, 1, t->st));
+    TRY_CUDA(launch_set_len(t->d_len, stream, len, t->st));
+    t->launches += (len > 0) + 1;
+    t->len[stream] = len;
+    return TALKER_OK;
+}
+
+talker_status talker_kv_export(const talker_t *t, int stream, void *k, void *v, int len) {
+    TRY(check_stream(t, stream));
+    if (!k || !v || len < 0) return TALKER_EINVAL;
+    if (len > t->max_seq) return TALKER_EOVERFLOW;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    TRY_CUDA(launch_kv_copy(cache_view(t), stream, k, v, len, 0, t->st));
+    const_cast<talker *>(t)->launches += (len > 0);
+    return TALKER_OK;
+}
+
+talker_status talker_sync_status(talker_t *t, int32_t *code) {
+    if (!t) return TALKER_EINVAL;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    TRY_CUDA(cudaStreamSynchronize(t->st));
+    int h = 0;
+    TRY_CUDA(cudaMemcpy(&h, t->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+    if (code) *code = h;
+    if (h != 0) {
+        TRY_CUDA(cudaMemset(t->d_status, 0, sizeof(int)));
+        return TALKER_EDEVICE;
+    }
+    return TALKER_OK;
+}
+
+int64_t talker_kernel_launches(const talker_t *t) { return t ? t->launches : 0; }
+
+}  // extern "C"
