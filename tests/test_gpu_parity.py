@@ -1,0 +1,101 @@
+"""GPU parity: the CUDA library against the fp64 oracle on the same seeded inputs.
+
+Every test calls the library through its C-ABI (ctypes binding) and compares
+element by element with the oracle (tolerances in parity_util)."""
+import numpy as np
+import pytest
+
+from kv_cached_qwen3_gb300 import inputs
+from oracle import Oracle, OracleCache
+from parity_util import check_rows, top1_agreement, TOL_TOP1
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kv_cached_qwen3_gb300 import talker
+    talker.load_library()
+    return torch.device("cuda", 0)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+def host(t):
+    return t.detach().float().cpu().numpy()
+
+
+def run_prefill_decode(geom, weights, emb, T0, n_dec, max_seq):
+    from kv_cached_qwen3_gb300.talker import Talker
+    tk = Talker(geom, weights)
+    tk.kv_init_batched(1, max_seq)
+    hid, lg, am = tk.prefill(0, dev(emb[:T0]))
+    hids, lgs, ams = [host(hid)], [host(lg)], [int(host(am)[0])]
+    assert tk.cur_len(0) == T0
+    H, V = geom.hidden, geom.vocab
+    out_l = torch.empty(1, V, device="cuda")
+    out_h = torch.empty(1, H, device="cuda")
+    out_a = torch.empty(1, device="cuda", dtype=torch.int32)
+    e = torch.empty(1, H, device="cuda")
+    for t in range(n_dec):
+        e.copy_(dev(emb[T0 + t:T0 + t + 1]))
+        tk.decode(e, out_l, out_h, out_a)
+        hids.append(host(out_h)[0])
+        lgs.append(host(out_l)[0])
+        ams.append(int(host(out_a)[0]))
+    assert tk.sync_status() == 0
+    assert tk.cur_len(0) == T0 + n_dec
+    tk.close()
+    return np.stack(hids), np.stack(lgs), np.array(ams)
+
+
+def test_tiny_prefill_and_decode_fp32(cuda):
+    wl = inputs.WORKLOADS["tiny"]
+    g = wl.geometry
+    w = inputs.make_weights(g, wl.seed)
+    T0, n = wl.prefill_T, wl.decode_steps
+    emb = inputs.make_embeddings(g, wl.seed, 0, T0 + n)
+    hid, lg, am = run_prefill_decode(g, w, emb, T0, n, 64)
+    rh, rl = Oracle(g, w).forward_full(emb)
+    check_rows(hid, rh[T0 - 1:], bf16=False, what="tiny hidden")
+    check_rows(lg, rl[T0 - 1:], bf16=False, what="tiny logits")
+    # the fused argmax equals the host argmax of the returned logits, bit for bit
+    np.testing.assert_array_equal(am, np.argmax(lg, axis=-1))
+
+
+def test_tiny_prefill_all_rows_and_ragged_lengths(cuda):
+    from kv_cached_qwen3_gb300.talker import Talker
+    wl = inputs.WORKLOADS["tiny"]
+    g = wl.geometry
+    w = inputs.make_weights(g, wl.seed)
+    o = Oracle(g, w)
+    tk = Talker(g, w)
+    tk.kv_init_batched(1, 200)
+    for T in (1, 7, 16, 17, 65, 130):     # several tiles, ragged tails, page boundaries
+        emb = inputs.make_embeddings(g, 11, 0, T)
+        hid, lg = tk.prefill_all_rows(0, dev(emb))
+        rh, rl = o.forward_full(emb)
+        check_rows(host(hid), rh, bf16=False, what="tiny all rows T=%d hidden" % T)
+        check_rows(host(lg), rl, bf16=False, what="tiny all rows T=%d logits" % T)
+        assert tk.cur_len(0) == T
+    assert tk.sync_status() == 0
+
+
+def test_talker_b1_prefill96_decode512_bf16(cuda):
+    wl = inputs.WORKLOADS["talker_b1"]
+    g = wl.geometry
+    w = inputs.make_weights(g, wl.seed)
+    T0, n = wl.prefill_T, wl.decode_steps
+    emb = inputs.make_embeddings(g, wl.seed, 0, T0 + n)
+    hid, lg, am = run_prefill_decode(g, w, emb, T0, n, T0 + n)
+    rh, rl = Oracle(g, w).forward_full(emb)
+    check_rows(hid, rh[T0 - 1:], bf16=True, what="talker hidden")
+    check_rows(lg, rl[T0 - 1:], bf16=True, what="talker logits")
+    agree = top1_agreement(lg[1:], rl[T0:])
+    assert agree >= TOL_TOP1, agree
+    np.testing.assert_array_equal(am, np.argmax(lg, axis=-1))
