@@ -158,6 +158,10 @@ talker_status talker_sync_status(talker_t *t, int32_t *code);
 /* Human-readable name of a status code (static string). */
 const char *talker_status_str(talker_status s);
 
+/* Text of the last CUDA error that made a call on this thread return ECUDA or
+ * ENOMEM (static thread-local buffer; empty if none). */
+const char *talker_last_error(void);
+
 /* Test support: count of kernel launches the library enqueued since creation
  * (a graph replay counts each of its kernels). */
 int64_t talker_kernel_launches(const talker_t *t);

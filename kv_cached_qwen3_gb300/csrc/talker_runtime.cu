@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <vector>
 
@@ -32,8 +33,11 @@ struct GraphEntry {
     int n_kernels;
 };
 
+thread_local char g_last_error[256] = "";
+
 talker_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return TALKER_OK;
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
     cudaGetLastError();  // clear a non-sticky error so the handle stays usable
     return e == cudaErrorMemoryAllocation ? TALKER_ENOMEM : TALKER_ECUDA;
 }
@@ -57,6 +61,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct talker {
     talker_config c{};
     cudaStream_t st = nullptr;
+    cudaStream_t cap_st = nullptr;  // private stream for graph capture (the caller's may be the legacy stream)
     int dev = 0, n_sm = 0;
     int H = 0, nq = 0, nkv = 0, hd = 0, qd = 0, kvd = 0, qkv_n = 0, I = 0, V = 0, G = 0;
     int w_bf16 = 0, kv_bf16 = 0;
@@ -302,8 +307,8 @@ struct ForwardOut {
 // append), attention, o_proj + residual, gate/up SwiGLU, down + residual; then
 // the final norm + codec_head (+argmax). Returns the number of kernels enqueued
 // through *n_kernels.
-talker_status enqueue_forward(talker *t, int rows, const RowMap &rm, const float *emb, int splits,
-                              const ForwardOut &out, int *n_kernels) {
+talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap &rm, const float *emb,
+                              int splits, const ForwardOut &out, int *n_kernels) {
     const CacheView cv = cache_view(t);
     const int nh = t->c.n_layers;
     int nk = 0;
@@ -335,7 +340,7 @@ talker_status enqueue_forward(talker *t, int rows, const RowMap &rm, const float
         p.cache = cv;
         p.rowmap = rm;
         p.cnt = t->qkv_cnt;
-        TRY_CUDA(launch_gemv(EPI_QKV, t->w_bf16, pick_rows(rows, t->H), p, t->st, pdl));
+        TRY_CUDA(launch_gemv(EPI_QKV, t->w_bf16, pick_rows(rows, t->H), p, st, pdl));
         pdl = true;
         ++nk;
         // 2) attention over [0, pos]
@@ -354,7 +359,7 @@ talker_status enqueue_forward(talker *t, int rows, const RowMap &rm, const float
         a.ws = t->attn_ws;
         a.cnt = t->attn_cnt;
         a.status = t->d_status;
-        TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, rows, t->st, pdl));
+        TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, rows, st, pdl));
         ++nk;
         // 3) o_proj + residual
         GemvParams o{};
@@ -367,7 +372,7 @@ talker_status enqueue_forward(talker *t, int rows, const RowMap &rm, const float
         o.n_out = t->H;
         o.out = t->x;
         o.out_ld = t->H;
-        TRY_CUDA(launch_gemv(EPI_RESID, t->w_bf16, pick_rows(rows, t->qd), o, t->st, pdl));
+        TRY_CUDA(launch_gemv(EPI_RESID, t->w_bf16, pick_rows(rows, t->qd), o, st, pdl));
         ++nk;
         // 4) post-norm -> [Wg;Wu] -> silu(gate) * up
         GemvParams m{};
@@ -382,7 +387,7 @@ talker_status enqueue_forward(talker *t, int rows, const RowMap &rm, const float
         m.n_out = t->I;
         m.out = t->act;
         m.out_ld = t->I;
-        TRY_CUDA(launch_gemv(EPI_SWIGLU, t->w_bf16, pick_rows(rows, t->H), m, t->st, pdl));
+        TRY_CUDA(launch_gemv(EPI_SWIGLU, t->w_bf16, pick_rows(rows, t->H), m, st, pdl));
         ++nk;
         // 5) down + residual
         GemvParams dn{};
@@ -395,7 +400,7 @@ talker_status enqueue_forward(talker *t, int rows, const RowMap &rm, const float
         dn.n_out = t->H;
         dn.out = t->x;
         dn.out_ld = t->H;
-        TRY_CUDA(launch_gemv(EPI_RESID, t->w_bf16, pick_rows(rows, t->I), dn, t->st, pdl));
+        TRY_CUDA(launch_gemv(EPI_RESID, t->w_bf16, pick_rows(rows, t->I), dn, st, pdl));
         ++nk;
     }
     // final norm -> codec_head -> logits, hidden, argmax
@@ -419,7 +424,7 @@ talker_status enqueue_forward(talker *t, int rows, const RowMap &rm, const float
     h.head_cnt = t->head_cnt;
     h.inc_len = out.inc_len;
     h.cur_len_rw = t->d_len;
-    TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, t->st, pdl));
+    TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, st, pdl));
     ++nk;
     *n_kernels = nk;
     return TALKER_OK;
@@ -442,7 +447,7 @@ talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float
     RowMap rm{1, stream, 0, t->d_len};
     ForwardOut out{logits, hidden, all_rows ? nullptr : argmax, all_rows, 0};
     int nk = 0;
-    TRY(enqueue_forward(t, T, rm, emb, 1, out, &nk));
+    TRY(enqueue_forward(t, t->st, T, rm, emb, 1, out, &nk));
     TRY_CUDA(launch_set_len(t->d_len, stream, T, t->st));
     t->launches += nk + 1;
     t->len[stream] = T;
@@ -492,6 +497,7 @@ talker_status talker_create(const talker_config *cfg, const talker_weight_ptrs *
     talker_status s = from_cuda(cudaGetDevice(&t->dev));
     if (s == TALKER_OK) s = from_cuda(cudaDeviceGetAttribute(&t->n_sm, cudaDevAttrMultiProcessorCount, t->dev));
     if (s == TALKER_OK) s = from_cuda(prepare_kernels());
+    if (s == TALKER_OK) s = from_cuda(cudaStreamCreateWithFlags(&t->cap_st, cudaStreamNonBlocking));
     if (s == TALKER_OK) s = from_cuda(cudaMalloc(&t->d_status, sizeof(int)));
     if (s == TALKER_OK) s = from_cuda(cudaMemsetAsync(t->d_status, 0, sizeof(int), t->st));
     if (s == TALKER_OK) s = build_store(t, weights);
@@ -513,6 +519,7 @@ void talker_destroy(talker_t *t) {
     free_cache(t);
     free_ptr(t->wstore);
     free_ptr(t->d_status);
+    if (t->cap_st) cudaStreamDestroy(t->cap_st);
     delete t;
 }
 
@@ -605,9 +612,9 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
         ForwardOut out{logits, hidden, argmax, true, 1};
         int nk = 0;
         cudaGraph_t graph = nullptr;
-        TRY_CUDA(cudaStreamBeginCapture(t->st, cudaStreamCaptureModeThreadLocal));
-        talker_status s = enqueue_forward(t, B, rm, emb, splits, out, &nk);
-        cudaError_t e = cudaStreamEndCapture(t->st, &graph);
+        TRY_CUDA(cudaStreamBeginCapture(t->cap_st, cudaStreamCaptureModeThreadLocal));
+        talker_status s = enqueue_forward(t, t->cap_st, B, rm, emb, splits, out, &nk);
+        cudaError_t e = cudaStreamEndCapture(t->cap_st, &graph);
         if (s != TALKER_OK) {
             if (graph) cudaGraphDestroy(graph);
             return s;
@@ -663,5 +670,7 @@ talker_status talker_sync_status(talker_t *t, int32_t *code) {
 }
 
 int64_t talker_kernel_launches(const talker_t *t) { return t ? t->launches : 0; }
+
+const char *talker_last_error(void) { return g_last_error; }
 
 }  // extern "C"

@@ -23,7 +23,10 @@ LAYER_FIELDS = ("input_norm", "q_proj", "k_proj", "v_proj", "q_norm", "k_norm", 
 
 class TalkerError(RuntimeError):
     def __init__(self, status, what):
-        super().__init__("%s failed: %s" % (what, STATUS.get(status, status)))
+        detail = ""
+        if _lib is not None and status in (3, 4):
+            detail = " (%s)" % _lib.talker_last_error().decode(errors="replace")
+        super().__init__("%s failed: %s%s" % (what, STATUS.get(status, status), detail))
         self.status = status
         self.name = STATUS.get(status, str(status))
 
@@ -72,6 +75,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_sync_status": (st, [vp, ctypes.POINTER(i32)]),
         "talker_status_str": (ctypes.c_char_p, [st]),
         "talker_kernel_launches": (i64, [vp]),
+        "talker_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in proto.items():
         fn = getattr(lib, name)
