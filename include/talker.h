@@ -162,6 +162,13 @@ const char *talker_status_str(talker_status s);
  * ENOMEM (static thread-local buffer; empty if none). */
 const char *talker_last_error(void);
 
+/* Choose how talker_decode runs a step: 0 = automatic (the persistent kernel
+ * when it fits: B <= 4, one cooperative CTA per SM, weight rows and KV page
+ * pairs within one 32 KB ring slot; otherwise the CUDA graph), 1 = always the
+ * persistent kernel (talker_decode returns EINVAL where it cannot run),
+ * 2 = always the multi-kernel CUDA graph. Errors: EINVAL. */
+talker_status talker_set_decode_mode(talker_t *t, int mode);
+
 /* Test support: count of kernel launches the library enqueued since creation
  * (a graph replay counts each of its kernels). */
 int64_t talker_kernel_launches(const talker_t *t);

@@ -86,6 +86,35 @@ struct AttnParams {
     int *status;
 };
 
+// One layer's weights as the persistent decode kernel reads them (device array).
+struct PersistLayer {
+    const float *in_norm, *post_norm, *q_norm, *k_norm;
+    const void *qkv, *o, *gu, *down;
+};
+
+struct PersistParams {
+    int n_layers, H, nq, nkv, hd, I, V, G;
+    float eps, scale;
+    int rows;                         // streams 0..rows-1, one row each
+    const PersistLayer *layers;       // device array [n_layers]
+    const float *final_norm;
+    const void *head;
+    CacheView cache;
+    const float2 *rope;
+    int *cur_len;
+    const float *emb;                 // [rows, H]
+    float *logits;                    // [rows, V]
+    float *hidden_out;                // [rows, H] or null
+    int *argmax_out;                  // [rows] or null
+    float *x, *raw, *attn, *act;      // [rows, H], [rows, qkv_n], [rows, nq*hd], [rows, I]
+    float *attn_ws;                   // [rows][nq][splits][hd+4]
+    int *attn_cnt;                    // [rows][nkv], zero between launches
+    float *head_val;                  // [grid][R]
+    int *head_idx;
+    int *sync;                        // barrier/exit/abort/head words, then per-head row counters; zero between launches
+    int *status;
+};
+
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = 256;
 constexpr int kAttnThreads = 256;
@@ -101,6 +130,15 @@ cudaError_t launch_set_len(int *cur_len, int stream, int value, cudaStream_t st)
 // Copy len rows of a stream between a dense [n_layers][n_kv][len][hd] buffer and the cache.
 cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *dense_v, int len, int to_cache,
                            cudaStream_t st);
-cudaError_t prepare_kernels();  // raise dynamic shared-memory limits once per process
+cudaError_t prepare_kernels();
+
+// Persistent decode kernel (one cooperative launch per decode step, one CTA per SM).
+size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax);
+int persist_threads();
+int persist_slot_bytes();
+int persist_sync_words(int n_heads);
+cudaError_t setup_persistent(int w_bf16, int head_dim, int R, size_t smem, int *blocks_per_sm);
+cudaError_t launch_persistent(int w_bf16, int head_dim, int R, const PersistParams &p, int grid, size_t smem,
+                              cudaStream_t st);  // raise dynamic shared-memory limits once per process
 
 }  // namespace talker_k

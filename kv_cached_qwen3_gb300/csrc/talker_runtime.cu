@@ -89,6 +89,11 @@ struct talker {
     int *d_status = nullptr;
     int64_t launches = 0;
     std::vector<GraphEntry> graphs;
+    // persistent decode kernel
+    int decode_mode = 0;                 // 0 auto, 1 persistent kernel, 2 multi-kernel CUDA graph
+    PersistLayer *d_layers = nullptr;    // device copy of the layer pointer table
+    int *d_sync = nullptr;               // barrier / counter words of the persistent kernel
+    int persist_ok[2] = {-1, -1};        // per R template (1, 4): -1 unknown, 0 unusable, 1 usable
 };
 
 namespace {
@@ -116,6 +121,13 @@ void free_workspaces(talker *t) {
     t->cap_rows = 0;
     t->cap_attn_ws = t->cap_head_part = 0;
     t->cap_cnt_rows = 0;
+}
+
+void free_persist(talker *t) {
+    free_ptr(t->d_layers);
+    free_ptr(t->d_sync);
+    t->d_layers = nullptr;
+    t->d_sync = nullptr;
 }
 
 void free_cache(talker *t) {
@@ -430,6 +442,108 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
     return TALKER_OK;
 }
 
+int persist_rows_tmpl(int B) { return B <= 1 ? 1 : 4; }
+
+int kmax_of(const talker *t) { return std::max(std::max(t->H, t->qd), t->I); }
+
+// Can the persistent kernel run this geometry with B rows? (one CTA per SM must fit,
+// every weight row group and KV page pair must fit one ring slot)
+bool persist_usable(talker *t, int B) {
+    if (B > 4 || t->w_bf16 != t->kv_bf16) return false;
+    const int R = persist_rows_tmpl(B);
+    int &ok = t->persist_ok[R == 1 ? 0 : 1];
+    if (ok >= 0) return ok == 1;
+    ok = 0;
+    const size_t slot = (size_t)persist_slot_bytes();
+    const size_t wsz = t->wsz;
+    if ((size_t)t->H * wsz > slot || (size_t)t->qd * wsz > slot || (size_t)2 * t->H * wsz > slot ||
+        (size_t)t->I * wsz > slot || (size_t)2 * 64 * t->hd * t->kvsz > slot)
+        return false;
+    const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t));
+    int per_sm = 0;
+    if (setup_persistent(t->w_bf16, t->hd, R, smem, &per_sm) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (per_sm < 1) return false;
+    ok = 1;
+    return true;
+}
+
+talker_status ensure_persist(talker *t, int B) {
+    const int n_heads = t->nq + 2 * t->nkv;
+    if (!t->d_layers) {
+        std::vector<PersistLayer> h(t->c.n_layers);
+        for (int l = 0; l < t->c.n_layers; ++l) {
+            const LayerDev &d = t->L[l];
+            h[l] = PersistLayer{d.in_norm, d.post_norm, d.q_norm, d.k_norm, d.qkv, d.o, d.gu, d.down};
+        }
+        TRY_CUDA(cudaMalloc(&t->d_layers, h.size() * sizeof(PersistLayer)));
+        TRY_CUDA(cudaMemcpy(t->d_layers, h.data(), h.size() * sizeof(PersistLayer), cudaMemcpyHostToDevice));
+        const size_t words = persist_sync_words(n_heads);
+        TRY_CUDA(cudaMalloc(&t->d_sync, words * sizeof(int)));
+        TRY_CUDA(cudaMemset(t->d_sync, 0, words * sizeof(int)));
+    }
+    const int splits = std::max(1, t->n_sm / (B * t->nkv));
+    TRY(ensure_capacity(t, std::max(B, 4), splits));
+    // head partials: one per (CTA, row template slot)
+    const size_t need_head = (size_t)t->n_sm * 4;
+    if (need_head > t->cap_head_part) {
+        TRY_CUDA(cudaStreamSynchronize(t->st));
+        drop_graphs(t);
+        free_ptr(t->head_val);
+        free_ptr(t->head_idx);
+        t->head_val = nullptr;
+        t->head_idx = nullptr;
+        TRY_CUDA(cudaMalloc(&t->head_val, need_head * sizeof(float)));
+        TRY_CUDA(cudaMalloc(&t->head_idx, need_head * sizeof(int)));
+        t->cap_head_part = need_head;
+    }
+    return TALKER_OK;
+}
+
+talker_status decode_persistent(talker *t, const float *emb, int B, float *logits, float *hidden, int32_t *argmax) {
+    TRY(ensure_persist(t, B));
+    const int R = persist_rows_tmpl(B);
+    PersistParams p{};
+    p.n_layers = t->c.n_layers;
+    p.H = t->H;
+    p.nq = t->nq;
+    p.nkv = t->nkv;
+    p.hd = t->hd;
+    p.I = t->I;
+    p.V = t->V;
+    p.G = t->G;
+    p.eps = t->c.rms_eps;
+    p.scale = 1.0f / sqrtf((float)t->hd);
+    p.rows = B;
+    p.layers = t->d_layers;
+    p.final_norm = t->fnorm;
+    p.head = t->head;
+    p.cache = cache_view(t);
+    p.rope = t->d_rope;
+    p.cur_len = t->d_len;
+    p.emb = emb;
+    p.logits = logits;
+    p.hidden_out = hidden;
+    p.argmax_out = argmax;
+    p.x = t->x;
+    p.raw = t->raw;
+    p.attn = t->attn;
+    p.act = t->act;
+    p.attn_ws = t->attn_ws;
+    p.attn_cnt = t->attn_cnt;
+    p.head_val = t->head_val;
+    p.head_idx = t->head_idx;
+    p.sync = t->d_sync;
+    p.status = t->d_status;
+    const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t));
+    TRY_CUDA(launch_persistent(t->w_bf16, t->hd, R, p, t->n_sm, smem, t->st));
+    t->launches += 1;
+    for (int b = 0; b < B; ++b) t->len[b] += 1;
+    return TALKER_OK;
+}
+
 talker_status check_stream(const talker *t, int stream) {
     if (!t) return TALKER_EINVAL;
     if (t->n_streams == 0) return TALKER_ESTATE;
@@ -518,6 +632,7 @@ void talker_destroy(talker_t *t) {
     free_workspaces(t);
     free_cache(t);
     free_ptr(t->wstore);
+    free_persist(t);
     free_ptr(t->d_status);
     if (t->cap_st) cudaStreamDestroy(t->cap_st);
     delete t;
@@ -598,6 +713,8 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
     for (int b = 0; b < B; ++b)
         if (t->len[b] + 1 > t->max_seq) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));
+    if (t->decode_mode != 2 && persist_usable(t, B)) return decode_persistent(t, emb, B, logits, hidden, argmax);
+    if (t->decode_mode == 1) return TALKER_EINVAL;
     const int splits = decode_splits(t, B);
     TRY(ensure_capacity(t, B, splits));
     GraphEntry *ge = nullptr;
@@ -672,5 +789,11 @@ talker_status talker_sync_status(talker_t *t, int32_t *code) {
 int64_t talker_kernel_launches(const talker_t *t) { return t ? t->launches : 0; }
 
 const char *talker_last_error(void) { return g_last_error; }
+
+talker_status talker_set_decode_mode(talker_t *t, int mode) {
+    if (!t || mode < 0 || mode > 2) return TALKER_EINVAL;
+    t->decode_mode = mode;
+    return TALKER_OK;
+}
 
 }  // extern "C"

@@ -76,6 +76,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_status_str": (ctypes.c_char_p, [st]),
         "talker_kernel_launches": (i64, [vp]),
         "talker_last_error": (ctypes.c_char_p, []),
+        "talker_set_decode_mode": (st, [vp, ctypes.c_int]),
     }
     for name, (res, args) in proto.items():
         fn = getattr(lib, name)
@@ -190,6 +191,10 @@ class Talker:
         self._check(self.lib.talker_decode(self.h, _ptr(emb), B, _ptr(logits), _ptr(hidden), _ptr(argmax)),
                     "talker_decode")
         return logits, hidden, argmax
+
+    def set_decode_mode(self, mode: int):
+        """0 automatic, 1 persistent decode kernel, 2 multi-kernel CUDA graph."""
+        self._check(self.lib.talker_set_decode_mode(self.h, mode), "talker_set_decode_mode")
 
     def sync_status(self) -> int:
         code = ctypes.c_int32(0)

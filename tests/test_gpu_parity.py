@@ -30,9 +30,13 @@ def host(t):
     return t.detach().float().cpu().numpy()
 
 
-def run_prefill_decode(geom, weights, emb, T0, n_dec, max_seq):
+DECODE_MODES = [pytest.param(1, id="persistent"), pytest.param(2, id="graph")]
+
+
+def run_prefill_decode(geom, weights, emb, T0, n_dec, max_seq, mode=0):
     from kv_cached_qwen3_gb300.talker import Talker
     tk = Talker(geom, weights)
+    tk.set_decode_mode(mode)
     tk.kv_init_batched(1, max_seq)
     hid, lg, am = tk.prefill(0, dev(emb[:T0]))
     hids, lgs, ams = [host(hid)], [host(lg)], [int(host(am)[0])]
@@ -54,13 +58,14 @@ def run_prefill_decode(geom, weights, emb, T0, n_dec, max_seq):
     return np.stack(hids), np.stack(lgs), np.array(ams)
 
 
-def test_tiny_prefill_and_decode_fp32(cuda):
+@pytest.mark.parametrize("mode", DECODE_MODES)
+def test_tiny_prefill_and_decode_fp32(cuda, mode):
     wl = inputs.WORKLOADS["tiny"]
     g = wl.geometry
     w = inputs.make_weights(g, wl.seed)
     T0, n = wl.prefill_T, wl.decode_steps
     emb = inputs.make_embeddings(g, wl.seed, 0, T0 + n)
-    hid, lg, am = run_prefill_decode(g, w, emb, T0, n, 64)
+    hid, lg, am = run_prefill_decode(g, w, emb, T0, n, 64, mode)
     rh, rl = Oracle(g, w).forward_full(emb)
     check_rows(hid, rh[T0 - 1:], bf16=False, what="tiny hidden")
     check_rows(lg, rl[T0 - 1:], bf16=False, what="tiny logits")
@@ -86,14 +91,23 @@ def test_tiny_prefill_all_rows_and_ragged_lengths(cuda):
     assert tk.sync_status() == 0
 
 
-def test_talker_b1_prefill96_decode512_bf16(cuda):
+@pytest.fixture(scope="module")
+def talker_b1_ref():
     wl = inputs.WORKLOADS["talker_b1"]
     g = wl.geometry
     w = inputs.make_weights(g, wl.seed)
-    T0, n = wl.prefill_T, wl.decode_steps
-    emb = inputs.make_embeddings(g, wl.seed, 0, T0 + n)
-    hid, lg, am = run_prefill_decode(g, w, emb, T0, n, T0 + n)
+    emb = inputs.make_embeddings(g, wl.seed, 0, wl.prefill_T + wl.decode_steps)
     rh, rl = Oracle(g, w).forward_full(emb)
+    return w, emb, rh, rl
+
+
+@pytest.mark.parametrize("mode", DECODE_MODES)
+def test_talker_b1_prefill96_decode512_bf16(cuda, talker_b1_ref, mode):
+    wl = inputs.WORKLOADS["talker_b1"]
+    g = wl.geometry
+    w, emb, rh, rl = talker_b1_ref
+    T0, n = wl.prefill_T, wl.decode_steps
+    hid, lg, am = run_prefill_decode(g, w, emb, T0, n, T0 + n, mode)
     check_rows(hid, rh[T0 - 1:], bf16=True, what="talker hidden")
     check_rows(lg, rl[T0 - 1:], bf16=True, what="talker logits")
     agree = top1_agreement(lg[1:], rl[T0:])
