@@ -169,6 +169,14 @@ const char *talker_last_error(void);
  * 2 = always the multi-kernel CUDA graph. Errors: EINVAL. */
 talker_status talker_set_decode_mode(talker_t *t, int mode);
 
+/* Test support: when buf is not NULL, every persistent-kernel decode step
+ * writes globaltimer stamps (ns) of its consumer phases into
+ * buf[cta * talker_trace_slots() + event] (15 events per layer, then 3 for the
+ * head); buf is a caller-owned device buffer of n_SM * talker_trace_slots()
+ * uint64 values. NULL turns tracing off. Errors: EINVAL. */
+talker_status talker_set_trace(talker_t *t, unsigned long long *buf);
+int talker_trace_slots(void);
+
 /* Test support: count of kernel launches the library enqueued since creation
  * (a graph replay counts each of its kernels). */
 int64_t talker_kernel_launches(const talker_t *t);

@@ -414,14 +414,22 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
 
     // ------------------------------------------------------------------ consumers
     const int ctid = tid;
+    unsigned long long *trace = (p.trace != nullptr && ctid == 0) ? p.trace + (size_t)cta * kTraceSlots : nullptr;
+#define TR(slot)                                      \
+    do {                                              \
+        if (trace) trace[(slot)] = globaltimer_ns();  \
+    } while (0)
     Ring rc{ring, full, empty, 0};
     int nbar = 0;
     int *rows_done = p.sync + SY_ROWS;
 
     for (int l = 0; l < p.n_layers; ++l) {
         const LayerW &L = p.layers[l];
+        const int tb = l * kTracePerLayer;
+        TR(tb + 0);
         // ---- RMSNorm -> [Wq;Wk;Wv] (raw rows)
         stage<EPV, R>(act, l == 0 ? p.emb : p.x, H, H, rows, L.in_norm, p.eps, red, ctid);
+        TR(tb + 1);
         if (l == 0 && cta == 0)
             for (int i = ctid; i < rows * H; i += NCT) p.x[i] = p.emb[i];
         {
@@ -438,6 +446,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 rc.release(lane);
             }
             cbar();
+            TR(tb + 2);
             if (ctid == 0 && s.n > 0) {
                 __threadfence();
                 for (int h = s.u0 / HD; h <= (s.u0 + s.n - 1) / HD; ++h) {
@@ -457,6 +466,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 __threadfence();
             }
             cbar();
+            TR(tb + 3);
             if (warp < G + 2) {
                 const int h = (warp < G) ? g * G + warp : (warp == G ? p.nq + g : p.nq + p.nkv + g);
                 const float *src = p.raw + (size_t)r * qkv_n + (size_t)h * HD;
@@ -622,10 +632,13 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 }
             }
         }
+        TR(tb + 4);
         grid_barrier(p.sync + SY_BAR, ++nbar * P, c, ctid);
+        TR(tb + 5);
 
         // ---- o_proj + residual
         stage<EPV, R>(act, p.attn, qd, qd, rows, nullptr, 0.f, red, ctid);
+        TR(tb + 6);
         {
             const Span s = cta_span(H, cta, P);
             const int upc = max(1, (int)(SLOT / (qd * WSZ)));
@@ -643,10 +656,13 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 rc.release(lane);
             }
         }
+        TR(tb + 7);
         grid_barrier(p.sync + SY_BAR, ++nbar * P, c, ctid);
+        TR(tb + 8);
 
         // ---- post-norm -> [Wg;Wu] -> silu(gate) * up
         stage<EPV, R>(act, p.x, H, H, rows, L.post_norm, p.eps, red, ctid);
+        TR(tb + 9);
         {
             const Span s = cta_span(p.I, cta, P);
             const int upc = max(1, (int)(SLOT / (2 * H * WSZ)));
@@ -662,10 +678,13 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 rc.release(lane);
             }
         }
+        TR(tb + 10);
         grid_barrier(p.sync + SY_BAR, ++nbar * P, c, ctid);
+        TR(tb + 11);
 
         // ---- down + residual
         stage<EPV, R>(act, p.act, p.I, p.I, rows, nullptr, 0.f, red, ctid);
+        TR(tb + 12);
         {
             const Span s = cta_span(H, cta, P);
             const int upc = max(1, (int)(SLOT / (p.I * WSZ)));
@@ -683,11 +702,15 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 rc.release(lane);
             }
         }
+        TR(tb + 13);
         grid_barrier(p.sync + SY_BAR, ++nbar * P, c, ctid);
+        TR(tb + 14);
     }
 
     // ---- final norm -> codec_head -> logits, hidden, argmax
+    const int th = p.n_layers * kTracePerLayer;
     stage<EPV, R>(act, p.x, H, H, rows, p.final_norm, p.eps, red, ctid);
+    TR(th + 0);
     if (cta == 0 && p.hidden_out != nullptr)
         for (int i = ctid; i < rows * H; i += NCT) {
             const int r = i / H, k = i - r * H;
@@ -717,6 +740,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
             rc.release(lane);
         }
     }
+    TR(th + 1);
     if (lane < R) {
         bv_s[warp][lane] = bv;
         bi_s[warp][lane] = bi;
@@ -785,6 +809,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
     }
     // ---- exit: the last CTA out resets the sync words for the next launch
     cbar();
+    TR(th + 2);
+#undef TR
     if (ctid == 0) {
         __threadfence();
         if (atomicAdd(p.sync + SY_EXIT, 1) == P - 1) {

@@ -113,7 +113,11 @@ struct PersistParams {
     int *head_idx;
     int *sync;                        // barrier/exit/abort/head words, then per-head row counters; zero between launches
     int *status;
+    unsigned long long *trace;        // optional: [grid][kTraceSlots] globaltimer stamps of consumer phases
 };
+
+constexpr int kTraceSlots = 512;      // trace stamps per CTA (15 per layer + 3 for the head)
+constexpr int kTracePerLayer = 15;
 
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = 256;

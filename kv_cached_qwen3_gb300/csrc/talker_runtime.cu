@@ -94,6 +94,7 @@ struct talker {
     PersistLayer *d_layers = nullptr;    // device copy of the layer pointer table
     int *d_sync = nullptr;               // barrier / counter words of the persistent kernel
     int persist_ok[2] = {-1, -1};        // per R template (1, 4): -1 unknown, 0 unusable, 1 usable
+    unsigned long long *trace = nullptr; // optional phase stamps of the persistent kernel (caller-owned)
 };
 
 namespace {
@@ -537,6 +538,7 @@ talker_status decode_persistent(talker *t, const float *emb, int B, float *logit
     p.head_idx = t->head_idx;
     p.sync = t->d_sync;
     p.status = t->d_status;
+    p.trace = t->trace;
     const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t));
     TRY_CUDA(launch_persistent(t->w_bf16, t->hd, R, p, t->n_sm, smem, t->st));
     t->launches += 1;
@@ -789,6 +791,14 @@ talker_status talker_sync_status(talker_t *t, int32_t *code) {
 int64_t talker_kernel_launches(const talker_t *t) { return t ? t->launches : 0; }
 
 const char *talker_last_error(void) { return g_last_error; }
+
+talker_status talker_set_trace(talker_t *t, unsigned long long *buf) {
+    if (!t) return TALKER_EINVAL;
+    t->trace = buf;
+    return TALKER_OK;
+}
+
+int talker_trace_slots(void) { return kTraceSlots; }
 
 talker_status talker_set_decode_mode(talker_t *t, int mode) {
     if (!t || mode < 0 || mode > 2) return TALKER_EINVAL;

@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_kernel_launches": (i64, [vp]),
         "talker_last_error": (ctypes.c_char_p, []),
         "talker_set_decode_mode": (st, [vp, ctypes.c_int]),
+        "talker_set_trace": (st, [vp, vp]),
+        "talker_trace_slots": (ctypes.c_int, []),
     }
     for name, (res, args) in proto.items():
         fn = getattr(lib, name)
@@ -195,6 +197,10 @@ class Talker:
     def set_decode_mode(self, mode: int):
         """0 automatic, 1 persistent decode kernel, 2 multi-kernel CUDA graph."""
         self._check(self.lib.talker_set_decode_mode(self.h, mode), "talker_set_decode_mode")
+
+    def set_trace(self, buf):
+        """buf: int64 cuda tensor [n_sm * trace_slots] or None (persistent decode phase stamps)."""
+        self._check(self.lib.talker_set_trace(self.h, _ptr(buf)), "talker_set_trace")
 
     def sync_status(self) -> int:
         code = ctypes.c_int32(0)
