@@ -180,6 +180,8 @@ __device__ void producer(const PersistParams &p, unsigned char *ring, uint64_t *
         const int slot = k % NS;
         const uint32_t use = k / NS;
         if (use > 0) ring_wait(&empty[slot], (use - 1) & 1, c);
+        if (p.trace != nullptr && k < (uint32_t)kTraceChunks)
+            p.trace[(size_t)blockIdx.x * kTraceSlots + kTraceProducer + k] = globaltimer_ns();
         if (!*c.abort_s) {
             unsigned char *dst = ring + (size_t)slot * SLOT;
             mbar_arrive_expect_tx(&full[slot], b1 + b2);
@@ -224,8 +226,10 @@ struct Ring {
     unsigned char *base;
     uint64_t *full, *empty;
     uint32_t k;
+    unsigned long long *trace;   // this CTA's trace row (consumer thread 0 only) or null
     __device__ __forceinline__ const unsigned char *acquire(const Ctx &c) {
         ring_wait(&full[k % NS], (k / NS) & 1, c);
+        if (trace != nullptr && k < (uint32_t)kTraceChunks) trace[kTraceAcquire + k] = globaltimer_ns();
         return base + (size_t)(k % NS) * SLOT;
     }
     // Every consumer warp arrives once per slot (the empty barrier counts NCW arrivals).
@@ -415,11 +419,11 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
     // ------------------------------------------------------------------ consumers
     const int ctid = tid;
     unsigned long long *trace = (p.trace != nullptr && ctid == 0) ? p.trace + (size_t)cta * kTraceSlots : nullptr;
+    Ring rc{ring, full, empty, 0, trace};
 #define TR(slot)                                      \
     do {                                              \
         if (trace) trace[(slot)] = globaltimer_ns();  \
     } while (0)
-    Ring rc{ring, full, empty, 0};
     int nbar = 0;
     int *rows_done = p.sync + SY_ROWS;
 

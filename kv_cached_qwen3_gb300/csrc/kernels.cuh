@@ -116,7 +116,12 @@ struct PersistParams {
     unsigned long long *trace;        // optional: [grid][kTraceSlots] globaltimer stamps of consumer phases
 };
 
-constexpr int kTraceSlots = 512;      // trace stamps per CTA (15 per layer + 3 for the head)
+// Trace stamps per CTA: [0, 512) consumer phase events (15 per layer + 3 for the head),
+// [512, 1280) time the producer issued ring chunk k, [1280, 2048) time the consumers got chunk k.
+constexpr int kTraceSlots = 2048;
+constexpr int kTraceProducer = 512;
+constexpr int kTraceAcquire = 1280;
+constexpr int kTraceChunks = 768;
 constexpr int kTracePerLayer = 15;
 
 constexpr int kGemvWarps = 8;
