@@ -33,7 +33,7 @@ using namespace talker_dev;
 namespace talker_k {
 namespace pk {
 
-constexpr int NCW = 16;             // consumer warps
+constexpr int NCW = 15;             // consumer warps
 constexpr int NCT = NCW * 32;       // consumer threads
 constexpr int NT = NCT + 32;        // + one producer warp
 constexpr int SLOT = 32 * 1024;     // ring slot bytes
@@ -149,7 +149,7 @@ struct AttnWork {
 __device__ __forceinline__ AttnWork attn_work(const PersistParams &p, int cta, int P, const int *curlen_s) {
     AttnWork w{};
     const int items = p.rows * p.nkv;
-    const int S = max(1, P / items);
+    const int S = p.splits;
     if (cta >= items * S) return w;
     const int item = cta % items;
     w.r = item / p.nkv;
@@ -361,6 +361,132 @@ __device__ __forceinline__ void dot_rows(const unsigned char *w, int K, const fl
 namespace talker_k {
 namespace pk {
 
+// ---- flag-carrying words: value in the low 32 bits, flag in the high 32 bits,
+// written with one 8-byte store, so a reader that sees the flag sees the value.
+__device__ __forceinline__ unsigned long long ll_pack(float v, uint32_t f) {
+    return ((unsigned long long)f << 32) | __float_as_uint(v);
+}
+__device__ __forceinline__ void st_ll(unsigned long long *p, float v, uint32_t f) {
+    asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(ll_pack(v, f)) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_ll(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void ld_ll2(const unsigned long long *p, unsigned long long &a, unsigned long long &b) {
+    asm volatile("ld.volatile.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ uint32_t ll_flag(unsigned long long w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ float ll_val(unsigned long long w) { return __uint_as_float((uint32_t)w); }
+
+// Re-read one word until its flag is f (bounded; returns at once after an abort).
+__device__ __noinline__ unsigned long long repoll_ll(const unsigned long long *p, uint32_t f, const Ctx &c) {
+    unsigned long long w = ld_ll(p);
+    if (ll_flag(w) == f || *c.abort_s) return w;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        w = ld_ll(p);
+        if (ll_flag(w) == f) return w;
+        if ((it & 63) == 0) {
+            if (*c.abort_s || ld_volatile(c.abort_g)) {
+                *c.abort_s = 1;
+                return w;
+            }
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                raise_abort(c);
+                return w;
+            }
+        }
+    }
+}
+
+// Flags: one per (step, layer, tensor). base = step epoch * 256, never 0.
+enum : uint32_t { FL_RAW = 0, FL_PART = 1, FL_O = 2, FL_X1 = 3, FL_ACT = 4, FL_X2 = 5 };
+__device__ __forceinline__ uint32_t flag_of(uint32_t base, int layer, uint32_t what) {
+    return base + (uint32_t)layer * 8u + what;
+}
+
+constexpr int KCAP = 3072;   // widest activation row the LL staging handles (R * KCAP / 2 pairs)
+
+// Stage rows [0, rows) of a flag-word tensor (row stride ld words): every load
+// is issued before any flag is checked, so a ready tensor costs one round trip.
+// With `gain`, applies RMSNorm and the gain. Ends with a consumer barrier.
+template <int EPV, int R>
+__device__ void stage_ll(float *act, const unsigned long long *src, int ld, int K, int rows, uint32_t flag,
+                         const float *gain, float eps, float *red, int ctid, const Ctx &c) {
+    constexpr int NP = (R * KCAP / 2 + NCT - 1) / NCT;
+    const int K2 = K >> 1;
+    const int total = rows * K2;
+    const int warp = ctid >> 5, lane = ctid & 31;
+    unsigned long long wa[NP], wb[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        const int idx = ctid + i * NCT;
+        if (idx < total) {
+            const int r = idx / K2, k = (idx - r * K2) * 2;
+            ld_ll2(src + (size_t)r * ld + k, wa[i], wb[i]);
+        }
+    }
+    float ss[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) ss[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        const int idx = ctid + i * NCT;
+        if (idx < total) {
+            const int r = idx / K2, k = (idx - r * K2) * 2;
+            const unsigned long long *pp = src + (size_t)r * ld + k;
+            if (ll_flag(wa[i]) != flag) wa[i] = repoll_ll(pp, flag, c);
+            if (ll_flag(wb[i]) != flag) wb[i] = repoll_ll(pp + 1, flag, c);
+            const float v0 = ll_val(wa[i]), v1 = ll_val(wb[i]);
+            act[aidx<EPV>(r, k, K)] = v0;
+            act[aidx<EPV>(r, k + 1, K)] = v1;
+            const float s2 = v0 * v0 + v1 * v1;
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr)
+                if (rr == r) ss[rr] += s2;
+        }
+    }
+    if (gain != nullptr) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float v = warp_sum(ss[r]);
+            if (lane == 0) red[warp * R + r] = v;
+        }
+        cbar();
+        float inv[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float t = 0.f;
+            for (int w = 0; w < NCW; ++w) t += red[w * R + r];
+            inv[r] = 1.0f / sqrtf(t / (float)K + eps);
+        }
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const int idx = ctid + i * NCT;
+            if (idx < total) {
+                const int r = idx / K2, k = (idx - r * K2) * 2;
+                float iv = inv[0];
+#pragma unroll
+                for (int rr = 1; rr < R; ++rr)
+                    if (rr == r) iv = inv[rr];
+                float *a0 = act + aidx<EPV>(r, k, K);
+                float *a1 = act + aidx<EPV>(r, k + 1, K);
+                *a0 = *a0 * iv * gain[k];
+                *a1 = *a1 * iv * gain[k + 1];
+            }
+        }
+    }
+    cbar();
+}
+
+}  // namespace pk
+}  // namespace talker_k
+
+namespace talker_k {
+namespace pk {
+
 template <int R>
 __device__ __forceinline__ float pick(const float (&a)[R], int r) {
     float v = a[0];
@@ -372,6 +498,8 @@ __device__ __forceinline__ float pick(const float (&a)[R], int r) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+constexpr int XO = 64;   // owned residual rows per CTA (ceil(H / grid) <= XO)
+
 template <typename WT, typename KT, int HD, int R>
 __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams p) {
     constexpr int EPV = Elem<WT>::kPerVec;
@@ -380,6 +508,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
     __shared__ __align__(8) uint64_t full[NS], empty[NS];
     __shared__ float red[NCW * R];
     __shared__ float m_s[MAXG], l_s[MAXG], al_s[MAXG];
+    __shared__ float ml_s[MAXG][kMaxSplits][2];
+    __shared__ float xown[R][XO];
     __shared__ float bv_s[NCW][R];
     __shared__ int bi_s[NCW][R];
     __shared__ int curlen_s[R];
@@ -424,20 +554,29 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
     do {                                              \
         if (trace) trace[(slot)] = globaltimer_ns();  \
     } while (0)
-    int nbar = 0;
-    int *rows_done = p.sync + SY_ROWS;
+    const Span own = cta_span(H, cta, P);           // residual rows this CTA updates (o_proj and down)
+    for (int i = ctid; i < rows * own.n; i += NCT) {
+        const int r = i / own.n, j = i - r * own.n;
+        xown[r][j] = p.emb[(size_t)r * H + own.u0 + j];
+    }
 
     for (int l = 0; l < p.n_layers; ++l) {
         const LayerW &L = p.layers[l];
         const int tb = l * kTracePerLayer;
         TR(tb + 0);
-        // ---- RMSNorm -> [Wq;Wk;Wv] (raw rows)
-        stage<EPV, R>(act, l == 0 ? p.emb : p.x, H, H, rows, L.in_norm, p.eps, red, ctid);
+        // ---- RMSNorm -> [Wq;Wk;Wv] -> raw q|k|v words
+        // (A CTA with no rows in a phase skips that phase's input: it would have no
+        // output that orders its reads before the next overwrite of the input words.)
+        const Span sq = cta_span(qkv_n, cta, P);
+        if (sq.n > 0) {
+            if (l == 0) stage<EPV, R>(act, p.emb, H, H, rows, L.in_norm, p.eps, red, ctid);
+            else stage_ll<EPV, R>(act, p.x_ll, H, H, rows, flag_of(p.flag_base, l - 1, FL_X2), L.in_norm, p.eps,
+                                  red, ctid, c);
+        }
         TR(tb + 1);
-        if (l == 0 && cta == 0)
-            for (int i = ctid; i < rows * H; i += NCT) p.x[i] = p.emb[i];
         {
-            const Span s = cta_span(qkv_n, cta, P);
+            const uint32_t f = flag_of(p.flag_base, l, FL_RAW);
+            const Span s = sq;
             const int upc = max(1, (int)(SLOT / (H * WSZ)));
             for (int u = s.u0; u < s.u0 + s.n; u += upc) {
                 const int n = min(upc, s.u0 + s.n - u);
@@ -445,43 +584,42 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 for (int j = warp; j < n; j += NCW) {
                     float acc[1][R];
                     dot_rows<WT, R, 1>(w + (size_t)j * H * WSZ, H, act, rows, acc, lane);
-                    if (lane < rows) p.raw[(size_t)lane * qkv_n + u + j] = pick<R>(acc[0], lane);
+                    if (lane < rows) st_ll(p.raw_ll + (size_t)lane * qkv_n + u + j, pick<R>(acc[0], lane), f);
                 }
                 rc.release(lane);
             }
-            cbar();
-            TR(tb + 2);
-            if (ctid == 0 && s.n > 0) {
-                __threadfence();
-                for (int h = s.u0 / HD; h <= (s.u0 + s.n - 1) / HD; ++h) {
-                    const int lo = max(s.u0, h * HD), hi = min(s.u0 + s.n, (h + 1) * HD);
-                    red_release_add(&rows_done[h], hi - lo);
-                }
-            }
         }
+        TR(tb + 2);
         // ---- attention of (row r, KV group g, split) over [0, pos]
         if (aw.has) {
             const int r = aw.r, g = aw.g, pos = aw.pos;
-            if (ctid == 0) {
-                for (int j = 0; j < G + 2; ++j) {
-                    const int h = (j < G) ? g * G + j : (j == G ? p.nq + g : p.nq + p.nkv + g);
-                    spin_geq(&rows_done[h], HD * (l + 1), c);
-                }
-                __threadfence();
-            }
-            cbar();
-            TR(tb + 3);
             if (warp < G + 2) {
+                // QK-norm + RoPE of this row's q heads of the group and k; v as is
                 const int h = (warp < G) ? g * G + warp : (warp == G ? p.nq + g : p.nq + p.nkv + g);
-                const float *src = p.raw + (size_t)r * qkv_n + (size_t)h * HD;
+                const unsigned long long *src = p.raw_ll + (size_t)r * qkv_n + (size_t)h * HD;
+                const uint32_t f = flag_of(p.flag_base, l, FL_RAW);
+                unsigned long long wv[4];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int i = lane + 32 * t;
+                    if (i < half) {
+                        wv[2 * t] = ld_ll(src + i);
+                        wv[2 * t + 1] = ld_ll(src + i + half);
+                    }
+                }
                 float a[2], b[2];
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const int i = lane + 32 * t;
-                    a[t] = (i < half) ? __ldcg(src + i) : 0.f;
-                    b[t] = (i < half) ? __ldcg(src + i + half) : 0.f;
+                    a[t] = b[t] = 0.f;
+                    if (i < half) {
+                        if (ll_flag(wv[2 * t]) != f) wv[2 * t] = repoll_ll(src + i, f, c);
+                        if (ll_flag(wv[2 * t + 1]) != f) wv[2 * t + 1] = repoll_ll(src + i + half, f, c);
+                        a[t] = ll_val(wv[2 * t]);
+                        b[t] = ll_val(wv[2 * t + 1]);
+                    }
                 }
-                if (warp <= G) {   // q heads and the k head: QK-norm then RoPE
+                if (warp <= G) {
                     const float *gain = (warp < G) ? L.q_norm : L.k_norm;
                     const float ss = warp_sum(a[0] * a[0] + b[0] * b[0] + a[1] * a[1] + b[1] * b[1]);
                     const float inv = 1.0f / sqrtf(ss / (float)HD + p.eps);
@@ -527,6 +665,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
 #pragma unroll
             for (int o = 0; o < NO; ++o) o_acc[o] = 0.f;
             cbar();
+            TR(tb + 3);
             for (int pg = aw.pb; pg < aw.pe; ++pg) {
                 KT *Ks = reinterpret_cast<KT *>(const_cast<unsigned char *>(rc.acquire(c)));
                 KT *Vs = Ks + kPage * HD;
@@ -585,90 +724,137 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 rc.release(lane);
                 cbar();
             }
-            // partial (m, l, o) of this split, or the final output when there is one split
             const int hq0 = g * G;
-            float *orow = p.attn + (size_t)r * qd;
+            unsigned long long *orow = p.o_ll + (size_t)r * qd;
+            const uint32_t fo = flag_of(p.flag_base, l, FL_O);
+            constexpr int WS = HD + 2;
             if (aw.nact == 1) {
 #pragma unroll
                 for (int o = 0; o < NO; ++o) {
                     const int idx = ctid + o * NCT;
                     if (idx < G * HD) {
                         const int gi = idx / HD, d = idx - gi * HD;
-                        orow[(hq0 + gi) * HD + d] = o_acc[o] / l_s[gi];
+                        st_ll(orow + (hq0 + gi) * HD + d, o_acc[o] / l_s[gi], fo);
                     }
                 }
-            } else {
-                constexpr int WS = HD + 4;
+            } else if (aw.split != 0) {
+                // publish this split's (m, l, o) for the combining CTA (split 0)
+                const uint32_t fp = flag_of(p.flag_base, l, FL_PART);
 #pragma unroll
                 for (int o = 0; o < NO; ++o) {
                     const int idx = ctid + o * NCT;
                     if (idx < G * HD) {
                         const int gi = idx / HD, d = idx - gi * HD;
-                        float *w = p.attn_ws + (((size_t)r * p.nq + hq0 + gi) * aw.S + aw.split) * WS;
-                        w[4 + d] = o_acc[o];
+                        unsigned long long *w =
+                            p.part_ll + (((size_t)r * p.nq + hq0 + gi) * kMaxSplits + aw.split) * WS;
+                        st_ll(w + 2 + d, o_acc[o], fp);
                         if (d == 0) {
-                            w[0] = m_s[gi];
-                            w[1] = l_s[gi];
+                            st_ll(w, m_s[gi], fp);
+                            st_ll(w + 1, l_s[gi], fp);
                         }
                     }
                 }
-                __threadfence();
-                cbar();
-                int *cnt = p.attn_cnt + (size_t)r * p.nkv + g;
-                if (ctid == 0) flag_s = (atomicAdd(cnt, 1) == aw.nact - 1);
-                cbar();
-                if (flag_s) {
-                    __threadfence();
-                    for (int idx = ctid; idx < G * HD; idx += NCT) {
-                        const int gi = idx / HD, d = idx - gi * HD;
-                        const float *w0 = p.attn_ws + (((size_t)r * p.nq + hq0 + gi) * aw.S) * WS;
-                        float M = -INFINITY;
-                        for (int s = 0; s < aw.nact; ++s) M = fmaxf(M, __ldcg(w0 + (size_t)s * WS));
-                        float Lsum = 0.f, O = 0.f;
-                        for (int s = 0; s < aw.nact; ++s) {
-                            const float f = expf(__ldcg(w0 + (size_t)s * WS) - M);
-                            Lsum = fmaf(__ldcg(w0 + (size_t)s * WS + 1), f, Lsum);
-                            O = fmaf(__ldcg(w0 + (size_t)s * WS + 4 + d), f, O);
+            } else {
+                // split 0 combines all splits in split order (deterministic)
+                const uint32_t fp = flag_of(p.flag_base, l, FL_PART);
+                const int ns = aw.nact;
+                // Issue this thread's o loads of every split first (all in flight together),
+                // then gather (m, l) of splits 1..ns-1 into shared memory.
+                auto gather_o = [&](int idx, float (&ov)[kMaxSplits]) {
+                    const int gi = idx / HD, d = idx - gi * HD;
+                    const unsigned long long *wb =
+                        p.part_ll + (((size_t)r * p.nq + hq0 + gi) * kMaxSplits) * WS + 2 + d;
+                    unsigned long long wv2[kMaxSplits];
+#pragma unroll
+                    for (int sp = 1; sp < kMaxSplits; ++sp)
+                        if (sp < ns) wv2[sp] = ld_ll(wb + (size_t)sp * WS);
+#pragma unroll
+                    for (int sp = 1; sp < kMaxSplits; ++sp) {
+                        ov[sp] = 0.f;
+                        if (sp < ns) {
+                            if (ll_flag(wv2[sp]) != fp) wv2[sp] = repoll_ll(wb + (size_t)sp * WS, fp, c);
+                            ov[sp] = ll_val(wv2[sp]);
                         }
-                        orow[(hq0 + gi) * HD + d] = O / Lsum;
                     }
-                    if (ctid == 0) *cnt = 0;
+                };
+                auto combine_o = [&](int idx, float own_o, float (&ov)[kMaxSplits]) {
+                    const int gi = idx / HD, d = idx - gi * HD;
+                    ov[0] = own_o;
+                    float M = -INFINITY;
+                    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ml_s[gi][sp][0]);
+                    float Ls = 0.f, O = 0.f;
+#pragma unroll
+                    for (int sp = 0; sp < kMaxSplits; ++sp)
+                        if (sp < ns) {
+                            const float f = expf(ml_s[gi][sp][0] - M);
+                            Ls = fmaf(ml_s[gi][sp][1], f, Ls);
+                            O = fmaf(ov[sp], f, O);
+                        }
+                    st_ll(orow + (hq0 + gi) * HD + d, O / Ls, fo);
+                };
+                float ov[kMaxSplits];
+                if (ctid < G * HD) gather_o(ctid, ov);
+                for (int idx = ctid; idx < G * (ns - 1) * 2; idx += NCT) {
+                    const int gi = idx / ((ns - 1) * 2), rem = idx - gi * (ns - 1) * 2;
+                    const int sp = 1 + rem / 2, which = rem & 1;
+                    const unsigned long long *w =
+                        p.part_ll + (((size_t)r * p.nq + hq0 + gi) * kMaxSplits + sp) * WS + which;
+                    unsigned long long v = ld_ll(w);
+                    if (ll_flag(v) != fp) v = repoll_ll(w, fp, c);
+                    ml_s[gi][sp][which] = ll_val(v);
+                }
+                if (ctid < G) {
+                    ml_s[ctid][0][0] = m_s[ctid];
+                    ml_s[ctid][0][1] = l_s[ctid];
+                }
+                cbar();
+                if (ctid < G * HD) combine_o(ctid, o_acc[0], ov);
+#pragma unroll
+                for (int o = 1; o < NO; ++o) {
+                    const int idx = ctid + o * NCT;
+                    if (idx < G * HD) {
+                        gather_o(idx, ov);
+                        combine_o(idx, o_acc[o], ov);
+                    }
                 }
             }
         }
         TR(tb + 4);
-        grid_barrier(p.sync + SY_BAR, ++nbar * P, c, ctid);
-        TR(tb + 5);
 
         // ---- o_proj + residual
-        stage<EPV, R>(act, p.attn, qd, qd, rows, nullptr, 0.f, red, ctid);
+        if (own.n > 0)
+            stage_ll<EPV, R>(act, p.o_ll, qd, qd, rows, flag_of(p.flag_base, l, FL_O), nullptr, 0.f, red, ctid, c);
         TR(tb + 6);
         {
-            const Span s = cta_span(H, cta, P);
+            const uint32_t f = flag_of(p.flag_base, l, FL_X1);
             const int upc = max(1, (int)(SLOT / (qd * WSZ)));
-            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-                const int n = min(upc, s.u0 + s.n - u);
+            for (int u = own.u0; u < own.u0 + own.n; u += upc) {
+                const int n = min(upc, own.u0 + own.n - u);
                 const unsigned char *w = rc.acquire(c);
                 for (int j = warp; j < n; j += NCW) {
                     float acc[1][R];
                     dot_rows<WT, R, 1>(w + (size_t)j * qd * WSZ, qd, act, rows, acc, lane);
                     if (lane < rows) {
-                        float *xp = p.x + (size_t)lane * H + u + j;
-                        *xp = __ldcg(xp) + pick<R>(acc[0], lane);
+                        const int jj = u + j - own.u0;
+                        const float x1 = xown[lane][jj] + pick<R>(acc[0], lane);
+                        xown[lane][jj] = x1;
+                        st_ll(p.x_ll + (size_t)lane * H + u + j, x1, f);
                     }
                 }
                 rc.release(lane);
             }
         }
         TR(tb + 7);
-        grid_barrier(p.sync + SY_BAR, ++nbar * P, c, ctid);
-        TR(tb + 8);
 
         // ---- post-norm -> [Wg;Wu] -> silu(gate) * up
-        stage<EPV, R>(act, p.x, H, H, rows, L.post_norm, p.eps, red, ctid);
+        const Span sg = cta_span(p.I, cta, P);
+        if (sg.n > 0)
+            stage_ll<EPV, R>(act, p.x_ll, H, H, rows, flag_of(p.flag_base, l, FL_X1), L.post_norm, p.eps, red, ctid,
+                             c);
         TR(tb + 9);
         {
-            const Span s = cta_span(p.I, cta, P);
+            const uint32_t f = flag_of(p.flag_base, l, FL_ACT);
+            const Span s = sg;
             const int upc = max(1, (int)(SLOT / (2 * H * WSZ)));
             for (int u = s.u0; u < s.u0 + s.n; u += upc) {
                 const int n = min(upc, s.u0 + s.n - u);
@@ -677,43 +863,45 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                     float acc[2][R];
                     dot_rows<WT, R, 2>(w + (size_t)j * 2 * H * WSZ, H, act, rows, acc, lane);
                     if (lane < rows)
-                        p.act[(size_t)lane * p.I + u + j] = silu_f(pick<R>(acc[0], lane)) * pick<R>(acc[1], lane);
+                        st_ll(p.act_ll + (size_t)lane * p.I + u + j,
+                              silu_f(pick<R>(acc[0], lane)) * pick<R>(acc[1], lane), f);
                 }
                 rc.release(lane);
             }
         }
         TR(tb + 10);
-        grid_barrier(p.sync + SY_BAR, ++nbar * P, c, ctid);
-        TR(tb + 11);
 
         // ---- down + residual
-        stage<EPV, R>(act, p.act, p.I, p.I, rows, nullptr, 0.f, red, ctid);
+        if (own.n > 0)
+            stage_ll<EPV, R>(act, p.act_ll, p.I, p.I, rows, flag_of(p.flag_base, l, FL_ACT), nullptr, 0.f, red, ctid,
+                             c);
         TR(tb + 12);
         {
-            const Span s = cta_span(H, cta, P);
+            const uint32_t f = flag_of(p.flag_base, l, FL_X2);
             const int upc = max(1, (int)(SLOT / (p.I * WSZ)));
-            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-                const int n = min(upc, s.u0 + s.n - u);
+            for (int u = own.u0; u < own.u0 + own.n; u += upc) {
+                const int n = min(upc, own.u0 + own.n - u);
                 const unsigned char *w = rc.acquire(c);
                 for (int j = warp; j < n; j += NCW) {
                     float acc[1][R];
                     dot_rows<WT, R, 1>(w + (size_t)j * p.I * WSZ, p.I, act, rows, acc, lane);
                     if (lane < rows) {
-                        float *xp = p.x + (size_t)lane * H + u + j;
-                        *xp = __ldcg(xp) + pick<R>(acc[0], lane);
+                        const int jj = u + j - own.u0;
+                        const float x2 = xown[lane][jj] + pick<R>(acc[0], lane);
+                        xown[lane][jj] = x2;
+                        st_ll(p.x_ll + (size_t)lane * H + u + j, x2, f);
                     }
                 }
                 rc.release(lane);
             }
         }
         TR(tb + 13);
-        grid_barrier(p.sync + SY_BAR, ++nbar * P, c, ctid);
-        TR(tb + 14);
     }
 
     // ---- final norm -> codec_head -> logits, hidden, argmax
     const int th = p.n_layers * kTracePerLayer;
-    stage<EPV, R>(act, p.x, H, H, rows, p.final_norm, p.eps, red, ctid);
+    stage_ll<EPV, R>(act, p.x_ll, H, H, rows, flag_of(p.flag_base, p.n_layers - 1, FL_X2), p.final_norm, p.eps, red,
+                     ctid, c);
     TR(th + 0);
     if (cta == 0 && p.hidden_out != nullptr)
         for (int i = ctid; i < rows * H; i += NCT) {
@@ -761,8 +949,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 ib = i;
             }
         }
-        p.head_val[(size_t)cta * R + ctid] = b;
-        p.head_idx[(size_t)cta * R + ctid] = ib;
+        p.head_val[(size_t)cta * 4 + ctid] = b;
+        p.head_idx[(size_t)cta * 4 + ctid] = ib;
     }
     __threadfence();
     cbar();
@@ -770,14 +958,14 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
     cbar();
     if (flag_s) {
         __threadfence();
-        // rows x 4 warps: each row reduced by 128 threads, then across its 4 warps
+        // each row is reduced by 4 warps (128 threads), then across those warps
         const int r = warp >> 2, sub = ctid & 127;
         float b = -INFINITY;
         int ib = 0x7fffffff;
         if (r < rows) {
-            for (int s = sub; s < P; s += 128) {
-                const float v = __ldcg(p.head_val + (size_t)s * R + r);
-                const int i = __ldcg(p.head_idx + (size_t)s * R + r);
+            for (int s2 = sub; s2 < P; s2 += 128) {
+                const float v = __ldcg(p.head_val + (size_t)s2 * 4 + r);
+                const int i = __ldcg(p.head_idx + (size_t)s2 * 4 + r);
                 if (v > b || (v == b && i < ib)) {
                     b = v;
                     ib = i;
@@ -793,7 +981,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 ib = i2;
             }
         }
-        if (lane == 0 && r < R) {
+        if (lane == 0) {
             bv_s[warp][0] = b;
             bi_s[warp][0] = ib;
         }
@@ -801,7 +989,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
         if (ctid < rows) {
             float bb = -INFINITY;
             int ii = 0x7fffffff;
-            for (int w = 4 * ctid; w < 4 * ctid + 4; ++w) {
+            for (int w = 4 * ctid; w < min(4 * ctid + 4, NCW); ++w) {
                 if (bv_s[w][0] > bb || (bv_s[w][0] == bb && bi_s[w][0] < ii)) {
                     bb = bv_s[w][0];
                     ii = bi_s[w][0];
@@ -810,23 +998,13 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
             if (p.argmax_out != nullptr) p.argmax_out[ctid] = ii;
             p.cur_len[ctid] = curlen_s[ctid] + 1;
         }
-    }
-    // ---- exit: the last CTA out resets the sync words for the next launch
-    cbar();
-    TR(th + 2);
-#undef TR
-    if (ctid == 0) {
-        __threadfence();
-        if (atomicAdd(p.sync + SY_EXIT, 1) == P - 1) {
-            const int nh = p.nq + 2 * p.nkv;
-            for (int h = 0; h < nh; ++h) p.sync[SY_ROWS + h] = 0;
-            p.sync[SY_BAR] = 0;
-            p.sync[SY_HEAD] = 0;
+        if (ctid == 0) {
+            p.sync[SY_HEAD] = 0;     // every CTA has arrived: ready for the next launch
             p.sync[SY_ABORT] = 0;
-            __threadfence();
-            p.sync[SY_EXIT] = 0;
         }
     }
+    TR(th + 2);
+#undef TR
 }
 
 size_t persist_smem_bytes(int R, int head_dim, int kv_bf16, int kmax) {
@@ -836,7 +1014,6 @@ size_t persist_smem_bytes(int R, int head_dim, int kv_bf16, int kmax) {
 
 }  // namespace pk
 }  // namespace talker_k
-
 namespace talker_k {
 
 template <typename WT, typename KT, int HD, int R>

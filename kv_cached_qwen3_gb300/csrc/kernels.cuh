@@ -92,10 +92,14 @@ struct PersistLayer {
     const void *qkv, *o, *gu, *down;
 };
 
+constexpr int kMaxSplits = 16;        // attention splits per (row, KV group) in the persistent kernel
+
 struct PersistParams {
     int n_layers, H, nq, nkv, hd, I, V, G;
     float eps, scale;
     int rows;                         // streams 0..rows-1, one row each
+    uint32_t flag_base;               // step epoch * 256 (never 0): flags of this step's words
+    int splits;                       // attention splits per (row, KV group), <= kMaxSplits
     const PersistLayer *layers;       // device array [n_layers]
     const float *final_norm;
     const void *head;
@@ -106,14 +110,17 @@ struct PersistParams {
     float *logits;                    // [rows, V]
     float *hidden_out;                // [rows, H] or null
     int *argmax_out;                  // [rows] or null
-    float *x, *raw, *attn, *act;      // [rows, H], [rows, qkv_n], [rows, nq*hd], [rows, I]
-    float *attn_ws;                   // [rows][nq][splits][hd+4]
-    int *attn_cnt;                    // [rows][nkv], zero between launches
-    float *head_val;                  // [grid][R]
+    // flag words (value | flag << 32), single-buffered, rows of the 4-row template:
+    unsigned long long *x_ll;         // [4][H]      residual stream after o_proj / after down
+    unsigned long long *raw_ll;       // [4][qkv_n]  raw q|k|v
+    unsigned long long *o_ll;         // [4][nq*hd]  attention output
+    unsigned long long *act_ll;       // [4][I]      silu(gate) * up
+    unsigned long long *part_ll;      // [4][nq][kMaxSplits][hd + 2]  split partials (m, l, o)
+    float *head_val;                  // [grid][4] per-CTA argmax partials
     int *head_idx;
-    int *sync;                        // barrier/exit/abort/head words, then per-head row counters; zero between launches
+    int *sync;                        // [0] argmax arrival counter, [2] abort flag; zero between launches
     int *status;
-    unsigned long long *trace;        // optional: [grid][kTraceSlots] globaltimer stamps of consumer phases
+    unsigned long long *trace;        // optional: [grid][kTraceSlots] globaltimer stamps
 };
 
 // Trace stamps per CTA: [0, 512) consumer phase events (15 per layer + 3 for the head),

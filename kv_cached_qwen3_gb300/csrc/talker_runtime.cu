@@ -92,7 +92,12 @@ struct talker {
     // persistent decode kernel
     int decode_mode = 0;                 // 0 auto, 1 persistent kernel, 2 multi-kernel CUDA graph
     PersistLayer *d_layers = nullptr;    // device copy of the layer pointer table
-    int *d_sync = nullptr;               // barrier / counter words of the persistent kernel
+    int *d_sync = nullptr;               // counter words of the persistent kernel
+    unsigned long long *ll = nullptr;    // flag-word buffers of the persistent kernel (one allocation)
+    float *pk_head_val = nullptr;        // per-CTA argmax partials of the persistent kernel
+    int *pk_head_idx = nullptr;
+    size_t ll_words = 0;
+    uint32_t epoch = 0;                  // step counter for the persistent kernel's flags
     int persist_ok[2] = {-1, -1};        // per R template (1, 4): -1 unknown, 0 unusable, 1 usable
     unsigned long long *trace = nullptr; // optional phase stamps of the persistent kernel (caller-owned)
 };
@@ -127,8 +132,15 @@ void free_workspaces(talker *t) {
 void free_persist(talker *t) {
     free_ptr(t->d_layers);
     free_ptr(t->d_sync);
+    free_ptr(t->ll);
+    free_ptr(t->pk_head_val);
+    free_ptr(t->pk_head_idx);
+    t->pk_head_val = nullptr;
+    t->pk_head_idx = nullptr;
     t->d_layers = nullptr;
     t->d_sync = nullptr;
+    t->ll = nullptr;
+    t->ll_words = 0;
 }
 
 void free_cache(talker *t) {
@@ -460,6 +472,7 @@ bool persist_usable(talker *t, int B) {
     if ((size_t)t->H * wsz > slot || (size_t)t->qd * wsz > slot || (size_t)2 * t->H * wsz > slot ||
         (size_t)t->I * wsz > slot || (size_t)2 * 64 * t->hd * t->kvsz > slot)
         return false;
+    if (kmax_of(t) > 3072 || (t->H + t->n_sm - 1) / t->n_sm > 64 || t->G > 8) return false;
     const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t));
     int per_sm = 0;
     if (setup_persistent(t->w_bf16, t->hd, R, smem, &per_sm) != cudaSuccess) {
@@ -471,7 +484,11 @@ bool persist_usable(talker *t, int B) {
     return true;
 }
 
-talker_status ensure_persist(talker *t, int B) {
+int persist_splits(const talker *t, int B) {
+    return std::max(1, std::min(kMaxSplits, t->n_sm / (B * t->nkv)));
+}
+
+talker_status ensure_persist(talker *t) {
     const int n_heads = t->nq + 2 * t->nkv;
     if (!t->d_layers) {
         std::vector<PersistLayer> h(t->c.n_layers);
@@ -481,31 +498,25 @@ talker_status ensure_persist(talker *t, int B) {
         }
         TRY_CUDA(cudaMalloc(&t->d_layers, h.size() * sizeof(PersistLayer)));
         TRY_CUDA(cudaMemcpy(t->d_layers, h.data(), h.size() * sizeof(PersistLayer), cudaMemcpyHostToDevice));
-        const size_t words = persist_sync_words(n_heads);
+        const size_t words = 8 + n_heads;
         TRY_CUDA(cudaMalloc(&t->d_sync, words * sizeof(int)));
         TRY_CUDA(cudaMemset(t->d_sync, 0, words * sizeof(int)));
-    }
-    const int splits = std::max(1, t->n_sm / (B * t->nkv));
-    TRY(ensure_capacity(t, std::max(B, 4), splits));
-    // head partials: one per (CTA, row template slot)
-    const size_t need_head = (size_t)t->n_sm * 4;
-    if (need_head > t->cap_head_part) {
-        TRY_CUDA(cudaStreamSynchronize(t->st));
-        drop_graphs(t);
-        free_ptr(t->head_val);
-        free_ptr(t->head_idx);
-        t->head_val = nullptr;
-        t->head_idx = nullptr;
-        TRY_CUDA(cudaMalloc(&t->head_val, need_head * sizeof(float)));
-        TRY_CUDA(cudaMalloc(&t->head_idx, need_head * sizeof(int)));
-        t->cap_head_part = need_head;
+        // flag words for 4 rows: x, raw, o, act, split partials; zero flags never match a step's flags
+        const size_t words_ll = 4 * ((size_t)t->H + t->qkv_n + t->qd + t->I) +
+                                4 * (size_t)t->nq * kMaxSplits * (t->hd + 2);
+        TRY_CUDA(cudaMalloc(&t->ll, words_ll * 8));
+        TRY_CUDA(cudaMemset(t->ll, 0, words_ll * 8));
+        t->ll_words = words_ll;
+        TRY_CUDA(cudaMalloc(&t->pk_head_val, (size_t)t->n_sm * 4 * sizeof(float)));
+        TRY_CUDA(cudaMalloc(&t->pk_head_idx, (size_t)t->n_sm * 4 * sizeof(int)));
     }
     return TALKER_OK;
 }
 
 talker_status decode_persistent(talker *t, const float *emb, int B, float *logits, float *hidden, int32_t *argmax) {
-    TRY(ensure_persist(t, B));
+    TRY(ensure_persist(t));
     const int R = persist_rows_tmpl(B);
+    if (++t->epoch >= (1u << 24)) t->epoch = 1;
     PersistParams p{};
     p.n_layers = t->c.n_layers;
     p.H = t->H;
@@ -518,6 +529,8 @@ talker_status decode_persistent(talker *t, const float *emb, int B, float *logit
     p.eps = t->c.rms_eps;
     p.scale = 1.0f / sqrtf((float)t->hd);
     p.rows = B;
+    p.flag_base = t->epoch << 8;
+    p.splits = persist_splits(t, B);
     p.layers = t->d_layers;
     p.final_norm = t->fnorm;
     p.head = t->head;
@@ -528,14 +541,18 @@ talker_status decode_persistent(talker *t, const float *emb, int B, float *logit
     p.logits = logits;
     p.hidden_out = hidden;
     p.argmax_out = argmax;
-    p.x = t->x;
-    p.raw = t->raw;
-    p.attn = t->attn;
-    p.act = t->act;
-    p.attn_ws = t->attn_ws;
-    p.attn_cnt = t->attn_cnt;
-    p.head_val = t->head_val;
-    p.head_idx = t->head_idx;
+    unsigned long long *q = t->ll;
+    p.x_ll = q;
+    q += 4 * (size_t)t->H;
+    p.raw_ll = q;
+    q += 4 * (size_t)t->qkv_n;
+    p.o_ll = q;
+    q += 4 * (size_t)t->qd;
+    p.act_ll = q;
+    q += 4 * (size_t)t->I;
+    p.part_ll = q;
+    p.head_val = t->pk_head_val;
+    p.head_idx = t->pk_head_idx;
     p.sync = t->d_sync;
     p.status = t->d_status;
     p.trace = t->trace;
