@@ -169,6 +169,11 @@ const char *talker_last_error(void);
  * 2 = always the multi-kernel CUDA graph. Errors: EINVAL. */
 talker_status talker_set_decode_mode(talker_t *t, int mode);
 
+/* Tuning / test support: cap the number of CTAs that share one (stream, KV
+ * group) along the sequence in the persistent decode kernel (0 = no cap).
+ * Errors: EINVAL. */
+talker_status talker_set_attn_splits(talker_t *t, int max_splits);
+
 /* Test support: when buf is not NULL, every persistent-kernel decode step
  * writes globaltimer stamps (ns) of its consumer phases into
  * buf[cta * talker_trace_slots() + event] (15 events per layer, then 3 for the

@@ -98,6 +98,7 @@ struct talker {
     int *pk_head_idx = nullptr;
     size_t ll_words = 0;
     uint32_t epoch = 0;                  // step counter for the persistent kernel's flags
+    int max_splits = 0;                  // cap on the persistent kernel's attention splits (0 = none)
     int persist_ok[2] = {-1, -1};        // per R template (1, 4): -1 unknown, 0 unusable, 1 usable
     unsigned long long *trace = nullptr; // optional phase stamps of the persistent kernel (caller-owned)
 };
@@ -485,7 +486,9 @@ bool persist_usable(talker *t, int B) {
 }
 
 int persist_splits(const talker *t, int B) {
-    return std::max(1, std::min(kMaxSplits, t->n_sm / (B * t->nkv)));
+    int s = std::max(1, std::min(kMaxSplits, t->n_sm / (B * t->nkv)));
+    if (t->max_splits > 0) s = std::min(s, t->max_splits);
+    return s;
 }
 
 talker_status ensure_persist(talker *t) {
@@ -816,6 +819,12 @@ talker_status talker_set_trace(talker_t *t, unsigned long long *buf) {
 }
 
 int talker_trace_slots(void) { return kTraceSlots; }
+
+talker_status talker_set_attn_splits(talker_t *t, int max_splits) {
+    if (!t || max_splits < 0) return TALKER_EINVAL;
+    t->max_splits = max_splits;
+    return TALKER_OK;
+}
 
 talker_status talker_set_decode_mode(talker_t *t, int mode) {
     if (!t || mode < 0 || mode > 2) return TALKER_EINVAL;

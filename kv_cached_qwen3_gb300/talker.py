@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_last_error": (ctypes.c_char_p, []),
         "talker_set_decode_mode": (st, [vp, ctypes.c_int]),
         "talker_set_trace": (st, [vp, vp]),
+        "talker_set_attn_splits": (st, [vp, ctypes.c_int]),
         "talker_trace_slots": (ctypes.c_int, []),
     }
     for name, (res, args) in proto.items():
@@ -197,6 +198,9 @@ class Talker:
     def set_decode_mode(self, mode: int):
         """0 automatic, 1 persistent decode kernel, 2 multi-kernel CUDA graph."""
         self._check(self.lib.talker_set_decode_mode(self.h, mode), "talker_set_decode_mode")
+
+    def set_attn_splits(self, n: int):
+        self._check(self.lib.talker_set_attn_splits(self.h, n), "talker_set_attn_splits")
 
     def set_trace(self, buf):
         """buf: int64 cuda tensor [n_sm * trace_slots] or None (persistent decode phase stamps)."""
