@@ -257,6 +257,7 @@ __device__ void stage(float *act, const float *src, int ld, int K, int rows, con
     float ss[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) ss[r] = 0.f;
+    cbar();   // every warp is done reading the previous contents of act
     for (int idx = ctid; idx < rows * K4; idx += NCT) {
         const int r = idx / K4, k = (idx - r * K4) * 4;
         const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)r * ld + k));
@@ -431,6 +432,7 @@ __device__ void stage_ll(float *act, const unsigned long long *src, int ld, int 
     float ss[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) ss[r] = 0.f;
+    cbar();   // every warp is done reading the previous contents of act (the loads above are in flight)
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         const int idx = ctid + i * NCT;
