@@ -362,6 +362,103 @@ __device__ __forceinline__ void dot_rows(const unsigned char *w, int K, const fl
 namespace talker_k {
 namespace pk {
 
+constexpr int UMAX = 64;   // weight units per ring chunk the partial buffer holds
+
+// Partial dot products of the n weight units (NU rows each, K inputs) of one
+// ring chunk with the staged activation rows, using every consumer warp:
+// with n >= NCW each warp takes whole units; otherwise the NCW / n warps of a
+// unit split its K range. Two accumulators per product and two vectors per
+// iteration keep several shared-memory loads in flight. Warp results go to
+// part[slot][R * NU] (slot = unit when n >= NCW, else warp); combine them with
+// unit_sum after a consumer barrier.
+template <typename WT, int R, int NU>
+__device__ __forceinline__ void chunk_dots(const unsigned char *w, int n, int K, const float *act, int rows,
+                                           float (*part)[R * 2], int warp, int lane) {
+    constexpr int EPV = Elem<WT>::kPerVec;
+    const int nvec = K / EPV;
+    const size_t row_bytes = (size_t)K * sizeof(WT);
+    const int wpr = (n >= NCW) ? 1 : NCW / n;
+    for (int job = warp; job < ((n >= NCW) ? n : n * wpr); job += NCW) {
+        const int j = job / wpr, seg = job - j * wpr;
+        const int v0 = (int)((long long)nvec * seg / wpr), v1 = (int)((long long)nvec * (seg + 1) / wpr);
+        const unsigned char *wj = w + (size_t)j * NU * row_bytes;
+        float a0[NU][R], a1[NU][R];
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+#pragma unroll
+            for (int r = 0; r < R; ++r) a0[u][r] = a1[u][r] = 0.f;
+        auto fma_vec = [&](int v, float (&acc)[NU][R]) {
+            uint4 wv[NU];
+#pragma unroll
+            for (int u = 0; u < NU; ++u) wv[u] = *reinterpret_cast<const uint4 *>(wj + u * row_bytes + (size_t)v * 16);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (r < rows) {
+                    if (EPV == 8) {
+                        const float4 x0 = *reinterpret_cast<const float4 *>(act + r * K + v * 4);
+                        const float4 x1 = *reinterpret_cast<const float4 *>(act + r * K + (K >> 1) + v * 4);
+#pragma unroll
+                        for (int u = 0; u < NU; ++u) {
+                            const uint4 q = wv[u];
+                            float s = acc[u][r];
+                            s = fmaf(bf16lo(q.x), x0.x, s);
+                            s = fmaf(bf16hi(q.x), x0.y, s);
+                            s = fmaf(bf16lo(q.y), x0.z, s);
+                            s = fmaf(bf16hi(q.y), x0.w, s);
+                            s = fmaf(bf16lo(q.z), x1.x, s);
+                            s = fmaf(bf16hi(q.z), x1.y, s);
+                            s = fmaf(bf16lo(q.w), x1.z, s);
+                            s = fmaf(bf16hi(q.w), x1.w, s);
+                            acc[u][r] = s;
+                        }
+                    } else {
+                        const float4 x0 = *reinterpret_cast<const float4 *>(act + r * K + v * 4);
+#pragma unroll
+                        for (int u = 0; u < NU; ++u) {
+                            const uint4 q = wv[u];
+                            float s = acc[u][r];
+                            s = fmaf(__uint_as_float(q.x), x0.x, s);
+                            s = fmaf(__uint_as_float(q.y), x0.y, s);
+                            s = fmaf(__uint_as_float(q.z), x0.z, s);
+                            s = fmaf(__uint_as_float(q.w), x0.w, s);
+                            acc[u][r] = s;
+                        }
+                    }
+                }
+            }
+        };
+        int v = v0 + lane;
+        for (; v + 32 < v1; v += 64) {
+            fma_vec(v, a0);
+            fma_vec(v + 32, a1);
+        }
+        if (v < v1) fma_vec(v, a0);
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float t = warp_sum(a0[u][r] + a1[u][r]);
+                if (lane == 0) part[(n >= NCW) ? j : job][r * NU + u] = t;
+            }
+    }
+}
+
+// Sum of the warp partials of unit j, row r, sub-row u (after a consumer barrier).
+template <int R, int NU>
+__device__ __forceinline__ float unit_sum(const float (*part)[R * 2], int n, int j, int r, int u) {
+    if (n >= NCW) return part[j][r * NU + u];
+    const int wpr = NCW / n;
+    float t = 0.f;
+    for (int q = 0; q < wpr; ++q) t += part[j * wpr + q][r * NU + u];
+    return t;
+}
+
+}  // namespace pk
+}  // namespace talker_k
+
+namespace talker_k {
+namespace pk {
+
 // ---- flag-carrying words: value in the low 32 bits, flag in the high 32 bits,
 // written with one 8-byte store, so a reader that sees the flag sees the value.
 __device__ __forceinline__ unsigned long long ll_pack(float v, uint32_t f) {
@@ -516,6 +613,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
     __shared__ int bi_s[NCW][R];
     __shared__ int curlen_s[R];
     __shared__ int abort_sh, flag_s;
+    __shared__ float part_s[2][UMAX][R * 2];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, cta = blockIdx.x;
@@ -552,6 +650,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
     const int ctid = tid;
     unsigned long long *trace = (p.trace != nullptr && ctid == 0) ? p.trace + (size_t)cta * kTraceSlots : nullptr;
     Ring rc{ring, full, empty, 0, trace};
+    int pb = 0;   // which half of part_s the next chunk writes
 #define TR(slot)                                      \
     do {                                              \
         if (trace) trace[(slot)] = globaltimer_ns();  \
@@ -582,13 +681,13 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
             const int upc = max(1, (int)(SLOT / (H * WSZ)));
             for (int u = s.u0; u < s.u0 + s.n; u += upc) {
                 const int n = min(upc, s.u0 + s.n - u);
-                const unsigned char *w = rc.acquire(c);
-                for (int j = warp; j < n; j += NCW) {
-                    float acc[1][R];
-                    dot_rows<WT, R, 1>(w + (size_t)j * H * WSZ, H, act, rows, acc, lane);
-                    if (lane < rows) st_ll(p.raw_ll + (size_t)lane * qkv_n + u + j, pick<R>(acc[0], lane), f);
-                }
+                chunk_dots<WT, R, 1>(rc.acquire(c), n, H, act, rows, part_s[pb], warp, lane);
                 rc.release(lane);
+                cbar();
+                if (ctid < n)
+                    for (int r = 0; r < rows; ++r)
+                        st_ll(p.raw_ll + (size_t)r * qkv_n + u + ctid, unit_sum<R, 1>(part_s[pb], n, ctid, r, 0), f);
+                pb ^= 1;
             }
         }
         TR(tb + 2);
@@ -685,13 +784,24 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                     float kv[E];
 #pragma unroll
                     for (int e = 0; e < E; ++e) kv[e] = Elem<KT>::load(Ks, (size_t)j * HD + lane * E + e);
-                    for (int gi = 0; gi < G; ++gi) {
-                        float d = 0.f;
+                    float dv[MAXG];
 #pragma unroll
-                        for (int e = 0; e < E; ++e) d = fmaf(qs[gi * HD + lane * E + e], kv[e], d);
-                        d = warp_sum(d);
-                        if (lane == 0) sc[gi * kPage + j] = (j < valid) ? d : -INFINITY;
+                    for (int gi = 0; gi < MAXG; ++gi) {
+                        dv[gi] = 0.f;
+                        if (gi < G) {
+#pragma unroll
+                            for (int e = 0; e < E; ++e) dv[gi] = fmaf(qs[gi * HD + lane * E + e], kv[e], dv[gi]);
+                        }
                     }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                        for (int gi = 0; gi < MAXG; ++gi)
+                            if (gi < G) dv[gi] += __shfl_xor_sync(0xffffffffu, dv[gi], o);
+                    if (lane == 0)
+#pragma unroll
+                        for (int gi = 0; gi < MAXG; ++gi)
+                            if (gi < G) sc[gi * kPage + j] = (j < valid) ? dv[gi] : -INFINITY;
                 }
                 cbar();
                 if (warp < G) {
@@ -717,10 +827,17 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                     const int idx = ctid + o * NCT;
                     if (idx < G * HD) {
                         const int gi = idx / HD, d = idx - gi * HD;
-                        float acc = o_acc[o] * al_s[gi];
+                        float c0 = o_acc[o] * al_s[gi], c1 = 0.f, c2 = 0.f, c3 = 0.f;
                         const float *pj = sc + gi * kPage;
-                        for (int j = 0; j < valid; ++j) acc = fmaf(pj[j], Elem<KT>::load(Vs, (size_t)j * HD + d), acc);
-                        o_acc[o] = acc;
+                        int j = 0;
+                        for (; j + 3 < valid; j += 4) {
+                            c0 = fmaf(pj[j], Elem<KT>::load(Vs, (size_t)j * HD + d), c0);
+                            c1 = fmaf(pj[j + 1], Elem<KT>::load(Vs, (size_t)(j + 1) * HD + d), c1);
+                            c2 = fmaf(pj[j + 2], Elem<KT>::load(Vs, (size_t)(j + 2) * HD + d), c2);
+                            c3 = fmaf(pj[j + 3], Elem<KT>::load(Vs, (size_t)(j + 3) * HD + d), c3);
+                        }
+                        for (; j < valid; ++j) c0 = fmaf(pj[j], Elem<KT>::load(Vs, (size_t)j * HD + d), c0);
+                        o_acc[o] = (c0 + c1) + (c2 + c3);
                     }
                 }
                 rc.release(lane);
@@ -832,18 +949,17 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
             const int upc = max(1, (int)(SLOT / (qd * WSZ)));
             for (int u = own.u0; u < own.u0 + own.n; u += upc) {
                 const int n = min(upc, own.u0 + own.n - u);
-                const unsigned char *w = rc.acquire(c);
-                for (int j = warp; j < n; j += NCW) {
-                    float acc[1][R];
-                    dot_rows<WT, R, 1>(w + (size_t)j * qd * WSZ, qd, act, rows, acc, lane);
-                    if (lane < rows) {
-                        const int jj = u + j - own.u0;
-                        const float x1 = xown[lane][jj] + pick<R>(acc[0], lane);
-                        xown[lane][jj] = x1;
-                        st_ll(p.x_ll + (size_t)lane * H + u + j, x1, f);
-                    }
-                }
+                chunk_dots<WT, R, 1>(rc.acquire(c), n, qd, act, rows, part_s[pb], warp, lane);
                 rc.release(lane);
+                cbar();
+                if (ctid < n)
+                    for (int r = 0; r < rows; ++r) {
+                        const int jj = u + ctid - own.u0;
+                        const float x1 = xown[r][jj] + unit_sum<R, 1>(part_s[pb], n, ctid, r, 0);
+                        xown[r][jj] = x1;
+                        st_ll(p.x_ll + (size_t)r * H + u + ctid, x1, f);
+                    }
+                pb ^= 1;
             }
         }
         TR(tb + 7);
@@ -860,15 +976,16 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
             const int upc = max(1, (int)(SLOT / (2 * H * WSZ)));
             for (int u = s.u0; u < s.u0 + s.n; u += upc) {
                 const int n = min(upc, s.u0 + s.n - u);
-                const unsigned char *w = rc.acquire(c);
-                for (int j = warp; j < n; j += NCW) {
-                    float acc[2][R];
-                    dot_rows<WT, R, 2>(w + (size_t)j * 2 * H * WSZ, H, act, rows, acc, lane);
-                    if (lane < rows)
-                        st_ll(p.act_ll + (size_t)lane * p.I + u + j,
-                              silu_f(pick<R>(acc[0], lane)) * pick<R>(acc[1], lane), f);
-                }
+                chunk_dots<WT, R, 2>(rc.acquire(c), n, H, act, rows, part_s[pb], warp, lane);
                 rc.release(lane);
+                cbar();
+                if (ctid < n)
+                    for (int r = 0; r < rows; ++r) {
+                        const float gt = unit_sum<R, 2>(part_s[pb], n, ctid, r, 0);
+                        const float up = unit_sum<R, 2>(part_s[pb], n, ctid, r, 1);
+                        st_ll(p.act_ll + (size_t)r * p.I + u + ctid, silu_f(gt) * up, f);
+                    }
+                pb ^= 1;
             }
         }
         TR(tb + 10);
@@ -883,18 +1000,17 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
             const int upc = max(1, (int)(SLOT / (p.I * WSZ)));
             for (int u = own.u0; u < own.u0 + own.n; u += upc) {
                 const int n = min(upc, own.u0 + own.n - u);
-                const unsigned char *w = rc.acquire(c);
-                for (int j = warp; j < n; j += NCW) {
-                    float acc[1][R];
-                    dot_rows<WT, R, 1>(w + (size_t)j * p.I * WSZ, p.I, act, rows, acc, lane);
-                    if (lane < rows) {
-                        const int jj = u + j - own.u0;
-                        const float x2 = xown[lane][jj] + pick<R>(acc[0], lane);
-                        xown[lane][jj] = x2;
-                        st_ll(p.x_ll + (size_t)lane * H + u + j, x2, f);
-                    }
-                }
+                chunk_dots<WT, R, 1>(rc.acquire(c), n, p.I, act, rows, part_s[pb], warp, lane);
                 rc.release(lane);
+                cbar();
+                if (ctid < n)
+                    for (int r = 0; r < rows; ++r) {
+                        const int jj = u + ctid - own.u0;
+                        const float x2 = xown[r][jj] + unit_sum<R, 1>(part_s[pb], n, ctid, r, 0);
+                        xown[r][jj] = x2;
+                        st_ll(p.x_ll + (size_t)r * H + u + ctid, x2, f);
+                    }
+                pb ^= 1;
             }
         }
         TR(tb + 13);
@@ -910,28 +1026,58 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
             const int r = i / H, k = i - r * H;
             p.hidden_out[i] = act[aidx<EPV>(r, k, H)];
         }
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    float bvr[R];
+    int bir[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        bvr[r] = -INFINITY;
+        bir[r] = 0x7fffffff;
+    }
     {
         const Span s = cta_span(p.V, cta, P);
         const int upc = max(1, (int)(SLOT / (H * WSZ)));
         for (int u = s.u0; u < s.u0 + s.n; u += upc) {
             const int n = min(upc, s.u0 + s.n - u);
-            const unsigned char *w = rc.acquire(c);
-            for (int j = warp; j < n; j += NCW) {
-                float acc[1][R];
-                dot_rows<WT, R, 1>(w + (size_t)j * H * WSZ, H, act, rows, acc, lane);
-                if (lane < rows) {
-                    const float v = pick<R>(acc[0], lane);
-                    p.logits[(size_t)lane * p.V + u + j] = v;
-                    if (isnan(v)) atomicOr(p.status, ST_NAN_LOGIT);
-                    else if (v > bv || (v == bv && u + j < bi)) {
-                        bv = v;
-                        bi = u + j;
+            chunk_dots<WT, R, 1>(rc.acquire(c), n, H, act, rows, part_s[pb], warp, lane);
+            rc.release(lane);
+            cbar();
+            if (ctid < n) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r < rows) {
+                        const float v = unit_sum<R, 1>(part_s[pb], n, ctid, r, 0);
+                        const int idx = u + ctid;
+                        p.logits[(size_t)r * p.V + idx] = v;
+                        if (isnan(v)) atomicOr(p.status, ST_NAN_LOGIT);
+                        else if (v > bvr[r] || (v == bvr[r] && idx < bir[r])) {
+                            bvr[r] = v;
+                            bir[r] = idx;
+                        }
                     }
                 }
             }
-            rc.release(lane);
+            pb ^= 1;
+        }
+    }
+    // per-warp best of each row (lowest index on ties)
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float b = bvr[r];
+        int ib = bir[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float v2 = __shfl_xor_sync(0xffffffffu, b, o);
+            const int i2 = __shfl_xor_sync(0xffffffffu, ib, o);
+            if (v2 > b || (v2 == b && i2 < ib)) {
+                b = v2;
+                ib = i2;
+            }
+        }
+        if (lane == r) {
+            bv = b;
+            bi = ib;
         }
     }
     TR(th + 1);
