@@ -170,7 +170,7 @@ __device__ __forceinline__ AttnWork attn_work(const PersistParams &p, int cta, i
 // The producer lane: streams the CTA's schedule into the ring, in exactly the
 // order the consumers read it.
 template <typename WT, typename KT, int HD>
-__device__ void producer(const PersistParams &p, unsigned char *ring, uint64_t *full, uint64_t *empty, const Ctx &c,
+__device__ __noinline__ void producer(const PersistParams &p, unsigned char *ring, uint64_t *full, uint64_t *empty, const Ctx &c,
                          const AttnWork &aw) {
     const int P = gridDim.x, cta = blockIdx.x;
     const size_t wsz = sizeof(WT);
@@ -250,7 +250,7 @@ __device__ __forceinline__ int aidx(int r, int k, int K) {
 // layout of the dot products; with `gain`, apply RMSNorm and the gain
 // (x / sqrt(mean(x^2) + eps) * gain). Ends with a consumer barrier.
 template <int EPV, int R>
-__device__ void stage(float *act, const float *src, int ld, int K, int rows, const float *gain, float eps,
+__device__ __noinline__ void stage(float *act, const float *src, int ld, int K, int rows, const float *gain, float eps,
                       float *red, int ctid) {
     const int K4 = K >> 2;
     const int warp = ctid >> 5, lane = ctid & 31;
@@ -372,7 +372,7 @@ constexpr int UMAX = 64;   // weight units per ring chunk the partial buffer hol
 // part[slot][R * NU] (slot = unit when n >= NCW, else warp); combine them with
 // unit_sum after a consumer barrier.
 template <typename WT, int R, int NU>
-__device__ __forceinline__ void chunk_dots(const unsigned char *w, int n, int K, const float *act, int rows,
+__device__ __noinline__ void chunk_dots(const unsigned char *w, int n, int K, const float *act, int rows,
                                            float (*part)[R * 2], int warp, int lane) {
     constexpr int EPV = Elem<WT>::kPerVec;
     const int nvec = K / EPV;
@@ -511,7 +511,7 @@ constexpr int KCAP = 3072;   // widest activation row the LL staging handles (R 
 // is issued before any flag is checked, so a ready tensor costs one round trip.
 // With `gain`, applies RMSNorm and the gain. Ends with a consumer barrier.
 template <int EPV, int R>
-__device__ void stage_ll(float *act, const unsigned long long *src, int ld, int K, int rows, uint32_t flag,
+__device__ __noinline__ void stage_ll(float *act, const unsigned long long *src, int ld, int K, int rows, uint32_t flag,
                          const float *gain, float eps, float *red, int ctid, const Ctx &c) {
     constexpr int NP = (R * KCAP / 2 + NCT - 1) / NCT;
     const int K2 = K >> 1;
@@ -599,100 +599,20 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 
 constexpr int XO = 64;   // owned residual rows per CTA (ceil(H / grid) <= XO)
 
+// One attention work item of one layer: QK-norm + RoPE of this row's q heads
+// and k (v as is) from the raw words, the cache row for later steps (split 0),
+// online-softmax attention over this split's pages (the step's own row patched
+// into the cached copy), then either the output words or this split's partial;
+// split 0 combines the partials of all splits in split order.
 template <typename WT, typename KT, int HD, int R>
-__global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams p) {
-    constexpr int EPV = Elem<WT>::kPerVec;
-    constexpr size_t WSZ = sizeof(WT);
-    extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t full[NS], empty[NS];
-    __shared__ float red[NCW * R];
-    __shared__ float m_s[MAXG], l_s[MAXG], al_s[MAXG];
-    __shared__ float ml_s[MAXG][kMaxSplits][2];
-    __shared__ float xown[R][XO];
-    __shared__ float bv_s[NCW][R];
-    __shared__ int bi_s[NCW][R];
-    __shared__ int curlen_s[R];
-    __shared__ int abort_sh, flag_s;
-    __shared__ float part_s[2][UMAX][R * 2];
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int P = gridDim.x, cta = blockIdx.x;
-    const int H = p.H, half = HD / 2, G = p.G;
+__device__ __noinline__ void attn_phase(const PersistParams &p, const LayerW &L, int l, const AttnWork &aw, Ring &rc,
+                                        const Ctx &c, float *qs, float *sc, KT *knew, KT *vnew, float *m_s,
+                                        float *l_s, float *al_s, float (*ml_s)[kMaxSplits][2], float *comb,
+                                        int ctid, unsigned long long *trace, int tb) {
+    const int warp = ctid >> 5, lane = ctid & 31;
+    const int half = HD / 2, G = p.G;
     const int qd = p.nq * HD, qkv_n = (p.nq + 2 * p.nkv) * HD;
-    const int KMAX = max(max(H, qd), p.I);
-    const int rows = p.rows;
-    unsigned char *ring = smem;
-    float *act = reinterpret_cast<float *>(smem + (size_t)NS * SLOT);
-    float *qs = act + (size_t)R * KMAX;            // [G][HD] scaled q of the attention row
-    float *sc = qs + MAXG * HD;                     // [G][kPage] scores / probabilities
-    KT *knew = reinterpret_cast<KT *>(sc + MAXG * kPage);
-    KT *vnew = knew + HD;
 
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NCW);
-        }
-        abort_sh = 0;
-        fence_barrier_init();
-    }
-    if (tid < R) curlen_s[tid] = (tid < rows) ? p.cur_len[tid] : 0;
-    __syncthreads();
-    const Ctx c{reinterpret_cast<volatile int *>(&abort_sh), p.sync + SY_ABORT, p.status};
-    const AttnWork aw = attn_work(p, cta, P, curlen_s);
-
-    if (warp == NCW) {
-        if (lane == 0) producer<WT, KT, HD>(p, ring, full, empty, c, aw);
-        return;
-    }
-
-    // ------------------------------------------------------------------ consumers
-    const int ctid = tid;
-    unsigned long long *trace = (p.trace != nullptr && ctid == 0) ? p.trace + (size_t)cta * kTraceSlots : nullptr;
-    Ring rc{ring, full, empty, 0, trace};
-    int pb = 0;   // which half of part_s the next chunk writes
-#define TR(slot)                                      \
-    do {                                              \
-        if (trace) trace[(slot)] = globaltimer_ns();  \
-    } while (0)
-    const Span own = cta_span(H, cta, P);           // residual rows this CTA updates (o_proj and down)
-    for (int i = ctid; i < rows * own.n; i += NCT) {
-        const int r = i / own.n, j = i - r * own.n;
-        xown[r][j] = p.emb[(size_t)r * H + own.u0 + j];
-    }
-
-    for (int l = 0; l < p.n_layers; ++l) {
-        const LayerW &L = p.layers[l];
-        const int tb = l * kTracePerLayer;
-        TR(tb + 0);
-        // ---- RMSNorm -> [Wq;Wk;Wv] -> raw q|k|v words
-        // (A CTA with no rows in a phase skips that phase's input: it would have no
-        // output that orders its reads before the next overwrite of the input words.)
-        const Span sq = cta_span(qkv_n, cta, P);
-        if (sq.n > 0) {
-            if (l == 0) stage<EPV, R>(act, p.emb, H, H, rows, L.in_norm, p.eps, red, ctid);
-            else stage_ll<EPV, R>(act, p.x_ll, H, H, rows, flag_of(p.flag_base, l - 1, FL_X2), L.in_norm, p.eps,
-                                  red, ctid, c);
-        }
-        TR(tb + 1);
-        {
-            const uint32_t f = flag_of(p.flag_base, l, FL_RAW);
-            const Span s = sq;
-            const int upc = max(1, (int)(SLOT / (H * WSZ)));
-            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-                const int n = min(upc, s.u0 + s.n - u);
-                chunk_dots<WT, R, 1>(rc.acquire(c), n, H, act, rows, part_s[pb], warp, lane);
-                rc.release(lane);
-                cbar();
-                if (ctid < n)
-                    for (int r = 0; r < rows; ++r)
-                        st_ll(p.raw_ll + (size_t)r * qkv_n + u + ctid, unit_sum<R, 1>(part_s[pb], n, ctid, r, 0), f);
-                pb ^= 1;
-            }
-        }
-        TR(tb + 2);
-        // ---- attention of (row r, KV group g, split) over [0, pos]
-        if (aw.has) {
             const int r = aw.r, g = aw.g, pos = aw.pos;
             if (warp < G + 2) {
                 // QK-norm + RoPE of this row's q heads of the group and k; v as is
@@ -766,7 +686,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
 #pragma unroll
             for (int o = 0; o < NO; ++o) o_acc[o] = 0.f;
             cbar();
-            TR(tb + 3);
+            if (trace) trace[tb + 3] = globaltimer_ns();
             for (int pg = aw.pb; pg < aw.pe; ++pg) {
                 KT *Ks = reinterpret_cast<KT *>(const_cast<unsigned char *>(rc.acquire(c)));
                 KT *Vs = Ks + kPage * HD;
@@ -877,42 +797,34 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 // split 0 combines all splits in split order (deterministic)
                 const uint32_t fp = flag_of(p.flag_base, l, FL_PART);
                 const int ns = aw.nact;
-                // Issue this thread's o loads of every split first (all in flight together),
-                // then gather (m, l) of splits 1..ns-1 into shared memory.
-                auto gather_o = [&](int idx, float (&ov)[kMaxSplits]) {
-                    const int gi = idx / HD, d = idx - gi * HD;
-                    const unsigned long long *wb =
-                        p.part_ll + (((size_t)r * p.nq + hq0 + gi) * kMaxSplits) * WS + 2 + d;
-                    unsigned long long wv2[kMaxSplits];
+                // Gather o of splits 1..ns-1 into comb[gi][sp][d] (8 loads in flight per
+                // thread per round), and (m, l) of every split into ml_s.
+                const int per_g = (ns - 1) * HD;
+                const int total = G * per_g;
+                for (int base = 0; base < total; base += 8 * NCT) {
+                    unsigned long long wv[8];
+                    const unsigned long long *ad[8];
 #pragma unroll
-                    for (int sp = 1; sp < kMaxSplits; ++sp)
-                        if (sp < ns) wv2[sp] = ld_ll(wb + (size_t)sp * WS);
-#pragma unroll
-                    for (int sp = 1; sp < kMaxSplits; ++sp) {
-                        ov[sp] = 0.f;
-                        if (sp < ns) {
-                            if (ll_flag(wv2[sp]) != fp) wv2[sp] = repoll_ll(wb + (size_t)sp * WS, fp, c);
-                            ov[sp] = ll_val(wv2[sp]);
+                    for (int k = 0; k < 8; ++k) {
+                        const int idx = base + k * NCT + ctid;
+                        ad[k] = nullptr;
+                        if (idx < total) {
+                            const int gi = idx / per_g, rem = idx - gi * per_g;
+                            const int sp = 1 + rem / HD, d = rem - (sp - 1) * HD;
+                            ad[k] = p.part_ll + (((size_t)r * p.nq + hq0 + gi) * kMaxSplits + sp) * WS + 2 + d;
+                            wv[k] = ld_ll(ad[k]);
                         }
                     }
-                };
-                auto combine_o = [&](int idx, float own_o, float (&ov)[kMaxSplits]) {
-                    const int gi = idx / HD, d = idx - gi * HD;
-                    ov[0] = own_o;
-                    float M = -INFINITY;
-                    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ml_s[gi][sp][0]);
-                    float Ls = 0.f, O = 0.f;
 #pragma unroll
-                    for (int sp = 0; sp < kMaxSplits; ++sp)
-                        if (sp < ns) {
-                            const float f = expf(ml_s[gi][sp][0] - M);
-                            Ls = fmaf(ml_s[gi][sp][1], f, Ls);
-                            O = fmaf(ov[sp], f, O);
+                    for (int k = 0; k < 8; ++k) {
+                        if (ad[k] != nullptr) {
+                            if (ll_flag(wv[k]) != fp) wv[k] = repoll_ll(ad[k], fp, c);
+                            const int idx = base + k * NCT + ctid;
+                            const int gi = idx / per_g, rem = idx - gi * per_g;
+                            comb[(gi * aw.S + 1 + rem / HD) * HD + rem % HD] = ll_val(wv[k]);
                         }
-                    st_ll(orow + (hq0 + gi) * HD + d, O / Ls, fo);
-                };
-                float ov[kMaxSplits];
-                if (ctid < G * HD) gather_o(ctid, ov);
+                    }
+                }
                 for (int idx = ctid; idx < G * (ns - 1) * 2; idx += NCT) {
                     const int gi = idx / ((ns - 1) * 2), rem = idx - gi * (ns - 1) * 2;
                     const int sp = 1 + rem / 2, which = rem & 1;
@@ -926,18 +838,124 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                     ml_s[ctid][0][0] = m_s[ctid];
                     ml_s[ctid][0][1] = l_s[ctid];
                 }
-                cbar();
-                if (ctid < G * HD) combine_o(ctid, o_acc[0], ov);
-#pragma unroll
-                for (int o = 1; o < NO; ++o) {
+                for (int o = 0; o < NO; ++o) {
                     const int idx = ctid + o * NCT;
-                    if (idx < G * HD) {
-                        gather_o(idx, ov);
-                        combine_o(idx, o_acc[o], ov);
+                    if (idx < G * HD) comb[((idx / HD) * aw.S) * HD + idx % HD] = o_acc[o];
+                }
+                cbar();
+                for (int idx = ctid; idx < G * HD; idx += NCT) {
+                    const int gi = idx / HD, d = idx - gi * HD;
+                    float M = -INFINITY;
+                    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ml_s[gi][sp][0]);
+                    float Ls = 0.f, O = 0.f;
+                    for (int sp = 0; sp < ns; ++sp) {
+                        const float f = expf(ml_s[gi][sp][0] - M);
+                        Ls = fmaf(ml_s[gi][sp][1], f, Ls);
+                        O = fmaf(comb[(gi * aw.S + sp) * HD + d], f, O);
                     }
+                    st_ll(orow + (hq0 + gi) * HD + d, O / Ls, fo);
                 }
             }
         }
+
+
+template <typename WT, typename KT, int HD, int R>
+__global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_constant__ PersistParams p) {
+    constexpr int EPV = Elem<WT>::kPerVec;
+    constexpr size_t WSZ = sizeof(WT);
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[NS], empty[NS];
+    __shared__ float red[NCW * R];
+    __shared__ float m_s[MAXG], l_s[MAXG], al_s[MAXG];
+    __shared__ float ml_s[MAXG][kMaxSplits][2];
+    __shared__ float xown[R][XO];
+    __shared__ float bv_s[NCW][R];
+    __shared__ int bi_s[NCW][R];
+    __shared__ int curlen_s[R];
+    __shared__ int abort_sh, flag_s;
+    __shared__ float part_s[2][UMAX][R * 2];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = gridDim.x, cta = blockIdx.x;
+    const int H = p.H, half = HD / 2, G = p.G;
+    const int qd = p.nq * HD, qkv_n = (p.nq + 2 * p.nkv) * HD;
+    const int KMAX = max(max(H, qd), p.I);
+    const int rows = p.rows;
+    unsigned char *ring = smem;
+    float *act = reinterpret_cast<float *>(smem + (size_t)NS * SLOT);
+    float *qs = act + (size_t)R * KMAX;            // [G][HD] scaled q of the attention row
+    float *sc = qs + MAXG * HD;                     // [G][kPage] scores / probabilities
+    float *comb = sc + MAXG * kPage;                // [G][splits][HD] gathered split outputs
+    KT *knew = reinterpret_cast<KT *>(comb + (size_t)G * p.splits * HD);
+    KT *vnew = knew + HD;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCW);
+        }
+        abort_sh = 0;
+        fence_barrier_init();
+    }
+    if (tid < R) curlen_s[tid] = (tid < rows) ? p.cur_len[tid] : 0;
+    __syncthreads();
+    const Ctx c{reinterpret_cast<volatile int *>(&abort_sh), p.sync + SY_ABORT, p.status};
+    const AttnWork aw = attn_work(p, cta, P, curlen_s);
+
+    if (warp == NCW) {
+        if (lane == 0) producer<WT, KT, HD>(p, ring, full, empty, c, aw);
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    const int ctid = tid;
+    unsigned long long *trace = (p.trace != nullptr && ctid == 0) ? p.trace + (size_t)cta * kTraceSlots : nullptr;
+    Ring rc{ring, full, empty, 0, trace};
+    int pb = 0;   // which half of part_s the next chunk writes
+#define TR(slot)                                      \
+    do {                                              \
+        if (trace) trace[(slot)] = globaltimer_ns();  \
+    } while (0)
+    const Span own = cta_span(H, cta, P);           // residual rows this CTA updates (o_proj and down)
+    for (int i = ctid; i < rows * own.n; i += NCT) {
+        const int r = i / own.n, j = i - r * own.n;
+        xown[r][j] = p.emb[(size_t)r * H + own.u0 + j];
+    }
+
+    for (int l = 0; l < p.n_layers; ++l) {
+        const LayerW &L = p.layers[l];
+        const int tb = l * kTracePerLayer;
+        TR(tb + 0);
+        // ---- RMSNorm -> [Wq;Wk;Wv] -> raw q|k|v words
+        // (A CTA with no rows in a phase skips that phase's input: it would have no
+        // output that orders its reads before the next overwrite of the input words.)
+        const Span sq = cta_span(qkv_n, cta, P);
+        if (sq.n > 0) {
+            if (l == 0) stage<EPV, R>(act, p.emb, H, H, rows, L.in_norm, p.eps, red, ctid);
+            else stage_ll<EPV, R>(act, p.x_ll, H, H, rows, flag_of(p.flag_base, l - 1, FL_X2), L.in_norm, p.eps,
+                                  red, ctid, c);
+        }
+        TR(tb + 1);
+        {
+            const uint32_t f = flag_of(p.flag_base, l, FL_RAW);
+            const Span s = sq;
+            const int upc = max(1, (int)(SLOT / (H * WSZ)));
+            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
+                const int n = min(upc, s.u0 + s.n - u);
+                chunk_dots<WT, R, 1>(rc.acquire(c), n, H, act, rows, part_s[pb], warp, lane);
+                rc.release(lane);
+                cbar();
+                if (ctid < n)
+                    for (int r = 0; r < rows; ++r)
+                        st_ll(p.raw_ll + (size_t)r * qkv_n + u + ctid, unit_sum<R, 1>(part_s[pb], n, ctid, r, 0), f);
+                pb ^= 1;
+            }
+        }
+        TR(tb + 2);
+        // ---- attention of (row r, KV group g, split) over [0, pos]
+        if (aw.has)
+            attn_phase<WT, KT, HD, R>(p, L, l, aw, rc, c, qs, sc, knew, vnew, m_s, l_s, al_s, ml_s, comb, ctid, trace,
+                                      tb);
         TR(tb + 4);
 
         // ---- o_proj + residual
@@ -1155,9 +1173,9 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
 #undef TR
 }
 
-size_t persist_smem_bytes(int R, int head_dim, int kv_bf16, int kmax) {
+size_t persist_smem_bytes(int R, int head_dim, int kv_bf16, int kmax, int group, int splits) {
     return (size_t)NS * SLOT + (size_t)R * kmax * 4 + (size_t)MAXG * head_dim * 4 + (size_t)MAXG * kPage * 4 +
-           2 * (size_t)head_dim * (kv_bf16 ? 2 : 4) + 16;
+           (size_t)group * splits * head_dim * 4 + 2 * (size_t)head_dim * (kv_bf16 ? 2 : 4) + 16;
 }
 
 }  // namespace pk
@@ -1199,7 +1217,9 @@ static cudaError_t setup_pk(size_t smem, int *blocks_per_sm) {
         return cudaErrorInvalidValue;                                                        \
     } while (0)
 
-size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax) { return pk::persist_smem_bytes(R, head_dim, kv_bf16, kmax); }
+size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax, int group, int splits) {
+    return pk::persist_smem_bytes(R, head_dim, kv_bf16, kmax, group, splits);
+}
 int persist_threads() { return pk::NT; }
 int persist_slot_bytes() { return pk::SLOT; }
 int persist_sync_words(int n_heads) { return pk::SY_ROWS + n_heads; }

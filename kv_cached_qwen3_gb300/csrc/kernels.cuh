@@ -149,7 +149,7 @@ cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *
 cudaError_t prepare_kernels();
 
 // Persistent decode kernel (one cooperative launch per decode step, one CTA per SM).
-size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax);
+size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax, int group, int splits);
 int persist_threads();
 int persist_slot_bytes();
 int persist_sync_words(int n_heads);

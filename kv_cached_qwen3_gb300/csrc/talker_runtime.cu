@@ -458,6 +458,14 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
 
 int persist_rows_tmpl(int B) { return B <= 1 ? 1 : 4; }
 
+int persist_splits(const talker *t, int B) {
+    int s = std::max(1, std::min(kMaxSplits, t->n_sm / (B * t->nkv)));
+    if (t->max_splits > 0) s = std::min(s, t->max_splits);
+    return s;
+}
+
+
+
 int kmax_of(const talker *t) { return std::max(std::max(t->H, t->qd), t->I); }
 
 // Can the persistent kernel run this geometry with B rows? (one CTA per SM must fit,
@@ -474,7 +482,9 @@ bool persist_usable(talker *t, int B) {
         (size_t)t->I * wsz > slot || (size_t)2 * 64 * t->hd * t->kvsz > slot)
         return false;
     if (kmax_of(t) > 3072 || (t->H + t->n_sm - 1) / t->n_sm > 64 || t->G > 8) return false;
-    const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t));
+    // shared memory is largest at the smallest B of the row template (most attention splits)
+    const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t), t->G, persist_splits(t, R == 1 ? 1 : 2));
+    if (smem > 227 * 1024 - 8 * 1024) return false;
     int per_sm = 0;
     if (setup_persistent(t->w_bf16, t->hd, R, smem, &per_sm) != cudaSuccess) {
         cudaGetLastError();
@@ -483,12 +493,6 @@ bool persist_usable(talker *t, int B) {
     if (per_sm < 1) return false;
     ok = 1;
     return true;
-}
-
-int persist_splits(const talker *t, int B) {
-    int s = std::max(1, std::min(kMaxSplits, t->n_sm / (B * t->nkv)));
-    if (t->max_splits > 0) s = std::min(s, t->max_splits);
-    return s;
 }
 
 talker_status ensure_persist(talker *t) {
@@ -559,7 +563,7 @@ talker_status decode_persistent(talker *t, const float *emb, int B, float *logit
     p.sync = t->d_sync;
     p.status = t->d_status;
     p.trace = t->trace;
-    const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t));
+    const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t), t->G, p.splits);
     TRY_CUDA(launch_persistent(t->w_bf16, t->hd, R, p, t->n_sm, smem, t->st));
     t->launches += 1;
     for (int b = 0; b < B; ++b) t->len[b] += 1;
