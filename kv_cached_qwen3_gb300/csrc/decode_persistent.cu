@@ -77,8 +77,8 @@ __device__ __forceinline__ void ring_wait(uint64_t *bar, uint32_t parity, const 
     if (mbar_try_wait(bar, parity)) return;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return;
-        if ((it & 255) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, 20000)) return;
+        if ((it & 3) == 0) {
             if (*c.abort_s || ld_volatile(c.abort_g)) {
                 *c.abort_s = 1;
                 return;
