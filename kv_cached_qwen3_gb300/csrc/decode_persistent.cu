@@ -75,7 +75,7 @@ __device__ __forceinline__ void raise_abort(const Ctx &c) {
 __device__ __forceinline__ void ring_wait(uint64_t *bar, uint32_t parity, const Ctx &c) {
     if (*c.abort_s) return;
     if (mbar_try_wait(bar, parity)) return;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_sleep(bar, parity, 20000)) return;
         if ((it & 3) == 0) {
@@ -83,7 +83,7 @@ __device__ __forceinline__ void ring_wait(uint64_t *bar, uint32_t parity, const 
                 *c.abort_s = 1;
                 return;
             }
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (clock64() - t0 > kWaitLimitCycles) {
                 raise_abort(c);
                 return;
             }
@@ -95,7 +95,7 @@ __device__ __forceinline__ void ring_wait(uint64_t *bar, uint32_t parity, const 
 __device__ __forceinline__ void spin_geq(const int *ctr, int target, const Ctx &c) {
     if (*c.abort_s) return;
     if (ld_acquire(ctr) >= target) return;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (ld_acquire(ctr) >= target) return;
         if ((it & 63) == 0) {
@@ -103,7 +103,7 @@ __device__ __forceinline__ void spin_geq(const int *ctr, int target, const Ctx &
                 *c.abort_s = 1;
                 return;
             }
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (clock64() - t0 > kWaitLimitCycles) {
                 raise_abort(c);
                 return;
             }
@@ -128,7 +128,9 @@ struct Span {
 };
 // Contiguous, balanced share of N units for CTA `cta` out of P.
 __device__ __forceinline__ Span cta_span(int N, int cta, int P) {
-    const int a = (int)((long long)N * cta / P), b = (int)((long long)N * (cta + 1) / P);
+    // N * P < 2^32 for every matrix here (checked on the host); 32-bit division only
+    const int a = (int)((unsigned)N * (unsigned)cta / (unsigned)P);
+    const int b = (int)((unsigned)N * (unsigned)(cta + 1) / (unsigned)P);
     return {a, b - a};
 }
 
@@ -139,6 +141,109 @@ using LayerW = PersistLayer;
 
 namespace talker_k {
 namespace pk {
+
+// ---- chunk geometry shared by the producer and the consumers
+constexpr int SEG = 1024;   // K elements one warp covers with its register copy of the activations
+__device__ __forceinline__ int nseg_of(int K) { return (K + SEG - 1) / SEG; }
+// Units per ring chunk: as many as fit a slot; with one row (R = 1) rounded down to a
+// multiple of the warps that share a K segment, so the units spread evenly over the warps.
+template <int R>
+__device__ __forceinline__ int units_per_chunk(size_t unit_bytes, int K) {
+    int u = max(1, (int)(SLOT / unit_bytes));
+    if (R == 1) {
+        const int ngrp = NCW / nseg_of(K);
+        if (u >= ngrp) u = (u / ngrp) * ngrp;
+    }
+    return u;
+}
+
+// One warp's activation registers for its K segment (R = 1): vector i of the lane is
+// v = seg * SEG / EPV + lane + 32 i, holding EPV floats.
+template <int EPV>
+struct ActRegs {
+    static constexpr int NV = SEG / EPV / 32;
+    float a[NV][EPV];
+};
+
+template <int EPV>
+__device__ __forceinline__ void load_act_regs(ActRegs<EPV> &ar, uint32_t act_s, int K, int seg, int lane) {
+    const int nvec = K / EPV;
+#pragma unroll
+    for (int i = 0; i < ActRegs<EPV>::NV; ++i) {
+        const int v = seg * (SEG / EPV) + lane + 32 * i;
+        if (v < nvec) {
+            const uint32_t a0 = act_s + (uint32_t)v * 16u;
+            const float4 x0 = lds_f4(a0);
+            ar.a[i][0] = x0.x; ar.a[i][1] = x0.y; ar.a[i][2] = x0.z; ar.a[i][3] = x0.w;
+            if (EPV == 8) {
+                const float4 x1 = lds_f4(a0 + (uint32_t)(K >> 1) * 4u);
+                ar.a[i][EPV > 4 ? 4 : 0] = x1.x; ar.a[i][EPV > 5 ? 5 : 0] = x1.y;
+                ar.a[i][EPV > 6 ? 6 : 0] = x1.z; ar.a[i][EPV > 7 ? 7 : 0] = x1.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) ar.a[i][e] = 0.f;
+        }
+    }
+}
+
+// R = 1 chunk dot products from the register activations: warp w covers segment
+// w % nseg of units w / nseg, w / nseg + ngrp, ...; results in part[j * nseg + seg][u].
+template <typename WT, int NU>
+__device__ __forceinline__ void dots_r1(uint32_t w_s, int n, int K, const ActRegs<Elem<WT>::kPerVec> &ar,
+                                        float (*part)[2], int warp, int lane) {
+    constexpr int EPV = Elem<WT>::kPerVec;
+    const int nseg = nseg_of(K), ngrp = NCW / nseg;
+    const int seg = warp % nseg, grp = warp / nseg;
+    if (grp >= ngrp) return;
+    const int nvec = K / EPV;
+    const uint32_t row_bytes = (uint32_t)K * sizeof(WT);
+    for (int j = grp; j < n; j += ngrp) {
+        float acc[NU][2];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) acc[u][0] = acc[u][1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < ActRegs<EPV>::NV; ++i) {
+            const int v = seg * (SEG / EPV) + lane + 32 * i;
+            if (v < nvec) {
+#pragma unroll
+                for (int u = 0; u < NU; ++u) {
+                    const uint4 q = lds_u4(w_s + ((uint32_t)j * NU + u) * row_bytes + (uint32_t)v * 16u);
+                    float s = acc[u][i & 1];
+                    if (EPV == 8) {
+                        s = fmaf(bf16lo(q.x), ar.a[i][0], s);
+                        s = fmaf(bf16hi(q.x), ar.a[i][1], s);
+                        s = fmaf(bf16lo(q.y), ar.a[i][2], s);
+                        s = fmaf(bf16hi(q.y), ar.a[i][3], s);
+                        s = fmaf(bf16lo(q.z), ar.a[i][EPV > 4 ? 4 : 0], s);
+                        s = fmaf(bf16hi(q.z), ar.a[i][EPV > 5 ? 5 : 0], s);
+                        s = fmaf(bf16lo(q.w), ar.a[i][EPV > 6 ? 6 : 0], s);
+                        s = fmaf(bf16hi(q.w), ar.a[i][EPV > 7 ? 7 : 0], s);
+                    } else {
+                        s = fmaf(__uint_as_float(q.x), ar.a[i][0], s);
+                        s = fmaf(__uint_as_float(q.y), ar.a[i][1], s);
+                        s = fmaf(__uint_as_float(q.z), ar.a[i][2], s);
+                        s = fmaf(__uint_as_float(q.w), ar.a[i][3], s);
+                    }
+                    acc[u][i & 1] = s;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            const float t = warp_sum(acc[u][0] + acc[u][1]);
+            if (lane == 0) part[j * nseg + seg][u] = t;
+        }
+    }
+}
+
+__device__ __forceinline__ float unit_sum_r1(const float (*part)[2], int K, int j, int u) {
+    const int nseg = nseg_of(K);
+    float t = 0.f;
+    for (int q = 0; q < nseg; ++q) t += part[j * nseg + q][u];
+    return t;
+}
+
 
 // Attention work of one CTA: query row r (stream r), KV group g, split `split`
 // of S over the pages [0, npages) of positions [0, pos].
@@ -169,7 +274,7 @@ __device__ __forceinline__ AttnWork attn_work(const PersistParams &p, int cta, i
 
 // The producer lane: streams the CTA's schedule into the ring, in exactly the
 // order the consumers read it.
-template <typename WT, typename KT, int HD>
+template <typename WT, typename KT, int HD, int R>
 __device__ __noinline__ void producer(const PersistParams &p, unsigned char *ring, uint64_t *full, uint64_t *empty, const Ctx &c,
                          const AttnWork &aw) {
     const int P = gridDim.x, cta = blockIdx.x;
@@ -180,8 +285,6 @@ __device__ __noinline__ void producer(const PersistParams &p, unsigned char *rin
         const int slot = k % NS;
         const uint32_t use = k / NS;
         if (use > 0) ring_wait(&empty[slot], (use - 1) & 1, c);
-        if (p.trace != nullptr && k < (uint32_t)kTraceChunks)
-            p.trace[(size_t)blockIdx.x * kTraceSlots + kTraceProducer + k] = globaltimer_ns();
         if (!*c.abort_s) {
             unsigned char *dst = ring + (size_t)slot * SLOT;
             mbar_arrive_expect_tx(&full[slot], b1 + b2);
@@ -190,9 +293,9 @@ __device__ __noinline__ void producer(const PersistParams &p, unsigned char *rin
         }
         ++k;
     };
-    auto stream_rows = [&](const void *W, int N, size_t unit_bytes) {
+    auto stream_rows = [&](const void *W, int N, size_t unit_bytes, int K) {
         const Span s = cta_span(N, cta, P);
-        const int upc = max(1, (int)(SLOT / unit_bytes));
+        const int upc = units_per_chunk<R>(unit_bytes, K);
         for (int u = s.u0; u < s.u0 + s.n; u += upc) {
             const int n = min(upc, s.u0 + s.n - u);
             issue(static_cast<const char *>(W) + (size_t)u * unit_bytes, (uint32_t)(n * unit_bytes), nullptr, 0);
@@ -203,7 +306,7 @@ __device__ __noinline__ void producer(const PersistParams &p, unsigned char *rin
     const KT *vpool = static_cast<const KT *>(p.cache.v);
     for (int l = 0; l < p.n_layers; ++l) {
         const LayerW &L = p.layers[l];
-        stream_rows(L.qkv, qkv_n, (size_t)p.H * wsz);
+        stream_rows(L.qkv, qkv_n, (size_t)p.H * wsz, p.H);
         if (aw.has) {
             const int *ptab = p.cache.page_table + (size_t)aw.r * p.cache.pages_per_stream;
             const size_t head_off = (size_t)(l * p.cache.n_kv + aw.g) * kPage * HD;
@@ -212,11 +315,11 @@ __device__ __noinline__ void producer(const PersistParams &p, unsigned char *rin
                 issue(kpool + off, tile, vpool + off, tile);
             }
         }
-        stream_rows(L.o, p.H, (size_t)p.nq * p.hd * wsz);
-        stream_rows(L.gu, p.I, (size_t)2 * p.H * wsz);
-        stream_rows(L.down, p.H, (size_t)p.I * wsz);
+        stream_rows(L.o, p.H, (size_t)p.nq * p.hd * wsz, p.nq * p.hd);
+        stream_rows(L.gu, p.I, (size_t)2 * p.H * wsz, p.H);
+        stream_rows(L.down, p.H, (size_t)p.I * wsz, p.I);
     }
-    stream_rows(p.head, p.V, (size_t)p.H * wsz);
+    stream_rows(p.head, p.V, (size_t)p.H * wsz, p.H);
     // Let the last copies land before the CTA may exit.
     for (uint32_t j = (k > (uint32_t)NS ? k - NS : 0); j < k; ++j) ring_wait(&full[j % NS], (j / NS) & 1, c);
 }
@@ -229,7 +332,6 @@ struct Ring {
     unsigned long long *trace;   // this CTA's trace row (consumer thread 0 only) or null
     __device__ __forceinline__ const unsigned char *acquire(const Ctx &c) {
         ring_wait(&full[k % NS], (k / NS) & 1, c);
-        if (trace != nullptr && k < (uint32_t)kTraceChunks) trace[kTraceAcquire + k] = globaltimer_ns();
         return base + (size_t)(k % NS) * SLOT;
     }
     // Every consumer warp arrives once per slot (the empty barrier counts NCW arrivals).
@@ -372,16 +474,23 @@ constexpr int UMAX = 64;   // weight units per ring chunk the partial buffer hol
 // part[slot][R * NU] (slot = unit when n >= NCW, else warp); combine them with
 // unit_sum after a consumer barrier.
 template <typename WT, int R, int NU>
-__device__ __noinline__ void chunk_dots(const unsigned char *w, int n, int K, const float *act, int rows,
-                                           float (*part)[R * 2], int warp, int lane) {
+__device__ __noinline__ void chunk_dots(uint32_t w_s, int n, int K, uint32_t act_s, int rows, float (*part)[R * 2],
+                                        int warp, int lane) {
     constexpr int EPV = Elem<WT>::kPerVec;
     const int nvec = K / EPV;
-    const size_t row_bytes = (size_t)K * sizeof(WT);
+    const uint32_t row_bytes = (uint32_t)K * sizeof(WT);
+    const uint32_t plane1 = (uint32_t)(K >> 1) * 4u;   // byte offset of the second act plane (bf16 layout)
     const int wpr = (n >= NCW) ? 1 : NCW / n;
     for (int job = warp; job < ((n >= NCW) ? n : n * wpr); job += NCW) {
-        const int j = job / wpr, seg = job - j * wpr;
-        const int v0 = (int)((long long)nvec * seg / wpr), v1 = (int)((long long)nvec * (seg + 1) / wpr);
-        const unsigned char *wj = w + (size_t)j * NU * row_bytes;
+        // (32-bit arithmetic only: a 64-bit division here costs more than the dot product)
+        int j = job, v0 = 0, v1 = nvec;
+        if (wpr > 1) {
+            j = (int)((unsigned)job / (unsigned)wpr);
+            const unsigned seg = (unsigned)(job - j * wpr);
+            v0 = (int)((unsigned)nvec * seg / (unsigned)wpr);
+            v1 = (int)((unsigned)nvec * (seg + 1) / (unsigned)wpr);
+        }
+        const uint32_t wj = w_s + (uint32_t)j * NU * row_bytes;
         float a0[NU][R], a1[NU][R];
 #pragma unroll
         for (int u = 0; u < NU; ++u)
@@ -390,13 +499,14 @@ __device__ __noinline__ void chunk_dots(const unsigned char *w, int n, int K, co
         auto fma_vec = [&](int v, float (&acc)[NU][R]) {
             uint4 wv[NU];
 #pragma unroll
-            for (int u = 0; u < NU; ++u) wv[u] = *reinterpret_cast<const uint4 *>(wj + u * row_bytes + (size_t)v * 16);
+            for (int u = 0; u < NU; ++u) wv[u] = lds_u4(wj + u * row_bytes + (uint32_t)v * 16u);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 if (r < rows) {
+                    const uint32_t ar = act_s + (uint32_t)(r * K) * 4u + (uint32_t)v * 16u;
                     if (EPV == 8) {
-                        const float4 x0 = *reinterpret_cast<const float4 *>(act + r * K + v * 4);
-                        const float4 x1 = *reinterpret_cast<const float4 *>(act + r * K + (K >> 1) + v * 4);
+                        const float4 x0 = lds_f4(ar);
+                        const float4 x1 = lds_f4(ar + plane1);
 #pragma unroll
                         for (int u = 0; u < NU; ++u) {
                             const uint4 q = wv[u];
@@ -412,7 +522,7 @@ __device__ __noinline__ void chunk_dots(const unsigned char *w, int n, int K, co
                             acc[u][r] = s;
                         }
                     } else {
-                        const float4 x0 = *reinterpret_cast<const float4 *>(act + r * K + v * 4);
+                        const float4 x0 = lds_f4(ar);
 #pragma unroll
                         for (int u = 0; u < NU; ++u) {
                             const uint4 q = wv[u];
@@ -442,6 +552,7 @@ __device__ __noinline__ void chunk_dots(const unsigned char *w, int n, int K, co
             }
     }
 }
+
 
 // Sum of the warp partials of unit j, row r, sub-row u (after a consumer barrier).
 template <int R, int NU>
@@ -482,7 +593,7 @@ __device__ __forceinline__ float ll_val(unsigned long long w) { return __uint_as
 __device__ __noinline__ unsigned long long repoll_ll(const unsigned long long *p, uint32_t f, const Ctx &c) {
     unsigned long long w = ld_ll(p);
     if (ll_flag(w) == f || *c.abort_s) return w;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         w = ld_ll(p);
         if (ll_flag(w) == f) return w;
@@ -491,7 +602,7 @@ __device__ __noinline__ unsigned long long repoll_ll(const unsigned long long *p
                 *c.abort_s = 1;
                 return w;
             }
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (clock64() - t0 > kWaitLimitCycles) {
                 raise_abort(c);
                 return w;
             }
@@ -686,7 +797,7 @@ __device__ __noinline__ void attn_phase(const PersistParams &p, const LayerW &L,
 #pragma unroll
             for (int o = 0; o < NO; ++o) o_acc[o] = 0.f;
             cbar();
-            if (trace) trace[tb + 3] = globaltimer_ns();
+            if (trace) trace[tb + 3] = clock64();
             for (int pg = aw.pb; pg < aw.pe; ++pg) {
                 KT *Ks = reinterpret_cast<KT *>(const_cast<unsigned char *>(rc.acquire(c)));
                 KT *Vs = Ks + kPage * HD;
@@ -873,7 +984,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
     __shared__ int bi_s[NCW][R];
     __shared__ int curlen_s[R];
     __shared__ int abort_sh, flag_s;
-    __shared__ float part_s[2][UMAX][R * 2];
+    __shared__ float part_raw[2][512];   // per-chunk warp partials, double buffered
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, cta = blockIdx.x;
@@ -903,18 +1014,22 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
     const AttnWork aw = attn_work(p, cta, P, curlen_s);
 
     if (warp == NCW) {
-        if (lane == 0) producer<WT, KT, HD>(p, ring, full, empty, c, aw);
+        if (lane == 0) producer<WT, KT, HD, R>(p, ring, full, empty, c, aw);
         return;
     }
 
     // ------------------------------------------------------------------ consumers
     const int ctid = tid;
     unsigned long long *trace = (p.trace != nullptr && ctid == 0) ? p.trace + (size_t)cta * kTraceSlots : nullptr;
+    if (trace) {   // clock64 stamps; this pair aligns them across CTAs
+        trace[kTraceSlots - 2] = globaltimer_ns();
+        trace[kTraceSlots - 1] = clock64();
+    }
     Ring rc{ring, full, empty, 0, trace};
     int pb = 0;   // which half of part_s the next chunk writes
 #define TR(slot)                                      \
     do {                                              \
-        if (trace) trace[(slot)] = globaltimer_ns();  \
+        if (trace) trace[(slot)] = clock64();         \
     } while (0)
     const Span own = cta_span(H, cta, P);           // residual rows this CTA updates (o_proj and down)
     for (int i = ctid; i < rows * own.n; i += NCT) {
@@ -939,15 +1054,24 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
         {
             const uint32_t f = flag_of(p.flag_base, l, FL_RAW);
             const Span s = sq;
-            const int upc = max(1, (int)(SLOT / (H * WSZ)));
+            const int Kp = H;
+            const int upc = units_per_chunk<R>((size_t)H * WSZ, Kp);
+            ActRegs<EPV> ar;
+            if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
             for (int u = s.u0; u < s.u0 + s.n; u += upc) {
                 const int n = min(upc, s.u0 + s.n - u);
-                chunk_dots<WT, R, 1>(rc.acquire(c), n, H, act, rows, part_s[pb], warp, lane);
+                const uint32_t wch = smem_u32(rc.acquire(c));
+                if (R == 1)
+                    dots_r1<WT, 1>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
+                else
+                    chunk_dots<WT, R, 1>(wch, n, Kp, smem_u32(act), rows,
+                                            reinterpret_cast<float (*)[R * 2]>(part_raw[pb]), warp, lane);
                 rc.release(lane);
                 cbar();
                 if (ctid < n)
-                    for (int r = 0; r < rows; ++r)
-                        st_ll(p.raw_ll + (size_t)r * qkv_n + u + ctid, unit_sum<R, 1>(part_s[pb], n, ctid, r, 0), f);
+                    for (int r = 0; r < rows; ++r) {
+                        st_ll(p.raw_ll + (size_t)r * qkv_n + u + ctid, ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 1>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0)), f);
+                    }
                 pb ^= 1;
             }
         }
@@ -964,16 +1088,25 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
         TR(tb + 6);
         {
             const uint32_t f = flag_of(p.flag_base, l, FL_X1);
-            const int upc = max(1, (int)(SLOT / (qd * WSZ)));
-            for (int u = own.u0; u < own.u0 + own.n; u += upc) {
-                const int n = min(upc, own.u0 + own.n - u);
-                chunk_dots<WT, R, 1>(rc.acquire(c), n, qd, act, rows, part_s[pb], warp, lane);
+            const Span s = own;
+            const int Kp = qd;
+            const int upc = units_per_chunk<R>((size_t)qd * WSZ, Kp);
+            ActRegs<EPV> ar;
+            if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
+            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
+                const int n = min(upc, s.u0 + s.n - u);
+                const uint32_t wch = smem_u32(rc.acquire(c));
+                if (R == 1)
+                    dots_r1<WT, 1>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
+                else
+                    chunk_dots<WT, R, 1>(wch, n, Kp, smem_u32(act), rows,
+                                            reinterpret_cast<float (*)[R * 2]>(part_raw[pb]), warp, lane);
                 rc.release(lane);
                 cbar();
                 if (ctid < n)
                     for (int r = 0; r < rows; ++r) {
                         const int jj = u + ctid - own.u0;
-                        const float x1 = xown[r][jj] + unit_sum<R, 1>(part_s[pb], n, ctid, r, 0);
+                        const float x1 = xown[r][jj] + ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 1>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0));
                         xown[r][jj] = x1;
                         st_ll(p.x_ll + (size_t)r * H + u + ctid, x1, f);
                     }
@@ -991,17 +1124,25 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
         {
             const uint32_t f = flag_of(p.flag_base, l, FL_ACT);
             const Span s = sg;
-            const int upc = max(1, (int)(SLOT / (2 * H * WSZ)));
+            const int Kp = H;
+            const int upc = units_per_chunk<R>((size_t)2 * H * WSZ, Kp);
+            ActRegs<EPV> ar;
+            if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
             for (int u = s.u0; u < s.u0 + s.n; u += upc) {
                 const int n = min(upc, s.u0 + s.n - u);
-                chunk_dots<WT, R, 2>(rc.acquire(c), n, H, act, rows, part_s[pb], warp, lane);
+                const uint32_t wch = smem_u32(rc.acquire(c));
+                if (R == 1)
+                    dots_r1<WT, 2>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
+                else
+                    chunk_dots<WT, R, 2>(wch, n, Kp, smem_u32(act), rows,
+                                            reinterpret_cast<float (*)[R * 2]>(part_raw[pb]), warp, lane);
                 rc.release(lane);
                 cbar();
                 if (ctid < n)
                     for (int r = 0; r < rows; ++r) {
-                        const float gt = unit_sum<R, 2>(part_s[pb], n, ctid, r, 0);
-                        const float up = unit_sum<R, 2>(part_s[pb], n, ctid, r, 1);
-                        st_ll(p.act_ll + (size_t)r * p.I + u + ctid, silu_f(gt) * up, f);
+                        const float gt = ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 2>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0));
+                        const float upv = ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 1) : unit_sum<R, 2>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 1));
+                        st_ll(p.act_ll + (size_t)r * p.I + u + ctid, silu_f(gt) * upv, f);
                     }
                 pb ^= 1;
             }
@@ -1015,16 +1156,25 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
         TR(tb + 12);
         {
             const uint32_t f = flag_of(p.flag_base, l, FL_X2);
-            const int upc = max(1, (int)(SLOT / (p.I * WSZ)));
-            for (int u = own.u0; u < own.u0 + own.n; u += upc) {
-                const int n = min(upc, own.u0 + own.n - u);
-                chunk_dots<WT, R, 1>(rc.acquire(c), n, p.I, act, rows, part_s[pb], warp, lane);
+            const Span s = own;
+            const int Kp = p.I;
+            const int upc = units_per_chunk<R>((size_t)p.I * WSZ, Kp);
+            ActRegs<EPV> ar;
+            if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
+            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
+                const int n = min(upc, s.u0 + s.n - u);
+                const uint32_t wch = smem_u32(rc.acquire(c));
+                if (R == 1)
+                    dots_r1<WT, 1>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
+                else
+                    chunk_dots<WT, R, 1>(wch, n, Kp, smem_u32(act), rows,
+                                            reinterpret_cast<float (*)[R * 2]>(part_raw[pb]), warp, lane);
                 rc.release(lane);
                 cbar();
                 if (ctid < n)
                     for (int r = 0; r < rows; ++r) {
                         const int jj = u + ctid - own.u0;
-                        const float x2 = xown[r][jj] + unit_sum<R, 1>(part_s[pb], n, ctid, r, 0);
+                        const float x2 = xown[r][jj] + ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 1>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0));
                         xown[r][jj] = x2;
                         st_ll(p.x_ll + (size_t)r * H + u + ctid, x2, f);
                     }
@@ -1053,17 +1203,25 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
     }
     {
         const Span s = cta_span(p.V, cta, P);
-        const int upc = max(1, (int)(SLOT / (H * WSZ)));
+        const int Kp = H;
+        const int upc = units_per_chunk<R>((size_t)H * WSZ, Kp);
+        ActRegs<EPV> ar;
+        if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
         for (int u = s.u0; u < s.u0 + s.n; u += upc) {
             const int n = min(upc, s.u0 + s.n - u);
-            chunk_dots<WT, R, 1>(rc.acquire(c), n, H, act, rows, part_s[pb], warp, lane);
+            const uint32_t wch = smem_u32(rc.acquire(c));
+            if (R == 1)
+                dots_r1<WT, 1>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
+            else
+                chunk_dots<WT, R, 1>(wch, n, Kp, smem_u32(act), rows, reinterpret_cast<float (*)[R * 2]>(part_raw[pb]),
+                                     warp, lane);
             rc.release(lane);
             cbar();
             if (ctid < n) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (r < rows) {
-                        const float v = unit_sum<R, 1>(part_s[pb], n, ctid, r, 0);
+                        const float v = ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 1>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0));
                         const int idx = u + ctid;
                         p.logits[(size_t)r * p.V + idx] = v;
                         if (isnan(v)) atomicOr(p.status, ST_NAN_LOGIT);

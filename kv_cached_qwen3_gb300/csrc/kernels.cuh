@@ -125,9 +125,12 @@ struct PersistParams {
 
 // Trace stamps per CTA: [0, 512) consumer phase events (15 per layer + 3 for the head),
 // [512, 1280) time the producer issued ring chunk k, [1280, 2048) time the consumers got chunk k.
-constexpr int kTraceSlots = 2048;
+// [2048, 2816) time chunk k's dot products were done (consumer thread 0), [2816, 3584) its epilogue.
+constexpr int kTraceSlots = 4096;
 constexpr int kTraceProducer = 512;
 constexpr int kTraceAcquire = 1280;
+constexpr int kTraceDots = 2048;
+constexpr int kTraceEpi = 2816;
 constexpr int kTraceChunks = 768;
 constexpr int kTracePerLayer = 15;
 

@@ -482,6 +482,8 @@ bool persist_usable(talker *t, int B) {
         (size_t)t->I * wsz > slot || (size_t)2 * 64 * t->hd * t->kvsz > slot)
         return false;
     if (kmax_of(t) > 3072 || (t->H + t->n_sm - 1) / t->n_sm > 64 || t->G > 8) return false;
+    // 32-bit span arithmetic in the kernel: every (units x grid) product below 2^32
+    if ((uint64_t)std::max(std::max(t->qkv_n, t->V), t->I) * (uint64_t)(t->n_sm + 1) >= (1ull << 32)) return false;
     // shared memory is largest at the smallest B of the row template (most attention splits)
     const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t), t->G, persist_splits(t, R == 1 ? 1 : 2));
     if (smem > 227 * 1024 - 8 * 1024) return false;
