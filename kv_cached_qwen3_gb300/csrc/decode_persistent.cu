@@ -590,14 +590,19 @@ __device__ __forceinline__ uint32_t ll_flag(unsigned long long w) { return (uint
 __device__ __forceinline__ float ll_val(unsigned long long w) { return __uint_as_float((uint32_t)w); }
 
 // Re-read one word until its flag is f (bounded; returns at once after an abort).
-__device__ __noinline__ unsigned long long repoll_ll(const unsigned long long *p, uint32_t f, const Ctx &c) {
+// Sleeps between reads, so waiting threads leave the issue slots and the L1 to the
+// warps that are computing.
+__device__ __forceinline__ unsigned long long repoll_ll(const unsigned long long *p, uint32_t f, const Ctx &c) {
     unsigned long long w = ld_ll(p);
     if (ll_flag(w) == f || *c.abort_s) return w;
     const long long t0 = clock64();
+    uint32_t ns = 32;
     for (uint32_t it = 1;; ++it) {
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
         w = ld_ll(p);
         if (ll_flag(w) == f) return w;
-        if ((it & 63) == 0) {
+        if ((it & 15) == 0) {
             if (*c.abort_s || ld_volatile(c.abort_g)) {
                 *c.abort_s = 1;
                 return w;
@@ -706,9 +711,73 @@ __device__ __forceinline__ float pick(const float (&a)[R], int r) {
     return v;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 constexpr int XO = 64;   // owned residual rows per CTA (ceil(H / grid) <= XO)
+constexpr int XO_ROWS = XO;
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+enum : int { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_D = 3, PH_HEAD = 4 };
+
+// One weight phase of the CTA: every ring chunk of its span [s.u0, s.u0 + s.n)
+// (units of NU rows, K inputs) against the staged activations, then the
+// phase's epilogue per (unit, row):
+//   QKV: raw q|k|v words; O, D: residual stream x += result (this CTA's own
+//   rows, kept in xown) and its words; GU: silu(gate) * up words; HEAD: logits
+//   and this thread's running argmax per row.
+template <typename WT, int R, int NU, int KIND>
+__device__ __noinline__ void gemv_phase(const PersistParams &p, Ring &rc, const Ctx &c, float *act, float *part_raw,
+                                        int &pb, Span s, int Kp, uint32_t f, int ctid, float *xown, float *bvr,
+                                        int *bir) {
+    constexpr int EPV = Elem<WT>::kPerVec;
+    const int warp = ctid >> 5, lane = ctid & 31;
+    const int rows = p.rows;
+    const int qkv_n = (p.nq + 2 * p.nkv) * p.hd;
+    const size_t unit_bytes = (size_t)NU * Kp * sizeof(WT);
+    const int upc = units_per_chunk<R>(unit_bytes, Kp);
+    ActRegs<EPV> ar;
+    if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
+    for (int u = s.u0; u < s.u0 + s.n; u += upc) {
+        const int n = min(upc, s.u0 + s.n - u);
+        float *pr = part_raw + pb * 512;
+        const uint32_t wch = smem_u32(rc.acquire(c));
+        if (R == 1)
+            dots_r1<WT, NU>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(pr), warp, lane);
+        else
+            chunk_dots<WT, R, NU>(wch, n, Kp, smem_u32(act), rows, reinterpret_cast<float (*)[R * 2]>(pr), warp, lane);
+        rc.release(lane);
+        cbar();
+        if (ctid < n) {
+            for (int r = 0; r < rows; ++r) {
+                float v[NU];
+#pragma unroll
+                for (int q = 0; q < NU; ++q)
+                    v[q] = (R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(pr), Kp, ctid, q)
+                                    : unit_sum<R, NU>(reinterpret_cast<const float (*)[R * 2]>(pr), n, ctid, r, q);
+                const int idx = u + ctid;
+                if (KIND == PH_QKV) {
+                    st_ll(p.raw_ll + (size_t)r * qkv_n + idx, v[0], f);
+                } else if (KIND == PH_O || KIND == PH_D) {
+                    const int jj = idx - s.u0;
+                    const float x = xown[r * XO_ROWS + jj] + v[0];
+                    xown[r * XO_ROWS + jj] = x;
+                    st_ll(p.x_ll + (size_t)r * p.H + idx, x, f);
+                } else if (KIND == PH_GU) {
+                    st_ll(p.act_ll + (size_t)r * p.I + idx, silu_f(v[0]) * v[NU - 1], f);
+                } else {
+                    p.logits[(size_t)r * p.V + idx] = v[0];
+                    if (isnan(v[0])) atomicOr(p.status, ST_NAN_LOGIT);
+                    else if (v[0] > bvr[r] || (v[0] == bvr[r] && idx < bir[r])) {
+                        bvr[r] = v[0];
+                        bir[r] = idx;
+                    }
+                }
+            }
+        }
+        pb ^= 1;
+    }
+}
+
 
 // One attention work item of one layer: QK-norm + RoPE of this row's q heads
 // and k (v as is) from the raw words, the cache row for later steps (split 0),
@@ -1052,28 +1121,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
         }
         TR(tb + 1);
         {
-            const uint32_t f = flag_of(p.flag_base, l, FL_RAW);
-            const Span s = sq;
-            const int Kp = H;
-            const int upc = units_per_chunk<R>((size_t)H * WSZ, Kp);
-            ActRegs<EPV> ar;
-            if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
-            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-                const int n = min(upc, s.u0 + s.n - u);
-                const uint32_t wch = smem_u32(rc.acquire(c));
-                if (R == 1)
-                    dots_r1<WT, 1>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
-                else
-                    chunk_dots<WT, R, 1>(wch, n, Kp, smem_u32(act), rows,
-                                            reinterpret_cast<float (*)[R * 2]>(part_raw[pb]), warp, lane);
-                rc.release(lane);
-                cbar();
-                if (ctid < n)
-                    for (int r = 0; r < rows; ++r) {
-                        st_ll(p.raw_ll + (size_t)r * qkv_n + u + ctid, ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 1>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0)), f);
-                    }
-                pb ^= 1;
-            }
+            gemv_phase<WT, R, 1, PH_QKV>(p, rc, c, act, &part_raw[0][0], pb, sq, H, flag_of(p.flag_base, l, FL_RAW),
+                                         ctid, &xown[0][0], nullptr, nullptr);
         }
         TR(tb + 2);
         // ---- attention of (row r, KV group g, split) over [0, pos]
@@ -1087,31 +1136,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
             stage_ll<EPV, R>(act, p.o_ll, qd, qd, rows, flag_of(p.flag_base, l, FL_O), nullptr, 0.f, red, ctid, c);
         TR(tb + 6);
         {
-            const uint32_t f = flag_of(p.flag_base, l, FL_X1);
-            const Span s = own;
-            const int Kp = qd;
-            const int upc = units_per_chunk<R>((size_t)qd * WSZ, Kp);
-            ActRegs<EPV> ar;
-            if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
-            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-                const int n = min(upc, s.u0 + s.n - u);
-                const uint32_t wch = smem_u32(rc.acquire(c));
-                if (R == 1)
-                    dots_r1<WT, 1>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
-                else
-                    chunk_dots<WT, R, 1>(wch, n, Kp, smem_u32(act), rows,
-                                            reinterpret_cast<float (*)[R * 2]>(part_raw[pb]), warp, lane);
-                rc.release(lane);
-                cbar();
-                if (ctid < n)
-                    for (int r = 0; r < rows; ++r) {
-                        const int jj = u + ctid - own.u0;
-                        const float x1 = xown[r][jj] + ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 1>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0));
-                        xown[r][jj] = x1;
-                        st_ll(p.x_ll + (size_t)r * H + u + ctid, x1, f);
-                    }
-                pb ^= 1;
-            }
+            gemv_phase<WT, R, 1, PH_O>(p, rc, c, act, &part_raw[0][0], pb, own, qd, flag_of(p.flag_base, l, FL_X1),
+                                       ctid, &xown[0][0], nullptr, nullptr);
         }
         TR(tb + 7);
 
@@ -1122,30 +1148,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
                              c);
         TR(tb + 9);
         {
-            const uint32_t f = flag_of(p.flag_base, l, FL_ACT);
-            const Span s = sg;
-            const int Kp = H;
-            const int upc = units_per_chunk<R>((size_t)2 * H * WSZ, Kp);
-            ActRegs<EPV> ar;
-            if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
-            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-                const int n = min(upc, s.u0 + s.n - u);
-                const uint32_t wch = smem_u32(rc.acquire(c));
-                if (R == 1)
-                    dots_r1<WT, 2>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
-                else
-                    chunk_dots<WT, R, 2>(wch, n, Kp, smem_u32(act), rows,
-                                            reinterpret_cast<float (*)[R * 2]>(part_raw[pb]), warp, lane);
-                rc.release(lane);
-                cbar();
-                if (ctid < n)
-                    for (int r = 0; r < rows; ++r) {
-                        const float gt = ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 2>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0));
-                        const float upv = ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 1) : unit_sum<R, 2>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 1));
-                        st_ll(p.act_ll + (size_t)r * p.I + u + ctid, silu_f(gt) * upv, f);
-                    }
-                pb ^= 1;
-            }
+            gemv_phase<WT, R, 2, PH_GU>(p, rc, c, act, &part_raw[0][0], pb, sg, H, flag_of(p.flag_base, l, FL_ACT),
+                                        ctid, &xown[0][0], nullptr, nullptr);
         }
         TR(tb + 10);
 
@@ -1155,31 +1159,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
                              c);
         TR(tb + 12);
         {
-            const uint32_t f = flag_of(p.flag_base, l, FL_X2);
-            const Span s = own;
-            const int Kp = p.I;
-            const int upc = units_per_chunk<R>((size_t)p.I * WSZ, Kp);
-            ActRegs<EPV> ar;
-            if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
-            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-                const int n = min(upc, s.u0 + s.n - u);
-                const uint32_t wch = smem_u32(rc.acquire(c));
-                if (R == 1)
-                    dots_r1<WT, 1>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
-                else
-                    chunk_dots<WT, R, 1>(wch, n, Kp, smem_u32(act), rows,
-                                            reinterpret_cast<float (*)[R * 2]>(part_raw[pb]), warp, lane);
-                rc.release(lane);
-                cbar();
-                if (ctid < n)
-                    for (int r = 0; r < rows; ++r) {
-                        const int jj = u + ctid - own.u0;
-                        const float x2 = xown[r][jj] + ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 1>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0));
-                        xown[r][jj] = x2;
-                        st_ll(p.x_ll + (size_t)r * H + u + ctid, x2, f);
-                    }
-                pb ^= 1;
-            }
+            gemv_phase<WT, R, 1, PH_D>(p, rc, c, act, &part_raw[0][0], pb, own, p.I, flag_of(p.flag_base, l, FL_X2),
+                                       ctid, &xown[0][0], nullptr, nullptr);
         }
         TR(tb + 13);
     }
@@ -1202,38 +1183,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
         bir[r] = 0x7fffffff;
     }
     {
-        const Span s = cta_span(p.V, cta, P);
-        const int Kp = H;
-        const int upc = units_per_chunk<R>((size_t)H * WSZ, Kp);
-        ActRegs<EPV> ar;
-        if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
-        for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-            const int n = min(upc, s.u0 + s.n - u);
-            const uint32_t wch = smem_u32(rc.acquire(c));
-            if (R == 1)
-                dots_r1<WT, 1>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(part_raw[pb]), warp, lane);
-            else
-                chunk_dots<WT, R, 1>(wch, n, Kp, smem_u32(act), rows, reinterpret_cast<float (*)[R * 2]>(part_raw[pb]),
-                                     warp, lane);
-            rc.release(lane);
-            cbar();
-            if (ctid < n) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    if (r < rows) {
-                        const float v = ((R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(part_raw[pb]), Kp, ctid, 0) : unit_sum<R, 1>(reinterpret_cast<const float (*)[R * 2]>(part_raw[pb]), n, ctid, r, 0));
-                        const int idx = u + ctid;
-                        p.logits[(size_t)r * p.V + idx] = v;
-                        if (isnan(v)) atomicOr(p.status, ST_NAN_LOGIT);
-                        else if (v > bvr[r] || (v == bvr[r] && idx < bir[r])) {
-                            bvr[r] = v;
-                            bir[r] = idx;
-                        }
-                    }
-                }
-            }
-            pb ^= 1;
-        }
+        gemv_phase<WT, R, 1, PH_HEAD>(p, rc, c, act, &part_raw[0][0], pb, cta_span(p.V, cta, P), H, 0u, ctid,
+                                      &xown[0][0], bvr, bir);
     }
     // per-warp best of each row (lowest index on ties)
     float bv = -INFINITY;
