@@ -77,8 +77,8 @@ __device__ __forceinline__ void ring_wait(uint64_t *bar, uint32_t parity, const 
     if (mbar_try_wait(bar, parity)) return;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_sleep(bar, parity, 20000)) return;
-        if ((it & 3) == 0) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((it & 255) == 0) {
             if (*c.abort_s || ld_volatile(c.abort_g)) {
                 *c.abort_s = 1;
                 return;
@@ -128,7 +128,8 @@ struct Span {
 };
 // Contiguous, balanced share of N units for CTA `cta` out of P.
 __device__ __forceinline__ Span cta_span(int N, int cta, int P) {
-    // N * P < 2^32 for every matrix here (checked on the host); 32-bit division only
+    // 32-bit division only (a 64-bit division costs hundreds of cycles); N * P < 2^32 is
+    // checked on the host
     const int a = (int)((unsigned)N * (unsigned)cta / (unsigned)P);
     const int b = (int)((unsigned)N * (unsigned)(cta + 1) / (unsigned)P);
     return {a, b - a};
@@ -141,109 +142,6 @@ using LayerW = PersistLayer;
 
 namespace talker_k {
 namespace pk {
-
-// ---- chunk geometry shared by the producer and the consumers
-constexpr int SEG = 1024;   // K elements one warp covers with its register copy of the activations
-__device__ __forceinline__ int nseg_of(int K) { return (K + SEG - 1) / SEG; }
-// Units per ring chunk: as many as fit a slot; with one row (R = 1) rounded down to a
-// multiple of the warps that share a K segment, so the units spread evenly over the warps.
-template <int R>
-__device__ __forceinline__ int units_per_chunk(size_t unit_bytes, int K) {
-    int u = max(1, (int)(SLOT / unit_bytes));
-    if (R == 1) {
-        const int ngrp = NCW / nseg_of(K);
-        if (u >= ngrp) u = (u / ngrp) * ngrp;
-    }
-    return u;
-}
-
-// One warp's activation registers for its K segment (R = 1): vector i of the lane is
-// v = seg * SEG / EPV + lane + 32 i, holding EPV floats.
-template <int EPV>
-struct ActRegs {
-    static constexpr int NV = SEG / EPV / 32;
-    float a[NV][EPV];
-};
-
-template <int EPV>
-__device__ __forceinline__ void load_act_regs(ActRegs<EPV> &ar, uint32_t act_s, int K, int seg, int lane) {
-    const int nvec = K / EPV;
-#pragma unroll
-    for (int i = 0; i < ActRegs<EPV>::NV; ++i) {
-        const int v = seg * (SEG / EPV) + lane + 32 * i;
-        if (v < nvec) {
-            const uint32_t a0 = act_s + (uint32_t)v * 16u;
-            const float4 x0 = lds_f4(a0);
-            ar.a[i][0] = x0.x; ar.a[i][1] = x0.y; ar.a[i][2] = x0.z; ar.a[i][3] = x0.w;
-            if (EPV == 8) {
-                const float4 x1 = lds_f4(a0 + (uint32_t)(K >> 1) * 4u);
-                ar.a[i][EPV > 4 ? 4 : 0] = x1.x; ar.a[i][EPV > 5 ? 5 : 0] = x1.y;
-                ar.a[i][EPV > 6 ? 6 : 0] = x1.z; ar.a[i][EPV > 7 ? 7 : 0] = x1.w;
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) ar.a[i][e] = 0.f;
-        }
-    }
-}
-
-// R = 1 chunk dot products from the register activations: warp w covers segment
-// w % nseg of units w / nseg, w / nseg + ngrp, ...; results in part[j * nseg + seg][u].
-template <typename WT, int NU>
-__device__ __forceinline__ void dots_r1(uint32_t w_s, int n, int K, const ActRegs<Elem<WT>::kPerVec> &ar,
-                                        float (*part)[2], int warp, int lane) {
-    constexpr int EPV = Elem<WT>::kPerVec;
-    const int nseg = nseg_of(K), ngrp = NCW / nseg;
-    const int seg = warp % nseg, grp = warp / nseg;
-    if (grp >= ngrp) return;
-    const int nvec = K / EPV;
-    const uint32_t row_bytes = (uint32_t)K * sizeof(WT);
-    for (int j = grp; j < n; j += ngrp) {
-        float acc[NU][2];
-#pragma unroll
-        for (int u = 0; u < NU; ++u) acc[u][0] = acc[u][1] = 0.f;
-#pragma unroll
-        for (int i = 0; i < ActRegs<EPV>::NV; ++i) {
-            const int v = seg * (SEG / EPV) + lane + 32 * i;
-            if (v < nvec) {
-#pragma unroll
-                for (int u = 0; u < NU; ++u) {
-                    const uint4 q = lds_u4(w_s + ((uint32_t)j * NU + u) * row_bytes + (uint32_t)v * 16u);
-                    float s = acc[u][i & 1];
-                    if (EPV == 8) {
-                        s = fmaf(bf16lo(q.x), ar.a[i][0], s);
-                        s = fmaf(bf16hi(q.x), ar.a[i][1], s);
-                        s = fmaf(bf16lo(q.y), ar.a[i][2], s);
-                        s = fmaf(bf16hi(q.y), ar.a[i][3], s);
-                        s = fmaf(bf16lo(q.z), ar.a[i][EPV > 4 ? 4 : 0], s);
-                        s = fmaf(bf16hi(q.z), ar.a[i][EPV > 5 ? 5 : 0], s);
-                        s = fmaf(bf16lo(q.w), ar.a[i][EPV > 6 ? 6 : 0], s);
-                        s = fmaf(bf16hi(q.w), ar.a[i][EPV > 7 ? 7 : 0], s);
-                    } else {
-                        s = fmaf(__uint_as_float(q.x), ar.a[i][0], s);
-                        s = fmaf(__uint_as_float(q.y), ar.a[i][1], s);
-                        s = fmaf(__uint_as_float(q.z), ar.a[i][2], s);
-                        s = fmaf(__uint_as_float(q.w), ar.a[i][3], s);
-                    }
-                    acc[u][i & 1] = s;
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const float t = warp_sum(acc[u][0] + acc[u][1]);
-            if (lane == 0) part[j * nseg + seg][u] = t;
-        }
-    }
-}
-
-__device__ __forceinline__ float unit_sum_r1(const float (*part)[2], int K, int j, int u) {
-    const int nseg = nseg_of(K);
-    float t = 0.f;
-    for (int q = 0; q < nseg; ++q) t += part[j * nseg + q][u];
-    return t;
-}
-
 
 // Attention work of one CTA: query row r (stream r), KV group g, split `split`
 // of S over the pages [0, npages) of positions [0, pos].
@@ -274,8 +172,8 @@ __device__ __forceinline__ AttnWork attn_work(const PersistParams &p, int cta, i
 
 // The producer lane: streams the CTA's schedule into the ring, in exactly the
 // order the consumers read it.
-template <typename WT, typename KT, int HD, int R>
-__device__ __noinline__ void producer(const PersistParams &p, unsigned char *ring, uint64_t *full, uint64_t *empty, const Ctx &c,
+template <typename WT, typename KT, int HD>
+__device__ void producer(const PersistParams &p, unsigned char *ring, uint64_t *full, uint64_t *empty, const Ctx &c,
                          const AttnWork &aw) {
     const int P = gridDim.x, cta = blockIdx.x;
     const size_t wsz = sizeof(WT);
@@ -293,9 +191,9 @@ __device__ __noinline__ void producer(const PersistParams &p, unsigned char *rin
         }
         ++k;
     };
-    auto stream_rows = [&](const void *W, int N, size_t unit_bytes, int K) {
+    auto stream_rows = [&](const void *W, int N, size_t unit_bytes) {
         const Span s = cta_span(N, cta, P);
-        const int upc = units_per_chunk<R>(unit_bytes, K);
+        const int upc = max(1, (int)(SLOT / unit_bytes));
         for (int u = s.u0; u < s.u0 + s.n; u += upc) {
             const int n = min(upc, s.u0 + s.n - u);
             issue(static_cast<const char *>(W) + (size_t)u * unit_bytes, (uint32_t)(n * unit_bytes), nullptr, 0);
@@ -306,7 +204,7 @@ __device__ __noinline__ void producer(const PersistParams &p, unsigned char *rin
     const KT *vpool = static_cast<const KT *>(p.cache.v);
     for (int l = 0; l < p.n_layers; ++l) {
         const LayerW &L = p.layers[l];
-        stream_rows(L.qkv, qkv_n, (size_t)p.H * wsz, p.H);
+        stream_rows(L.qkv, qkv_n, (size_t)p.H * wsz);
         if (aw.has) {
             const int *ptab = p.cache.page_table + (size_t)aw.r * p.cache.pages_per_stream;
             const size_t head_off = (size_t)(l * p.cache.n_kv + aw.g) * kPage * HD;
@@ -315,11 +213,11 @@ __device__ __noinline__ void producer(const PersistParams &p, unsigned char *rin
                 issue(kpool + off, tile, vpool + off, tile);
             }
         }
-        stream_rows(L.o, p.H, (size_t)p.nq * p.hd * wsz, p.nq * p.hd);
-        stream_rows(L.gu, p.I, (size_t)2 * p.H * wsz, p.H);
-        stream_rows(L.down, p.H, (size_t)p.I * wsz, p.I);
+        stream_rows(L.o, p.H, (size_t)p.nq * p.hd * wsz);
+        stream_rows(L.gu, p.I, (size_t)2 * p.H * wsz);
+        stream_rows(L.down, p.H, (size_t)p.I * wsz);
     }
-    stream_rows(p.head, p.V, (size_t)p.H * wsz, p.H);
+    stream_rows(p.head, p.V, (size_t)p.H * wsz);
     // Let the last copies land before the CTA may exit.
     for (uint32_t j = (k > (uint32_t)NS ? k - NS : 0); j < k; ++j) ring_wait(&full[j % NS], (j / NS) & 1, c);
 }
@@ -352,7 +250,7 @@ __device__ __forceinline__ int aidx(int r, int k, int K) {
 // layout of the dot products; with `gain`, apply RMSNorm and the gain
 // (x / sqrt(mean(x^2) + eps) * gain). Ends with a consumer barrier.
 template <int EPV, int R>
-__device__ __noinline__ void stage(float *act, const float *src, int ld, int K, int rows, const float *gain, float eps,
+__device__ void stage(float *act, const float *src, int ld, int K, int rows, const float *gain, float eps,
                       float *red, int ctid) {
     const int K4 = K >> 2;
     const int warp = ctid >> 5, lane = ctid & 31;
@@ -464,112 +362,6 @@ __device__ __forceinline__ void dot_rows(const unsigned char *w, int K, const fl
 namespace talker_k {
 namespace pk {
 
-constexpr int UMAX = 64;   // weight units per ring chunk the partial buffer holds
-
-// Partial dot products of the n weight units (NU rows each, K inputs) of one
-// ring chunk with the staged activation rows, using every consumer warp:
-// with n >= NCW each warp takes whole units; otherwise the NCW / n warps of a
-// unit split its K range. Two accumulators per product and two vectors per
-// iteration keep several shared-memory loads in flight. Warp results go to
-// part[slot][R * NU] (slot = unit when n >= NCW, else warp); combine them with
-// unit_sum after a consumer barrier.
-template <typename WT, int R, int NU>
-__device__ __noinline__ void chunk_dots(uint32_t w_s, int n, int K, uint32_t act_s, int rows, float (*part)[R * 2],
-                                        int warp, int lane) {
-    constexpr int EPV = Elem<WT>::kPerVec;
-    const int nvec = K / EPV;
-    const uint32_t row_bytes = (uint32_t)K * sizeof(WT);
-    const uint32_t plane1 = (uint32_t)(K >> 1) * 4u;   // byte offset of the second act plane (bf16 layout)
-    const int wpr = (n >= NCW) ? 1 : NCW / n;
-    for (int job = warp; job < ((n >= NCW) ? n : n * wpr); job += NCW) {
-        // (32-bit arithmetic only: a 64-bit division here costs more than the dot product)
-        int j = job, v0 = 0, v1 = nvec;
-        if (wpr > 1) {
-            j = (int)((unsigned)job / (unsigned)wpr);
-            const unsigned seg = (unsigned)(job - j * wpr);
-            v0 = (int)((unsigned)nvec * seg / (unsigned)wpr);
-            v1 = (int)((unsigned)nvec * (seg + 1) / (unsigned)wpr);
-        }
-        const uint32_t wj = w_s + (uint32_t)j * NU * row_bytes;
-        float a0[NU][R], a1[NU][R];
-#pragma unroll
-        for (int u = 0; u < NU; ++u)
-#pragma unroll
-            for (int r = 0; r < R; ++r) a0[u][r] = a1[u][r] = 0.f;
-        auto fma_vec = [&](int v, float (&acc)[NU][R]) {
-            uint4 wv[NU];
-#pragma unroll
-            for (int u = 0; u < NU; ++u) wv[u] = lds_u4(wj + u * row_bytes + (uint32_t)v * 16u);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (r < rows) {
-                    const uint32_t ar = act_s + (uint32_t)(r * K) * 4u + (uint32_t)v * 16u;
-                    if (EPV == 8) {
-                        const float4 x0 = lds_f4(ar);
-                        const float4 x1 = lds_f4(ar + plane1);
-#pragma unroll
-                        for (int u = 0; u < NU; ++u) {
-                            const uint4 q = wv[u];
-                            float s = acc[u][r];
-                            s = fmaf(bf16lo(q.x), x0.x, s);
-                            s = fmaf(bf16hi(q.x), x0.y, s);
-                            s = fmaf(bf16lo(q.y), x0.z, s);
-                            s = fmaf(bf16hi(q.y), x0.w, s);
-                            s = fmaf(bf16lo(q.z), x1.x, s);
-                            s = fmaf(bf16hi(q.z), x1.y, s);
-                            s = fmaf(bf16lo(q.w), x1.z, s);
-                            s = fmaf(bf16hi(q.w), x1.w, s);
-                            acc[u][r] = s;
-                        }
-                    } else {
-                        const float4 x0 = lds_f4(ar);
-#pragma unroll
-                        for (int u = 0; u < NU; ++u) {
-                            const uint4 q = wv[u];
-                            float s = acc[u][r];
-                            s = fmaf(__uint_as_float(q.x), x0.x, s);
-                            s = fmaf(__uint_as_float(q.y), x0.y, s);
-                            s = fmaf(__uint_as_float(q.z), x0.z, s);
-                            s = fmaf(__uint_as_float(q.w), x0.w, s);
-                            acc[u][r] = s;
-                        }
-                    }
-                }
-            }
-        };
-        int v = v0 + lane;
-        for (; v + 32 < v1; v += 64) {
-            fma_vec(v, a0);
-            fma_vec(v + 32, a1);
-        }
-        if (v < v1) fma_vec(v, a0);
-#pragma unroll
-        for (int u = 0; u < NU; ++u)
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float t = warp_sum(a0[u][r] + a1[u][r]);
-                if (lane == 0) part[(n >= NCW) ? j : job][r * NU + u] = t;
-            }
-    }
-}
-
-
-// Sum of the warp partials of unit j, row r, sub-row u (after a consumer barrier).
-template <int R, int NU>
-__device__ __forceinline__ float unit_sum(const float (*part)[R * 2], int n, int j, int r, int u) {
-    if (n >= NCW) return part[j][r * NU + u];
-    const int wpr = NCW / n;
-    float t = 0.f;
-    for (int q = 0; q < wpr; ++q) t += part[j * wpr + q][r * NU + u];
-    return t;
-}
-
-}  // namespace pk
-}  // namespace talker_k
-
-namespace talker_k {
-namespace pk {
-
 // ---- flag-carrying words: value in the low 32 bits, flag in the high 32 bits,
 // written with one 8-byte store, so a reader that sees the flag sees the value.
 __device__ __forceinline__ unsigned long long ll_pack(float v, uint32_t f) {
@@ -590,9 +382,9 @@ __device__ __forceinline__ uint32_t ll_flag(unsigned long long w) { return (uint
 __device__ __forceinline__ float ll_val(unsigned long long w) { return __uint_as_float((uint32_t)w); }
 
 // Re-read one word until its flag is f (bounded; returns at once after an abort).
-// Sleeps between reads, so waiting threads leave the issue slots and the L1 to the
-// warps that are computing.
-__device__ __forceinline__ unsigned long long repoll_ll(const unsigned long long *p, uint32_t f, const Ctx &c) {
+// Sleeps between reads so that waiting threads leave issue slots and L1 bandwidth
+// to the warps that are computing.
+__device__ __noinline__ unsigned long long repoll_ll(const unsigned long long *p, uint32_t f, const Ctx &c) {
     unsigned long long w = ld_ll(p);
     if (ll_flag(w) == f || *c.abort_s) return w;
     const long long t0 = clock64();
@@ -627,7 +419,7 @@ constexpr int KCAP = 3072;   // widest activation row the LL staging handles (R 
 // is issued before any flag is checked, so a ready tensor costs one round trip.
 // With `gain`, applies RMSNorm and the gain. Ends with a consumer barrier.
 template <int EPV, int R>
-__device__ __noinline__ void stage_ll(float *act, const unsigned long long *src, int ld, int K, int rows, uint32_t flag,
+__device__ void stage_ll(float *act, const unsigned long long *src, int ld, int K, int rows, uint32_t flag,
                          const float *gain, float eps, float *red, int ctid, const Ctx &c) {
     constexpr int NP = (R * KCAP / 2 + NCT - 1) / NCT;
     const int K2 = K >> 1;
@@ -711,88 +503,106 @@ __device__ __forceinline__ float pick(const float (&a)[R], int r) {
     return v;
 }
 
-
-constexpr int XO = 64;   // owned residual rows per CTA (ceil(H / grid) <= XO)
-constexpr int XO_ROWS = XO;
-
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-enum : int { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_D = 3, PH_HEAD = 4 };
+constexpr int XO = 64;   // owned residual rows per CTA (ceil(H / grid) <= XO)
 
-// One weight phase of the CTA: every ring chunk of its span [s.u0, s.u0 + s.n)
-// (units of NU rows, K inputs) against the staged activations, then the
-// phase's epilogue per (unit, row):
-//   QKV: raw q|k|v words; O, D: residual stream x += result (this CTA's own
-//   rows, kept in xown) and its words; GU: silu(gate) * up words; HEAD: logits
-//   and this thread's running argmax per row.
-template <typename WT, int R, int NU, int KIND>
-__device__ __noinline__ void gemv_phase(const PersistParams &p, Ring &rc, const Ctx &c, float *act, float *part_raw,
-                                        int &pb, Span s, int Kp, uint32_t f, int ctid, float *xown, float *bvr,
-                                        int *bir) {
+template <typename WT, typename KT, int HD, int R>
+__global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams p) {
     constexpr int EPV = Elem<WT>::kPerVec;
-    const int warp = ctid >> 5, lane = ctid & 31;
+    constexpr size_t WSZ = sizeof(WT);
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[NS], empty[NS];
+    __shared__ float red[NCW * R];
+    __shared__ float m_s[MAXG], l_s[MAXG], al_s[MAXG];
+    __shared__ float ml_s[MAXG][kMaxSplits][2];
+    __shared__ float xown[R][XO];
+    __shared__ float bv_s[NCW][R];
+    __shared__ int bi_s[NCW][R];
+    __shared__ int curlen_s[R];
+    __shared__ int abort_sh, flag_s;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = gridDim.x, cta = blockIdx.x;
+    const int H = p.H, half = HD / 2, G = p.G;
+    const int qd = p.nq * HD, qkv_n = (p.nq + 2 * p.nkv) * HD;
+    const int KMAX = max(max(H, qd), p.I);
     const int rows = p.rows;
-    const int qkv_n = (p.nq + 2 * p.nkv) * p.hd;
-    const size_t unit_bytes = (size_t)NU * Kp * sizeof(WT);
-    const int upc = units_per_chunk<R>(unit_bytes, Kp);
-    ActRegs<EPV> ar;
-    if (R == 1 && s.n > 0) load_act_regs<EPV>(ar, smem_u32(act), Kp, warp % nseg_of(Kp), lane);
-    for (int u = s.u0; u < s.u0 + s.n; u += upc) {
-        const int n = min(upc, s.u0 + s.n - u);
-        float *pr = part_raw + pb * 512;
-        const uint32_t wch = smem_u32(rc.acquire(c));
-        if (R == 1)
-            dots_r1<WT, NU>(wch, n, Kp, ar, reinterpret_cast<float (*)[2]>(pr), warp, lane);
-        else
-            chunk_dots<WT, R, NU>(wch, n, Kp, smem_u32(act), rows, reinterpret_cast<float (*)[R * 2]>(pr), warp, lane);
-        rc.release(lane);
-        cbar();
-        if (ctid < n) {
-            for (int r = 0; r < rows; ++r) {
-                float v[NU];
-#pragma unroll
-                for (int q = 0; q < NU; ++q)
-                    v[q] = (R == 1) ? unit_sum_r1(reinterpret_cast<const float (*)[2]>(pr), Kp, ctid, q)
-                                    : unit_sum<R, NU>(reinterpret_cast<const float (*)[R * 2]>(pr), n, ctid, r, q);
-                const int idx = u + ctid;
-                if (KIND == PH_QKV) {
-                    st_ll(p.raw_ll + (size_t)r * qkv_n + idx, v[0], f);
-                } else if (KIND == PH_O || KIND == PH_D) {
-                    const int jj = idx - s.u0;
-                    const float x = xown[r * XO_ROWS + jj] + v[0];
-                    xown[r * XO_ROWS + jj] = x;
-                    st_ll(p.x_ll + (size_t)r * p.H + idx, x, f);
-                } else if (KIND == PH_GU) {
-                    st_ll(p.act_ll + (size_t)r * p.I + idx, silu_f(v[0]) * v[NU - 1], f);
-                } else {
-                    p.logits[(size_t)r * p.V + idx] = v[0];
-                    if (isnan(v[0])) atomicOr(p.status, ST_NAN_LOGIT);
-                    else if (v[0] > bvr[r] || (v[0] == bvr[r] && idx < bir[r])) {
-                        bvr[r] = v[0];
-                        bir[r] = idx;
-                    }
+    unsigned char *ring = smem;
+    float *act = reinterpret_cast<float *>(smem + (size_t)NS * SLOT);
+    float *qs = act + (size_t)R * KMAX;            // [G][HD] scaled q of the attention row
+    float *sc = qs + MAXG * HD;                     // [G][kPage] scores / probabilities
+    KT *knew = reinterpret_cast<KT *>(sc + MAXG * kPage);
+    KT *vnew = knew + HD;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCW);
+        }
+        abort_sh = 0;
+        fence_barrier_init();
+    }
+    if (tid < R) curlen_s[tid] = (tid < rows) ? p.cur_len[tid] : 0;
+    __syncthreads();
+    const Ctx c{reinterpret_cast<volatile int *>(&abort_sh), p.sync + SY_ABORT, p.status};
+    const AttnWork aw = attn_work(p, cta, P, curlen_s);
+
+    if (warp == NCW) {
+        if (lane == 0) producer<WT, KT, HD>(p, ring, full, empty, c, aw);
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    const int ctid = tid;
+    unsigned long long *trace = (p.trace != nullptr && ctid == 0) ? p.trace + (size_t)cta * kTraceSlots : nullptr;
+    if (trace) {   // clock64 stamps; this pair aligns them across CTAs
+        trace[kTraceSlots - 2] = globaltimer_ns();
+        trace[kTraceSlots - 1] = clock64();
+    }
+    Ring rc{ring, full, empty, 0, trace};
+#define TR(slot)                                      \
+    do {                                              \
+        if (trace) trace[(slot)] = clock64();         \
+    } while (0)
+    const Span own = cta_span(H, cta, P);           // residual rows this CTA updates (o_proj and down)
+    for (int i = ctid; i < rows * own.n; i += NCT) {
+        const int r = i / own.n, j = i - r * own.n;
+        xown[r][j] = p.emb[(size_t)r * H + own.u0 + j];
+    }
+
+    for (int l = 0; l < p.n_layers; ++l) {
+        const LayerW &L = p.layers[l];
+        const int tb = l * kTracePerLayer;
+        TR(tb + 0);
+        // ---- RMSNorm -> [Wq;Wk;Wv] -> raw q|k|v words
+        // (A CTA with no rows in a phase skips that phase's input: it would have no
+        // output that orders its reads before the next overwrite of the input words.)
+        const Span sq = cta_span(qkv_n, cta, P);
+        if (sq.n > 0) {
+            if (l == 0) stage<EPV, R>(act, p.emb, H, H, rows, L.in_norm, p.eps, red, ctid);
+            else stage_ll<EPV, R>(act, p.x_ll, H, H, rows, flag_of(p.flag_base, l - 1, FL_X2), L.in_norm, p.eps,
+                                  red, ctid, c);
+        }
+        TR(tb + 1);
+        {
+            const uint32_t f = flag_of(p.flag_base, l, FL_RAW);
+            const Span s = sq;
+            const int upc = max(1, (int)(SLOT / (H * WSZ)));
+            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
+                const int n = min(upc, s.u0 + s.n - u);
+                const unsigned char *w = rc.acquire(c);
+                for (int j = warp; j < n; j += NCW) {
+                    float acc[1][R];
+                    dot_rows<WT, R, 1>(w + (size_t)j * H * WSZ, H, act, rows, acc, lane);
+                    if (lane < rows) st_ll(p.raw_ll + (size_t)lane * qkv_n + u + j, pick<R>(acc[0], lane), f);
                 }
+                rc.release(lane);
             }
         }
-        pb ^= 1;
-    }
-}
-
-
-// One attention work item of one layer: QK-norm + RoPE of this row's q heads
-// and k (v as is) from the raw words, the cache row for later steps (split 0),
-// online-softmax attention over this split's pages (the step's own row patched
-// into the cached copy), then either the output words or this split's partial;
-// split 0 combines the partials of all splits in split order.
-template <typename WT, typename KT, int HD, int R>
-__device__ __noinline__ void attn_phase(const PersistParams &p, const LayerW &L, int l, const AttnWork &aw, Ring &rc,
-                                        const Ctx &c, float *qs, float *sc, KT *knew, KT *vnew, float *m_s,
-                                        float *l_s, float *al_s, float (*ml_s)[kMaxSplits][2], float *comb,
-                                        int ctid, unsigned long long *trace, int tb) {
-    const int warp = ctid >> 5, lane = ctid & 31;
-    const int half = HD / 2, G = p.G;
-    const int qd = p.nq * HD, qkv_n = (p.nq + 2 * p.nkv) * HD;
-
+        TR(tb + 2);
+        // ---- attention of (row r, KV group g, split) over [0, pos]
+        if (aw.has) {
             const int r = aw.r, g = aw.g, pos = aw.pos;
             if (warp < G + 2) {
                 // QK-norm + RoPE of this row's q heads of the group and k; v as is
@@ -866,7 +676,7 @@ __device__ __noinline__ void attn_phase(const PersistParams &p, const LayerW &L,
 #pragma unroll
             for (int o = 0; o < NO; ++o) o_acc[o] = 0.f;
             cbar();
-            if (trace) trace[tb + 3] = clock64();
+            TR(tb + 3);
             for (int pg = aw.pb; pg < aw.pe; ++pg) {
                 KT *Ks = reinterpret_cast<KT *>(const_cast<unsigned char *>(rc.acquire(c)));
                 KT *Vs = Ks + kPage * HD;
@@ -884,24 +694,13 @@ __device__ __noinline__ void attn_phase(const PersistParams &p, const LayerW &L,
                     float kv[E];
 #pragma unroll
                     for (int e = 0; e < E; ++e) kv[e] = Elem<KT>::load(Ks, (size_t)j * HD + lane * E + e);
-                    float dv[MAXG];
+                    for (int gi = 0; gi < G; ++gi) {
+                        float d = 0.f;
 #pragma unroll
-                    for (int gi = 0; gi < MAXG; ++gi) {
-                        dv[gi] = 0.f;
-                        if (gi < G) {
-#pragma unroll
-                            for (int e = 0; e < E; ++e) dv[gi] = fmaf(qs[gi * HD + lane * E + e], kv[e], dv[gi]);
-                        }
+                        for (int e = 0; e < E; ++e) d = fmaf(qs[gi * HD + lane * E + e], kv[e], d);
+                        d = warp_sum(d);
+                        if (lane == 0) sc[gi * kPage + j] = (j < valid) ? d : -INFINITY;
                     }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                        for (int gi = 0; gi < MAXG; ++gi)
-                            if (gi < G) dv[gi] += __shfl_xor_sync(0xffffffffu, dv[gi], o);
-                    if (lane == 0)
-#pragma unroll
-                        for (int gi = 0; gi < MAXG; ++gi)
-                            if (gi < G) sc[gi * kPage + j] = (j < valid) ? dv[gi] : -INFINITY;
                 }
                 cbar();
                 if (warp < G) {
@@ -927,17 +726,10 @@ __device__ __noinline__ void attn_phase(const PersistParams &p, const LayerW &L,
                     const int idx = ctid + o * NCT;
                     if (idx < G * HD) {
                         const int gi = idx / HD, d = idx - gi * HD;
-                        float c0 = o_acc[o] * al_s[gi], c1 = 0.f, c2 = 0.f, c3 = 0.f;
+                        float acc = o_acc[o] * al_s[gi];
                         const float *pj = sc + gi * kPage;
-                        int j = 0;
-                        for (; j + 3 < valid; j += 4) {
-                            c0 = fmaf(pj[j], Elem<KT>::load(Vs, (size_t)j * HD + d), c0);
-                            c1 = fmaf(pj[j + 1], Elem<KT>::load(Vs, (size_t)(j + 1) * HD + d), c1);
-                            c2 = fmaf(pj[j + 2], Elem<KT>::load(Vs, (size_t)(j + 2) * HD + d), c2);
-                            c3 = fmaf(pj[j + 3], Elem<KT>::load(Vs, (size_t)(j + 3) * HD + d), c3);
-                        }
-                        for (; j < valid; ++j) c0 = fmaf(pj[j], Elem<KT>::load(Vs, (size_t)j * HD + d), c0);
-                        o_acc[o] = (c0 + c1) + (c2 + c3);
+                        for (int j = 0; j < valid; ++j) acc = fmaf(pj[j], Elem<KT>::load(Vs, (size_t)j * HD + d), acc);
+                        o_acc[o] = acc;
                     }
                 }
                 rc.release(lane);
@@ -977,34 +769,42 @@ __device__ __noinline__ void attn_phase(const PersistParams &p, const LayerW &L,
                 // split 0 combines all splits in split order (deterministic)
                 const uint32_t fp = flag_of(p.flag_base, l, FL_PART);
                 const int ns = aw.nact;
-                // Gather o of splits 1..ns-1 into comb[gi][sp][d] (8 loads in flight per
-                // thread per round), and (m, l) of every split into ml_s.
-                const int per_g = (ns - 1) * HD;
-                const int total = G * per_g;
-                for (int base = 0; base < total; base += 8 * NCT) {
-                    unsigned long long wv[8];
-                    const unsigned long long *ad[8];
+                // Issue this thread's o loads of every split first (all in flight together),
+                // then gather (m, l) of splits 1..ns-1 into shared memory.
+                auto gather_o = [&](int idx, float (&ov)[kMaxSplits]) {
+                    const int gi = idx / HD, d = idx - gi * HD;
+                    const unsigned long long *wb =
+                        p.part_ll + (((size_t)r * p.nq + hq0 + gi) * kMaxSplits) * WS + 2 + d;
+                    unsigned long long wv2[kMaxSplits];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int idx = base + k * NCT + ctid;
-                        ad[k] = nullptr;
-                        if (idx < total) {
-                            const int gi = idx / per_g, rem = idx - gi * per_g;
-                            const int sp = 1 + rem / HD, d = rem - (sp - 1) * HD;
-                            ad[k] = p.part_ll + (((size_t)r * p.nq + hq0 + gi) * kMaxSplits + sp) * WS + 2 + d;
-                            wv[k] = ld_ll(ad[k]);
+                    for (int sp = 1; sp < kMaxSplits; ++sp)
+                        if (sp < ns) wv2[sp] = ld_ll(wb + (size_t)sp * WS);
+#pragma unroll
+                    for (int sp = 1; sp < kMaxSplits; ++sp) {
+                        ov[sp] = 0.f;
+                        if (sp < ns) {
+                            if (ll_flag(wv2[sp]) != fp) wv2[sp] = repoll_ll(wb + (size_t)sp * WS, fp, c);
+                            ov[sp] = ll_val(wv2[sp]);
                         }
                     }
+                };
+                auto combine_o = [&](int idx, float own_o, float (&ov)[kMaxSplits]) {
+                    const int gi = idx / HD, d = idx - gi * HD;
+                    ov[0] = own_o;
+                    float M = -INFINITY;
+                    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ml_s[gi][sp][0]);
+                    float Ls = 0.f, O = 0.f;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        if (ad[k] != nullptr) {
-                            if (ll_flag(wv[k]) != fp) wv[k] = repoll_ll(ad[k], fp, c);
-                            const int idx = base + k * NCT + ctid;
-                            const int gi = idx / per_g, rem = idx - gi * per_g;
-                            comb[(gi * aw.S + 1 + rem / HD) * HD + rem % HD] = ll_val(wv[k]);
+                    for (int sp = 0; sp < kMaxSplits; ++sp)
+                        if (sp < ns) {
+                            const float f = expf(ml_s[gi][sp][0] - M);
+                            Ls = fmaf(ml_s[gi][sp][1], f, Ls);
+                            O = fmaf(ov[sp], f, O);
                         }
-                    }
-                }
+                    st_ll(orow + (hq0 + gi) * HD + d, O / Ls, fo);
+                };
+                float ov[kMaxSplits];
+                if (ctid < G * HD) gather_o(ctid, ov);
                 for (int idx = ctid; idx < G * (ns - 1) * 2; idx += NCT) {
                     const int gi = idx / ((ns - 1) * 2), rem = idx - gi * (ns - 1) * 2;
                     const int sp = 1 + rem / 2, which = rem & 1;
@@ -1018,117 +818,18 @@ __device__ __noinline__ void attn_phase(const PersistParams &p, const LayerW &L,
                     ml_s[ctid][0][0] = m_s[ctid];
                     ml_s[ctid][0][1] = l_s[ctid];
                 }
-                for (int o = 0; o < NO; ++o) {
-                    const int idx = ctid + o * NCT;
-                    if (idx < G * HD) comb[((idx / HD) * aw.S) * HD + idx % HD] = o_acc[o];
-                }
                 cbar();
-                for (int idx = ctid; idx < G * HD; idx += NCT) {
-                    const int gi = idx / HD, d = idx - gi * HD;
-                    float M = -INFINITY;
-                    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ml_s[gi][sp][0]);
-                    float Ls = 0.f, O = 0.f;
-                    for (int sp = 0; sp < ns; ++sp) {
-                        const float f = expf(ml_s[gi][sp][0] - M);
-                        Ls = fmaf(ml_s[gi][sp][1], f, Ls);
-                        O = fmaf(comb[(gi * aw.S + sp) * HD + d], f, O);
+                if (ctid < G * HD) combine_o(ctid, o_acc[0], ov);
+#pragma unroll
+                for (int o = 1; o < NO; ++o) {
+                    const int idx = ctid + o * NCT;
+                    if (idx < G * HD) {
+                        gather_o(idx, ov);
+                        combine_o(idx, o_acc[o], ov);
                     }
-                    st_ll(orow + (hq0 + gi) * HD + d, O / Ls, fo);
                 }
             }
         }
-
-
-template <typename WT, typename KT, int HD, int R>
-__global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_constant__ PersistParams p) {
-    constexpr int EPV = Elem<WT>::kPerVec;
-    constexpr size_t WSZ = sizeof(WT);
-    extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t full[NS], empty[NS];
-    __shared__ float red[NCW * R];
-    __shared__ float m_s[MAXG], l_s[MAXG], al_s[MAXG];
-    __shared__ float ml_s[MAXG][kMaxSplits][2];
-    __shared__ float xown[R][XO];
-    __shared__ float bv_s[NCW][R];
-    __shared__ int bi_s[NCW][R];
-    __shared__ int curlen_s[R];
-    __shared__ int abort_sh, flag_s;
-    __shared__ float part_raw[2][512];   // per-chunk warp partials, double buffered
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int P = gridDim.x, cta = blockIdx.x;
-    const int H = p.H, half = HD / 2, G = p.G;
-    const int qd = p.nq * HD, qkv_n = (p.nq + 2 * p.nkv) * HD;
-    const int KMAX = max(max(H, qd), p.I);
-    const int rows = p.rows;
-    unsigned char *ring = smem;
-    float *act = reinterpret_cast<float *>(smem + (size_t)NS * SLOT);
-    float *qs = act + (size_t)R * KMAX;            // [G][HD] scaled q of the attention row
-    float *sc = qs + MAXG * HD;                     // [G][kPage] scores / probabilities
-    float *comb = sc + MAXG * kPage;                // [G][splits][HD] gathered split outputs
-    KT *knew = reinterpret_cast<KT *>(comb + (size_t)G * p.splits * HD);
-    KT *vnew = knew + HD;
-
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NCW);
-        }
-        abort_sh = 0;
-        fence_barrier_init();
-    }
-    if (tid < R) curlen_s[tid] = (tid < rows) ? p.cur_len[tid] : 0;
-    __syncthreads();
-    const Ctx c{reinterpret_cast<volatile int *>(&abort_sh), p.sync + SY_ABORT, p.status};
-    const AttnWork aw = attn_work(p, cta, P, curlen_s);
-
-    if (warp == NCW) {
-        if (lane == 0) producer<WT, KT, HD, R>(p, ring, full, empty, c, aw);
-        return;
-    }
-
-    // ------------------------------------------------------------------ consumers
-    const int ctid = tid;
-    unsigned long long *trace = (p.trace != nullptr && ctid == 0) ? p.trace + (size_t)cta * kTraceSlots : nullptr;
-    if (trace) {   // clock64 stamps; this pair aligns them across CTAs
-        trace[kTraceSlots - 2] = globaltimer_ns();
-        trace[kTraceSlots - 1] = clock64();
-    }
-    Ring rc{ring, full, empty, 0, trace};
-    int pb = 0;   // which half of part_s the next chunk writes
-#define TR(slot)                                      \
-    do {                                              \
-        if (trace) trace[(slot)] = clock64();         \
-    } while (0)
-    const Span own = cta_span(H, cta, P);           // residual rows this CTA updates (o_proj and down)
-    for (int i = ctid; i < rows * own.n; i += NCT) {
-        const int r = i / own.n, j = i - r * own.n;
-        xown[r][j] = p.emb[(size_t)r * H + own.u0 + j];
-    }
-
-    for (int l = 0; l < p.n_layers; ++l) {
-        const LayerW &L = p.layers[l];
-        const int tb = l * kTracePerLayer;
-        TR(tb + 0);
-        // ---- RMSNorm -> [Wq;Wk;Wv] -> raw q|k|v words
-        // (A CTA with no rows in a phase skips that phase's input: it would have no
-        // output that orders its reads before the next overwrite of the input words.)
-        const Span sq = cta_span(qkv_n, cta, P);
-        if (sq.n > 0) {
-            if (l == 0) stage<EPV, R>(act, p.emb, H, H, rows, L.in_norm, p.eps, red, ctid);
-            else stage_ll<EPV, R>(act, p.x_ll, H, H, rows, flag_of(p.flag_base, l - 1, FL_X2), L.in_norm, p.eps,
-                                  red, ctid, c);
-        }
-        TR(tb + 1);
-        {
-            gemv_phase<WT, R, 1, PH_QKV>(p, rc, c, act, &part_raw[0][0], pb, sq, H, flag_of(p.flag_base, l, FL_RAW),
-                                         ctid, &xown[0][0], nullptr, nullptr);
-        }
-        TR(tb + 2);
-        // ---- attention of (row r, KV group g, split) over [0, pos]
-        if (aw.has)
-            attn_phase<WT, KT, HD, R>(p, L, l, aw, rc, c, qs, sc, knew, vnew, m_s, l_s, al_s, ml_s, comb, ctid, trace,
-                                      tb);
         TR(tb + 4);
 
         // ---- o_proj + residual
@@ -1136,8 +837,23 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
             stage_ll<EPV, R>(act, p.o_ll, qd, qd, rows, flag_of(p.flag_base, l, FL_O), nullptr, 0.f, red, ctid, c);
         TR(tb + 6);
         {
-            gemv_phase<WT, R, 1, PH_O>(p, rc, c, act, &part_raw[0][0], pb, own, qd, flag_of(p.flag_base, l, FL_X1),
-                                       ctid, &xown[0][0], nullptr, nullptr);
+            const uint32_t f = flag_of(p.flag_base, l, FL_X1);
+            const int upc = max(1, (int)(SLOT / (qd * WSZ)));
+            for (int u = own.u0; u < own.u0 + own.n; u += upc) {
+                const int n = min(upc, own.u0 + own.n - u);
+                const unsigned char *w = rc.acquire(c);
+                for (int j = warp; j < n; j += NCW) {
+                    float acc[1][R];
+                    dot_rows<WT, R, 1>(w + (size_t)j * qd * WSZ, qd, act, rows, acc, lane);
+                    if (lane < rows) {
+                        const int jj = u + j - own.u0;
+                        const float x1 = xown[lane][jj] + pick<R>(acc[0], lane);
+                        xown[lane][jj] = x1;
+                        st_ll(p.x_ll + (size_t)lane * H + u + j, x1, f);
+                    }
+                }
+                rc.release(lane);
+            }
         }
         TR(tb + 7);
 
@@ -1148,8 +864,21 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
                              c);
         TR(tb + 9);
         {
-            gemv_phase<WT, R, 2, PH_GU>(p, rc, c, act, &part_raw[0][0], pb, sg, H, flag_of(p.flag_base, l, FL_ACT),
-                                        ctid, &xown[0][0], nullptr, nullptr);
+            const uint32_t f = flag_of(p.flag_base, l, FL_ACT);
+            const Span s = sg;
+            const int upc = max(1, (int)(SLOT / (2 * H * WSZ)));
+            for (int u = s.u0; u < s.u0 + s.n; u += upc) {
+                const int n = min(upc, s.u0 + s.n - u);
+                const unsigned char *w = rc.acquire(c);
+                for (int j = warp; j < n; j += NCW) {
+                    float acc[2][R];
+                    dot_rows<WT, R, 2>(w + (size_t)j * 2 * H * WSZ, H, act, rows, acc, lane);
+                    if (lane < rows)
+                        st_ll(p.act_ll + (size_t)lane * p.I + u + j,
+                              silu_f(pick<R>(acc[0], lane)) * pick<R>(acc[1], lane), f);
+                }
+                rc.release(lane);
+            }
         }
         TR(tb + 10);
 
@@ -1159,8 +888,23 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
                              c);
         TR(tb + 12);
         {
-            gemv_phase<WT, R, 1, PH_D>(p, rc, c, act, &part_raw[0][0], pb, own, p.I, flag_of(p.flag_base, l, FL_X2),
-                                       ctid, &xown[0][0], nullptr, nullptr);
+            const uint32_t f = flag_of(p.flag_base, l, FL_X2);
+            const int upc = max(1, (int)(SLOT / (p.I * WSZ)));
+            for (int u = own.u0; u < own.u0 + own.n; u += upc) {
+                const int n = min(upc, own.u0 + own.n - u);
+                const unsigned char *w = rc.acquire(c);
+                for (int j = warp; j < n; j += NCW) {
+                    float acc[1][R];
+                    dot_rows<WT, R, 1>(w + (size_t)j * p.I * WSZ, p.I, act, rows, acc, lane);
+                    if (lane < rows) {
+                        const int jj = u + j - own.u0;
+                        const float x2 = xown[lane][jj] + pick<R>(acc[0], lane);
+                        xown[lane][jj] = x2;
+                        st_ll(p.x_ll + (size_t)lane * H + u + j, x2, f);
+                    }
+                }
+                rc.release(lane);
+            }
         }
         TR(tb + 13);
     }
@@ -1175,36 +919,28 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
             const int r = i / H, k = i - r * H;
             p.hidden_out[i] = act[aidx<EPV>(r, k, H)];
         }
-    float bvr[R];
-    int bir[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        bvr[r] = -INFINITY;
-        bir[r] = 0x7fffffff;
-    }
-    {
-        gemv_phase<WT, R, 1, PH_HEAD>(p, rc, c, act, &part_raw[0][0], pb, cta_span(p.V, cta, P), H, 0u, ctid,
-                                      &xown[0][0], bvr, bir);
-    }
-    // per-warp best of each row (lowest index on ties)
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        float b = bvr[r];
-        int ib = bir[r];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float v2 = __shfl_xor_sync(0xffffffffu, b, o);
-            const int i2 = __shfl_xor_sync(0xffffffffu, ib, o);
-            if (v2 > b || (v2 == b && i2 < ib)) {
-                b = v2;
-                ib = i2;
+    {
+        const Span s = cta_span(p.V, cta, P);
+        const int upc = max(1, (int)(SLOT / (H * WSZ)));
+        for (int u = s.u0; u < s.u0 + s.n; u += upc) {
+            const int n = min(upc, s.u0 + s.n - u);
+            const unsigned char *w = rc.acquire(c);
+            for (int j = warp; j < n; j += NCW) {
+                float acc[1][R];
+                dot_rows<WT, R, 1>(w + (size_t)j * H * WSZ, H, act, rows, acc, lane);
+                if (lane < rows) {
+                    const float v = pick<R>(acc[0], lane);
+                    p.logits[(size_t)lane * p.V + u + j] = v;
+                    if (isnan(v)) atomicOr(p.status, ST_NAN_LOGIT);
+                    else if (v > bv || (v == bv && u + j < bi)) {
+                        bv = v;
+                        bi = u + j;
+                    }
+                }
             }
-        }
-        if (lane == r) {
-            bv = b;
-            bi = ib;
+            rc.release(lane);
         }
     }
     TR(th + 1);
@@ -1282,9 +1018,9 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const __grid_consta
 #undef TR
 }
 
-size_t persist_smem_bytes(int R, int head_dim, int kv_bf16, int kmax, int group, int splits) {
+size_t persist_smem_bytes(int R, int head_dim, int kv_bf16, int kmax) {
     return (size_t)NS * SLOT + (size_t)R * kmax * 4 + (size_t)MAXG * head_dim * 4 + (size_t)MAXG * kPage * 4 +
-           (size_t)group * splits * head_dim * 4 + 2 * (size_t)head_dim * (kv_bf16 ? 2 : 4) + 16;
+           2 * (size_t)head_dim * (kv_bf16 ? 2 : 4) + 16;
 }
 
 }  // namespace pk
@@ -1327,7 +1063,9 @@ static cudaError_t setup_pk(size_t smem, int *blocks_per_sm) {
     } while (0)
 
 size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax, int group, int splits) {
-    return pk::persist_smem_bytes(R, head_dim, kv_bf16, kmax, group, splits);
+    (void)group;
+    (void)splits;
+    return pk::persist_smem_bytes(R, head_dim, kv_bf16, kmax);
 }
 int persist_threads() { return pk::NT; }
 int persist_slot_bytes() { return pk::SLOT; }
