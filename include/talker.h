@@ -169,6 +169,14 @@ const char *talker_last_error(void);
  * 2 = always the multi-kernel CUDA graph. Errors: EINVAL. */
 talker_status talker_set_decode_mode(talker_t *t, int mode);
 
+/* Test support: the tensor-core GEMM of the prefill path on its own,
+ * out[M, N] (+)= A[M, K] B[N, K]^T with bf16 A and B and f32 out (device
+ * pointers; N % 128 == 0, K % 64 == 0). With accumulate or splits > 1 the
+ * product is added to out. Synchronises the stream. Errors: EINVAL, ECUDA,
+ * EDEVICE (a wait in the kernel gave up). */
+talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, int N, float *out, int accumulate,
+                                    int splits, void *cuda_stream);
+
 /* Tuning / test support: cap the number of CTAs that share one (stream, KV
  * group) along the sequence in the persistent decode kernel (0 = no cap).
  * Errors: EINVAL. */

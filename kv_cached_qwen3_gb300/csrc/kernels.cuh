@@ -134,6 +134,15 @@ constexpr int kTraceEpi = 2816;
 constexpr int kTraceChunks = 768;
 constexpr int kTracePerLayer = 15;
 
+// Tensor-core GEMM C[M, N] (+)= A[M, K] B[N, K]^T, bf16 inputs, fp32 output.
+struct GemmParams {
+    int M, N, K;
+    float *out;
+    int ld_out;
+    int accumulate;   // 1: reduce-add into out (residual stream or split-K), 0: store
+    int *status;
+};
+
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = 256;
 constexpr int kAttnThreads = 256;
@@ -149,7 +158,15 @@ cudaError_t launch_set_len(int *cur_len, int stream, int value, cudaStream_t st)
 // Copy len rows of a stream between a dense [n_layers][n_kv][len][hd] buffer and the cache.
 cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *dense_v, int len, int to_cache,
                            cudaStream_t st);
-cudaError_t prepare_kernels();
+cudaError_t prepare_kernels();  // raise dynamic shared-memory limits once per process
+
+bool gemm_tc_supported(int N, int K);
+int gemm_tc_splits(int M, int N, int K, int n_sm);
+cudaError_t prepare_gemm_tc();
+// A: bf16 [M, K], B: bf16 [N, K] (device); out: f32 [M, ld_out]. With splits > 1 the
+// result is reduce-added, so out must hold zeros (or the residual stream).
+cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, float *out, int ld_out, int accumulate,
+                           int splits, int *status, cudaStream_t st);
 
 // Persistent decode kernel (one cooperative launch per decode step, one CTA per SM).
 size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax, int group, int splits);
@@ -158,6 +175,6 @@ int persist_slot_bytes();
 int persist_sync_words(int n_heads);
 cudaError_t setup_persistent(int w_bf16, int head_dim, int R, size_t smem, int *blocks_per_sm);
 cudaError_t launch_persistent(int w_bf16, int head_dim, int R, const PersistParams &p, int grid, size_t smem,
-                              cudaStream_t st);  // raise dynamic shared-memory limits once per process
+                              cudaStream_t st);
 
 }  // namespace talker_k

@@ -826,6 +826,23 @@ talker_status talker_set_trace(talker_t *t, unsigned long long *buf) {
 
 int talker_trace_slots(void) { return kTraceSlots; }
 
+talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, int N, float *out, int accumulate,
+                                    int splits, void *cuda_stream) {
+    if (!A || !B || !out || M < 1 || splits < 1 || !gemm_tc_supported(N, K)) return TALKER_EINVAL;
+    static int *d_status = nullptr;
+    if (!d_status) {
+        TRY_CUDA(cudaMalloc(&d_status, sizeof(int)));
+        TRY_CUDA(cudaMemset(d_status, 0, sizeof(int)));
+    }
+    TRY_CUDA(prepare_gemm_tc());
+    TRY_CUDA(launch_gemm_tc(A, M, K, B, N, out, N, accumulate, splits, d_status,
+                            static_cast<cudaStream_t>(cuda_stream)));
+    TRY_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)));
+    int h = 0;
+    TRY_CUDA(cudaMemcpy(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost));
+    return h ? TALKER_EDEVICE : TALKER_OK;
+}
+
 talker_status talker_set_attn_splits(talker_t *t, int max_splits) {
     if (!t || max_splits < 0) return TALKER_EINVAL;
     t->max_splits = max_splits;

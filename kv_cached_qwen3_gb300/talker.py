@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_set_decode_mode": (st, [vp, ctypes.c_int]),
         "talker_set_trace": (st, [vp, vp]),
         "talker_set_attn_splits": (st, [vp, ctypes.c_int]),
+        "talker_test_gemm_bf16": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+                                       ctypes.c_int, vp]),
         "talker_trace_slots": (ctypes.c_int, []),
     }
     for name, (res, args) in proto.items():
@@ -215,3 +217,16 @@ class Talker:
 
     def kernel_launches(self) -> int:
         return int(self.lib.talker_kernel_launches(self.h))
+
+
+def test_gemm_bf16(A, B, out, accumulate=False, splits=1):
+    """Test support: out (+)= A @ B.T on the tensor-core GEMM (A [M,K], B [N,K] bf16; out f32 [M,N])."""
+    import torch
+    lib = load_library()
+    M, K = A.shape
+    N = B.shape[0]
+    st = lib.talker_test_gemm_bf16(_ptr(A), M, K, _ptr(B), N, _ptr(out), int(accumulate), splits,
+                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if st != 0:
+        raise TalkerError(st, "talker_test_gemm_bf16")
+    return out

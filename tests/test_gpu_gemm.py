@@ -1,0 +1,41 @@
+"""GPU: the tensor-core (tcgen05/TMEM) GEMM against a float64 matmul of the same bf16 inputs."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kv_cached_qwen3_gb300 import talker
+    talker.load_library()
+    return torch.device("cuda", 0)
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(1, 128, 64, 1), (96, 4096, 1024, 1), (96, 1024, 3072, 12),
+                                          (130, 256, 128, 1), (300, 384, 2048, 4), (4096, 1024, 1024, 1)])
+def test_gemm_matches_fp64(cuda, M, N, K, splits):
+    from kv_cached_qwen3_gb300.talker import test_gemm_bf16
+    g = torch.Generator(device="cpu").manual_seed(M * 7 + N + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = (0.02 * torch.randn(N, K, generator=g)).to(torch.bfloat16)
+    ref = A.double() @ B.double().T
+    out = torch.zeros(M, N, device="cuda")
+    test_gemm_bf16(A.cuda(), B.cuda(), out, splits=splits)
+    got = out.cpu().double()
+    err = (got - ref).norm() / ref.norm()
+    assert float(err) < 1e-5, float(err)
+
+
+def test_gemm_accumulates_into_output(cuda):
+    from kv_cached_qwen3_gb300.talker import test_gemm_bf16
+    A = torch.randn(64, 256).to(torch.bfloat16).cuda()
+    B = (0.02 * torch.randn(128, 256)).to(torch.bfloat16).cuda()
+    base = torch.randn(64, 128, device="cuda")
+    out = base.clone()
+    test_gemm_bf16(A, B, out, accumulate=True)
+    ref = base.double().cpu() + A.double().cpu() @ B.double().cpu().T
+    assert float((out.cpu().double() - ref).norm() / ref.norm()) < 1e-5
