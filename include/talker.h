@@ -169,6 +169,11 @@ const char *talker_last_error(void);
  * 2 = always the multi-kernel CUDA graph. Errors: EINVAL. */
 talker_status talker_set_decode_mode(talker_t *t, int mode);
 
+/* Choose how prefill runs: 0 = automatic (tensor-core GEMMs when the weights
+ * are bf16, T >= 16 and every projection shape is a multiple of the GEMM tile;
+ * otherwise the GEMV kernels), 2 = always the GEMV kernels. Errors: EINVAL. */
+talker_status talker_set_prefill_mode(talker_t *t, int mode);
+
 /* Test support: the tensor-core GEMM of the prefill path on its own,
  * out[M, N] (+)= A[M, K] B[N, K]^T with bf16 A and B and f32 out (device
  * pointers; N % 128 == 0, K % 64 == 0). With accumulate or splits > 1 the

@@ -168,6 +168,14 @@ cudaError_t prepare_gemm_tc();
 cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, float *out, int ld_out, int accumulate,
                            int splits, int *status, cudaStream_t st);
 
+// Element-wise stages of the tensor-core prefill path (prefill.cu).
+cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H, void *out,
+                                cudaStream_t st);
+cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
+                            const float *k_norm, const float2 *rope, float eps, float *q_out, const CacheView &cache,
+                            int layer, int stream, int pos0, int *status, cudaStream_t st);
+cudaError_t launch_swiglu_bf16(const float *gu, int rows, int I, void *out, cudaStream_t st);
+
 // Persistent decode kernel (one cooperative launch per decode step, one CTA per SM).
 size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax, int group, int splits);
 int persist_threads();

@@ -1,0 +1,153 @@
+// Element-wise stages of the tensor-core prefill path (the projections run on
+// the tcgen05 GEMM):
+//   k_rmsnorm_bf16: x / sqrt(mean(x^2) + eps) * w, rounded to bf16 as the next
+//                   GEMM's A operand ("talker-forward.h", talker_layer_forward
+//                   pre-norm and MLP pre-norm);
+//   k_qkv_post:     per (row, head) of the raw projections: QK-RMSNorm with the
+//                   [hd] gain and NEOX RoPE at the row's position for q and k,
+//                   k and v appended to the cache at that position (set_rows),
+//                   q kept in f32 for attention;
+//   k_swiglu_bf16:  silu(gate) * up from the row-interleaved [gate; up]
+//                   projection (columns 2j, 2j+1), rounded to bf16.
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace talker_dev;
+
+namespace talker_k {
+
+// One warp per row.
+__global__ void k_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H,
+                               __nv_bfloat16 *out) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const float *xr = x + (size_t)warp * ld;
+    float ss = 0.f;
+    for (int k = lane * 4; k < H; k += 128) {
+        const float4 v = *reinterpret_cast<const float4 *>(xr + k);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+    __nv_bfloat16 *o = out + (size_t)warp * H;
+    for (int k = lane * 4; k < H; k += 128) {
+        const float4 v = *reinterpret_cast<const float4 *>(xr + k);
+        const float4 g = *reinterpret_cast<const float4 *>(w + k);
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x * inv * g.x, v.y * inv * g.y);
+        __nv_bfloat162 b = __floats2bfloat162_rn(v.z * inv * g.z, v.w * inv * g.w);
+        *reinterpret_cast<__nv_bfloat162 *>(o + k) = a;
+        *reinterpret_cast<__nv_bfloat162 *>(o + k + 2) = b;
+    }
+}
+
+// One warp per (row, head); row r is at position pos0 + r of stream `stream`.
+__global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
+                           const float *k_norm, const float2 *rope, float eps, float *q_out, CacheView cache, int layer,
+                           int stream, int pos0, int *status) {
+    const int n_heads = n_q + 2 * n_kv;
+    const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (item >= rows * n_heads) return;
+    const int r = item / n_heads, h = item - r * n_heads;
+    const int half = hd >> 1;
+    const int qkv_n = n_heads * hd;
+    const float *src = raw + (size_t)r * qkv_n + (size_t)h * hd;
+    const bool is_q = h < n_q, is_k = !is_q && h < n_q + n_kv;
+    float a[2], b[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int i = lane + 32 * t;
+        a[t] = (i < half) ? src[i] : 0.f;
+        b[t] = (i < half) ? src[i + half] : 0.f;
+    }
+    const int pos = pos0 + r;
+    if (pos < 0 || pos >= cache.max_seq) {
+        if (lane == 0) atomicOr(status, ST_BAD_POSITION);
+        return;
+    }
+    if (is_q || is_k) {
+        const float *gain = is_q ? q_norm : k_norm;
+        const float ss = warp_sum(a[0] * a[0] + b[0] * b[0] + a[1] * a[1] + b[1] * b[1]);
+        const float inv = 1.0f / sqrtf(ss / (float)hd + eps);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int i = lane + 32 * t;
+            if (i < half) {
+                const float x0 = a[t] * inv * gain[i], x1 = b[t] * inv * gain[i + half];
+                const float2 cs = rope[(size_t)pos * half + i];
+                a[t] = x0 * cs.x - x1 * cs.y;
+                b[t] = x1 * cs.x + x0 * cs.y;
+            }
+        }
+    }
+    if (is_q) {
+        float *d = q_out + (size_t)r * n_q * hd + (size_t)h * hd;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int i = lane + 32 * t;
+            if (i < half) {
+                d[i] = a[t];
+                d[i + half] = b[t];
+            }
+        }
+        return;
+    }
+    const int kvh = is_k ? h - n_q : h - n_q - n_kv;
+    const int page = cache.page_table[(size_t)stream * cache.pages_per_stream + pos / kPage];
+    const size_t off = (size_t)page * cache.page_elems + ((size_t)(layer * n_kv + kvh) * kPage + pos % kPage) * hd;
+    void *base = is_k ? cache.k : cache.v;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int i = lane + 32 * t;
+        if (i < half) {
+            if (cache.kv_bf16) {
+                __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(base) + off;
+                d[i] = __float2bfloat16_rn(a[t]);
+                d[i + half] = __float2bfloat16_rn(b[t]);
+            } else {
+                float *d = static_cast<float *>(base) + off;
+                d[i] = a[t];
+                d[i + half] = b[t];
+            }
+        }
+    }
+}
+
+__global__ void k_swiglu_bf16(const float *gu, int rows, int I, __nv_bfloat16 *out) {
+    const size_t n = (size_t)rows * I;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / I, j = i - r * I;
+        const float2 v = *reinterpret_cast<const float2 *>(gu + r * 2 * I + 2 * j);
+        out[i] = __float2bfloat16_rn(v.x / (1.0f + expf(-v.x)) * v.y);
+    }
+}
+
+cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H, void *out,
+                                cudaStream_t st) {
+    const int warps_per_block = 8;
+    k_rmsnorm_bf16<<<(rows + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, st>>>(
+        x, ld, w, eps, rows, H, static_cast<__nv_bfloat16 *>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
+                            const float *k_norm, const float2 *rope, float eps, float *q_out, const CacheView &cache,
+                            int layer, int stream, int pos0, int *status, cudaStream_t st) {
+    const long long items = (long long)rows * (n_q + 2 * n_kv);
+    const int per_block = 8;
+    k_qkv_post<<<(unsigned)((items + per_block - 1) / per_block), per_block * 32, 0, st>>>(
+        raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, stream, pos0, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bf16(const float *gu, int rows, int I, void *out, cudaStream_t st) {
+    const size_t n = (size_t)rows * I;
+    const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+    k_swiglu_bf16<<<blocks, 256, 0, st>>>(gu, rows, I, static_cast<__nv_bfloat16 *>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace talker_k

@@ -99,8 +99,14 @@ struct talker {
     size_t ll_words = 0;
     uint32_t epoch = 0;                  // step counter for the persistent kernel's flags
     int max_splits = 0;                  // cap on the persistent kernel's attention splits (0 = none)
+    int prefill_mode = 0;                // 0 automatic, 2 always the GEMV kernels
     int persist_ok[2] = {-1, -1};        // per R template (1, 4): -1 unknown, 0 unusable, 1 usable
     unsigned long long *trace = nullptr; // optional phase stamps of the persistent kernel (caller-owned)
+    // tensor-core prefill buffers (bf16 GEMM operands and the f32 gate/up projection)
+    int cap_tc_rows = 0;
+    void *hb = nullptr, *ab = nullptr, *gb = nullptr;
+    float *gu = nullptr;
+    int tc_ok = -1;                      // tensor-core prefill usable for this geometry (-1 unknown)
 };
 
 namespace {
@@ -128,6 +134,15 @@ void free_workspaces(talker *t) {
     t->cap_rows = 0;
     t->cap_attn_ws = t->cap_head_part = 0;
     t->cap_cnt_rows = 0;
+}
+
+void free_tc(talker *t) {
+    void **bl[] = {&t->hb, &t->ab, &t->gb, reinterpret_cast<void **>(&t->gu)};
+    for (auto pp : bl) {
+        free_ptr(*pp);
+        *pp = nullptr;
+    }
+    t->cap_tc_rows = 0;
 }
 
 void free_persist(talker *t) {
@@ -572,6 +587,111 @@ talker_status decode_persistent(talker *t, const float *emb, int B, float *logit
     return TALKER_OK;
 }
 
+
+constexpr int kTcMinRows = 16;   // prefills shorter than this stay on the GEMV kernels
+
+bool tc_usable(talker *t) {
+    if (t->tc_ok < 0) {
+        t->tc_ok = t->w_bf16 && gemm_tc_supported(t->qkv_n, t->H) && gemm_tc_supported(t->H, t->qd) &&
+                   gemm_tc_supported(2 * t->I, t->H) && gemm_tc_supported(t->H, t->I) &&
+                   prepare_gemm_tc() == cudaSuccess;
+        cudaGetLastError();
+    }
+    return t->tc_ok == 1;
+}
+
+talker_status ensure_tc(talker *t, int rows) {
+    if (rows <= t->cap_tc_rows) return TALKER_OK;
+    TRY_CUDA(cudaStreamSynchronize(t->st));
+    free_tc(t);
+    const int cap = std::max(rows, 128);
+    TRY_CUDA(cudaMalloc(&t->hb, (size_t)cap * t->H * 2));
+    TRY_CUDA(cudaMalloc(&t->ab, (size_t)cap * t->qd * 2));
+    TRY_CUDA(cudaMalloc(&t->gb, (size_t)cap * t->I * 2));
+    TRY_CUDA(cudaMalloc(&t->gu, (size_t)cap * 2 * t->I * sizeof(float)));
+    t->cap_tc_rows = cap;
+    return TALKER_OK;
+}
+
+// GEMM into `out`; with split-K into a non-residual output, zero it first.
+talker_status tc_gemm(talker *t, const void *A, int M, int K, const void *W, int N, float *out, int ld, bool residual,
+                      int *nk) {
+    const int splits = gemm_tc_splits(M, N, K, t->n_sm);
+    if (splits > 1 && !residual) TRY_CUDA(cudaMemsetAsync(out, 0, (size_t)M * ld * sizeof(float), t->st));
+    TRY_CUDA(launch_gemm_tc(A, M, K, W, N, out, ld, residual ? 1 : 0, splits, t->d_status, t->st));
+    ++*nk;
+    return TALKER_OK;
+}
+
+// Prefill of T rows at positions 0..T-1 on the tensor cores: per layer RMSNorm -> bf16,
+// [Wq;Wk;Wv] GEMM, QK-norm + RoPE + KV append, causal attention, o_proj GEMM reduce-added
+// into the residual stream, RMSNorm -> bf16, [Wg;Wu] GEMM, SwiGLU -> bf16, down GEMM
+// reduce-added into the residual stream; then the final norm + codec_head GEMV.
+talker_status enqueue_prefill_tc(talker *t, int stream, const float *emb, int T, const ForwardOut &out,
+                                 int *n_kernels) {
+    const CacheView cv = cache_view(t);
+    int nk = 0;
+    TRY_CUDA(cudaMemcpyAsync(t->x, emb, (size_t)T * t->H * sizeof(float), cudaMemcpyDeviceToDevice, t->st));
+    const RowMap rm{1, stream, 0, t->d_len};
+    for (int l = 0; l < t->c.n_layers; ++l) {
+        const LayerDev &d = t->L[l];
+        TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.in_norm, t->c.rms_eps, T, t->H, t->hb, t->st));
+        ++nk;
+        TRY(tc_gemm(t, t->hb, T, t->H, d.qkv, t->qkv_n, t->raw, t->qkv_n, false, &nk));
+        TRY_CUDA(launch_qkv_post(t->raw, T, t->nq, t->nkv, t->hd, d.q_norm, d.k_norm, t->d_rope, t->c.rms_eps, t->q,
+                                 cv, l, stream, 0, t->d_status, t->st));
+        ++nk;
+        AttnParams a{};
+        a.q = t->q;
+        a.out = t->ab;
+        a.out_bf16 = 1;
+        a.cache = cv;
+        a.rowmap = rm;
+        a.layer = l;
+        a.n_q = t->nq;
+        a.n_kv = t->nkv;
+        a.group = t->G;
+        a.splits = 1;
+        a.scale = 1.0f / sqrtf((float)t->hd);
+        a.ws = t->attn_ws;
+        a.cnt = t->attn_cnt;
+        a.status = t->d_status;
+        TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, T, t->st, false));
+        ++nk;
+        TRY(tc_gemm(t, t->ab, T, t->qd, d.o, t->H, t->x, t->H, true, &nk));
+        TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.post_norm, t->c.rms_eps, T, t->H, t->hb, t->st));
+        ++nk;
+        TRY(tc_gemm(t, t->hb, T, t->H, d.gu, 2 * t->I, t->gu, 2 * t->I, false, &nk));
+        TRY_CUDA(launch_swiglu_bf16(t->gu, T, t->I, t->gb, t->st));
+        ++nk;
+        TRY(tc_gemm(t, t->gb, T, t->I, d.down, t->H, t->x, t->H, true, &nk));
+    }
+    const int hrows = out.head_all_rows ? T : 1;
+    GemvParams h{};
+    h.eps = t->c.rms_eps;
+    h.rows = hrows;
+    h.status = t->d_status;
+    h.W = t->head;
+    h.act = out.head_all_rows ? t->x : t->x + (size_t)(T - 1) * t->H;
+    h.act_ld = t->H;
+    h.norm_w = t->fnorm;
+    h.K = t->H;
+    h.n_out = t->V;
+    h.out = out.logits;
+    h.out_ld = t->V;
+    h.hidden_out = out.hidden;
+    h.argmax_out = out.argmax;
+    h.part_val = t->head_val;
+    h.part_idx = t->head_idx;
+    h.head_cnt = t->head_cnt;
+    h.inc_len = 0;
+    h.cur_len_rw = t->d_len;
+    TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, t->st, false));
+    ++nk;
+    *n_kernels = nk;
+    return TALKER_OK;
+}
+
 talker_status check_stream(const talker *t, int stream) {
     if (!t) return TALKER_EINVAL;
     if (t->n_streams == 0) return TALKER_ESTATE;
@@ -589,7 +709,12 @@ talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float
     RowMap rm{1, stream, 0, t->d_len};
     ForwardOut out{logits, hidden, all_rows ? nullptr : argmax, all_rows, 0};
     int nk = 0;
-    TRY(enqueue_forward(t, t->st, T, rm, emb, 1, out, &nk));
+    if (T >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t)) {
+        TRY(ensure_tc(t, T));
+        TRY(enqueue_prefill_tc(t, stream, emb, T, out, &nk));
+    } else {
+        TRY(enqueue_forward(t, t->st, T, rm, emb, 1, out, &nk));
+    }
     TRY_CUDA(launch_set_len(t->d_len, stream, T, t->st));
     t->launches += nk + 1;
     t->len[stream] = T;
@@ -661,6 +786,7 @@ void talker_destroy(talker_t *t) {
     free_cache(t);
     free_ptr(t->wstore);
     free_persist(t);
+    free_tc(t);
     free_ptr(t->d_status);
     if (t->cap_st) cudaStreamDestroy(t->cap_st);
     delete t;
@@ -846,6 +972,12 @@ talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, 
 talker_status talker_set_attn_splits(talker_t *t, int max_splits) {
     if (!t || max_splits < 0) return TALKER_EINVAL;
     t->max_splits = max_splits;
+    return TALKER_OK;
+}
+
+talker_status talker_set_prefill_mode(talker_t *t, int mode) {
+    if (!t || (mode != 0 && mode != 2)) return TALKER_EINVAL;
+    t->prefill_mode = mode;
     return TALKER_OK;
 }
 

@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_set_decode_mode": (st, [vp, ctypes.c_int]),
         "talker_set_trace": (st, [vp, vp]),
         "talker_set_attn_splits": (st, [vp, ctypes.c_int]),
+        "talker_set_prefill_mode": (st, [vp, ctypes.c_int]),
         "talker_test_gemm_bf16": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
                                        ctypes.c_int, vp]),
         "talker_trace_slots": (ctypes.c_int, []),
@@ -200,6 +201,10 @@ class Talker:
     def set_decode_mode(self, mode: int):
         """0 automatic, 1 persistent decode kernel, 2 multi-kernel CUDA graph."""
         self._check(self.lib.talker_set_decode_mode(self.h, mode), "talker_set_decode_mode")
+
+    def set_prefill_mode(self, mode: int):
+        """0 automatic (tensor cores for bf16 weights and T >= 16), 2 GEMV kernels."""
+        self._check(self.lib.talker_set_prefill_mode(self.h, mode), "talker_set_prefill_mode")
 
     def set_attn_splits(self, n: int):
         self._check(self.lib.talker_set_attn_splits(self.h, n), "talker_set_attn_splits")
