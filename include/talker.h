@@ -164,9 +164,11 @@ const char *talker_last_error(void);
 
 /* Choose how talker_decode runs a step: 0 = automatic (the persistent kernel
  * when it fits: B <= 4, one cooperative CTA per SM, weight rows and KV page
- * pairs within one 32 KB ring slot; otherwise the CUDA graph), 1 = always the
- * persistent kernel (talker_decode returns EINVAL where it cannot run),
- * 2 = always the multi-kernel CUDA graph. Errors: EINVAL. */
+ * pairs within one 32 KB ring slot; B >= 8 with bf16 weights: the CUDA graph
+ * of tensor-core GEMMs; otherwise the CUDA graph of GEMV kernels), 1 = always
+ * the persistent kernel, 2 = always the GEMV graph, 3 = always the tensor-core
+ * graph (talker_decode returns EINVAL where the chosen path cannot run).
+ * Errors: EINVAL. */
 talker_status talker_set_decode_mode(talker_t *t, int mode);
 
 /* Choose how prefill runs: 0 = automatic (tensor-core GEMMs when the weights

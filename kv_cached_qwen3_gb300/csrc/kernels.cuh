@@ -173,7 +173,7 @@ cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float ep
                                 cudaStream_t st);
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
                             const float *k_norm, const float2 *rope, float eps, float *q_out, const CacheView &cache,
-                            int layer, int stream, int pos0, int *status, cudaStream_t st);
+                            int layer, const RowMap &rm, int *status, cudaStream_t st);
 cudaError_t launch_swiglu_bf16(const float *gu, int rows, int I, void *out, cudaStream_t st);
 
 // Persistent decode kernel (one cooperative launch per decode step, one CTA per SM).

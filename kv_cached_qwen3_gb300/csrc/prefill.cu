@@ -44,10 +44,11 @@ __global__ void k_rmsnorm_bf16(const float *x, int ld, const float *w, float eps
     }
 }
 
-// One warp per (row, head); row r is at position pos0 + r of stream `stream`.
+// One warp per (row, head); the row map gives each row's stream and position
+// (prefill: stream0 at pos0 + r; decode: stream r at cur_len[r]).
 __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
                            const float *k_norm, const float2 *rope, float eps, float *q_out, CacheView cache, int layer,
-                           int stream, int pos0, int *status) {
+                           RowMap rm, int *status) {
     const int n_heads = n_q + 2 * n_kv;
     const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (item >= rows * n_heads) return;
@@ -63,7 +64,8 @@ __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd
         a[t] = (i < half) ? src[i] : 0.f;
         b[t] = (i < half) ? src[i + half] : 0.f;
     }
-    const int pos = pos0 + r;
+    const int pos = rm.mode == 0 ? rm.cur_len[r] : rm.pos0 + r;
+    const int stream = rm.mode == 0 ? r : rm.stream0;
     if (pos < 0 || pos >= cache.max_seq) {
         if (lane == 0) atomicOr(status, ST_BAD_POSITION);
         return;
@@ -135,11 +137,11 @@ cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float ep
 
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
                             const float *k_norm, const float2 *rope, float eps, float *q_out, const CacheView &cache,
-                            int layer, int stream, int pos0, int *status, cudaStream_t st) {
+                            int layer, const RowMap &rm, int *status, cudaStream_t st) {
     const long long items = (long long)rows * (n_q + 2 * n_kv);
     const int per_block = 8;
     k_qkv_post<<<(unsigned)((items + per_block - 1) / per_block), per_block * 32, 0, st>>>(
-        raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, stream, pos0, status);
+        raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, rm, status);
     return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@ struct LayerDev {
 };
 
 struct GraphEntry {
+    int kind;   // 0: GEMV kernels, 1: tensor-core GEMMs
     int B;
     const float *emb;
     float *logits, *hidden;
@@ -588,7 +589,8 @@ talker_status decode_persistent(talker *t, const float *emb, int B, float *logit
 }
 
 
-constexpr int kTcMinRows = 16;   // prefills shorter than this stay on the GEMV kernels
+constexpr int kTcMinRows = 16;        // prefills shorter than this stay on the GEMV kernels
+constexpr int kTcMinDecodeRows = 8;   // decode batches at least this wide use the tensor-core GEMMs
 
 bool tc_usable(talker *t) {
     if (t->tc_ok < 0) {
@@ -614,11 +616,11 @@ talker_status ensure_tc(talker *t, int rows) {
 }
 
 // GEMM into `out`; with split-K into a non-residual output, zero it first.
-talker_status tc_gemm(talker *t, const void *A, int M, int K, const void *W, int N, float *out, int ld, bool residual,
-                      int *nk) {
+talker_status tc_gemm(talker *t, cudaStream_t st, const void *A, int M, int K, const void *W, int N, float *out, int ld,
+                      bool residual, int *nk) {
     const int splits = gemm_tc_splits(M, N, K, t->n_sm);
-    if (splits > 1 && !residual) TRY_CUDA(cudaMemsetAsync(out, 0, (size_t)M * ld * sizeof(float), t->st));
-    TRY_CUDA(launch_gemm_tc(A, M, K, W, N, out, ld, residual ? 1 : 0, splits, t->d_status, t->st));
+    if (splits > 1 && !residual) TRY_CUDA(cudaMemsetAsync(out, 0, (size_t)M * ld * sizeof(float), st));
+    TRY_CUDA(launch_gemm_tc(A, M, K, W, N, out, ld, residual ? 1 : 0, splits, t->d_status, st));
     ++*nk;
     return TALKER_OK;
 }
@@ -627,19 +629,18 @@ talker_status tc_gemm(talker *t, const void *A, int M, int K, const void *W, int
 // [Wq;Wk;Wv] GEMM, QK-norm + RoPE + KV append, causal attention, o_proj GEMM reduce-added
 // into the residual stream, RMSNorm -> bf16, [Wg;Wu] GEMM, SwiGLU -> bf16, down GEMM
 // reduce-added into the residual stream; then the final norm + codec_head GEMV.
-talker_status enqueue_prefill_tc(talker *t, int stream, const float *emb, int T, const ForwardOut &out,
-                                 int *n_kernels) {
+talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, const float *emb, int attn_splits,
+                         const ForwardOut &out, int *n_kernels) {
     const CacheView cv = cache_view(t);
     int nk = 0;
-    TRY_CUDA(cudaMemcpyAsync(t->x, emb, (size_t)T * t->H * sizeof(float), cudaMemcpyDeviceToDevice, t->st));
-    const RowMap rm{1, stream, 0, t->d_len};
+    TRY_CUDA(cudaMemcpyAsync(t->x, emb, (size_t)T * t->H * sizeof(float), cudaMemcpyDeviceToDevice, st));
     for (int l = 0; l < t->c.n_layers; ++l) {
         const LayerDev &d = t->L[l];
-        TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.in_norm, t->c.rms_eps, T, t->H, t->hb, t->st));
+        TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.in_norm, t->c.rms_eps, T, t->H, t->hb, st));
         ++nk;
-        TRY(tc_gemm(t, t->hb, T, t->H, d.qkv, t->qkv_n, t->raw, t->qkv_n, false, &nk));
+        TRY(tc_gemm(t, st, t->hb, T, t->H, d.qkv, t->qkv_n, t->raw, t->qkv_n, false, &nk));
         TRY_CUDA(launch_qkv_post(t->raw, T, t->nq, t->nkv, t->hd, d.q_norm, d.k_norm, t->d_rope, t->c.rms_eps, t->q,
-                                 cv, l, stream, 0, t->d_status, t->st));
+                                 cv, l, rm, t->d_status, st));
         ++nk;
         AttnParams a{};
         a.q = t->q;
@@ -651,20 +652,20 @@ talker_status enqueue_prefill_tc(talker *t, int stream, const float *emb, int T,
         a.n_q = t->nq;
         a.n_kv = t->nkv;
         a.group = t->G;
-        a.splits = 1;
+        a.splits = attn_splits;
         a.scale = 1.0f / sqrtf((float)t->hd);
         a.ws = t->attn_ws;
         a.cnt = t->attn_cnt;
         a.status = t->d_status;
-        TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, T, t->st, false));
+        TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, T, st, false));
         ++nk;
-        TRY(tc_gemm(t, t->ab, T, t->qd, d.o, t->H, t->x, t->H, true, &nk));
-        TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.post_norm, t->c.rms_eps, T, t->H, t->hb, t->st));
+        TRY(tc_gemm(t, st, t->ab, T, t->qd, d.o, t->H, t->x, t->H, true, &nk));
+        TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.post_norm, t->c.rms_eps, T, t->H, t->hb, st));
         ++nk;
-        TRY(tc_gemm(t, t->hb, T, t->H, d.gu, 2 * t->I, t->gu, 2 * t->I, false, &nk));
-        TRY_CUDA(launch_swiglu_bf16(t->gu, T, t->I, t->gb, t->st));
+        TRY(tc_gemm(t, st, t->hb, T, t->H, d.gu, 2 * t->I, t->gu, 2 * t->I, false, &nk));
+        TRY_CUDA(launch_swiglu_bf16(t->gu, T, t->I, t->gb, st));
         ++nk;
-        TRY(tc_gemm(t, t->gb, T, t->I, d.down, t->H, t->x, t->H, true, &nk));
+        TRY(tc_gemm(t, st, t->gb, T, t->I, d.down, t->H, t->x, t->H, true, &nk));
     }
     const int hrows = out.head_all_rows ? T : 1;
     GemvParams h{};
@@ -684,9 +685,9 @@ talker_status enqueue_prefill_tc(talker *t, int stream, const float *emb, int T,
     h.part_val = t->head_val;
     h.part_idx = t->head_idx;
     h.head_cnt = t->head_cnt;
-    h.inc_len = 0;
+    h.inc_len = out.inc_len;
     h.cur_len_rw = t->d_len;
-    TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, t->st, false));
+    TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, st, false));
     ++nk;
     *n_kernels = nk;
     return TALKER_OK;
@@ -711,7 +712,7 @@ talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float
     int nk = 0;
     if (T >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t)) {
         TRY(ensure_tc(t, T));
-        TRY(enqueue_prefill_tc(t, stream, emb, T, out, &nk));
+        TRY(enqueue_tc(t, t->st, T, rm, emb, 1, out, &nk));
     } else {
         TRY(enqueue_forward(t, t->st, T, rm, emb, 1, out, &nk));
     }
@@ -867,13 +868,19 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
     for (int b = 0; b < B; ++b)
         if (t->len[b] + 1 > t->max_seq) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));
-    if (t->decode_mode != 2 && persist_usable(t, B)) return decode_persistent(t, emb, B, logits, hidden, argmax);
+    if ((t->decode_mode == 0 || t->decode_mode == 1) && persist_usable(t, B))
+        return decode_persistent(t, emb, B, logits, hidden, argmax);
     if (t->decode_mode == 1) return TALKER_EINVAL;
+    const int kind = (t->decode_mode == 3 || (t->decode_mode == 0 && B >= kTcMinDecodeRows)) && tc_usable(t) ? 1 : 0;
+    if (t->decode_mode == 3 && kind == 0) return TALKER_EINVAL;
     const int splits = decode_splits(t, B);
     TRY(ensure_capacity(t, B, splits));
+    if (kind == 1) TRY(ensure_tc(t, B));
     GraphEntry *ge = nullptr;
     for (auto &g : t->graphs)
-        if (g.B == B && g.emb == emb && g.logits == logits && g.hidden == hidden && g.argmax == argmax) ge = &g;
+        if (g.kind == kind && g.B == B && g.emb == emb && g.logits == logits && g.hidden == hidden &&
+            g.argmax == argmax)
+            ge = &g;
     if (!ge) {
         if ((int)t->graphs.size() >= kMaxGraphs) {
             cudaGraphExecDestroy(t->graphs.front().exec);
@@ -884,7 +891,8 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
         int nk = 0;
         cudaGraph_t graph = nullptr;
         TRY_CUDA(cudaStreamBeginCapture(t->cap_st, cudaStreamCaptureModeThreadLocal));
-        talker_status s = enqueue_forward(t, t->cap_st, B, rm, emb, splits, out, &nk);
+        talker_status s = kind == 1 ? enqueue_tc(t, t->cap_st, B, rm, emb, splits, out, &nk)
+                                    : enqueue_forward(t, t->cap_st, B, rm, emb, splits, out, &nk);
         cudaError_t e = cudaStreamEndCapture(t->cap_st, &graph);
         if (s != TALKER_OK) {
             if (graph) cudaGraphDestroy(graph);
@@ -895,7 +903,7 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
         e = cudaGraphInstantiate(&exec, graph, 0);
         cudaGraphDestroy(graph);
         if (e != cudaSuccess) return from_cuda(e);
-        t->graphs.push_back(GraphEntry{B, emb, logits, hidden, argmax, exec, nk});
+        t->graphs.push_back(GraphEntry{kind, B, emb, logits, hidden, argmax, exec, nk});
         ge = &t->graphs.back();
     }
     TRY_CUDA(cudaGraphLaunch(ge->exec, t->st));
@@ -982,7 +990,7 @@ talker_status talker_set_prefill_mode(talker_t *t, int mode) {
 }
 
 talker_status talker_set_decode_mode(talker_t *t, int mode) {
-    if (!t || mode < 0 || mode > 2) return TALKER_EINVAL;
+    if (!t || mode < 0 || mode > 3) return TALKER_EINVAL;
     t->decode_mode = mode;
     return TALKER_OK;
 }

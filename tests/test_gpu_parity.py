@@ -134,3 +134,46 @@ def test_talker_prefill_all_rows_tensor_cores(cuda, T):
     hid2, lg2 = tk.prefill_all_rows(0, dev(emb))
     check_rows(host(lg2), rl, bf16=True, what="gemv prefill logits T=%d" % T)
     tk.close()
+
+
+@pytest.mark.parametrize("mode", [pytest.param(2, id="gemv-graph"), pytest.param(3, id="tensor-core-graph"),
+                                  pytest.param(0, id="auto")])
+def test_batched16_ragged_decode(cuda, mode):
+    """16 streams with ragged imported caches, 4 decode steps, against the oracle stream by stream."""
+    from kv_cached_qwen3_gb300.talker import Talker
+    g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 3})
+    w = inputs.make_weights(g, 31)
+    lens = inputs.make_start_lengths(31, 16, 60, 300)
+    steps = 4
+    max_seq = int(lens.max()) + steps + 1
+    o = Oracle(g, w)
+    oc = OracleCache(o, 16, max_seq)
+    tk = Talker(g, w)
+    tk.set_decode_mode(mode)
+    tk.kv_init_batched(16, max_seq)
+    for s in range(16):
+        L = int(lens[s])
+        ks, vs = [], []
+        for l in range(g.n_layers):
+            k, v = inputs.make_kv_layer(g, 31, l, L, stream=s)
+            ks.append(k)
+            vs.append(v)
+        K = np.stack(ks)
+        V = np.stack(vs)
+        oc.kv_import(s, K, V, L)
+        kt = torch.from_numpy(K).to(torch.bfloat16).cuda()
+        vt = torch.from_numpy(V).to(torch.bfloat16).cuda()
+        tk.kv_import(s, kt, vt, L)
+    lg = torch.empty(16, g.vocab, device="cuda")
+    hd = torch.empty(16, g.hidden, device="cuda")
+    am = torch.empty(16, device="cuda", dtype=torch.int32)
+    for t in range(steps):
+        emb = np.stack([inputs.make_embeddings(g, 31, t, t + 1, stream=s)[0] for s in range(16)])
+        tk.decode(dev(emb), lg, hd, am)
+        rh, rl = oc.decode(emb)
+        check_rows(host(hd), rh, bf16=True, what="batched hidden step %d" % t)
+        check_rows(host(lg), rl, bf16=True, what="batched logits step %d" % t)
+        np.testing.assert_array_equal(host(am).astype(np.int64), np.argmax(host(lg), axis=-1))
+    assert tk.sync_status() == 0
+    assert [tk.cur_len(s) for s in range(16)] == [int(L) + steps for L in lens]
+    tk.close()
