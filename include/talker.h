@@ -197,6 +197,29 @@ talker_status talker_set_attn_splits(talker_t *t, int max_splits);
 talker_status talker_set_trace(talker_t *t, unsigned long long *buf);
 int talker_trace_slots(void);
 
+/* Allocation-free codec_head + argmax, for callers that cannot allocate device
+ * memory (a real-time audio thread where cudaMalloc would stall, a host that
+ * hands the library fixed buffers only, a process whose allocator belongs to
+ * another framework). The pages have no counterpart: this is a packaging of
+ * the head kernel, not part of the method.
+ *   logits[r][v] = hidden[r] . W[v] (f32 accumulation), argmax[r] = the index of
+ *   the largest logit of row r, the lowest index on ties; 0 <= r < rows.
+ * hidden: device f32 [rows, hidden_size]; W: device [vocab, hidden_size] in
+ * weight_dtype (talker_dtype); logits: device f32 [rows, vocab]; argmax: device
+ * int32 [rows]; cuda_stream: cudaStream_t (NULL = legacy stream). No handle.
+ * The call allocates nothing: its scratch (per-CTA partial maxima and an
+ * arrival counter) is one fixed device array in the library, held by every GPU
+ * that loads the library until the process exits. Limits: rows <= 64 and
+ * vocab <= 8192; larger sizes return EINVAL. The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture. All calls share the
+ * array, so calls that may overlap on the GPU (other streams, other threads)
+ * race and give wrong results: serialise them. The arrival counter is put back
+ * to zero by every call. Asynchronous on cuda_stream.
+ * Errors: EINVAL, ECUDA. */
+talker_status talker_head_argmax_noalloc(const float *hidden, int rows, int hidden_size, const void *W, int vocab,
+                                         int weight_dtype, float *logits, int32_t *argmax, void *cuda_stream);
+
 /* Test support: count of kernel launches the library enqueued since creation
  * (a graph replay counts each of its kernels). */
 int64_t talker_kernel_launches(const talker_t *t);

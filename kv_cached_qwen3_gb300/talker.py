@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_set_trace": (st, [vp, vp]),
         "talker_set_attn_splits": (st, [vp, ctypes.c_int]),
         "talker_set_prefill_mode": (st, [vp, ctypes.c_int]),
+        "talker_head_argmax_noalloc": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, vp, vp,
+                                            vp]),
         "talker_test_gemm_bf16": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
                                        ctypes.c_int, vp]),
         "talker_trace_slots": (ctypes.c_int, []),
@@ -235,3 +237,15 @@ def test_gemm_bf16(A, B, out, accumulate=False, splits=1):
     if st != 0:
         raise TalkerError(st, "talker_test_gemm_bf16")
     return out
+
+
+def head_argmax_noalloc(hidden, W, logits, argmax, weight_dtype):
+    """logits = hidden @ W.T and per-row argmax through the allocation-free entry point."""
+    import torch
+    lib = load_library()
+    rows, H = hidden.shape
+    st = lib.talker_head_argmax_noalloc(_ptr(hidden), rows, H, _ptr(W), W.shape[0], DTYPE[weight_dtype],
+                                        _ptr(logits), _ptr(argmax),
+                                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if st != 0:
+        raise TalkerError(st, "talker_head_argmax_noalloc")
