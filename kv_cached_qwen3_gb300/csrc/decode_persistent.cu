@@ -50,11 +50,9 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-// GPU-scope relaxed accesses: the flag words are only shared by this GPU's SMs
-// (system-scope volatile accesses would also have to stay coherent with the host).
 __device__ __forceinline__ int ld_volatile(const int *p) {
     int v;
-    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.volatile.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ void red_release_add(int *p, int v) {
@@ -370,15 +368,15 @@ __device__ __forceinline__ unsigned long long ll_pack(float v, uint32_t f) {
     return ((unsigned long long)f << 32) | __float_as_uint(v);
 }
 __device__ __forceinline__ void st_ll(unsigned long long *p, float v, uint32_t f) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(ll_pack(v, f)) : "memory");
+    asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(ll_pack(v, f)) : "memory");
 }
 __device__ __forceinline__ unsigned long long ld_ll(const unsigned long long *p) {
     unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ void ld_ll2(const unsigned long long *p, unsigned long long &a, unsigned long long &b) {
-    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+    asm volatile("ld.volatile.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 __device__ __forceinline__ uint32_t ll_flag(unsigned long long w) { return (uint32_t)(w >> 32); }
 __device__ __forceinline__ float ll_val(unsigned long long w) { return __uint_as_float((uint32_t)w); }
