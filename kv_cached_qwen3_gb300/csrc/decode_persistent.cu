@@ -689,17 +689,59 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                     fence_proxy_async();   // generic writes into a slot that a later bulk copy refills
                     cbar();
                 }
+                // Scores: each warp takes rows j = warp + NCW * i, loads all of them first,
+                // forms every (row, head) partial dot, then reduces them in one interleaved
+                // butterfly, so the shuffle latency is paid once per warp, not per row.
                 constexpr int E = HD / 32;
-                for (int j = warp; j < kPage; j += NCW) {
-                    float kv[E];
+                constexpr int RPW = (kPage + NCW - 1) / NCW;   // rows per warp
+                float kv[RPW][E];
 #pragma unroll
-                    for (int e = 0; e < E; ++e) kv[e] = Elem<KT>::load(Ks, (size_t)j * HD + lane * E + e);
-                    for (int gi = 0; gi < G; ++gi) {
+                for (int i = 0; i < RPW; ++i) {
+                    const int j = warp + NCW * i;
+#pragma unroll
+                    for (int e = 0; e < E; ++e)
+                        kv[i][e] = (j < kPage) ? Elem<KT>::load(Ks, (size_t)j * HD + lane * E + e) : 0.f;
+                }
+                float qv[MAXG][E];
+#pragma unroll
+                for (int gi = 0; gi < MAXG; ++gi)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) qv[gi][e] = (gi < G) ? qs[gi * HD + lane * E + e] : 0.f;
+                float dv[RPW][MAXG];
+#pragma unroll
+                for (int i = 0; i < RPW; ++i)
+#pragma unroll
+                    for (int gi = 0; gi < MAXG; ++gi) {
                         float d = 0.f;
 #pragma unroll
-                        for (int e = 0; e < E; ++e) d = fmaf(qs[gi * HD + lane * E + e], kv[e], d);
-                        d = warp_sum(d);
-                        if (lane == 0) sc[gi * kPage + j] = (j < valid) ? d : -INFINITY;
+                        for (int e = 0; e < E; ++e) d = fmaf(qv[gi][e], kv[i][e], d);
+                        dv[i][gi] = d;
+                    }
+                if (G == 2) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                        for (int i = 0; i < RPW; ++i) {
+                            dv[i][0] += __shfl_xor_sync(0xffffffffu, dv[i][0], o);
+                            dv[i][1] += __shfl_xor_sync(0xffffffffu, dv[i][1], o);
+                        }
+                } else {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                        for (int i = 0; i < RPW; ++i)
+#pragma unroll
+                            for (int gi = 0; gi < MAXG; ++gi)
+                                if (gi < G) dv[i][gi] += __shfl_xor_sync(0xffffffffu, dv[i][gi], o);
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < RPW; ++i) {
+                        const int j = warp + NCW * i;
+                        if (j < kPage)
+#pragma unroll
+                            for (int gi = 0; gi < MAXG; ++gi)
+                                if (gi < G) sc[gi * kPage + j] = (j < valid) ? dv[i][gi] : -INFINITY;
                     }
                 }
                 cbar();
