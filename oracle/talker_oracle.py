@@ -287,3 +287,24 @@ class OracleCache:
         for s in range(B):
             self.cur_len[s] += 1
         return hid, logits
+
+
+def decode_row_lazy_cache(oracle: Oracle, x, pos, kv_layer):
+    """One decode row at position pos against a cache whose rows [0, pos) come from kv_layer(l).
+
+    kv_layer(l) returns (K, V) of layer l as [n_kv, >= pos, hd] arrays (the stored cache
+    values); the row's own k, v are appended at pos as in talker_forward_decode. Layers are
+    generated one at a time, so a long cache never has to be held for all layers at once.
+    Returns (hidden [H], logits [V]).
+    """
+    g = oracle.g
+    x = np.asarray(x, F64).reshape(1, -1)
+    for l in range(g.n_layers):
+        q, k, v = oracle.qkv(l, x, np.array([pos]))
+        Kp, Vp = kv_layer(l)
+        K = np.concatenate([np.asarray(Kp[:, :pos], F64), np.transpose(k, (1, 0, 2))], axis=1)
+        V = np.concatenate([np.asarray(Vp[:, :pos], F64), np.transpose(v, (1, 0, 2))], axis=1)
+        attn = attend_one(q[0], K, V, pos + 1)
+        x = oracle.post_attention(l, x, attn.reshape(1, -1))
+    hid, logits = oracle.head(x)
+    return hid[0], logits[0]

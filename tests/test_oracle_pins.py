@@ -393,3 +393,19 @@ def test_bf16_weights_are_representable():
     w = inputs.make_weights(g, 9)
     a = w["layers"][0]["q_proj"]
     assert np.all((a.view(np.uint32) & 0xFFFF) == 0)
+
+
+def test_lazy_cache_decode_equals_cached_decode(tiny):
+    """decode_row_lazy_cache against OracleCache.decode on an imported cache."""
+    from oracle import decode_row_lazy_cache
+    _, o = tiny
+    g = TINY
+    L = 37
+    layers = [inputs.make_kv_layer(g, 5, l, L) for l in range(g.n_layers)]
+    c = OracleCache(o, 1, 64)
+    c.kv_import(0, np.stack([k for k, _ in layers]), np.stack([v for _, v in layers]), L)
+    x = inputs.make_embeddings(g, 5, 0, 1)
+    h1, l1 = c.decode(x)
+    h2, l2 = decode_row_lazy_cache(o, x[0], L, lambda l: layers[l])
+    np.testing.assert_allclose(l2, l1[0], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(h2, h1[0], rtol=1e-13, atol=1e-14)
