@@ -214,15 +214,20 @@ def make_kv_layer(g: Geometry, seed: int, layer: int, length: int, stream: int =
     Row p of a (layer, head) does not depend on `length`: the draws are laid out position-major
     in chunks, [pos][head][dim].
     """
-    n = length * g.n_kv_heads * g.head_dim
+    nkv, hd = g.n_kv_heads, g.head_dim
+    n = length * nkv * hd
+    res = [np.empty((nkv, length, hd), np.float32) for _ in range(2)]
+    step = 512                                   # positions per conversion job
     with ThreadPoolExecutor(_threads()) as pool:
-        kz = _normal_chunked([seed + _KV_SEED_OFFSET, stream, layer, 0], n, pool)
-        vz = _normal_chunked([seed + _KV_SEED_OFFSET, stream, layer, 1], n, pool)
-    res = []
-    for z in (kz, vz):
-        a = z.astype(np.float32).reshape(length, g.n_kv_heads, g.head_dim).transpose(1, 0, 2)
-        a = np.ascontiguousarray(a)
-        if g.kv_dtype == "bf16":
-            a = round_to_bf16(a)
-        res.append(a)
+        zs = [_normal_chunked([seed + _KV_SEED_OFFSET, stream, layer, kind], n, pool) for kind in (0, 1)]
+
+        def convert(job):
+            kind, p0 = job
+            p1 = min(length, p0 + step)
+            src = zs[kind][p0 * nkv * hd:p1 * nkv * hd].reshape(p1 - p0, nkv, hd)
+            res[kind][:, p0:p1, :] = src.transpose(1, 0, 2)
+
+        list(pool.map(convert, [(kind, p0) for kind in (0, 1) for p0 in range(0, length, step)]))
+    if g.kv_dtype == "bf16":
+        res = [round_to_bf16(a) for a in res]
     return res[0], res[1]
