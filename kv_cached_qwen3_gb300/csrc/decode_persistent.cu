@@ -178,11 +178,25 @@ __device__ void producer(const PersistParams &p, unsigned char *ring, uint64_t *
     const int P = gridDim.x, cta = blockIdx.x;
     const size_t wsz = sizeof(WT);
     const int qkv_n = (p.nq + 2 * p.nkv) * p.hd;
+    unsigned long long *trace = p.trace != nullptr ? p.trace + (size_t)cta * kTraceSlots : nullptr;
     uint32_t k = 0;
+    // With tracing on, the producer stamps when each issued chunk has landed (seen while it waits).
+    uint32_t landed = 0;
+    auto poll_landed = [&]() {
+        while (landed < k && mbar_test_wait(&full[landed % NS], (landed / NS) & 1)) {
+            if (landed < (uint32_t)kTraceChunks) trace[kTraceDots + landed] = clock64();
+            ++landed;
+        }
+    };
     auto issue = [&](const void *s1, uint32_t b1, const void *s2, uint32_t b2) {
         const int slot = k % NS;
         const uint32_t use = k / NS;
-        if (use > 0) ring_wait(&empty[slot], (use - 1) & 1, c);
+        if (use > 0) {
+            if (trace)
+                for (int it = 0; it < (1 << 20) && !mbar_test_wait(&empty[slot], (use - 1) & 1); ++it) poll_landed();
+            ring_wait(&empty[slot], (use - 1) & 1, c);
+        }
+        if (trace && k < (uint32_t)kTraceChunks) trace[kTraceProducer + k] = clock64();
         if (!*c.abort_s) {
             unsigned char *dst = ring + (size_t)slot * SLOT;
             mbar_arrive_expect_tx(&full[slot], b1 + b2);
@@ -230,6 +244,7 @@ struct Ring {
     unsigned long long *trace;   // this CTA's trace row (consumer thread 0 only) or null
     __device__ __forceinline__ const unsigned char *acquire(const Ctx &c) {
         ring_wait(&full[k % NS], (k / NS) & 1, c);
+        if (trace && k < (uint32_t)kTraceChunks) trace[kTraceAcquire + k] = clock64();
         return base + (size_t)(k % NS) * SLOT;
     }
     // Every consumer warp arrives once per slot (the empty barrier counts NCW arrivals).
@@ -407,6 +422,20 @@ __device__ __noinline__ unsigned long long repoll_ll(const unsigned long long *p
     }
 }
 
+// Bounded wait shared by the batch polls below: true once the caller should stop
+// (grid abort seen, or the 1 s limit passed, which raises the abort).
+__device__ __noinline__ bool poll_give_up(long long t0, const Ctx &c) {
+    if (*c.abort_s || ld_volatile(c.abort_g)) {
+        *c.abort_s = 1;
+        return true;
+    }
+    if (clock64() - t0 > kWaitLimitCycles) {
+        raise_abort(c);
+        return true;
+    }
+    return false;
+}
+
 // Flags: one per (step, layer, tensor). base = step epoch * 256, never 0.
 enum : uint32_t { FL_RAW = 0, FL_PART = 1, FL_O = 2, FL_X1 = 3, FL_ACT = 4, FL_X2 = 5 };
 __device__ __forceinline__ uint32_t flag_of(uint32_t base, int layer, uint32_t what) {
@@ -422,6 +451,7 @@ template <int EPV, int R>
 __device__ void stage_ll(float *act, const unsigned long long *src, int ld, int K, int rows, uint32_t flag,
                          const float *gain, float eps, float *red, int ctid, const Ctx &c) {
     constexpr int NP = (R * KCAP / 2 + NCT - 1) / NCT;
+    static_assert(NP <= 32, "stale mask holds 32 pairs");
     const int K2 = K >> 1;
     const int total = rows * K2;
     const int warp = ctid >> 5, lane = ctid & 31;
@@ -438,14 +468,33 @@ __device__ void stage_ll(float *act, const unsigned long long *src, int ld, int 
 #pragma unroll
     for (int r = 0; r < R; ++r) ss[r] = 0.f;
     cbar();   // every warp is done reading the previous contents of act (the loads above are in flight)
+    // Re-read every stale pair together, so that one polling round costs one round trip.
+    uint32_t stale = 0;
+#pragma unroll
+    for (int i = 0; i < NP; ++i)
+        if (ctid + i * NCT < total && (ll_flag(wa[i]) != flag || ll_flag(wb[i]) != flag)) stale |= 1u << i;
+    if (stale != 0 && !*c.abort_s) {
+        const long long t0 = clock64();
+        for (uint32_t it = 1; stale != 0; ++it) {
+            __nanosleep(64);
+#pragma unroll
+            for (int i = 0; i < NP; ++i)
+                if (stale & (1u << i)) {
+                    const int idx = ctid + i * NCT;
+                    const int r = idx / K2, k = (idx - r * K2) * 2;
+                    ld_ll2(src + (size_t)r * ld + k, wa[i], wb[i]);
+                }
+#pragma unroll
+            for (int i = 0; i < NP; ++i)
+                if ((stale & (1u << i)) && ll_flag(wa[i]) == flag && ll_flag(wb[i]) == flag) stale &= ~(1u << i);
+            if (stale != 0 && (it & 15) == 0 && poll_give_up(t0, c)) break;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
         const int idx = ctid + i * NCT;
         if (idx < total) {
             const int r = idx / K2, k = (idx - r * K2) * 2;
-            const unsigned long long *pp = src + (size_t)r * ld + k;
-            if (ll_flag(wa[i]) != flag) wa[i] = repoll_ll(pp, flag, c);
-            if (ll_flag(wb[i]) != flag) wb[i] = repoll_ll(pp + 1, flag, c);
             const float v0 = ll_val(wa[i]), v1 = ll_val(wb[i]);
             act[aidx<EPV>(r, k, K)] = v0;
             act[aidx<EPV>(r, k + 1, K)] = v1;
@@ -618,14 +667,30 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                         wv[2 * t + 1] = ld_ll(src + i + half);
                     }
                 }
+                // word 2t + u sits at src + lane + 32t + u * half; stale words are re-read together
+                uint32_t stale = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (lane + 32 * (q >> 1) < half && ll_flag(wv[q]) != f) stale |= 1u << q;
+                if (stale != 0 && !*c.abort_s) {
+                    const long long t0 = clock64();
+                    for (uint32_t it = 1; stale != 0; ++it) {
+                        __nanosleep(64);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (stale & (1u << q)) wv[q] = ld_ll(src + lane + 32 * (q >> 1) + (q & 1) * half);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if ((stale & (1u << q)) && ll_flag(wv[q]) == f) stale &= ~(1u << q);
+                        if (stale != 0 && (it & 15) == 0 && poll_give_up(t0, c)) break;
+                    }
+                }
                 float a[2], b[2];
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const int i = lane + 32 * t;
                     a[t] = b[t] = 0.f;
                     if (i < half) {
-                        if (ll_flag(wv[2 * t]) != f) wv[2 * t] = repoll_ll(src + i, f, c);
-                        if (ll_flag(wv[2 * t + 1]) != f) wv[2 * t + 1] = repoll_ll(src + i + half, f, c);
                         a[t] = ll_val(wv[2 * t]);
                         b[t] = ll_val(wv[2 * t + 1]);
                     }
@@ -777,6 +842,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                 rc.release(lane);
                 cbar();
             }
+            TR(tb + 5);
             const int hq0 = g * G;
             unsigned long long *orow = p.o_ll + (size_t)r * qd;
             const uint32_t fo = flag_of(p.flag_base, l, FL_O);
@@ -821,14 +887,25 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
 #pragma unroll
                     for (int sp = 1; sp < kMaxSplits; ++sp)
                         if (sp < ns) wv2[sp] = ld_ll(wb + (size_t)sp * WS);
+                    uint32_t stale = 0;
 #pragma unroll
-                    for (int sp = 1; sp < kMaxSplits; ++sp) {
-                        ov[sp] = 0.f;
-                        if (sp < ns) {
-                            if (ll_flag(wv2[sp]) != fp) wv2[sp] = repoll_ll(wb + (size_t)sp * WS, fp, c);
-                            ov[sp] = ll_val(wv2[sp]);
+                    for (int sp = 1; sp < kMaxSplits; ++sp)
+                        if (sp < ns && ll_flag(wv2[sp]) != fp) stale |= 1u << sp;
+                    if (stale != 0 && !*c.abort_s) {
+                        const long long t0 = clock64();
+                        for (uint32_t it = 1; stale != 0; ++it) {
+                            __nanosleep(64);
+#pragma unroll
+                            for (int sp = 1; sp < kMaxSplits; ++sp)
+                                if (stale & (1u << sp)) wv2[sp] = ld_ll(wb + (size_t)sp * WS);
+#pragma unroll
+                            for (int sp = 1; sp < kMaxSplits; ++sp)
+                                if ((stale & (1u << sp)) && ll_flag(wv2[sp]) == fp) stale &= ~(1u << sp);
+                            if (stale != 0 && (it & 15) == 0 && poll_give_up(t0, c)) break;
                         }
                     }
+#pragma unroll
+                    for (int sp = 1; sp < kMaxSplits; ++sp) ov[sp] = (sp < ns) ? ll_val(wv2[sp]) : 0.f;
                 };
                 auto combine_o = [&](int idx, float own_o, float (&ov)[kMaxSplits]) {
                     const int gi = idx / HD, d = idx - gi * HD;
@@ -861,6 +938,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode_persistent(const PersistParams
                     ml_s[ctid][0][1] = l_s[ctid];
                 }
                 cbar();
+                TR(tb + 8);
                 if (ctid < G * HD) combine_o(ctid, o_acc[0], ov);
 #pragma unroll
                 for (int o = 1; o < NO; ++o) {

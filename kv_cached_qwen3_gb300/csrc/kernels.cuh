@@ -132,7 +132,7 @@ constexpr int kTraceAcquire = 1280;
 constexpr int kTraceDots = 2048;
 constexpr int kTraceEpi = 2816;
 constexpr int kTraceChunks = 768;
-constexpr int kTracePerLayer = 15;
+constexpr int kTracePerLayer = 16;
 
 // Tensor-core GEMM C[M, N] (+)= A[M, K] B[N, K]^T, bf16 inputs, fp32 output.
 struct GemmParams {
