@@ -158,6 +158,10 @@ cudaError_t launch_set_len(int *cur_len, int stream, int value, cudaStream_t st)
 // Copy len rows of a stream between a dense [n_layers][n_kv][len][hd] buffer and the cache.
 cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *dense_v, int len, int to_cache,
                            cudaStream_t st);
+// Causal prefill attention on the tensor cores (bf16 cache, head_dim 64 or 128, row map
+// mode 1, bf16 output).
+bool attn_prefill_supported(int kv_bf16, int head_dim);
+cudaError_t launch_attn_prefill(int head_dim, const AttnParams &a, int T, cudaStream_t st);
 cudaError_t prepare_kernels();  // raise dynamic shared-memory limits once per process
 
 bool gemm_tc_supported(int N, int K);

@@ -8,6 +8,7 @@ namespace talker_k {
 
 cudaError_t prepare_gemv();
 cudaError_t prepare_attn();
+cudaError_t prepare_attn_prefill();
 
 __global__ void k_set_len(int *cur_len, int stream, int value) { cur_len[stream] = value; }
 
@@ -53,6 +54,8 @@ cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *
 
 cudaError_t prepare_kernels() {
     cudaError_t e = prepare_gemv();
+    if (e != cudaSuccess) return e;
+    e = prepare_attn_prefill();
     if (e != cudaSuccess) return e;
     return prepare_attn();
 }

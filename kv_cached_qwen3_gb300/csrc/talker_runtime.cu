@@ -657,7 +657,10 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         a.ws = t->attn_ws;
         a.cnt = t->attn_cnt;
         a.status = t->d_status;
-        TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, T, st, false));
+        if (rm.mode == 1 && attn_prefill_supported(t->kv_bf16, t->hd))
+            TRY_CUDA(launch_attn_prefill(t->hd, a, T, st));   // causal tiles on the tensor cores
+        else
+            TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, T, st, false));
         ++nk;
         TRY(tc_gemm(t, st, t->ab, T, t->qd, d.o, t->H, t->x, t->H, true, &nk));
         TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.post_norm, t->c.rms_eps, T, t->H, t->hb, st));
