@@ -263,7 +263,61 @@ def side_measurements(tk, g, wl, torch, st, emb_all, pre, hbm, tc):
     out["batched16"] = {"streams": int(b.n_streams), "steps_per_s": 1.0 / s, "tokens_per_s": b.n_streams / s,
                         "ms_per_step": s * 1e3, "hbm_frac": (wbytes + kvb) / s / 1e9 / hbm,
                         "start_lengths": [int(x) for x in lens]}
+    out["long_context"] = long_context(tk, g, torch, st, hbm, tc)
     return out
+
+
+def timed(torch, st, fn, reps):
+    """Average seconds of fn() over reps runs, CUDA events on the library's stream."""
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(st)
+    for _ in range(reps):
+        fn()
+    ev1.record(st)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / 1e3 / reps
+
+
+def long_context(tk, g, torch, st, hbm, tc):
+    """Prefill T=4096 (tokens/s, tensor-core FLOP rate) and single-stream decode at 8K/16K/32K cached rows."""
+    lc = inputs.WORKLOADS["long_context"]
+    T = lc.prefill_T
+    res = {}
+    tk.kv_init_batched(1, max(lc.long_lengths) + 8)
+    emb = torch.randn(T, g.hidden, device="cuda")
+    for _ in range(2):
+        tk.prefill(0, emb)
+    torch.cuda.synchronize()
+    s = timed(torch, st, lambda: tk.prefill(0, emb), 3)
+    layer_params = g.n_linear_params() - g.vocab * g.hidden
+    gemm = 2.0 * layer_params * T
+    attn = 4.0 * g.n_layers * g.n_q_heads * g.head_dim * T * (T + 1) / 2
+    res["prefill"] = {"T": T, "ms": s * 1e3, "tokens_per_s": T / s, "gemm_tflop": gemm / 1e12,
+                      "attention_tflop": attn / 1e12, "tflops": (gemm + attn) / s / 1e12,
+                      "frac_bf16_peak": (gemm + attn) / s / 1e12 / tc}
+    kvd = torch.bfloat16 if g.kv_dtype == "bf16" else torch.float32
+    e1 = torch.randn(1, g.hidden, device="cuda")
+    lg = torch.empty(1, g.vocab, device="cuda")
+    wbytes, _ = step_bytes(g, 0)
+    res["decode"] = []
+    for L in lc.long_lengths:
+        kk = torch.randn(g.n_layers, g.n_kv_heads, L, g.head_dim, device="cuda").to(kvd)
+        vv = torch.randn(g.n_layers, g.n_kv_heads, L, g.head_dim, device="cuda").to(kvd)
+        tk.kv_import(0, kk, vv, L)
+        del kk, vv
+        steps = 5
+
+        def run():
+            tk.rewind(0, L)
+            for _ in range(steps):
+                tk.decode(e1, lg)
+        run()
+        torch.cuda.synchronize()
+        s = timed(torch, st, run, 2) / steps
+        kvb = step_bytes(g, L + steps // 2)[1]
+        res["decode"].append({"L": L, "ms_per_step": s * 1e3, "steps_per_s": 1.0 / s,
+                              "hbm_frac": (wbytes + kvb) / s / 1e9 / hbm})
+    return res
 
 
 # ----------------------------------------------------------------------------- oracle arms

@@ -162,11 +162,11 @@ const char *talker_status_str(talker_status s);
  * ENOMEM (static thread-local buffer; empty if none). */
 const char *talker_last_error(void);
 
-/* Choose how talker_decode runs a step: 0 = automatic (the persistent kernel
- * when it fits: B <= 4, one cooperative CTA per SM, weight rows and KV page
- * pairs within one 32 KB ring slot; B >= 8 with bf16 weights: the CUDA graph
- * of tensor-core GEMMs; otherwise the CUDA graph of GEMV kernels), 1 = always
- * the persistent kernel, 2 = always the GEMV graph, 3 = always the tensor-core
+/* Choose how talker_decode runs a step: 0 = automatic (B >= 4 with bf16
+ * weights: the CUDA graph of tensor-core GEMMs; otherwise the CUDA graph of
+ * GEMV kernels), 1 = the persistent kernel (one cooperative CTA per SM; needs
+ * B <= 4, a GQA group <= 8, weight rows and KV page pairs within
+ * one 32 KB ring slot), 2 = always the GEMV graph, 3 = always the tensor-core
  * graph (talker_decode returns EINVAL where the chosen path cannot run).
  * Errors: EINVAL. */
 talker_status talker_set_decode_mode(talker_t *t, int mode);

@@ -54,7 +54,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
     const int G = p.group;
 
     pdl_launch_dependents();
-    pdl_wait();
+    // Decode rows: before the wait on the previous kernel (which writes q and this step's
+    // k / v row) only data of earlier launches is read: the length, the page table and the
+    // cached pages. The page holding position pos is patched with the fresh row after the
+    // wait. Prefill rows (all of them fresh) wait first.
+    if (p.rowmap.mode != 0) pdl_wait();
 
     const int s = attn_row_stream(p.rowmap, r);
     const int pos = attn_row_pos(p.rowmap, r);
@@ -87,6 +91,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
         bulk_g2s(kbuf, kpool + off, kTileBytes, &bars[0]);
         bulk_g2s(vbuf, vpool + off, kTileBytes, &bars[0]);
     }
+    pdl_wait();
     const float *qsrc = p.q + (size_t)r * p.n_q * HD + (size_t)g * G * HD;
     for (int i = tid; i < G * HD; i += kAttnThreads) q_s[i] = qsrc[i] * p.scale;
     if (tid < G) {
@@ -120,6 +125,14 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
         const KT *Ks = kbuf + buf * kPage * HD;
         const KT *Vs = vbuf + buf * kPage * HD;
         const int valid = min(kPage, nvis - pg * kPage);
+        if (pg == npages - 1) {   // the fresh row (written by the previous kernel) over the copied page
+            const size_t off = (size_t)ptab[pg] * p.cache.page_elems + head_off + (size_t)(pos % kPage) * HD;
+            for (int i = tid; i < HD; i += kAttnThreads) {
+                kbuf[buf * kPage * HD + (pos % kPage) * HD + i] = kpool[off + i];
+                vbuf[buf * kPage * HD + (pos % kPage) * HD + i] = vpool[off + i];
+            }
+            __syncthreads();
+        }
 
         // scores: one warp per key row, lanes split the head dimension
         for (int j = warp; j < kPage; j += kAttnThreads / 32) {

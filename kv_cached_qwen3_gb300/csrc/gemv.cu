@@ -153,33 +153,52 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
                                                : make_uint4(0u, 0u, 0u, 0u);
             }
         if (base == 0) {
-            // Activations are produced by the previous kernel: wait for it only now.
+            // Activations are produced by the previous kernel: wait for it only now. All
+            // threads stage the rows (one round trip), then the RMSNorm is reduced from
+            // shared memory and applied in place.
             pdl_wait();
-            if (NORM) {
-                for (int r = warp; r < nrows; r += kGemvWarps) {
-                    const float *a = p.act + (size_t)(row0 + r) * p.act_ld;
-                    float ss = 0.f;
-                    for (int k = lane; k < K; k += 32) {
-                        const float v = a[k];
-                        ss += v * v;
-                    }
-                    ss = warp_sum(ss);
-                    if (lane == 0) inv_s[r] = 1.0f / sqrtf(ss / (float)K + p.eps);
-                }
-                __syncthreads();
-            }
             const int K4 = K >> 2;
             const bool do_copy = (p.copy_x != nullptr) && blockIdx.x == 0;
+            float ss[ROWS];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) ss[r] = 0.f;
             for (int idx = threadIdx.x; idx < nrows * K4; idx += kGemvThreads) {
                 const int r = idx / K4, k = (idx - r * K4) * 4;
                 const float4 v = *reinterpret_cast<const float4 *>(p.act + (size_t)(row0 + r) * p.act_ld + k);
                 if (do_copy) *reinterpret_cast<float4 *>(p.copy_x + (size_t)(row0 + r) * K + k) = v;
-                float e[4] = {v.x, v.y, v.z, v.w};
+                *reinterpret_cast<float4 *>(act_s + act_index<EPV>(r, k, K)) = v;
                 if (NORM) {
+                    const float q = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) e[t] = e[t] * inv_s[r] * p.norm_w[k + t];
+                    for (int rr = 0; rr < ROWS; ++rr)
+                        if (rr == r) ss[rr] += q;
                 }
-                *reinterpret_cast<float4 *>(act_s + act_index<EPV>(r, k, K)) = make_float4(e[0], e[1], e[2], e[3]);
+            }
+            if (NORM) {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const float t = warp_sum(ss[r]);
+                    if (lane == 0) hv_s[warp][r] = t;
+                }
+                __syncthreads();
+                if (threadIdx.x < nrows) {
+                    float t = 0.f;
+                    for (int w = 0; w < kGemvWarps; ++w) t += hv_s[w][threadIdx.x];
+                    inv_s[threadIdx.x] = 1.0f / sqrtf(t / (float)K + p.eps);
+                }
+                __syncthreads();
+                for (int idx = threadIdx.x; idx < nrows * K4; idx += kGemvThreads) {
+                    const int r = idx / K4, k = (idx - r * K4) * 4;
+                    float4 *a = reinterpret_cast<float4 *>(act_s + act_index<EPV>(r, k, K));
+                    const float4 g = *reinterpret_cast<const float4 *>(p.norm_w + k);
+                    float4 v = *a;
+                    const float iv = inv_s[r];
+                    v.x = v.x * iv * g.x;
+                    v.y = v.y * iv * g.y;
+                    v.z = v.z * iv * g.z;
+                    v.w = v.w * iv * g.w;
+                    *a = v;
+                }
             }
             __syncthreads();
         }
@@ -300,11 +319,12 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
         __syncthreads();
         if (flag_s) {
             __threadfence();
-            if (threadIdx.x < nrows) {
-                const int r = threadIdx.x;
+            // the last CTA reduces the per-CTA partials of each row with the whole block:
+            // strided loads (all in flight together), then warp and block argmax (lowest index on ties)
+            for (int r = 0; r < nrows; ++r) {
                 float best = -INFINITY;
                 int bi = 0x7fffffff;
-                for (int b = 0; b < (int)gridDim.x; ++b) {
+                for (int b = threadIdx.x; b < (int)gridDim.x; b += kGemvThreads) {
                     const size_t slot = ((size_t)rb * gridDim.x + b) * ROWS + r;
                     const float v = __ldcg(p.part_val + slot);
                     const int i = __ldcg(p.part_idx + slot);
@@ -313,8 +333,30 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
                         bi = i;
                     }
                 }
-                if (p.argmax_out != nullptr) p.argmax_out[row0 + r] = bi;
-                if (p.inc_len) p.cur_len_rw[row0 + r] += 1;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float v2 = __shfl_xor_sync(0xffffffffu, best, o);
+                    const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+                    if (v2 > best || (v2 == best && i2 < bi)) {
+                        best = v2;
+                        bi = i2;
+                    }
+                }
+                if (lane == 0) {
+                    hv_s[warp][0] = best;
+                    hi_s[warp][0] = bi;
+                }
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    for (int w = 1; w < kGemvWarps; ++w)
+                        if (hv_s[w][0] > best || (hv_s[w][0] == best && hi_s[w][0] < bi)) {
+                            best = hv_s[w][0];
+                            bi = hi_s[w][0];
+                        }
+                    if (p.argmax_out != nullptr) p.argmax_out[row0 + r] = bi;
+                    if (p.inc_len) p.cur_len_rw[row0 + r] += 1;
+                }
+                __syncthreads();
             }
             if (threadIdx.x == 0) p.head_cnt[rb] = 0;
         }

@@ -590,7 +590,7 @@ talker_status decode_persistent(talker *t, const float *emb, int B, float *logit
 
 
 constexpr int kTcMinRows = 16;        // prefills shorter than this stay on the GEMV kernels
-constexpr int kTcMinDecodeRows = 8;   // decode batches at least this wide use the tensor-core GEMMs
+constexpr int kTcMinDecodeRows = 4;   // decode batches at least this wide use the tensor-core GEMMs
 
 bool tc_usable(talker *t) {
     if (t->tc_ok < 0) {
@@ -871,8 +871,9 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
     for (int b = 0; b < B; ++b)
         if (t->len[b] + 1 > t->max_seq) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));
-    if ((t->decode_mode == 0 || t->decode_mode == 1) && persist_usable(t, B))
-        return decode_persistent(t, emb, B, logits, hidden, argmax);
+    // The persistent kernel runs on request only: on GB300 the graph of per-phase kernels
+    // is faster at every batch and length measured.
+    if (t->decode_mode == 1 && persist_usable(t, B)) return decode_persistent(t, emb, B, logits, hidden, argmax);
     if (t->decode_mode == 1) return TALKER_EINVAL;
     const int kind = (t->decode_mode == 3 || (t->decode_mode == 0 && B >= kTcMinDecodeRows)) && tc_usable(t) ? 1 : 0;
     if (t->decode_mode == 3 && kind == 0) return TALKER_EINVAL;
