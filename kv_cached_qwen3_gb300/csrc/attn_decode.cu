@@ -32,7 +32,8 @@ __device__ __forceinline__ int attn_row_pos(const RowMap &m, int r) {
 
 size_t attn_smem_bytes(int kv_bf16, int head_dim, int group) {
     const size_t esz = kv_bf16 ? 2 : 4;
-    return 4 * (size_t)kPage * head_dim * esz + (size_t)group * head_dim * 4 + (size_t)group * kPage * 4;
+    return 4 * (size_t)kPage * head_dim * esz + (size_t)group * head_dim * 4 + (size_t)group * kPage * 4 +
+           2 * (size_t)head_dim * esz;
 }
 
 template <typename KT, int HD>
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
     KT *vbuf = kbuf + 2 * kPage * HD;                                   // [2][kPage*HD]
     float *q_s = reinterpret_cast<float *>(vbuf + 2 * kPage * HD);      // [G][HD]
     float *sc = q_s + p.group * HD;                                     // [G][kPage]
+    KT *knew = reinterpret_cast<KT *>(sc + p.group * kPage);            // this step's k, v row
+    KT *vnew = knew + HD;
     __shared__ float m_s[kMaxGroup], l_s[kMaxGroup], al_s[kMaxGroup];
     __shared__ __align__(8) uint64_t bars[2];
     __shared__ int flag_s;
@@ -92,8 +95,60 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
         bulk_g2s(vbuf, vpool + off, kTileBytes, &bars[0]);
     }
     pdl_wait();
-    const float *qsrc = p.q + (size_t)r * p.n_q * HD + (size_t)g * G * HD;
-    for (int i = tid; i < G * HD; i += kAttnThreads) q_s[i] = qsrc[i] * p.scale;
+    if (p.raw == nullptr) {
+        const float *qsrc = p.q + (size_t)r * p.n_q * HD + (size_t)g * G * HD;
+        for (int i = tid; i < G * HD; i += kAttnThreads) q_s[i] = qsrc[i] * p.scale;
+    } else {
+        // heads of this group from the raw projections: q heads g*G.., k head g, v head g;
+        // QK-norm and RoPE ("talker-forward.h", talker_layer_forward), k / v appended by split 0
+        constexpr int half = HD / 2;
+        for (int hh = warp; hh < G + 2; hh += kAttnThreads / 32) {
+            const int hidx = hh < G ? g * G + hh : (hh == G ? p.n_q + g : p.n_q + p.n_kv + g);
+            const float *src = p.raw + (size_t)r * p.qkv_n + (size_t)hidx * HD;
+            float a[2], b[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = lane + 32 * j;
+                a[j] = (i < half) ? src[i] : 0.f;
+                b[j] = (i < half) ? src[i + half] : 0.f;
+            }
+            if (hh <= G) {
+                const float *gain = hh < G ? p.q_norm : p.k_norm;
+                const float ss = warp_sum(a[0] * a[0] + b[0] * b[0] + a[1] * a[1] + b[1] * b[1]);
+                const float inv = 1.0f / sqrtf(ss / (float)HD + p.eps);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int i = lane + 32 * j;
+                    if (i < half) {
+                        const float x0 = a[j] * inv * gain[i], x1 = b[j] * inv * gain[i + half];
+                        const float2 cs = p.rope[(size_t)pos * half + i];
+                        a[j] = x0 * cs.x - x1 * cs.y;
+                        b[j] = x1 * cs.x + x0 * cs.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = lane + 32 * j;
+                if (i >= half) continue;
+                if (hh < G) {
+                    q_s[hh * HD + i] = a[j] * p.scale;
+                    q_s[hh * HD + i + half] = b[j] * p.scale;
+                } else {
+                    KT *d = hh == G ? knew : vnew;
+                    Elem<KT>::store(d, i, a[j]);
+                    Elem<KT>::store(d, i + half, b[j]);
+                    if (sidx == 0) {   // the cache keeps the row for later steps
+                        const size_t off = (size_t)ptab[pos / kPage] * p.cache.page_elems + head_off +
+                                           (size_t)(pos % kPage) * HD;
+                        KT *c = const_cast<KT *>(hh == G ? kpool : vpool) + off;
+                        Elem<KT>::store(c, i, a[j]);
+                        Elem<KT>::store(c, i + half, b[j]);
+                    }
+                }
+            }
+        }
+    }
     if (tid < G) {
         m_s[tid] = -INFINITY;
         l_s[tid] = 0.f;
@@ -125,11 +180,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
         const KT *Ks = kbuf + buf * kPage * HD;
         const KT *Vs = vbuf + buf * kPage * HD;
         const int valid = min(kPage, nvis - pg * kPage);
-        if (pg == npages - 1) {   // the fresh row (written by the previous kernel) over the copied page
+        if (pg == npages - 1) {   // the fresh row over the copied page
             const size_t off = (size_t)ptab[pg] * p.cache.page_elems + head_off + (size_t)(pos % kPage) * HD;
             for (int i = tid; i < HD; i += kAttnThreads) {
-                kbuf[buf * kPage * HD + (pos % kPage) * HD + i] = kpool[off + i];
-                vbuf[buf * kPage * HD + (pos % kPage) * HD + i] = vpool[off + i];
+                kbuf[buf * kPage * HD + (pos % kPage) * HD + i] = p.raw ? knew[i] : kpool[off + i];
+                vbuf[buf * kPage * HD + (pos % kPage) * HD + i] = p.raw ? vnew[i] : vpool[off + i];
             }
             __syncthreads();
         }

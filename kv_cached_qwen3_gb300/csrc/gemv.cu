@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
         }
     }
 
-    if (EPI == EPI_QKV) {
+    if (EPI == EPI_QKV && p.q_out != nullptr) {
         __threadfence();
         __syncthreads();
         const int hidx = (blockIdx.x * kGemvWarps) / p.head_dim;

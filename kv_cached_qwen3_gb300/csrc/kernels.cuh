@@ -56,7 +56,7 @@ struct GemvParams {
     int layer, n_q, n_kv, head_dim;
     const float *q_norm, *k_norm;
     const float2 *rope;  // [max_seq][head_dim/2] (cos, sin)
-    float *q_out;        // [rows, n_q*head_dim]
+    float *q_out;        // [rows, n_q*head_dim]; null: raw projections only (attention finishes the heads)
     CacheView cache;
     RowMap rowmap;
     int *cnt;            // per (row block, head) completion counters, zero between launches
@@ -84,6 +84,14 @@ struct AttnParams {
     float *ws;           // partials [rows][n_q][splits][hd + 4]
     int *cnt;            // [rows][n_kv] completion counters, zero between launches
     int *status;
+    // Decode rows only (row map mode 0): when raw != null, q is not read; each CTA takes
+    // its heads from the raw projections [rows][qkv_n], applies QK-norm (q_norm / k_norm
+    // gains, eps) and RoPE at the row's position, and split 0 appends k / v to the cache.
+    const float *raw;
+    int qkv_n;
+    const float *q_norm, *k_norm;
+    const float2 *rope;  // [max_seq][head_dim/2] (cos, sin)
+    float eps;
 };
 
 // One layer's weights as the persistent decode kernel reads them (device array).

@@ -348,6 +348,16 @@ struct ForwardOut {
 // Enqueue the whole forward for `rows` rows: per layer QKV (+QK-norm, RoPE, KV
 // append), attention, o_proj + residual, gate/up SwiGLU, down + residual; then
 // the final norm + codec_head (+argmax). Returns the number of kernels enqueued
+// Decode attention reads the raw q|k|v projections and finishes the heads itself.
+void set_raw_heads(const talker *t, const LayerDev &d, AttnParams &a) {
+    a.raw = t->raw;
+    a.qkv_n = t->qkv_n;
+    a.q_norm = d.q_norm;
+    a.k_norm = d.k_norm;
+    a.rope = t->d_rope;
+    a.eps = t->c.rms_eps;
+}
+
 // through *n_kernels.
 talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap &rm, const float *emb,
                               int splits, const ForwardOut &out, int *n_kernels) {
@@ -378,7 +388,8 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
         p.q_norm = d.q_norm;
         p.k_norm = d.k_norm;
         p.rope = t->d_rope;
-        p.q_out = t->q;
+        // decode rows: the attention kernel finishes the heads from the raw projections
+        p.q_out = rm.mode == 0 ? nullptr : t->q;
         p.cache = cv;
         p.rowmap = rm;
         p.cnt = t->qkv_cnt;
@@ -401,6 +412,7 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
         a.ws = t->attn_ws;
         a.cnt = t->attn_cnt;
         a.status = t->d_status;
+        if (rm.mode == 0) set_raw_heads(t, d, a);
         TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, rows, st, pdl));
         ++nk;
         // 3) o_proj + residual
@@ -639,9 +651,11 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.in_norm, t->c.rms_eps, T, t->H, t->hb, st));
         ++nk;
         TRY(tc_gemm(t, st, t->hb, T, t->H, d.qkv, t->qkv_n, t->raw, t->qkv_n, false, &nk));
-        TRY_CUDA(launch_qkv_post(t->raw, T, t->nq, t->nkv, t->hd, d.q_norm, d.k_norm, t->d_rope, t->c.rms_eps, t->q,
-                                 cv, l, rm, t->d_status, st));
-        ++nk;
+        if (rm.mode != 0) {   // prefill rows; decode rows are finished inside the attention kernel
+            TRY_CUDA(launch_qkv_post(t->raw, T, t->nq, t->nkv, t->hd, d.q_norm, d.k_norm, t->d_rope, t->c.rms_eps,
+                                     t->q, cv, l, rm, t->d_status, st));
+            ++nk;
+        }
         AttnParams a{};
         a.q = t->q;
         a.out = t->ab;
@@ -657,6 +671,7 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         a.ws = t->attn_ws;
         a.cnt = t->attn_cnt;
         a.status = t->d_status;
+        if (rm.mode == 0) set_raw_heads(t, d, a);
         if (rm.mode == 1 && attn_prefill_supported(t->kv_bf16, t->hd))
             TRY_CUDA(launch_attn_prefill(t->hd, a, T, st));   // causal tiles on the tensor cores
         else
