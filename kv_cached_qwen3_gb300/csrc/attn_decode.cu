@@ -189,17 +189,47 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
             __syncthreads();
         }
 
-        // scores: one warp per key row, lanes split the head dimension
-        for (int j = warp; j < kPage; j += kAttnThreads / 32) {
-            float kv[E];
+        // scores: warp w takes key rows w, w + 8, ...; lanes split the head dimension. All of a
+        // warp's rows and heads are reduced in one interleaved butterfly (latency paid once).
+        {
+            constexpr int NWARP = kAttnThreads / 32;
+            constexpr int RPW = kPage / NWARP;   // rows per warp
+            float kv[RPW][E];
 #pragma unroll
-            for (int e = 0; e < E; ++e) kv[e] = Elem<KT>::load(Ks, (size_t)j * HD + lane * E + e);
-            for (int gi = 0; gi < G; ++gi) {
-                float d = 0.f;
+            for (int i = 0; i < RPW; ++i)
 #pragma unroll
-                for (int e = 0; e < E; ++e) d = fmaf(q_s[gi * HD + lane * E + e], kv[e], d);
-                d = warp_sum(d);
-                if (lane == 0) sc[gi * kPage + j] = (j < valid) ? d : -INFINITY;
+                for (int e = 0; e < E; ++e) kv[i][e] = Elem<KT>::load(Ks, (size_t)(warp + NWARP * i) * HD + lane * E + e);
+            for (int gi0 = 0; gi0 < G; gi0 += 2) {   // two heads per pass keeps the register count bounded
+                float dv[RPW][2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int gi = min(gi0 + u, G - 1);
+                    float qv[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) qv[e] = q_s[gi * HD + lane * E + e];
+#pragma unroll
+                    for (int i = 0; i < RPW; ++i) {
+                        float d = 0.f;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) d = fmaf(qv[e], kv[i][e], d);
+                        dv[i][u] = d;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int i = 0; i < RPW; ++i) {
+                        dv[i][0] += __shfl_xor_sync(0xffffffffu, dv[i][0], o);
+                        dv[i][1] += __shfl_xor_sync(0xffffffffu, dv[i][1], o);
+                    }
+                if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < RPW; ++i) {
+                        const int j = warp + NWARP * i;
+                        sc[gi0 * kPage + j] = (j < valid) ? dv[i][0] : -INFINITY;
+                        if (gi0 + 1 < G) sc[(gi0 + 1) * kPage + j] = (j < valid) ? dv[i][1] : -INFINITY;
+                    }
+                }
             }
         }
         __syncthreads();
@@ -229,10 +259,19 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
             const int idx = tid + o * kAttnThreads;
             if (idx < G * HD) {
                 const int gi = idx / HD, d = idx - gi * HD;
-                float a = o_acc[o] * al_s[gi];
+                // four independent chains over the page's rows
+                float a0 = o_acc[o] * al_s[gi], a1 = 0.f, a2 = 0.f, a3 = 0.f;
                 const float *pj = sc + gi * kPage;
-                for (int j = 0; j < valid; ++j) a = fmaf(pj[j], Elem<KT>::load(Vs, (size_t)j * HD + d), a);
-                o_acc[o] = a;
+                const KT *vd = Vs + d;
+                int j = 0;
+                for (; j + 4 <= valid; j += 4) {
+                    a0 = fmaf(pj[j], Elem<KT>::load(vd, (size_t)j * HD), a0);
+                    a1 = fmaf(pj[j + 1], Elem<KT>::load(vd, (size_t)(j + 1) * HD), a1);
+                    a2 = fmaf(pj[j + 2], Elem<KT>::load(vd, (size_t)(j + 2) * HD), a2);
+                    a3 = fmaf(pj[j + 3], Elem<KT>::load(vd, (size_t)(j + 3) * HD), a3);
+                }
+                for (; j < valid; ++j) a0 = fmaf(pj[j], Elem<KT>::load(vd, (size_t)j * HD), a0);
+                o_acc[o] = (a0 + a1) + (a2 + a3);
             }
         }
         __syncthreads();
