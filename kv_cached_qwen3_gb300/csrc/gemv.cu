@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
     for (int n = 0; n < NW; ++n)
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) acc[n][r] = 0.f;
+    float resid = 0.f;   // EPI_RESID: this lane's residual value, fetched right after the wait
 
     for (int base = 0; base < nvec; base += 32 * MAXC) {
         uint4 w[NW][MAXC];
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
             // threads stage the rows (one round trip), then the RMSNorm is reduced from
             // shared memory and applied in place.
             pdl_wait();
+            if (EPI == EPI_RESID && lane < nrows && fvalid) resid = p.out[(size_t)(row0 + lane) * p.out_ld + f];
             const int K4 = K >> 2;
             const bool do_copy = (p.copy_x != nullptr) && blockIdx.x == 0;
             float ss[ROWS];
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
         }
         if (lane == r && r < nrows && fvalid) {
             float *o = p.out + (size_t)(row0 + r) * p.out_ld + f;
-            if (EPI == EPI_RESID) *o += v0;
+            if (EPI == EPI_RESID) *o = resid + v0;
             else if (EPI == EPI_SWIGLU) *o = silu_f(v0) * v1;
             else *o = v0;
         }
