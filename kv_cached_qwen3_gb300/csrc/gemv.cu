@@ -112,11 +112,13 @@ __device__ void finish_head(const GemvParams &p, int hidx, int row0, int nrows) 
     }
 }
 
-template <typename WT, int ROWS, int EPI>
+// VPL: 16-byte weight vectors a lane holds in flight per weight row (sized to K at
+// launch, so that short rows leave registers free and more CTAs fit on an SM).
+template <typename WT, int ROWS, int EPI, int VPL>
 __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
     constexpr int EPV = Elem<WT>::kPerVec;
     constexpr int NW = (EPI == EPI_SWIGLU) ? 2 : 1;
-    constexpr int MAXC = (NW == 2) ? 8 : 16;
+    constexpr int MAXC = VPL;
     constexpr bool NORM = (EPI != EPI_RESID);
     extern __shared__ __align__(16) float act_s[];
     __shared__ float inv_s[ROWS];
@@ -369,8 +371,8 @@ int gemv_rows_for(int rows) { return rows <= 1 ? 1 : (rows <= 4 ? 4 : 16); }
 
 size_t gemv_smem_bytes(int rows_tmpl, int K) { return (size_t)rows_tmpl * K * sizeof(float); }
 
-template <typename WT, int ROWS, int EPI>
-static cudaError_t launch_one(const GemvParams &p, cudaStream_t st, bool pdl) {
+template <typename WT, int ROWS, int EPI, int VPL>
+static cudaError_t launch_vpl(const GemvParams &p, cudaStream_t st, bool pdl) {
     const int nfeat = p.n_out;
     dim3 grid((nfeat + kGemvWarps - 1) / kGemvWarps, (p.rows + ROWS - 1) / ROWS, 1);
     cudaLaunchConfig_t cfg = {};
@@ -383,7 +385,23 @@ static cudaError_t launch_one(const GemvParams &p, cudaStream_t st, bool pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_gemv<WT, ROWS, EPI>, p);
+    return cudaLaunchKernelEx(&cfg, k_gemv<WT, ROWS, EPI, VPL>, p);
+}
+
+// Vectors per lane of one weight row, rounded up to an instantiated size.
+template <typename WT>
+static int vpl_for(int K) {
+    const int v = (K / Elem<WT>::kPerVec + 31) / 32;
+    return v <= 4 ? 4 : (v <= 8 ? 8 : 16);
+}
+
+template <typename WT, int ROWS, int EPI>
+static cudaError_t launch_one(const GemvParams &p, cudaStream_t st, bool pdl) {
+    switch (vpl_for<WT>(p.K)) {
+        case 4: return launch_vpl<WT, ROWS, EPI, 4>(p, st, pdl);
+        case 8: return launch_vpl<WT, ROWS, EPI, 8>(p, st, pdl);
+    }
+    return launch_vpl<WT, ROWS, EPI, 16>(p, st, pdl);
 }
 
 template <typename WT, int ROWS>
@@ -412,15 +430,23 @@ cudaError_t launch_gemv(int epi, int w_bf16, int rows_tmpl, const GemvParams &p,
     return launch_wt<float>(epi, rows_tmpl, p, st, pdl);
 }
 
-template <typename WT, int ROWS>
-static cudaError_t raise_rows() {
+template <typename WT, int ROWS, int VPL>
+static cudaError_t raise_vpl() {
     const int bytes = 200 * 1024;
     cudaError_t e = cudaSuccess;
-    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_QKV, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_RESID, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_SWIGLU, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     bytes);
+    e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_HEAD, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     return e;
+}
+
+template <typename WT, int ROWS>
+static cudaError_t raise_rows() {
+    cudaError_t e = raise_vpl<WT, ROWS, 4>();
+    e = e ? e : raise_vpl<WT, ROWS, 8>();
+    return e ? e : raise_vpl<WT, ROWS, 16>();
 }
 
 cudaError_t prepare_gemv() {
