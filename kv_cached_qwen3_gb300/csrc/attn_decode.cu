@@ -36,6 +36,59 @@ size_t attn_smem_bytes(int kv_bf16, int head_dim, int group) {
            2 * (size_t)head_dim * esz;
 }
 
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Combination of the splits of one (row, KV group) when they form one thread-block
+// cluster: every CTA leaves its (m, l, o) in its own shared memory (o_part, m_part,
+// l_part; an empty split has m = -inf), the cluster synchronises, CTA rank 0 reads the
+// partials of all ranks through distributed shared memory in rank order and writes the
+// output row, and a second cluster barrier keeps every CTA (and its shared memory) alive
+// until rank 0 is done. Every CTA of the cluster calls this exactly once.
+template <int HD>
+__device__ void cluster_combine(const AttnParams &p, bool has, const float *o_part, float *m_part, float *l_part,
+                                int r, int g) {
+    const int G = p.group, tid = threadIdx.x;
+    if (!has && tid < G) {
+        m_part[tid] = -INFINITY;
+        l_part[tid] = 0.f;
+    }
+    __syncthreads();
+    cluster_sync_all();
+    uint32_t rank, nranks;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(nranks));
+    if (rank == 0) {
+        const size_t out_row = (size_t)r * p.n_q * HD;
+        for (int idx = tid; idx < G * HD; idx += kAttnThreads) {
+            const int gi = idx / HD, d = idx - gi * HD;
+            float M = -INFINITY;
+            for (uint32_t c = 0; c < nranks; ++c) M = fmaxf(M, ld_cluster_f32(m_part + gi, c));
+            float L = 0.f, O = 0.f;
+            for (uint32_t c = 0; c < nranks; ++c) {
+                const float mc = ld_cluster_f32(m_part + gi, c);
+                if (mc == -INFINITY) continue;
+                const float f = expf(mc - M);
+                L = fmaf(ld_cluster_f32(l_part + gi, c), f, L);
+                O = fmaf(ld_cluster_f32(o_part + idx, c), f, O);
+            }
+            const float v = O / L;
+            const size_t oi = out_row + (size_t)(g * G + gi) * HD + d;
+            if (p.out_bf16) static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(v);
+            else static_cast<float *>(p.out)[oi] = v;
+        }
+    }
+    cluster_sync_all();
+}
+
 template <typename KT, int HD>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p) {
     constexpr int E = HD / 32;                       // elements of a key row per lane
@@ -75,7 +128,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
     const int pb = sidx * per;
     const int pe = min(pb + per, npages);
     const int nact = (npages + per - 1) / per;
-    if (pb >= pe) return;
+    if (pb >= pe) {   // no pages for this split
+        if (p.cluster && nact > 1) cluster_combine<HD>(p, false, q_s, m_s, l_s, r, g);
+        return;
+    }
 
     const int *ptab = p.cache.page_table + (size_t)s * p.cache.pages_per_stream;
     const size_t head_off = (size_t)(p.layer * p.cache.n_kv + g) * kPage * HD;
@@ -93,6 +149,14 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
         mbar_arrive_expect_tx(&bars[0], 2 * kTileBytes);
         bulk_g2s(kbuf, kpool + off, kTileBytes, &bars[0]);
         bulk_g2s(vbuf, vpool + off, kTileBytes, &bars[0]);
+    }
+    // the RoPE row of this position (a table of earlier launches) is fetched before the wait
+    constexpr int half_hd = HD / 2;
+    float2 cs_pre[2] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
+    if (p.raw != nullptr && warp <= G) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (lane + 32 * j < half_hd) cs_pre[j] = p.rope[(size_t)pos * half_hd + lane + 32 * j];
     }
     pdl_wait();
     if (p.raw == nullptr) {
@@ -121,7 +185,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
                     const int i = lane + 32 * j;
                     if (i < half) {
                         const float x0 = a[j] * inv * gain[i], x1 = b[j] * inv * gain[i + half];
-                        const float2 cs = p.rope[(size_t)pos * half + i];
+                        const float2 cs = (hh == warp) ? cs_pre[j] : p.rope[(size_t)pos * half + i];
                         a[j] = x0 * cs.x - x1 * cs.y;
                         b[j] = x1 * cs.x + x0 * cs.y;
                     }
@@ -284,6 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
             if (pb + fail_it + 1 < pe) mbar_wait(&bars[(fail_it + 1) & 1], ((fail_it + 1) >> 1) & 1, p.status);
         }
         __syncthreads();
+        if (p.cluster && nact > 1) cluster_combine<HD>(p, false, q_s, m_s, l_s, r, g);
         return;
     }
 
@@ -301,6 +366,16 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
                 else static_cast<float *>(p.out)[oi] = v;
             }
         }
+        return;
+    }
+
+    if (p.cluster) {   // splits of this (row, group) form one cluster: combine on chip
+#pragma unroll
+        for (int o = 0; o < NO; ++o) {
+            const int idx = tid + o * kAttnThreads;
+            if (idx < G * HD) q_s[idx] = o_acc[o];
+        }
+        cluster_combine<HD>(p, true, q_s, m_s, l_s, r, g);
         return;
     }
 
@@ -355,11 +430,19 @@ static cudaError_t launch_attn_t(const AttnParams &p, int rows, cudaStream_t st,
     cfg.blockDim = dim3(kAttnThreads, 1, 1);
     cfg.dynamicSmemBytes = attn_smem_bytes(sizeof(KT) == 2, HD, p.group);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.cluster) {   // all splits of a (row, KV group) in one cluster
+        if (p.splits > kAttnClusterMax) return cudaErrorInvalidValue;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = p.splits;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, k_attn_decode<KT, HD>, p);
 }
 

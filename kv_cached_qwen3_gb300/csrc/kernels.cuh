@@ -92,7 +92,11 @@ struct AttnParams {
     const float *q_norm, *k_norm;
     const float2 *rope;  // [max_seq][head_dim/2] (cos, sin)
     float eps;
+    // 1: the splits of a (row, KV group) run as one thread-block cluster (splits <=
+    // kAttnClusterMax) and combine through distributed shared memory; ws / cnt unused
+    int cluster;
 };
+constexpr int kAttnClusterMax = 8;   // portable cluster size
 
 // One layer's weights as the persistent decode kernel reads them (device array).
 struct PersistLayer {

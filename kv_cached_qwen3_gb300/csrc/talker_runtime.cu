@@ -27,6 +27,7 @@ struct LayerDev {
 struct GraphEntry {
     int kind;   // 0: GEMV kernels, 1: tensor-core GEMMs
     int B;
+    int splits, cluster;   // attention splits per (row, KV group); 1: splits combine inside a cluster
     const float *emb;
     float *logits, *hidden;
     int32_t *argmax;
@@ -92,6 +93,7 @@ struct talker {
     std::vector<GraphEntry> graphs;
     // persistent decode kernel
     int decode_mode = 0;                 // 0 auto, 1 persistent kernel, 2 multi-kernel CUDA graph
+    int attn_cluster = 0;   // decode attention: splits combine inside a thread-block cluster
     PersistLayer *d_layers = nullptr;    // device copy of the layer pointer table
     int *d_sync = nullptr;               // counter words of the persistent kernel
     unsigned long long *ll = nullptr;    // flag-word buffers of the persistent kernel (one allocation)
@@ -408,6 +410,7 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
         a.n_kv = t->nkv;
         a.group = t->G;
         a.splits = splits;
+        a.cluster = rm.mode == 0 ? t->attn_cluster : 0;
         a.scale = 1.0f / sqrtf((float)t->hd);
         a.ws = t->attn_ws;
         a.cnt = t->attn_cnt;
@@ -667,6 +670,7 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         a.n_kv = t->nkv;
         a.group = t->G;
         a.splits = attn_splits;
+        a.cluster = rm.mode == 0 ? t->attn_cluster : 0;
         a.scale = 1.0f / sqrtf((float)t->hd);
         a.ws = t->attn_ws;
         a.cnt = t->attn_cnt;
@@ -892,13 +896,19 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
     if (t->decode_mode == 1) return TALKER_EINVAL;
     const int kind = (t->decode_mode == 3 || (t->decode_mode == 0 && B >= kTcMinDecodeRows)) && tc_usable(t) ? 1 : 0;
     if (t->decode_mode == 3 && kind == 0) return TALKER_EINVAL;
-    const int splits = decode_splits(t, B);
+    // One or two short streams: the splits of a (row, KV group) form one thread-block cluster
+    // (one page per split) and combine on chip; otherwise more splits, combined through L2
+    // (measured faster there on GB300).
+    int max_len = 0;
+    for (int b = 0; b < B; ++b) max_len = std::max(max_len, t->len[b]);
+    const int cluster = (B <= 2 && max_len + 1 <= kAttnClusterMax * kPageRows) ? 1 : 0;
+    const int splits = cluster ? kAttnClusterMax : decode_splits(t, B);
     TRY(ensure_capacity(t, B, splits));
     if (kind == 1) TRY(ensure_tc(t, B));
     GraphEntry *ge = nullptr;
     for (auto &g : t->graphs)
-        if (g.kind == kind && g.B == B && g.emb == emb && g.logits == logits && g.hidden == hidden &&
-            g.argmax == argmax)
+        if (g.kind == kind && g.B == B && g.splits == splits && g.cluster == cluster && g.emb == emb &&
+            g.logits == logits && g.hidden == hidden && g.argmax == argmax)
             ge = &g;
     if (!ge) {
         if ((int)t->graphs.size() >= kMaxGraphs) {
@@ -909,6 +919,7 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
         ForwardOut out{logits, hidden, argmax, true, 1};
         int nk = 0;
         cudaGraph_t graph = nullptr;
+        t->attn_cluster = cluster;
         TRY_CUDA(cudaStreamBeginCapture(t->cap_st, cudaStreamCaptureModeThreadLocal));
         talker_status s = kind == 1 ? enqueue_tc(t, t->cap_st, B, rm, emb, splits, out, &nk)
                                     : enqueue_forward(t, t->cap_st, B, rm, emb, splits, out, &nk);
@@ -922,7 +933,7 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
         e = cudaGraphInstantiate(&exec, graph, 0);
         cudaGraphDestroy(graph);
         if (e != cudaSuccess) return from_cuda(e);
-        t->graphs.push_back(GraphEntry{kind, B, emb, logits, hidden, argmax, exec, nk});
+        t->graphs.push_back(GraphEntry{kind, B, splits, cluster, emb, logits, hidden, argmax, exec, nk});
         ge = &t->graphs.back();
     }
     TRY_CUDA(cudaGraphLaunch(ge->exec, t->st));
