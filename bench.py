@@ -28,6 +28,11 @@ sys.path.insert(0, ROOT)
 from kv_cached_qwen3_gb300 import inputs  # noqa: E402
 
 METRIC = "decode steps/s (B=1, B=16) + prefill tok/s; % of HBM / bf16 TC roofline"
+# DRAM read + write of one decode step (all kernels of the graph) from one ncu capture of the current
+# kernels (profiles/decode_step_graph_talker_b1.md); set to None whenever a decode kernel changes.
+STEP_TRAFFIC = {"bytes": 907597824,
+                "note": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the 141 kernels of one decode "
+                        "step at cache length 100, where the algorithmic bytes are 898.8 MB"}
 UNIT = "steps/s"
 
 
@@ -39,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the prefill and batched side measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
+                    help="profiling aid: run `--steps` prefills of T rows on the Talker geometry and print their time")
     return ap.parse_args()
 
 
@@ -203,7 +210,7 @@ def run_ours(args, rank, world, local_rank):
                    "global_batch": world, "seq_len": T0 + K, "parallelism": "replicas (dp%d)" % world,
                    "l2": "inputs larger than L2 (887 MB of weights streamed per step)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "peak_kind": peak_kind,
+                     "traffic": STEP_TRAFFIC["bytes"], "traffic_note": STEP_TRAFFIC["note"], "peak_kind": peak_kind,
                      "kernel": "decode step (one CUDA graph of %d kernels)" % per_step_kernels,
                      "algorithmic_bytes_per_step": total_bytes / K},
         "e2e": {"value": world * K / e2e_secs, "unit": UNIT, "h2d_bytes_per_step": g.hidden * 4,
@@ -357,6 +364,24 @@ def run_reference(args, rank, world):
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def prefill_only(T, steps, warmup):
+    """Prefill of T rows (Talker geometry, long-context weights), `steps` timed runs after `warmup`."""
+    import torch
+    from kv_cached_qwen3_gb300.talker import Talker
+    lc = inputs.WORKLOADS["long_context"]
+    g = lc.geometry
+    tk = Talker(g, inputs.make_weights(g, lc.seed))
+    tk.kv_init_batched(1, T + 8)
+    emb = torch.from_numpy(inputs.make_embeddings(g, lc.seed, 0, T)).cuda()
+    for _ in range(warmup):
+        tk.prefill(0, emb)
+    torch.cuda.synchronize()
+    s = timed(torch, tk.stream, lambda: tk.prefill(0, emb), steps)
+    out = {"prefill_only": {"T": T, "ms": s * 1e3, "tokens_per_s": T / s, "status": tk.sync_status()}}
+    tk.close()
+    return out
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
@@ -370,6 +395,9 @@ def main():
         res = run_reference(args, rank, world)
         if res is not None:
             print(json.dumps(res))
+        return
+    if args.prefill_only:
+        print(json.dumps(prefill_only(args.prefill_only, max(1, args.steps), max(1, args.warmup))))
         return
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
