@@ -197,6 +197,160 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// Persistent variant: one CTA per SM walks the tile list (tile t = blockIdx.x, +gridDim.x,
+// ...; each tile is (row block, column block, K split)). The accumulator is double
+// buffered in TMEM (2 x BN columns): while warps 2..5 drain tile j from buffer j & 1,
+// the MMA thread already accumulates tile j + 1 into the other buffer, and the producer
+// keeps the shared-memory ring full across tile boundaries.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_gemm_tc_persist(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                      const GemmParams p, int splits) {
+    constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
+    constexpr uint32_t IDESC = instr_desc(BM, BN);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *sA = smem;
+    unsigned char *sB = smem + STAGES * A_BYTES;
+    __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int fail_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_n = p.N / BN, tiles_m = (p.M + BM - 1) / BM;
+    const int n_tiles = tiles_m * tiles_n * splits;
+    const int nk_total = p.K / BK;
+    const int per = (nk_total + splits - 1) / splits;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);   // one arrival per epilogue warp
+        }
+        fail_s = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_s)),
+                     "r"((uint32_t)(2 * BN))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    // tile t -> (row block, column block, split); column blocks vary fastest
+    auto tile_of = [&](int t, int &m0, int &n0, int &kb0, int &nk) {
+        const int sp = t / (tiles_m * tiles_n), rem = t - sp * tiles_m * tiles_n;
+        m0 = (rem / tiles_n) * BM;
+        n0 = (rem % tiles_n) * BN;
+        kb0 = sp * per;
+        nk = max(0, min(per, nk_total - kb0));
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer: one ring across all tiles of this CTA
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            int m0, n0, kb0, nk;
+            tile_of(t, m0, n0, kb0, nk);
+            for (int i = 0; i < nk; ++i, ++it) {
+                const int s = it % STAGES;
+                if (it >= (uint32_t)STAGES && !mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, p.status)) {
+                    fail_s = 1;
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+                tma_load_2d(sA + s * A_BYTES, &map_a, (kb0 + i) * BK, m0, &full[s]);
+                tma_load_2d(sB + s * B_BYTES, &map_b, (kb0 + i) * BK, n0, &full[s]);
+            }
+        }
+        // let the last copies land before the CTA can exit (no-op when they were consumed)
+        for (uint32_t j = (it > (uint32_t)STAGES ? it - STAGES : 0); j < it; ++j)
+            mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.status);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        uint32_t it = 0;
+        int j = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++j) {
+            int m0, n0, kb0, nk;
+            tile_of(t, m0, n0, kb0, nk);
+            const int b = j & 1;
+            if (j >= 2 && !mbar_wait(&tempty[b], ((j >> 1) - 1) & 1, p.status)) {
+                fail_s = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc = tmem + (uint32_t)(b * BN);
+            for (int i = 0; i < nk; ++i, ++it) {
+                const int s = it % STAGES;
+                if (!mbar_wait(&full[s], (it / STAGES) & 1, p.status)) {
+                    fail_s = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + s * A_BYTES), b0 = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_bf16(acc, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), IDESC, (i > 0 || k > 0) ? 1u : 0u);
+                umma_commit(&empty[s]);
+            }
+            umma_commit(&tfull[b]);   // arrives once this tile's MMAs have completed
+        }
+    } else if (warp >= 2) {
+        // ---- epilogue: TMEM lane quadrant (warp % 4) holds tile rows 32*(warp%4) .. +31
+        const int q = warp & 3;
+        int j = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+            int m0, n0, kb0, nk;
+            tile_of(t, m0, n0, kb0, nk);
+            const int b = j & 1;
+            const bool ok = mbar_wait(&tfull[b], (j >> 1) & 1, p.status);
+            tc_fence_after();
+            if (!ok || fail_s) break;
+            const int row = m0 + q * 32 + lane;
+            if (nk > 0) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), v);
+                    if (row < p.M) {
+                        float *o = p.out + (size_t)row * p.ld_out + n0 + c * 32;
+                        if (p.accumulate) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) red_add_v4(o + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4 *>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);   // this warp's quadrant of buffer b is free
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)(2 * BN))
+                     : "memory");
+    }
+}
+
 }  // namespace tc
 }  // namespace talker_k
 
@@ -250,9 +404,23 @@ int gemm_tc_splits(int M, int N, int K, int n_sm) {
 }
 
 cudaError_t prepare_gemm_tc() {
-    return cudaFuncSetAttribute(tc::k_gemm_tc<kBN, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tc::k_gemm_tc<kBN, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kGemmSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tc::k_gemm_tc_persist<kBN, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kGemmSmem);
 }
+
+namespace {
+int sm_count_current() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0 && cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cached[dev] = 0;
+    return cached[dev];
+}
+}  // namespace
 
 cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, float *out, int ld_out, int accumulate,
                            int splits, int *status, cudaStream_t st) {
@@ -267,8 +435,12 @@ cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, fl
     p.ld_out = ld_out;
     p.accumulate = (accumulate || splits > 1) ? 1 : 0;
     p.status = status;
-    dim3 grid(N / kBN, (M + tc::BM - 1) / tc::BM, std::max(1, splits));
-    tc::k_gemm_tc<kBN, kStages><<<grid, tc::NTHREADS, kGemmSmem, st>>>(ma, mb, p);
+    const int s = std::max(1, splits);
+    const int n_tiles = (N / kBN) * ((M + tc::BM - 1) / tc::BM) * s;
+    const int n_sm = sm_count_current();
+    if (n_sm <= 0) return cudaErrorInvalidDevice;
+    // persistent: one CTA per SM over the tile list, TMEM accumulators double buffered
+    tc::k_gemm_tc_persist<kBN, kStages><<<std::min(n_tiles, n_sm), tc::NTHREADS, kGemmSmem, st>>>(ma, mb, p, s);
     return cudaGetLastError();
 }
 
