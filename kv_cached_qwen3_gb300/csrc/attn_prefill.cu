@@ -20,8 +20,8 @@ using namespace talker_dev;
 namespace talker_k {
 namespace {
 
-constexpr int kBM = 64;    // query rows per CTA
-constexpr int kWarps = 4;  // 16 query rows per warp
+constexpr int kBM = 64;    // query rows per CTA (per head)
+constexpr int kWarpsPerHead = 4;   // 16 query rows per warp
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -69,8 +69,10 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 // q: f32 rows [T][n_q * HD] (QK-normed, rotated, unscaled); out: bf16 rows [T][n_q * HD].
 // Query row r sits at position pos0 + r of stream `stream`; the cache already holds the
 // keys and values of positions [0, pos0 + T).
-template <int HD>
-__global__ void __launch_bounds__(kWarps * 32) k_attn_prefill(const float *q, __nv_bfloat16 *out, int T, int pos0,
+// HPC q heads of one KV group per CTA (warps 4*i..4*i+3 take head i): each K / V page
+// staged in shared memory serves all of them.
+template <int HD, int HPC>
+__global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const float *q, __nv_bfloat16 *out, int T, int pos0,
                                                                int stream, int n_q, int group, int layer,
                                                                float scale_log2, CacheView cache) {
     constexpr int NKS = HD / 16;        // k-steps of S = Q K^T
@@ -79,13 +81,14 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_prefill(const float *q, __
     constexpr int CHUNKS = TILE * 2 / 16;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t sbase = smem_u32(smem);   // [2 buffers][K, V][TILE] bf16
+    constexpr int NTH = kWarpsPerHead * HPC * 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, t4 = lane & 3;
     const int qt = gridDim.x - 1 - blockIdx.x;   // longest tiles first
-    const int h = blockIdx.y;
-    const int kvh = h / group;
+    const int h = blockIdx.y * HPC + warp / kWarpsPerHead;
+    const int kvh = (blockIdx.y * HPC) / group;
     const int qd = n_q * HD;
-    const int row0 = qt * kBM + warp * 16;       // this warp's first query row
+    const int row0 = qt * kBM + (warp % kWarpsPerHead) * 16;   // this warp's first query row
 
     // Q fragments (A operand, row-major 16 x HD), scaled for base-2 exponentials
     uint32_t qa[NKS][4];
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_prefill(const float *q, __
         const size_t off = (size_t)ptab[kb] * cache.page_elems + head_off;
         const __nv_bfloat16 *ks = kpool + off, *vs = vpool + off;
         const uint32_t kdst = sbase + (uint32_t)(buf * 2) * TILE * 2, vdst = kdst + TILE * 2;
-        for (int i = threadIdx.x; i < CHUNKS; i += kWarps * 32) {
+        for (int i = threadIdx.x; i < CHUNKS; i += NTH) {
             const int r = i / (HD / 8), c = i % (HD / 8);
             cp_async16(kdst + swz<HD>(r, c), ks + r * HD + c * 8);
             cp_async16(vdst + swz<HD>(r, c), vs + r * HD + c * 8);
@@ -242,33 +245,40 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn_prefill(const float *q, __
 }
 
 template <int HD>
-constexpr size_t ap_smem() {
+constexpr size_t ap_smem() {   // (independent of the heads per CTA)
     return (size_t)2 * 2 * kPage * HD * 2;   // two buffers of a K page and a V page
 }
 
-template <int HD>
+template <int HD, int HPC>
 static cudaError_t launch_ap(const AttnParams &a, int T, cudaStream_t st) {
-    const dim3 grid((T + kBM - 1) / kBM, a.n_q);
+    const dim3 grid((T + kBM - 1) / kBM, a.n_q / HPC);
     const float scale_log2 = a.scale * 1.4426950408889634f;
-    k_attn_prefill<HD><<<grid, kWarps * 32, ap_smem<HD>(), st>>>(a.q, static_cast<__nv_bfloat16 *>(a.out), T,
-                                                                 a.rowmap.pos0, a.rowmap.stream0, a.n_q, a.group,
-                                                                 a.layer, scale_log2, a.cache);
+    k_attn_prefill<HD, HPC><<<grid, kWarpsPerHead * HPC * 32, ap_smem<HD>(), st>>>(
+        a.q, static_cast<__nv_bfloat16 *>(a.out), T, a.rowmap.pos0, a.rowmap.stream0, a.n_q, a.group, a.layer,
+        scale_log2, a.cache);
     return cudaGetLastError();
 }
 
+template <int HD, int HPC>
+static cudaError_t raise_ap() {
+    return cudaFuncSetAttribute(k_attn_prefill<HD, HPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)ap_smem<HD>());
+}
+
 cudaError_t prepare_attn_prefill() {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)ap_smem<128>());
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_attn_prefill<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ap_smem<64>());
+    cudaError_t e = raise_ap<128, 1>();
+    e = e ? e : raise_ap<128, 2>();
+    e = e ? e : raise_ap<64, 1>();
+    return e ? e : raise_ap<64, 2>();
 }
 
 bool attn_prefill_supported(int kv_bf16, int head_dim) { return kv_bf16 && (head_dim == 64 || head_dim == 128); }
 
 cudaError_t launch_attn_prefill(int head_dim, const AttnParams &a, int T, cudaStream_t st) {
     if (a.rowmap.mode != 1 || !a.out_bf16) return cudaErrorInvalidValue;
-    if (head_dim == 128) return launch_ap<128>(a, T, st);
-    if (head_dim == 64) return launch_ap<64>(a, T, st);
+    const bool pair = a.group % 2 == 0;   // two q heads of a KV group share each staged page
+    if (head_dim == 128) return pair ? launch_ap<128, 2>(a, T, st) : launch_ap<128, 1>(a, T, st);
+    if (head_dim == 64) return pair ? launch_ap<64, 2>(a, T, st) : launch_ap<64, 1>(a, T, st);
     return cudaErrorInvalidValue;
 }
 
