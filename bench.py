@@ -271,7 +271,41 @@ def side_measurements(tk, g, wl, torch, st, emb_all, pre, hbm, tc):
                         "ms_per_step": s * 1e3, "hbm_frac": (wbytes + kvb) / s / 1e9 / hbm,
                         "start_lengths": [int(x) for x in lens]}
     out["long_context"] = long_context(tk, g, torch, st, hbm, tc)
+    out["predictor_loop"] = predictor_loop(torch, hbm)
     return out
+
+
+def predictor_loop(torch, hbm):
+    """Frames/s of the predictor loop: per frame a T=2 prefill (rewinds to 0) and 15 decode steps."""
+    from kv_cached_qwen3_gb300.talker import Talker
+    pl = inputs.WORKLOADS["predictor_loop"]
+    g = pl.geometry
+    tk = Talker(g, inputs.make_weights(g, pl.seed))
+    T0, n = pl.prefill_T, pl.decode_steps
+    tk.kv_init_batched(1, T0 + n + 1)
+    emb = torch.from_numpy(inputs.make_embeddings(g, pl.seed, 0, T0 + n)).cuda()
+    rows = [emb[T0 + t:T0 + t + 1].contiguous() for t in range(n)]
+    lg = torch.empty(1, g.vocab, device="cuda")
+    am = torch.empty(1, device="cuda", dtype=torch.int32)
+    e1 = torch.empty(1, g.hidden, device="cuda")
+    pre = emb[:T0].contiguous()
+
+    def frame():
+        tk.prefill(0, pre)
+        for t in range(n):
+            e1.copy_(rows[t])
+            tk.decode(e1, lg, None, am)
+    for _ in range(3):
+        frame()
+    torch.cuda.synchronize()
+    frames = 32
+    s = timed(torch, tk.stream, frame, frames)
+    wbytes, _ = step_bytes(g, 0)
+    kv = sum(step_bytes(g, L)[1] for L in range(T0, T0 + n))
+    per_frame = (n + 1) * wbytes + kv
+    tk.close()
+    return {"frames_per_s": 1.0 / s, "ms_per_frame": s * 1e3, "passes_per_frame": n + 1,
+            "hbm_frac": per_frame / s / 1e9 / hbm}
 
 
 def timed(torch, st, fn, reps):

@@ -124,6 +124,15 @@ talker_status talker_cur_len(const talker_t *t, int stream, int *out_len);
 talker_status talker_prefill(talker_t *t, int stream, const float *emb, int T,
                              float *hidden_last, float *logits_last, int32_t *argmax_last);
 
+/* Chunked prefill ("talker-forward.h", talker_forward_core with n_past =
+ * cur_len): append T rows emb [T, H] f32 to `stream` without rewinding, at
+ * positions cur_len .. cur_len + T - 1; each row attends to every cached row
+ * before it. Afterwards the stream's length is cur_len + T. Outputs and
+ * errors as talker_prefill (EOVERFLOW when cur_len + T > max_seq_len, with
+ * nothing changed). */
+talker_status talker_prefill_append(talker_t *t, int stream, const float *emb, int T,
+                                    float *hidden_last, float *logits_last, int32_t *argmax_last);
+
 /* Decode ("talker-forward.h", talker_forward_decode): one row per stream for
  * streams 0..B-1. Row b of emb [B, H] f32 runs at position cur_len[b], its K/V
  * are appended at that row, it attends to [0, cur_len[b]], and afterwards

@@ -722,14 +722,17 @@ talker_status check_stream(const talker *t, int stream) {
     return TALKER_OK;
 }
 
+// Prefill rows at positions pos0 .. pos0 + T - 1 of `stream` (pos0 = 0: talker_prefill;
+// pos0 = cur_len: talker_prefill_append).
 talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float *hidden, float *logits,
-                           int32_t *argmax, bool all_rows) {
+                           int32_t *argmax, bool all_rows, bool append) {
     TRY(check_stream(t, stream));
     if (!emb || !logits || T < 1) return TALKER_EINVAL;
-    if (T > t->max_seq) return TALKER_EOVERFLOW;
+    const int pos0 = append ? t->len[stream] : 0;
+    if (T > t->max_seq - pos0) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));
     TRY(ensure_capacity(t, T, 1));
-    RowMap rm{1, stream, 0, t->d_len};
+    RowMap rm{1, stream, pos0, t->d_len};
     ForwardOut out{logits, hidden, all_rows ? nullptr : argmax, all_rows, 0};
     int nk = 0;
     if (T >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t)) {
@@ -738,9 +741,9 @@ talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float
     } else {
         TRY(enqueue_forward(t, t->st, T, rm, emb, 1, out, &nk));
     }
-    TRY_CUDA(launch_set_len(t->d_len, stream, T, t->st));
+    TRY_CUDA(launch_set_len(t->d_len, stream, pos0 + T, t->st));
     t->launches += nk + 1;
-    t->len[stream] = T;
+    t->len[stream] = pos0 + T;
     return TALKER_OK;
 }
 
@@ -875,12 +878,17 @@ talker_status talker_cur_len(const talker_t *t, int stream, int *out_len) {
 
 talker_status talker_prefill(talker_t *t, int stream, const float *emb, int T, float *hidden_last,
                              float *logits_last, int32_t *argmax_last) {
-    return prefill_impl(t, stream, emb, T, hidden_last, logits_last, argmax_last, false);
+    return prefill_impl(t, stream, emb, T, hidden_last, logits_last, argmax_last, false, false);
 }
 
 talker_status talker_prefill_all_rows(talker_t *t, int stream, const float *emb, int T, float *hidden,
                                       float *logits) {
-    return prefill_impl(t, stream, emb, T, hidden, logits, nullptr, true);
+    return prefill_impl(t, stream, emb, T, hidden, logits, nullptr, true, false);
+}
+
+talker_status talker_prefill_append(talker_t *t, int stream, const float *emb, int T, float *hidden_last,
+                                    float *logits_last, int32_t *argmax_last) {
+    return prefill_impl(t, stream, emb, T, hidden_last, logits_last, argmax_last, false, true);
 }
 
 talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits, float *hidden, int32_t *argmax) {

@@ -68,6 +68,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_kv_rewind": (st, [vp, ctypes.c_int, ctypes.c_int]),
         "talker_cur_len": (st, [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
         "talker_prefill": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
+        "talker_prefill_append": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
         "talker_decode": (st, [vp, vp, ctypes.c_int, vp, vp, vp]),
         "talker_prefill_all_rows": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp]),
         "talker_kv_import": (st, [vp, ctypes.c_int, vp, vp, ctypes.c_int]),
@@ -181,6 +182,16 @@ class Talker:
         am = self._out(1, dtype=self.torch.int32) if argmax else None
         self._check(self.lib.talker_prefill(self.h, stream, _ptr(emb), T, _ptr(hd), _ptr(lg), _ptr(am)),
                     "talker_prefill")
+        return hd, lg, am
+
+    def prefill_append(self, stream: int, emb, hidden=True, argmax=True):
+        """Append emb [T, H] after the stream's cached rows (chunked prefill). Returns like prefill."""
+        T = emb.shape[0]
+        lg = self._out(self.g.vocab)
+        hd = self._out(self.g.hidden) if hidden else None
+        am = self._out(1, dtype=self.torch.int32) if argmax else None
+        self._check(self.lib.talker_prefill_append(self.h, stream, _ptr(emb), T, _ptr(hd), _ptr(lg), _ptr(am)),
+                    "talker_prefill_append")
         return hd, lg, am
 
     def prefill_all_rows(self, stream: int, emb, hidden=True):

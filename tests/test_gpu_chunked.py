@@ -1,0 +1,95 @@
+"""GPU parity of chunked prefill (talker_prefill_append): rows appended after cached rows.
+
+The oracle appends the same chunks with n_past = cur_len (talker_forward_core); chunk
+sizes cross page boundaries and switch between the GEMV path (T < 16) and the
+tensor-core path (T >= 16, bf16 weights). Decode steps after the chunks read the cache
+the chunks wrote.
+"""
+import numpy as np
+import pytest
+
+from kv_cached_qwen3_gb300 import inputs
+from oracle import Oracle, OracleCache
+from parity_util import check_rows
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from kv_cached_qwen3_gb300 import talker
+    talker.load_library()
+    return torch.device("cuda", 0)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+def host(t):
+    return t.detach().float().cpu().numpy()
+
+
+def run_chunks(g, w, chunks, n_dec, seed, bf16):
+    from kv_cached_qwen3_gb300.talker import Talker
+    total = sum(chunks) + n_dec
+    emb = inputs.make_embeddings(g, seed, 0, total)
+    tk = Talker(g, w)
+    tk.kv_init_batched(1, total + 3)
+    oc = OracleCache(Oracle(g, w), 1, total + 3)
+    at = 0
+    for i, T in enumerate(chunks):
+        part = emb[at:at + T]
+        if i == 0:
+            hd, lg, am = tk.prefill(0, dev(part))
+            rh, rl = oc.prefill(0, part)
+        else:
+            hd, lg, am = tk.prefill_append(0, dev(part))
+            rhs, rls = oc.append_rows(0, part)
+            rh, rl = rhs[-1], rls[-1]
+        at += T
+        assert tk.cur_len(0) == at
+        check_rows(host(hd), rh[None], bf16=bf16, what="chunk %d (T=%d) hidden" % (i, T))
+        check_rows(host(lg), rl[None], bf16=bf16, what="chunk %d (T=%d) logits" % (i, T))
+        assert int(host(am)[0]) == int(np.argmax(host(lg)))
+    for t in range(n_dec):
+        e = emb[at + t:at + t + 1]
+        lg, hd = torch.empty(1, g.vocab, device="cuda"), torch.empty(1, g.hidden, device="cuda")
+        tk.decode(dev(e), lg, hd)
+        rh, rl = oc.decode(e)
+        check_rows(host(hd), rh, bf16=bf16, what="decode %d hidden" % t)
+        check_rows(host(lg), rl, bf16=bf16, what="decode %d logits" % t)
+    assert tk.cur_len(0) == total
+    assert tk.sync_status() == 0
+    tk.close()
+
+
+def test_chunked_prefill_fp32_gemv_path(cuda):
+    g = inputs.TINY
+    run_chunks(g, inputs.make_weights(g, 51), [20, 1, 7, 30, 40], 3, 52, bf16=False)
+
+
+def test_chunked_prefill_bf16_both_paths(cuda):
+    g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 4})
+    run_chunks(g, inputs.make_weights(g, 53), [100, 70, 5, 16, 64], 2, 54, bf16=True)
+
+
+def test_append_overflow_changes_nothing(cuda):
+    from kv_cached_qwen3_gb300.talker import Talker, TalkerError
+    g = inputs.TINY
+    w = inputs.make_weights(g, 55)
+    tk = Talker(g, w)
+    tk.kv_init_batched(1, 40)
+    emb = inputs.make_embeddings(g, 55, 0, 41)
+    tk.prefill(0, dev(emb[:30]))
+    with pytest.raises(TalkerError) as ei:
+        tk.prefill_append(0, dev(emb[30:41]))
+    assert ei.value.status == 2   # EOVERFLOW
+    assert tk.cur_len(0) == 30
+    tk.prefill_append(0, dev(emb[30:40]))
+    assert tk.cur_len(0) == 40
+    assert tk.sync_status() == 0
+    tk.close()
