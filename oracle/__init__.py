@@ -5,4 +5,5 @@ CPU-baseline leg of bench.py. The CUDA library and its Python binding never
 import it, and it never imports them.
 """
 from .talker_oracle import (Oracle, OracleCache, rms_norm, rope_neox, silu, softmax,  # noqa: F401
-                            attend_one, kv_group, argmax_low, decode_row_lazy_cache)
+                            attend_one, kv_group, argmax_low, decode_row_lazy_cache,
+                            embed_codes, suppress_logits)

@@ -308,3 +308,36 @@ def decode_row_lazy_cache(oracle: Oracle, x, pos, kv_layer):
         x = oracle.post_attention(l, x, attn.reshape(1, -1))
     hid, logits = oracle.head(x)
     return hid[0], logits[0]
+
+
+# ----------------------------------------------------------------------------- TTS loop input / output
+
+def embed_codes(tables, ids, overlay=None):
+    """Decode input rows from codebook ids (talker_forward_core batch input, "input_embed").
+
+    tables: list of G arrays [V_g, H] (table 0 = codec_embedding, then the acoustic tables);
+    ids: int array [G, N], group-major (ids[g, n] is slot n's code in codebook g);
+    overlay: [N, H] or None. Row n = sum_g tables[g][ids[g, n]] + overlay[n], in fp64.
+    """
+    ids = np.asarray(ids)
+    G, N = ids.shape
+    H = np.asarray(tables[0]).shape[1]
+    x = np.zeros((N, H), F64)
+    for g in range(G):
+        x += np.asarray(tables[g], F64)[ids[g]]
+    if overlay is not None:
+        x += np.asarray(overlay, F64)
+    return x
+
+
+def suppress_logits(logits, vocab_tail, eos_id):
+    """Codebook-0 logit suppression before selection: every token index >= V - vocab_tail except
+    eos_id gets -inf (qwen3-tts talker prefill/step, "suppress_start"). Returns a copy."""
+    out = np.array(logits, F64, copy=True)
+    V = out.shape[-1]
+    start = max(0, V - vocab_tail)
+    keep = out[..., eos_id].copy() if 0 <= eos_id < V else None
+    out[..., start:] = -np.inf
+    if keep is not None and eos_id >= start:
+        out[..., eos_id] = keep
+    return out

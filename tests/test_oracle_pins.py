@@ -409,3 +409,39 @@ def test_lazy_cache_decode_equals_cached_decode(tiny):
     h2, l2 = decode_row_lazy_cache(o, x[0], L, lambda l: layers[l])
     np.testing.assert_allclose(l2, l1[0], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(h2, h1[0], rtol=1e-13, atol=1e-14)
+
+
+def test_embed_codes_hand_example():
+    """Group-major ids: slot n sums row ids[g, n] of every table, plus its overlay row."""
+    from oracle import embed_codes
+    t0 = np.array([[1.0, 2.0], [10.0, 20.0], [100.0, 200.0]])   # codec table, V=3, H=2
+    t1 = np.array([[0.5, -0.5], [3.0, 4.0]])                    # acoustic table 1, V=2
+    t2 = np.array([[7.0, 0.0], [0.0, 7.0], [1.0, 1.0], [2.0, 2.0]])
+    ids = np.array([[2, 0], [1, 0], [3, 1]])                    # [G=3, N=2]
+    ov = np.array([[0.25, 0.25], [-1.0, 1.0]])
+    x = embed_codes([t0, t1, t2], ids, ov)
+    np.testing.assert_array_equal(x, [[100 + 3 + 2 + 0.25, 200 + 4 + 2 + 0.25],
+                                      [1 + 0.5 + 0 - 1.0, 2 - 0.5 + 7 + 1.0]])
+    np.testing.assert_array_equal(embed_codes([t0], np.array([[1, 1]])), [[10, 20], [10, 20]])
+
+
+def test_suppress_logits_tail_keeps_eos():
+    from oracle import suppress_logits, argmax_low
+    V = 3072
+    lg = np.zeros(V)
+    lg[V - 1] = 9.0        # in the suppressed tail, not EOS -> -inf
+    lg[V - 1024] = 8.0     # first suppressed index
+    lg[V - 1025] = 1.0     # last kept index below the tail
+    eos = V - 500
+    lg[eos] = 5.0
+    out = suppress_logits(lg, 1024, eos)
+    assert out[V - 1] == -np.inf and out[V - 1024] == -np.inf
+    assert out[eos] == 5.0 and out[V - 1025] == 1.0
+    assert np.isinf(out[V - 1024:]).sum() == 1023
+    assert argmax_low(out) == eos
+    # EOS below the tail: the whole tail goes
+    out2 = suppress_logits(lg, 1024, 7)
+    assert np.isinf(out2[V - 1024:]).all() and argmax_low(out2) == V - 1025
+    # vocab smaller than the tail: everything but EOS
+    small = suppress_logits(np.arange(10.0), 1024, 3)
+    assert argmax_low(small) == 3 and np.isinf(small).sum() == 9
