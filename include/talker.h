@@ -144,6 +144,31 @@ talker_status talker_prefill_append(talker_t *t, int stream, const float *emb, i
 talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits, float *hidden,
                             int32_t *argmax);
 
+/* TTS loop output ("qwen3-tts" talker prefill and step, codebook-0 selection):
+ * before every head's argmax (prefill, append, decode), the logits of token
+ * indices [vocab - vocab_tail, vocab) other than eos_id are set to -inf, in
+ * the returned logits too. vocab_tail = 0 turns it off (the default). Steps
+ * captured before the call are dropped and captured again. The persistent
+ * decode kernel does not run while it is on. Errors: EINVAL (vocab_tail < 0). */
+talker_status talker_set_logit_suppression(talker_t *t, int vocab_tail, int eos_id);
+
+/* TTS loop input ("talker-forward.h", batched forward "input_embed"): register
+ * n_tables codebook embedding tables [vocab[g], hidden] (device pointers in
+ * dtype TALKER_DTYPE_F32 or _BF16, table 0 = codec_embedding, then the acoustic
+ * tables). The tables stay owned by the caller and must outlive their use.
+ * n_tables = 0 unregisters. Errors: EINVAL (n_tables > 32, null table, vocab < 1). */
+talker_status talker_set_code_tables(talker_t *t, const void *const *tables, const int *vocab, int n_tables,
+                                     int dtype);
+
+/* Decode from codebook ids: row b of the step's input is
+ *   sum_g table_g[ids[g * B + b]] + overlay[b]
+ * (ids: device int32 [n_tables][B], group-major; overlay: device f32 [B, hidden]
+ * or NULL), built by one kernel into a library buffer, then talker_decode.
+ * An id outside its table sets the device status word (ST bad argument) and
+ * contributes nothing. Errors: as talker_decode; ESTATE without tables. */
+talker_status talker_decode_codes(talker_t *t, const int32_t *ids, const float *overlay, int B, float *logits,
+                                  float *hidden, int32_t *argmax);
+
 /* Test support: the prefill above, but writing every row's outputs:
  * hidden [T, H] (may be NULL) and logits [T, vocab] (required). */
 talker_status talker_prefill_all_rows(talker_t *t, int stream, const float *emb, int T,

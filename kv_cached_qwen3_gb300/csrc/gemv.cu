@@ -252,8 +252,10 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
     // ---- epilogue
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
-        const float v0 = warp_sum(acc[0][r]);
+        float v0 = warp_sum(acc[0][r]);
         const float v1 = (NW == 2) ? warp_sum(acc[NW - 1][r]) : 0.f;
+        if (EPI == EPI_HEAD && p.suppress_tail > 0 && f >= p.n_out - p.suppress_tail && f != p.eos_id)
+            v0 = -INFINITY;   // codebook-0 suppression of the vocabulary tail (EOS kept)
         if (EPI == EPI_HEAD && lane == r) {
             hv_s[warp][r] = (fvalid && r < nrows) ? v0 : -INFINITY;
             hi_s[warp][r] = f;

@@ -68,6 +68,8 @@ struct GemvParams {
     int *head_cnt;       // per row block counter
     int inc_len;         // decode: last CTA does cur_len[r] += 1
     int *cur_len_rw;
+    int suppress_tail;   // > 0: logits of features [n_out - suppress_tail, n_out) except eos_id become -inf
+    int eos_id;
     int *status;
 };
 
@@ -174,6 +176,16 @@ cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *
 // mode 1, bf16 output).
 bool attn_prefill_supported(int kv_bf16, int head_dim);
 cudaError_t launch_attn_prefill(int head_dim, const AttnParams &a, int T, cudaStream_t st);
+// Decode input rows from codebook ids: out[b] = sum_g table_g[ids[g * B + b]] + overlay[b]
+// (tables bf16 or f32 [V_g, H]); an id outside [0, V_g) sets ST_BAD_ARG and adds nothing.
+struct EmbedTables {
+    const void *table[32];
+    int vocab[32];
+    int n;
+    int bf16;
+};
+cudaError_t launch_embed_codes(const EmbedTables &t, const int32_t *ids, const float *overlay, int B, int H,
+                               float *out, int *status, cudaStream_t st);
 cudaError_t prepare_kernels();  // raise dynamic shared-memory limits once per process
 
 bool gemm_tc_supported(int N, int K);

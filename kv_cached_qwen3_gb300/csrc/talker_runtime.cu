@@ -110,6 +110,11 @@ struct talker {
     void *hb = nullptr, *ab = nullptr, *gb = nullptr;
     float *gu = nullptr;
     int tc_ok = -1;                      // tensor-core prefill usable for this geometry (-1 unknown)
+    // TTS loop input / output
+    int suppress_tail = 0, suppress_eos = -1;   // head: logits [V - tail, V) except eos become -inf
+    EmbedTables codes{};                        // caller-owned codebook tables (codes.n = 0: none)
+    float *code_emb = nullptr;                  // [code_emb_rows, H] rows built from codebook ids
+    int code_emb_rows = 0;
 };
 
 namespace {
@@ -124,7 +129,8 @@ void free_ptr(void *p) {
 }
 
 void free_workspaces(talker *t) {
-    float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->attn_ws, &t->head_val};
+    float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->attn_ws, &t->head_val, &t->code_emb};
+    t->code_emb_rows = 0;
     for (auto pp : fl) {
         free_ptr(*pp);
         *pp = nullptr;
@@ -481,6 +487,8 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
     h.head_cnt = t->head_cnt;
     h.inc_len = out.inc_len;
     h.cur_len_rw = t->d_len;
+    h.suppress_tail = t->suppress_tail;
+    h.eos_id = t->suppress_eos;
     TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, st, pdl));
     ++nk;
     *n_kernels = nk;
@@ -502,7 +510,7 @@ int kmax_of(const talker *t) { return std::max(std::max(t->H, t->qd), t->I); }
 // Can the persistent kernel run this geometry with B rows? (one CTA per SM must fit,
 // every weight row group and KV page pair must fit one ring slot)
 bool persist_usable(talker *t, int B) {
-    if (B > 4 || t->w_bf16 != t->kv_bf16) return false;
+    if (B > 4 || t->w_bf16 != t->kv_bf16 || t->suppress_tail > 0) return false;
     const int R = persist_rows_tmpl(B);
     int &ok = t->persist_ok[R == 1 ? 0 : 1];
     if (ok >= 0) return ok == 1;
@@ -709,6 +717,8 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
     h.head_cnt = t->head_cnt;
     h.inc_len = out.inc_len;
     h.cur_len_rw = t->d_len;
+    h.suppress_tail = t->suppress_tail;
+    h.eos_id = t->suppress_eos;
     TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, st, false));
     ++nk;
     *n_kernels = nk;
@@ -1019,6 +1029,52 @@ talker_status talker_set_attn_splits(talker_t *t, int max_splits) {
     if (!t || max_splits < 0) return TALKER_EINVAL;
     t->max_splits = max_splits;
     return TALKER_OK;
+}
+
+talker_status talker_set_logit_suppression(talker_t *t, int vocab_tail, int eos_id) {
+    if (!t || vocab_tail < 0) return TALKER_EINVAL;
+    t->suppress_tail = std::min(vocab_tail, t->V);
+    t->suppress_eos = eos_id;
+    drop_graphs(t);   // the head's parameters are baked into captured steps
+    return TALKER_OK;
+}
+
+talker_status talker_set_code_tables(talker_t *t, const void *const *tables, const int *vocab, int n_tables,
+                                     int dtype) {
+    if (!t || n_tables < 0 || n_tables > 32 || (n_tables > 0 && (!tables || !vocab))) return TALKER_EINVAL;
+    if (dtype != TALKER_DTYPE_F32 && dtype != TALKER_DTYPE_BF16) return TALKER_EINVAL;
+    EmbedTables e{};
+    for (int g = 0; g < n_tables; ++g) {
+        if (!tables[g] || vocab[g] < 1) return TALKER_EINVAL;
+        e.table[g] = tables[g];
+        e.vocab[g] = vocab[g];
+    }
+    e.n = n_tables;
+    e.bf16 = dtype == TALKER_DTYPE_BF16;
+    t->codes = e;
+    return TALKER_OK;
+}
+
+talker_status talker_decode_codes(talker_t *t, const int32_t *ids, const float *overlay, int B, float *logits,
+                                  float *hidden, int32_t *argmax) {
+    if (!t) return TALKER_EINVAL;
+    if (t->n_streams == 0) return TALKER_ESTATE;
+    if (t->codes.n == 0) return TALKER_ESTATE;
+    if (!ids || !logits || B < 1 || B > t->n_streams) return TALKER_EINVAL;
+    for (int b = 0; b < B; ++b)
+        if (t->len[b] + 1 > t->max_seq) return TALKER_EOVERFLOW;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    if (t->code_emb_rows < t->n_streams) {
+        drop_graphs(t);   // captured steps read the old buffer
+        free_ptr(t->code_emb);
+        t->code_emb = nullptr;
+        t->code_emb_rows = 0;
+        TRY_CUDA(cudaMalloc(&t->code_emb, (size_t)t->n_streams * t->H * sizeof(float)));
+        t->code_emb_rows = t->n_streams;
+    }
+    TRY_CUDA(launch_embed_codes(t->codes, ids, overlay, B, t->H, t->code_emb, t->d_status, t->st));
+    t->launches += 1;
+    return talker_decode(t, t->code_emb, B, logits, hidden, argmax);
 }
 
 talker_status talker_set_prefill_mode(talker_t *t, int mode) {

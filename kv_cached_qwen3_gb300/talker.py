@@ -69,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_cur_len": (st, [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
         "talker_prefill": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
         "talker_prefill_append": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
+        "talker_set_logit_suppression": (st, [vp, ctypes.c_int, ctypes.c_int]),
+        "talker_set_code_tables": (st, [vp, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_int), ctypes.c_int,
+                                        ctypes.c_int]),
+        "talker_decode_codes": (st, [vp, vp, vp, ctypes.c_int, vp, vp, vp]),
         "talker_decode": (st, [vp, vp, ctypes.c_int, vp, vp, vp]),
         "talker_prefill_all_rows": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp]),
         "talker_kv_import": (st, [vp, ctypes.c_int, vp, vp, ctypes.c_int]),
@@ -209,6 +213,27 @@ class Talker:
             logits = self._out(B, self.g.vocab)
         self._check(self.lib.talker_decode(self.h, _ptr(emb), B, _ptr(logits), _ptr(hidden), _ptr(argmax)),
                     "talker_decode")
+        return logits, hidden, argmax
+
+    def set_logit_suppression(self, vocab_tail: int, eos_id: int):
+        self._check(self.lib.talker_set_logit_suppression(self.h, vocab_tail, eos_id), "talker_set_logit_suppression")
+
+    def set_code_tables(self, tables, dtype_bf16: bool):
+        """tables: list of cuda tensors [V_g, H] (kept referenced by this object while registered)."""
+        self._code_tables = list(tables)
+        n = len(tables)
+        arr = (ctypes.c_void_p * max(1, n))(*[t.data_ptr() for t in tables])
+        voc = (ctypes.c_int * max(1, n))(*[int(t.shape[0]) for t in tables])
+        self._check(self.lib.talker_set_code_tables(self.h, arr, voc, n, 1 if dtype_bf16 else 0),
+                    "talker_set_code_tables")
+
+    def decode_codes(self, ids, overlay=None, logits=None, hidden=None, argmax=None):
+        """ids: int32 cuda [n_tables, B]; overlay: f32 cuda [B, H] or None."""
+        B = ids.shape[1]
+        if logits is None:
+            logits = self._out(B, self.g.vocab)
+        self._check(self.lib.talker_decode_codes(self.h, _ptr(ids), _ptr(overlay), B, _ptr(logits), _ptr(hidden),
+                                                 _ptr(argmax)), "talker_decode_codes")
         return logits, hidden, argmax
 
     def set_decode_mode(self, mode: int):
