@@ -191,6 +191,42 @@ class Oracle:
         return hid, logits
 
 
+# ----------------------------------------------------------------------------- Q8_0 KV storage
+
+Q8_BLOCK = 32
+
+
+def q8_0_quantize(x):
+    """ggml Q8_0 (the cache storage type the qwen3-tts talker casts from): blocks of 32 along the
+    last axis; d = max|x| / 127 in f32, codes = round-half-away-from-zero(x * (1/d)) in f32 (0 for
+    an all-zero block), d stored as fp16 (nearest even). Returns (codes int8 [..., n], d fp16
+    [..., n / 32])."""
+    x32 = np.asarray(x, np.float32)
+    shp = x32.shape
+    if shp[-1] % Q8_BLOCK:
+        raise ValueError("last axis must be a multiple of 32")
+    b = x32.reshape(shp[:-1] + (shp[-1] // Q8_BLOCK, Q8_BLOCK))
+    amax = np.max(np.abs(b), axis=-1, keepdims=True)
+    d = amax / np.float32(127.0)
+    safe = np.where(d > 0, d, np.float32(1.0))
+    inv = np.where(d > 0, np.float32(1.0) / safe, np.float32(0.0)).astype(np.float32)
+    t = (b * inv).astype(np.float32)
+    q = np.sign(t) * np.floor(np.abs(t) + np.float32(0.5))
+    return q.astype(np.int8).reshape(shp), d[..., 0].astype(np.float16)
+
+
+def q8_0_dequantize(codes, d):
+    """codes int8 [..., n], d fp16 [..., n / 32] -> fp64 values codes * d."""
+    c = np.asarray(codes, F64)
+    shp = c.shape
+    b = c.reshape(shp[:-1] + (shp[-1] // Q8_BLOCK, Q8_BLOCK))
+    return (b * np.asarray(d, np.float16).astype(F64)[..., None]).reshape(shp)
+
+
+def q8_0_roundtrip(x):
+    return q8_0_dequantize(*q8_0_quantize(x))
+
+
 class OracleCache:
     """Mode B: the incremental KV-cached forward over n_streams independent streams.
 
@@ -198,7 +234,7 @@ class OracleCache:
     counts the valid rows. Errors raise ValueError and leave the state unchanged.
     """
 
-    def __init__(self, oracle: Oracle, n_streams: int, max_seq_len: int, round_kv=None):
+    def __init__(self, oracle: Oracle, n_streams: int, max_seq_len: int, round_kv=None, kv_q8=False):
         g = oracle.g
         self.o = oracle
         self.max_seq_len = max_seq_len
@@ -208,10 +244,15 @@ class OracleCache:
         self.cur_len = [0] * n_streams
         # Diagnosis only: a callable applied to K/V rows before they are stored.
         self.round_kv = round_kv
+        # Q8_0 storage (qwen3-tts talker, TurboQuantQ8_0): rows are stored as Q8_0; a call
+        # attends the rows cached by earlier calls dequantized and its own rows exactly.
+        self.kv_q8 = kv_q8
 
     def _store(self, s, l, rows, k, v):
         if self.round_kv is not None:
             k, v = self.round_kv(k), self.round_kv(v)
+        if self.kv_q8:
+            k, v = q8_0_roundtrip(k), q8_0_roundtrip(v)
         self.K[s][l][:, rows, :] = np.transpose(k, (1, 0, 2))
         self.V[s][l][:, rows, :] = np.transpose(v, (1, 0, 2))
 
@@ -224,8 +265,11 @@ class OracleCache:
         """k, v: [n_layers, n_kv, length, hd]; sets cur_len[s] = length."""
         if length > self.max_seq_len:
             raise ValueError("import exceeds max_seq_len")
-        self.K[s][:, :, :length] = np.asarray(k, F64)
-        self.V[s][:, :, :length] = np.asarray(v, F64)
+        k, v = np.asarray(k, F64), np.asarray(v, F64)
+        if self.kv_q8:
+            k, v = q8_0_roundtrip(k), q8_0_roundtrip(v)
+        self.K[s][:, :, :length] = k
+        self.V[s][:, :, :length] = v
         self.cur_len[s] = length
 
     def kv_export(self, s, length):
@@ -243,8 +287,10 @@ class OracleCache:
         group = g.n_q_heads // g.n_kv_heads
         for l in range(g.n_layers):
             q, k, v = o.qkv(l, x, pos)
+            # the call's own rows enter exactly, earlier rows as stored
+            Kc = np.concatenate([self.K[s][l][:, :n_past], np.transpose(k, (1, 0, 2))], axis=1)
+            Vc = np.concatenate([self.V[s][l][:, :n_past], np.transpose(v, (1, 0, 2))], axis=1)
             self._store(s, l, pos, k, v)
-            Kc, Vc = self.K[s][l], self.V[s][l]
             attn = np.empty((T, g.n_q_heads, g.head_dim), F64)
             for h in range(g.n_q_heads):
                 kv = h // group
@@ -280,8 +326,10 @@ class OracleCache:
             q, k, v = o.qkv(l, x, pos)
             attn = np.empty((B, g.n_q_heads, g.head_dim), F64)
             for s in range(B):
+                Ks = np.concatenate([self.K[s][l][:, :pos[s]], np.transpose(k[s:s + 1], (1, 0, 2))], axis=1)
+                Vs = np.concatenate([self.V[s][l][:, :pos[s]], np.transpose(v[s:s + 1], (1, 0, 2))], axis=1)
                 self._store(s, l, pos[s:s + 1], k[s:s + 1], v[s:s + 1])
-                attn[s] = attend_one(q[s], self.K[s][l], self.V[s][l], pos[s] + 1)
+                attn[s] = attend_one(q[s], Ks, Vs, pos[s] + 1)
             x = o.post_attention(l, x, attn.reshape(B, -1))
         hid, logits = o.head(x)
         for s in range(B):

@@ -445,3 +445,62 @@ def test_suppress_logits_tail_keeps_eos():
     # vocab smaller than the tail: everything but EOS
     small = suppress_logits(np.arange(10.0), 1024, 3)
     assert argmax_low(small) == 3 and np.isinf(small).sum() == 9
+
+
+def test_q8_0_hand_block():
+    """Block 0..31: d = 31/127 -> fp16 0.244140625; codes round(x * 127/31) half away from zero."""
+    from oracle import q8_0_quantize, q8_0_dequantize
+    x = np.arange(32, dtype=np.float32)
+    q, d = q8_0_quantize(x)
+    assert d.dtype == np.float16 and float(d[0]) == 0.244140625
+    assert q[31] == 127 and q[1] == 4 and q[15] == 61 and q[16] == 66 and q[0] == 0
+    deq = q8_0_dequantize(q, d)
+    assert deq[31] == 127 * 0.244140625
+
+
+def test_q8_0_rounds_half_away_from_zero_and_zero_block():
+    from oracle import q8_0_quantize
+    x = np.zeros(64, np.float32)
+    x[0] = 127.0            # d = 1 exactly, so x * (1/d) = x
+    x[1], x[2], x[3], x[4] = 2.5, -2.5, 0.5, -0.5
+    q, d = q8_0_quantize(x)
+    assert float(d[0]) == 1.0 and list(q[1:5]) == [3, -3, 1, -1]
+    assert float(d[1]) == 0.0 and not q[32:].any()      # all-zero block
+
+
+def test_q8_0_error_bound_random():
+    """|x - dequant| <= d16 / 2 + 127 |d - d16| (rounding of the code, rounding of the scale)."""
+    from oracle import q8_0_quantize, q8_0_dequantize
+    rng = np.random.Generator(np.random.PCG64(7))
+    x = (rng.standard_normal((50, 128)) * np.exp(rng.uniform(-4, 4, (50, 1)))).astype(np.float32)
+    q, d = q8_0_quantize(x)
+    err = np.abs(q8_0_dequantize(q, d) - x.astype(np.float64)).reshape(50, 4, 32)
+    xb = x.reshape(50, 4, 32).astype(np.float64)
+    d32 = np.max(np.abs(xb), axis=-1) / 127.0
+    d16 = d.astype(np.float64)
+    bound = d16 / 2 + 127 * np.abs(d32 - d16) + 1e-6 * d16
+    assert np.all(err <= bound[..., None])
+
+
+def test_q8_cache_attends_own_row_exactly(tiny):
+    """Q8_0 storage: earlier rows dequantized, the step's own row exact, the stored row quantized."""
+    from oracle import q8_0_roundtrip
+    _, o = tiny
+    g = TINY
+    L = 20
+    layers = [inputs.make_kv_layer(g, 8, l, L) for l in range(g.n_layers)]
+    K = np.stack([k for k, _ in layers])
+    V = np.stack([v for _, v in layers])
+    x = inputs.make_embeddings(g, 8, 0, 1)
+    cq = OracleCache(o, 1, 64, kv_q8=True)
+    cq.kv_import(0, K, V, L)
+    cp = OracleCache(o, 1, 64)
+    cp.kv_import(0, q8_0_roundtrip(K), q8_0_roundtrip(V), L)
+    hq, lq = cq.decode(x)
+    hp, lp = cp.decode(x)
+    np.testing.assert_array_equal(lq, lp)
+    np.testing.assert_array_equal(hq, hp)
+    kq, _ = cq.kv_export(0, L + 1)
+    kp, _ = cp.kv_export(0, L + 1)
+    np.testing.assert_array_equal(kq[:, :, L], q8_0_roundtrip(kp[:, :, L]))
+    assert not np.array_equal(kp[:, :, L], kq[:, :, L])   # the plain cache keeps it exact
