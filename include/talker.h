@@ -52,7 +52,12 @@ typedef enum {
     TALKER_EDEVICE = 6    /* a kernel reported an error through the device status word */
 } talker_status;
 
-typedef enum { TALKER_DTYPE_F32 = 0, TALKER_DTYPE_BF16 = 1 } talker_dtype;
+/* TALKER_DTYPE_Q8_0 is a KV-cache storage type only ("qwen3-tts" talker TurboQuantQ8_0,
+ * ggml Q8_0 blocks): per head row, blocks of 32 int8 codes with an fp16 scale max|x|/127.
+ * A call attends the rows cached by earlier calls dequantized and its own rows exactly.
+ * It needs bf16 weights and head_dim 64 or 128; talker_prefill_append is not available
+ * with it. */
+typedef enum { TALKER_DTYPE_F32 = 0, TALKER_DTYPE_BF16 = 1, TALKER_DTYPE_Q8_0 = 2 } talker_dtype;
 
 /* Geometry and storage formats (names as in the rightkit-qts TtsTransformerConfig).
  * Supported: head_dim in {32, 64, 128}; n_q_heads a multiple of n_kv_heads with
@@ -177,7 +182,8 @@ talker_status talker_prefill_all_rows(talker_t *t, int stream, const float *emb,
 /* Test support, modelled on the state import/export of
  * "audio.cpp/src/models/vibevoice/decoder.cpp" (TransformerKVState):
  * copy `len` rows of a stream's cache in or out. k and v are device buffers
- * [n_layers][n_kv_heads][len][head_dim] in kv_dtype. Import sets the stream's
+ * [n_layers][n_kv_heads][len][head_dim] in kv_dtype (f32 for Q8_0 storage: import
+ * quantizes, export writes the dequantized values). Import sets the stream's
  * length to len. Errors: EINVAL, EOVERFLOW (len > max_seq_len), ESTATE, ECUDA. */
 talker_status talker_kv_import(talker_t *t, int stream, const void *k, const void *v, int len);
 talker_status talker_kv_export(const talker_t *t, int stream, void *k, void *v, int len);

@@ -16,6 +16,8 @@
 // in split order, so the result is deterministic.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -30,10 +32,31 @@ __device__ __forceinline__ int attn_row_pos(const RowMap &m, int r) {
     return m.mode == 0 ? m.cur_len[r] : m.pos0 + r;
 }
 
-size_t attn_smem_bytes(int kv_bf16, int head_dim, int group) {
-    const size_t esz = kv_bf16 ? 2 : 4;
-    return 4 * (size_t)kPage * head_dim * esz + (size_t)group * head_dim * 4 + (size_t)group * kPage * 4 +
-           2 * (size_t)head_dim * esz;
+// One (page, layer, KV head) tile of the cache as it sits in the pool and in shared memory.
+// bf16 / f32: [64][HD] values. Q8_0 (KT = int8_t): [64][HD] codes, then [64][HD/32] fp16 scales.
+template <typename KT, int HD>
+struct KvTile {
+    static constexpr uint32_t kBytes = kPage * HD * sizeof(KT);
+    static constexpr size_t kUnits = (size_t)kPage * HD;   // pool units (elements) per tile
+    __device__ static __forceinline__ float load(const unsigned char *t, int j, int d) {
+        return Elem<KT>::load(reinterpret_cast<const KT *>(t), (size_t)j * HD + d);
+    }
+};
+template <int HD>
+struct KvTile<int8_t, HD> {   // int8 stands for the Q8_0 storage type
+    static constexpr uint32_t kBytes = kPage * HD + kPage * (HD / 32) * 2;
+    static constexpr size_t kUnits = kBytes;                // pool units are bytes
+    __device__ static __forceinline__ float load(const unsigned char *t, int j, int d) {
+        const float c = (float)reinterpret_cast<const int8_t *>(t)[j * HD + d];
+        return c * __half2float(reinterpret_cast<const __half *>(t + kPage * HD)[j * (HD / 32) + (d >> 5)]);
+    }
+};
+
+size_t attn_smem_bytes(int kv_kind, int head_dim, int group) {
+    // kv_kind: 0 f32, 1 bf16, 2 Q8_0
+    const size_t tile = kv_kind == 2 ? (size_t)kPage * head_dim + (size_t)kPage * (head_dim / 32) * 2
+                                     : (size_t)kPage * head_dim * (kv_kind == 1 ? 2 : 4);
+    return 4 * tile + (size_t)group * head_dim * 4 + (size_t)group * kPage * 4 + 2 * (size_t)head_dim * 4;
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -91,16 +114,19 @@ __device__ void cluster_combine(const AttnParams &p, bool has, const float *o_pa
 
 template <typename KT, int HD>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p) {
+    using Tile = KvTile<KT, HD>;
+    constexpr bool kQ8 = std::is_same<KT, int8_t>::value;
     constexpr int E = HD / 32;                       // elements of a key row per lane
     constexpr int NO = (kMaxGroup * HD + kAttnThreads - 1) / kAttnThreads;
-    constexpr uint32_t kTileBytes = kPage * HD * sizeof(KT);
+    constexpr uint32_t kTileBytes = Tile::kBytes;
+    constexpr size_t kUnit = kQ8 ? 1 : sizeof(KT);   // bytes per pool unit
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    KT *kbuf = reinterpret_cast<KT *>(smem_raw);                       // [2][kPage*HD]
-    KT *vbuf = kbuf + 2 * kPage * HD;                                   // [2][kPage*HD]
-    float *q_s = reinterpret_cast<float *>(vbuf + 2 * kPage * HD);      // [G][HD]
-    float *sc = q_s + p.group * HD;                                     // [G][kPage]
-    KT *knew = reinterpret_cast<KT *>(sc + p.group * kPage);            // this step's k, v row
-    KT *vnew = knew + HD;
+    unsigned char *kbuf = smem_raw;                                      // [2][tile]
+    unsigned char *vbuf = kbuf + 2 * kTileBytes;                         // [2][tile]
+    float *q_s = reinterpret_cast<float *>(vbuf + 2 * kTileBytes);       // [G][HD]
+    float *sc = q_s + p.group * HD;                                      // [G][kPage]
+    float *knew = sc + p.group * kPage;                                  // this step's k, v row (as attended)
+    float *vnew = knew + HD;
     __shared__ float m_s[kMaxGroup], l_s[kMaxGroup], al_s[kMaxGroup];
     __shared__ __align__(8) uint64_t bars[2];
     __shared__ int flag_s;
@@ -134,9 +160,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
     }
 
     const int *ptab = p.cache.page_table + (size_t)s * p.cache.pages_per_stream;
-    const size_t head_off = (size_t)(p.layer * p.cache.n_kv + g) * kPage * HD;
-    const KT *kpool = static_cast<const KT *>(p.cache.k);
-    const KT *vpool = static_cast<const KT *>(p.cache.v);
+    const size_t head_off = (size_t)(p.layer * p.cache.n_kv + g) * Tile::kUnits;   // pool units
+    const unsigned char *kpool = static_cast<const unsigned char *>(p.cache.k);
+    const unsigned char *vpool = static_cast<const unsigned char *>(p.cache.v);
+    auto tile_ptr = [&](const unsigned char *pool, int page) {
+        return pool + ((size_t)page * p.cache.page_elems + head_off) * kUnit;
+    };
 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -145,10 +174,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
     }
     __syncthreads();
     if (tid == 0) {
-        const size_t off = (size_t)ptab[pb] * p.cache.page_elems + head_off;
         mbar_arrive_expect_tx(&bars[0], 2 * kTileBytes);
-        bulk_g2s(kbuf, kpool + off, kTileBytes, &bars[0]);
-        bulk_g2s(vbuf, vpool + off, kTileBytes, &bars[0]);
+        bulk_g2s(kbuf, tile_ptr(kpool, ptab[pb]), kTileBytes, &bars[0]);
+        bulk_g2s(vbuf, tile_ptr(vpool, ptab[pb]), kTileBytes, &bars[0]);
     }
     // the RoPE row of this position (a table of earlier launches) is fetched before the wait
     constexpr int half_hd = HD / 2;
@@ -199,17 +227,36 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
                     q_s[hh * HD + i] = a[j] * p.scale;
                     q_s[hh * HD + i + half] = b[j] * p.scale;
                 } else {
-                    KT *d = hh == G ? knew : vnew;
-                    Elem<KT>::store(d, i, a[j]);
-                    Elem<KT>::store(d, i + half, b[j]);
-                    if (sidx == 0) {   // the cache keeps the row for later steps
-                        const size_t off = (size_t)ptab[pos / kPage] * p.cache.page_elems + head_off +
-                                           (size_t)(pos % kPage) * HD;
-                        KT *c = const_cast<KT *>(hh == G ? kpool : vpool) + off;
-                        Elem<KT>::store(c, i, a[j]);
-                        Elem<KT>::store(c, i + half, b[j]);
+                    // the row as this step attends it: exact with Q8_0 storage, else as stored
+                    float *d = hh == G ? knew : vnew;
+                    if constexpr (kQ8) {
+                        d[i] = a[j];
+                        d[i + half] = b[j];
+                    } else {
+                        d[i] = Elem<KT>::round(a[j]);
+                        d[i + half] = Elem<KT>::round(b[j]);
+                        if (sidx == 0) {   // the cache keeps the row for later steps
+                            unsigned char *t =
+                                const_cast<unsigned char *>(tile_ptr(hh == G ? kpool : vpool, ptab[pos / kPage]));
+                            KT *c = reinterpret_cast<KT *>(t) + (size_t)(pos % kPage) * HD;
+                            Elem<KT>::store(c, i, a[j]);
+                            Elem<KT>::store(c, i + half, b[j]);
+                        }
                     }
                 }
+            }
+            if (kQ8 && hh >= G && sidx == 0) {
+                // Q8_0 row: each valid register of the warp is one block of 32 dims (lane = dim % 32)
+                unsigned char *t = const_cast<unsigned char *>(tile_ptr(hh == G ? kpool : vpool, ptab[pos / kPage]));
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int d0 = 32 * j + u * half;   // first dim of this register's block
+                        if (32 * j >= half) continue;
+                        q8_store_block(t, (pos % kPage) * HD + d0, kPage * HD + ((pos % kPage) * (HD / 32) + d0 / 32) * 2,
+                                       u ? b[j] : a[j], lane);
+                    }
             }
         }
     }
@@ -230,10 +277,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
         if (tid == 0 && pg + 1 < pe) {
             // The other buffer was released by the barrier that ended the previous iteration.
             fence_proxy_async();
-            const size_t off = (size_t)ptab[pg + 1] * p.cache.page_elems + head_off;
             mbar_arrive_expect_tx(&bars[buf ^ 1], 2 * kTileBytes);
-            bulk_g2s(kbuf + (buf ^ 1) * kPage * HD, kpool + off, kTileBytes, &bars[buf ^ 1]);
-            bulk_g2s(vbuf + (buf ^ 1) * kPage * HD, vpool + off, kTileBytes, &bars[buf ^ 1]);
+            bulk_g2s(kbuf + (buf ^ 1) * kTileBytes, tile_ptr(kpool, ptab[pg + 1]), kTileBytes, &bars[buf ^ 1]);
+            bulk_g2s(vbuf + (buf ^ 1) * kTileBytes, tile_ptr(vpool, ptab[pg + 1]), kTileBytes, &bars[buf ^ 1]);
         }
         const bool ok = mbar_wait(&bars[buf], parity, p.status);
         if (__syncthreads_or(!ok)) {
@@ -241,17 +287,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
             fail_it = it;
             break;
         }
-        const KT *Ks = kbuf + buf * kPage * HD;
-        const KT *Vs = vbuf + buf * kPage * HD;
+        const unsigned char *Ks = kbuf + buf * kTileBytes;
+        const unsigned char *Vs = vbuf + buf * kTileBytes;
         const int valid = min(kPage, nvis - pg * kPage);
-        if (pg == npages - 1) {   // the fresh row over the copied page
-            const size_t off = (size_t)ptab[pg] * p.cache.page_elems + head_off + (size_t)(pos % kPage) * HD;
-            for (int i = tid; i < HD; i += kAttnThreads) {
-                kbuf[buf * kPage * HD + (pos % kPage) * HD + i] = p.raw ? knew[i] : kpool[off + i];
-                vbuf[buf * kPage * HD + (pos % kPage) * HD + i] = p.raw ? vnew[i] : vpool[off + i];
-            }
-            __syncthreads();
-        }
+        // decode rows: row `newest` of this page is this step's row, read from knew / vnew (the
+        // copied page may predate it); prefill rows were all written before the page was copied
+        const int newest = (p.raw != nullptr) ? pos - pg * kPage : -1;
 
         // scores: warp w takes key rows w, w + 8, ...; lanes split the head dimension. All of a
         // warp's rows and heads are reduced in one interleaved butterfly (latency paid once).
@@ -262,7 +303,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
 #pragma unroll
             for (int i = 0; i < RPW; ++i)
 #pragma unroll
-                for (int e = 0; e < E; ++e) kv[i][e] = Elem<KT>::load(Ks, (size_t)(warp + NWARP * i) * HD + lane * E + e);
+                for (int e = 0; e < E; ++e) {
+                    const int j = warp + NWARP * i;
+                    kv[i][e] = (j == newest) ? knew[lane * E + e] : Tile::load(Ks, j, lane * E + e);
+                }
             for (int gi0 = 0; gi0 < G; gi0 += 2) {   // two heads per pass keeps the register count bounded
                 float dv[RPW][2];
 #pragma unroll
@@ -326,15 +370,15 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
                 // four independent chains over the page's rows
                 float a0 = o_acc[o] * al_s[gi], a1 = 0.f, a2 = 0.f, a3 = 0.f;
                 const float *pj = sc + gi * kPage;
-                const KT *vd = Vs + d;
+                auto vload = [&](int j) { return (j == newest) ? vnew[d] : Tile::load(Vs, j, d); };
                 int j = 0;
                 for (; j + 4 <= valid; j += 4) {
-                    a0 = fmaf(pj[j], Elem<KT>::load(vd, (size_t)j * HD), a0);
-                    a1 = fmaf(pj[j + 1], Elem<KT>::load(vd, (size_t)(j + 1) * HD), a1);
-                    a2 = fmaf(pj[j + 2], Elem<KT>::load(vd, (size_t)(j + 2) * HD), a2);
-                    a3 = fmaf(pj[j + 3], Elem<KT>::load(vd, (size_t)(j + 3) * HD), a3);
+                    a0 = fmaf(pj[j], vload(j), a0);
+                    a1 = fmaf(pj[j + 1], vload(j + 1), a1);
+                    a2 = fmaf(pj[j + 2], vload(j + 2), a2);
+                    a3 = fmaf(pj[j + 3], vload(j + 3), a3);
                 }
-                for (; j < valid; ++j) a0 = fmaf(pj[j], Elem<KT>::load(vd, (size_t)j * HD), a0);
+                for (; j < valid; ++j) a0 = fmaf(pj[j], vload(j), a0);
                 o_acc[o] = (a0 + a1) + (a2 + a3);
             }
         }
@@ -428,7 +472,7 @@ static cudaError_t launch_attn_t(const AttnParams &p, int rows, cudaStream_t st,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits, p.n_kv, rows);
     cfg.blockDim = dim3(kAttnThreads, 1, 1);
-    cfg.dynamicSmemBytes = attn_smem_bytes(sizeof(KT) == 2, HD, p.group);
+    cfg.dynamicSmemBytes = attn_smem_bytes(std::is_same<KT, int8_t>::value ? 2 : (sizeof(KT) == 2 ? 1 : 0), HD, p.group);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -446,8 +490,15 @@ static cudaError_t launch_attn_t(const AttnParams &p, int rows, cudaStream_t st,
     return cudaLaunchKernelEx(&cfg, k_attn_decode<KT, HD>, p);
 }
 
-cudaError_t launch_attn(int kv_bf16, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
-    if (kv_bf16) {
+cudaError_t launch_attn(int kv_kind, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
+    if (kv_kind == 2) {   // Q8_0 storage
+        switch (head_dim) {
+            case 64: return launch_attn_t<int8_t, 64>(p, rows, st, pdl);
+            case 128: return launch_attn_t<int8_t, 128>(p, rows, st, pdl);
+        }
+        return cudaErrorInvalidValue;
+    }
+    if (kv_kind == 1) {
         switch (head_dim) {
             case 32: return launch_attn_t<__nv_bfloat16, 32>(p, rows, st, pdl);
             case 64: return launch_attn_t<__nv_bfloat16, 64>(p, rows, st, pdl);
@@ -475,6 +526,8 @@ cudaError_t prepare_attn() {
                                      bytes);
     e = e ? e : cudaFuncSetAttribute(k_attn_decode<__nv_bfloat16, 128>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_decode<int8_t, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_decode<int8_t, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     return e;
 }
 

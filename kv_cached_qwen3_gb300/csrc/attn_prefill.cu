@@ -74,7 +74,9 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 template <int HD, int HPC>
 __global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const float *q, __nv_bfloat16 *out, int T, int pos0,
                                                                int stream, int n_q, int group, int layer,
-                                                               float scale_log2, CacheView cache) {
+                                                               float scale_log2, CacheView cache,
+                                                               const __nv_bfloat16 *dense_k,
+                                                               const __nv_bfloat16 *dense_v) {
     constexpr int NKS = HD / 16;        // k-steps of S = Q K^T
     constexpr int NNO = HD / 8;         // n-tiles of O
     constexpr int TILE = kPage * HD;    // elements of one K (or V) page of one head
@@ -116,14 +118,32 @@ __global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const
     const __nv_bfloat16 *vpool = static_cast<const __nv_bfloat16 *>(cache.v);
     const size_t head_off = (size_t)(layer * cache.n_kv + kvh) * kPage * HD;
 
+    // Keys [0, pos0 + T) exist; rows of a block past them are zero-filled, so that a stale or
+    // poisoned cache tail never reaches the products (a masked weight is 0, and 0 * NaN = NaN).
+    const int nkeys = pos0 + T;
     auto load_block = [&](int kb, int buf) {
-        const size_t off = (size_t)ptab[kb] * cache.page_elems + head_off;
-        const __nv_bfloat16 *ks = kpool + off, *vs = vpool + off;
+        const __nv_bfloat16 *ks, *vs;
+        size_t rs;   // row stride (elements)
+        if (dense_k != nullptr) {   // the call's own rows (Q8_0 storage; pos0 = 0)
+            ks = dense_k + ((size_t)kb * kPage * cache.n_kv + kvh) * HD;
+            vs = dense_v + ((size_t)kb * kPage * cache.n_kv + kvh) * HD;
+            rs = (size_t)cache.n_kv * HD;
+        } else {
+            const size_t off = (size_t)ptab[kb] * cache.page_elems + head_off;
+            ks = kpool + off;
+            vs = vpool + off;
+            rs = HD;
+        }
         const uint32_t kdst = sbase + (uint32_t)(buf * 2) * TILE * 2, vdst = kdst + TILE * 2;
         for (int i = threadIdx.x; i < CHUNKS; i += NTH) {
             const int r = i / (HD / 8), c = i % (HD / 8);
-            cp_async16(kdst + swz<HD>(r, c), ks + r * HD + c * 8);
-            cp_async16(vdst + swz<HD>(r, c), vs + r * HD + c * 8);
+            if (kb * kPage + r < nkeys) {
+                cp_async16(kdst + swz<HD>(r, c), ks + r * rs + c * 8);
+                cp_async16(vdst + swz<HD>(r, c), vs + r * rs + c * 8);
+            } else {
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(kdst + swz<HD>(r, c)), "r"(0) : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vdst + swz<HD>(r, c)), "r"(0) : "memory");
+            }
         }
     };
 
@@ -255,7 +275,7 @@ static cudaError_t launch_ap(const AttnParams &a, int T, cudaStream_t st) {
     const float scale_log2 = a.scale * 1.4426950408889634f;
     k_attn_prefill<HD, HPC><<<grid, kWarpsPerHead * HPC * 32, ap_smem<HD>(), st>>>(
         a.q, static_cast<__nv_bfloat16 *>(a.out), T, a.rowmap.pos0, a.rowmap.stream0, a.n_q, a.group, a.layer,
-        scale_log2, a.cache);
+        scale_log2, a.cache, a.dense_k, a.dense_v);
     return cudaGetLastError();
 }
 
@@ -272,10 +292,16 @@ cudaError_t prepare_attn_prefill() {
     return e ? e : raise_ap<64, 2>();
 }
 
-bool attn_prefill_supported(int kv_bf16, int head_dim) { return kv_bf16 && (head_dim == 64 || head_dim == 128); }
+// bf16 cache, or Q8_0 storage (whose prefill reads the call's rows from the dense bf16 copy)
+bool attn_prefill_supported(int kv_kind, int head_dim) {
+    return (kv_kind == 1 || kv_kind == 2) && (head_dim == 64 || head_dim == 128);
+}
 
 cudaError_t launch_attn_prefill(int head_dim, const AttnParams &a, int T, cudaStream_t st) {
     if (a.rowmap.mode != 1 || !a.out_bf16) return cudaErrorInvalidValue;
+    if ((a.dense_k != nullptr) != (a.dense_v != nullptr) || (a.dense_k != nullptr && a.rowmap.pos0 != 0))
+        return cudaErrorInvalidValue;
+    if (a.cache.kv_q8 && a.dense_k == nullptr) return cudaErrorInvalidValue;
     const bool pair = a.group % 2 == 0;   // two q heads of a KV group share each staged page
     if (head_dim == 128) return pair ? launch_ap<128, 2>(a, T, st) : launch_ap<128, 1>(a, T, st);
     if (head_dim == 64) return pair ? launch_ap<64, 2>(a, T, st) : launch_ap<64, 1>(a, T, st);

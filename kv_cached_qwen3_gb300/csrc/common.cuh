@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -176,16 +177,35 @@ __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u &
 template <typename T> struct Elem;
 template <> struct Elem<float> {
     static constexpr int kPerVec = 4;   // elements per 16-byte vector
+    __device__ static __forceinline__ float round(float v) { return v; }
     __device__ static __forceinline__ float load(const float *p, size_t i) { return p[i]; }
     __device__ static __forceinline__ void store(float *p, size_t i, float v) { p[i] = v; }
 };
 template <> struct Elem<__nv_bfloat16> {
     static constexpr int kPerVec = 8;
+    __device__ static __forceinline__ float round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
     __device__ static __forceinline__ float load(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
     __device__ static __forceinline__ void store(__nv_bfloat16 *p, size_t i, float v) {
         p[i] = __float2bfloat16_rn(v);
     }
 };
+
+__device__ __forceinline__ float warp_max_abs(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Q8_0 block (ggml layout, the talker's quantized KV storage): 32 values held one per lane of a
+// warp (lane = position in the block). d = max|x| / 127, code = x * (1/d) rounded half away from
+// zero (0 for an all-zero block); codes at t + code_off + lane, d as fp16 at t + scale_off.
+__device__ __forceinline__ void q8_store_block(unsigned char *t, int code_off, int scale_off, float x, int lane) {
+    const float amax = warp_max_abs(fabsf(x));
+    const float d = amax / 127.0f;
+    const float id = d > 0.f ? 1.0f / d : 0.f;
+    reinterpret_cast<int8_t *>(t)[code_off + lane] = (int8_t)roundf(x * id);
+    if (lane == 0) *reinterpret_cast<__half *>(t + scale_off) = __float2half_rn(d);
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

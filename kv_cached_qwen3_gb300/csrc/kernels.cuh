@@ -2,6 +2,7 @@
 // kernel translation units and by the host runtime (talker_runtime.cu).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -36,7 +37,8 @@ struct CacheView {
     int n_layers;
     int n_kv;
     int head_dim;
-    int kv_bf16;        // 1: bf16 cache, 0: f32
+    int kv_bf16;        // 1: bf16 cache, 0: f32 (Q8_0 storage: kv_q8 = 1, kv_bf16 = 0)
+    int kv_q8;          // 1: Q8_0 tiles ([64][hd] int8 codes + [64][hd/32] fp16 scales); page_elems in bytes
     size_t page_elems;
 };
 
@@ -97,6 +99,9 @@ struct AttnParams {
     // 1: the splits of a (row, KV group) run as one thread-block cluster (splits <=
     // kAttnClusterMax) and combine through distributed shared memory; ws / cnt unused
     int cluster;
+    // Prefill with Q8_0 storage: the call's own K / V rows, bf16 [rows][n_kv][head_dim]
+    // (exact up to bf16, not read back from the quantized cache); null otherwise
+    const __nv_bfloat16 *dense_k, *dense_v;
 };
 constexpr int kAttnClusterMax = 8;   // portable cluster size
 
@@ -167,7 +172,7 @@ size_t gemv_smem_bytes(int rows_tmpl, int K);
 size_t attn_smem_bytes(int kv_bf16, int head_dim, int group);
 
 cudaError_t launch_gemv(int epi, int w_bf16, int rows_tmpl, const GemvParams &p, cudaStream_t st, bool pdl);
-cudaError_t launch_attn(int kv_bf16, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl);
+cudaError_t launch_attn(int kv_kind, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl);  // kv_kind 0 f32, 1 bf16, 2 Q8_0
 cudaError_t launch_set_len(int *cur_len, int stream, int value, cudaStream_t st);
 // Copy len rows of a stream between a dense [n_layers][n_kv][len][hd] buffer and the cache.
 cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *dense_v, int len, int to_cache,
@@ -199,9 +204,11 @@ cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, fl
 // Element-wise stages of the tensor-core prefill path (prefill.cu).
 cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H, void *out,
                                 cudaStream_t st);
+// dense_kv (Q8_0 storage only, else null): the rows' k / v also go to bf16 [2][rows][n_kv][hd]
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
                             const float *k_norm, const float2 *rope, float eps, float *q_out, const CacheView &cache,
-                            int layer, const RowMap &rm, int *status, cudaStream_t st);
+                            int layer, const RowMap &rm, int *status, cudaStream_t st,
+                            __nv_bfloat16 *dense_kv = nullptr);
 cudaError_t launch_swiglu_bf16(const float *gu, int rows, int I, void *out, cudaStream_t st);
 
 // Persistent decode kernel (one cooperative launch per decode step, one CTA per SM).

@@ -48,7 +48,7 @@ __global__ void k_rmsnorm_bf16(const float *x, int ld, const float *w, float eps
 // (prefill: stream0 at pos0 + r; decode: stream r at cur_len[r]).
 __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
                            const float *k_norm, const float2 *rope, float eps, float *q_out, CacheView cache, int layer,
-                           RowMap rm, int *status) {
+                           RowMap rm, int *status, __nv_bfloat16 *dense_kv) {
     const int n_heads = n_q + 2 * n_kv;
     const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (item >= rows * n_heads) return;
@@ -99,6 +99,33 @@ __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd
     }
     const int kvh = is_k ? h - n_q : h - n_q - n_kv;
     const int page = cache.page_table[(size_t)stream * cache.pages_per_stream + pos / kPage];
+    if (cache.kv_q8) {
+        // Q8_0 tile of (page, layer, head): [64][hd] codes, then [64][hd/32] fp16 scales; each valid
+        // register of the warp holds one block of 32 dims (lane = dim % 32, hd is 64 or 128)
+        const size_t tile = (size_t)kPage * hd + (size_t)kPage * (hd / 32) * 2;
+        unsigned char *t = static_cast<unsigned char *>(is_k ? cache.k : cache.v) + (size_t)page * cache.page_elems +
+                           (size_t)(layer * n_kv + kvh) * tile;
+        const int row = pos % kPage;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (32 * j >= half) continue;
+                const int d0 = 32 * j + u * half;
+                q8_store_block(t, row * hd + d0, kPage * hd + (row * (hd / 32) + d0 / 32) * 2, u ? b[j] : a[j], lane);
+            }
+        // the call itself attends its rows unquantized
+        __nv_bfloat16 *dk = dense_kv + ((size_t)(is_k ? 0 : rows) * n_kv + (size_t)r * n_kv + kvh) * hd;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = lane + 32 * j;
+            if (i < half) {
+                dk[i] = __float2bfloat16_rn(a[j]);
+                dk[i + half] = __float2bfloat16_rn(b[j]);
+            }
+        }
+        return;
+    }
     const size_t off = (size_t)page * cache.page_elems + ((size_t)(layer * n_kv + kvh) * kPage + pos % kPage) * hd;
     void *base = is_k ? cache.k : cache.v;
 #pragma unroll
@@ -137,11 +164,12 @@ cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float ep
 
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
                             const float *k_norm, const float2 *rope, float eps, float *q_out, const CacheView &cache,
-                            int layer, const RowMap &rm, int *status, cudaStream_t st) {
+                            int layer, const RowMap &rm, int *status, cudaStream_t st, __nv_bfloat16 *dense_kv) {
+    if (cache.kv_q8 && dense_kv == nullptr) return cudaErrorInvalidValue;
     const long long items = (long long)rows * (n_q + 2 * n_kv);
     const int per_block = 8;
     k_qkv_post<<<(unsigned)((items + per_block - 1) / per_block), per_block * 32, 0, st>>>(
-        raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, rm, status);
+        raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, rm, status, dense_kv);
     return cudaGetLastError();
 }
 

@@ -66,7 +66,7 @@ struct talker {
     cudaStream_t cap_st = nullptr;  // private stream for graph capture (the caller's may be the legacy stream)
     int dev = 0, n_sm = 0;
     int H = 0, nq = 0, nkv = 0, hd = 0, qd = 0, kvd = 0, qkv_n = 0, I = 0, V = 0, G = 0;
-    int w_bf16 = 0, kv_bf16 = 0;
+    int w_bf16 = 0, kv_bf16 = 0, kv_q8 = 0, kv_kind = 0;   // kv_kind: 0 f32, 1 bf16, 2 Q8_0
     size_t wsz = 0, kvsz = 0;
     char *wstore = nullptr;
     std::vector<LayerDev> L;
@@ -108,6 +108,7 @@ struct talker {
     // tensor-core prefill buffers (bf16 GEMM operands and the f32 gate/up projection)
     int cap_tc_rows = 0;
     void *hb = nullptr, *ab = nullptr, *gb = nullptr;
+    __nv_bfloat16 *kv_dense = nullptr;   // Q8_0 storage: the prefill's own k / v rows, [2][rows][n_kv][hd]
     float *gu = nullptr;
     int tc_ok = -1;                      // tensor-core prefill usable for this geometry (-1 unknown)
     // TTS loop input / output
@@ -146,7 +147,7 @@ void free_workspaces(talker *t) {
 }
 
 void free_tc(talker *t) {
-    void **bl[] = {&t->hb, &t->ab, &t->gb, reinterpret_cast<void **>(&t->gu)};
+    void **bl[] = {&t->hb, &t->ab, &t->gb, reinterpret_cast<void **>(&t->gu), reinterpret_cast<void **>(&t->kv_dense)};
     for (auto pp : bl) {
         free_ptr(*pp);
         *pp = nullptr;
@@ -255,7 +256,10 @@ talker_status validate_config(const talker_config *c) {
     if (c->vocab < 8 || c->vocab % 8) return TALKER_EINVAL;
     if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return TALKER_EINVAL;
     if ((c->weight_dtype != TALKER_DTYPE_F32 && c->weight_dtype != TALKER_DTYPE_BF16) ||
-        (c->kv_dtype != TALKER_DTYPE_F32 && c->kv_dtype != TALKER_DTYPE_BF16))
+        (c->kv_dtype != TALKER_DTYPE_F32 && c->kv_dtype != TALKER_DTYPE_BF16 && c->kv_dtype != TALKER_DTYPE_Q8_0))
+        return TALKER_EINVAL;
+    // Q8_0 storage: bf16 weights (its prefill runs on the tensor-core path), blocks of 32 in a head
+    if (c->kv_dtype == TALKER_DTYPE_Q8_0 && (c->weight_dtype != TALKER_DTYPE_BF16 || c->head_dim < 64))
         return TALKER_EINVAL;
     // the widest GEMV input must fit one staged row in shared memory
     const int kmax = std::max(std::max(c->hidden, c->n_q_heads * c->head_dim), c->intermediate);
@@ -341,6 +345,7 @@ CacheView cache_view(const talker *t) {
     c.n_kv = t->nkv;
     c.head_dim = t->hd;
     c.kv_bf16 = t->kv_bf16;
+    c.kv_q8 = t->kv_q8;
     c.page_elems = t->page_elems;
     return c;
 }
@@ -422,7 +427,7 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
         a.cnt = t->attn_cnt;
         a.status = t->d_status;
         if (rm.mode == 0) set_raw_heads(t, d, a);
-        TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, rows, st, pdl));
+        TRY_CUDA(launch_attn(t->kv_kind, t->hd, a, rows, st, pdl));
         ++nk;
         // 3) o_proj + residual
         GemvParams o{};
@@ -634,6 +639,7 @@ talker_status ensure_tc(talker *t, int rows) {
     TRY_CUDA(cudaMalloc(&t->ab, (size_t)cap * t->qd * 2));
     TRY_CUDA(cudaMalloc(&t->gb, (size_t)cap * t->I * 2));
     TRY_CUDA(cudaMalloc(&t->gu, (size_t)cap * 2 * t->I * sizeof(float)));
+    if (t->kv_q8) TRY_CUDA(cudaMalloc(&t->kv_dense, (size_t)2 * cap * t->nkv * t->hd * 2));
     t->cap_tc_rows = cap;
     return TALKER_OK;
 }
@@ -664,7 +670,7 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         TRY(tc_gemm(t, st, t->hb, T, t->H, d.qkv, t->qkv_n, t->raw, t->qkv_n, false, &nk));
         if (rm.mode != 0) {   // prefill rows; decode rows are finished inside the attention kernel
             TRY_CUDA(launch_qkv_post(t->raw, T, t->nq, t->nkv, t->hd, d.q_norm, d.k_norm, t->d_rope, t->c.rms_eps,
-                                     t->q, cv, l, rm, t->d_status, st));
+                                     t->q, cv, l, rm, t->d_status, st, t->kv_q8 ? t->kv_dense : nullptr));
             ++nk;
         }
         AttnParams a{};
@@ -684,10 +690,14 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         a.cnt = t->attn_cnt;
         a.status = t->d_status;
         if (rm.mode == 0) set_raw_heads(t, d, a);
-        if (rm.mode == 1 && attn_prefill_supported(t->kv_bf16, t->hd))
+        if (rm.mode == 1 && t->kv_q8) {   // the call's rows from the dense copy (prefill from position 0)
+            a.dense_k = t->kv_dense;
+            a.dense_v = t->kv_dense + (size_t)T * t->nkv * t->hd;
+        }
+        if (rm.mode == 1 && attn_prefill_supported(t->kv_kind, t->hd))
             TRY_CUDA(launch_attn_prefill(t->hd, a, T, st));   // causal tiles on the tensor cores
         else
-            TRY_CUDA(launch_attn(t->kv_bf16, t->hd, a, T, st, false));
+            TRY_CUDA(launch_attn(t->kv_kind, t->hd, a, T, st, false));
         ++nk;
         TRY(tc_gemm(t, st, t->ab, T, t->qd, d.o, t->H, t->x, t->H, true, &nk));
         TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.post_norm, t->c.rms_eps, T, t->H, t->hb, st));
@@ -738,6 +748,7 @@ talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float
                            int32_t *argmax, bool all_rows, bool append) {
     TRY(check_stream(t, stream));
     if (!emb || !logits || T < 1) return TALKER_EINVAL;
+    if (append && t->kv_q8) return TALKER_EINVAL;   // Q8_0: the prefill attends only its own rows
     const int pos0 = append ? t->len[stream] : 0;
     if (T > t->max_seq - pos0) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));
@@ -745,7 +756,8 @@ talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float
     RowMap rm{1, stream, pos0, t->d_len};
     ForwardOut out{logits, hidden, all_rows ? nullptr : argmax, all_rows, 0};
     int nk = 0;
-    if (T >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t)) {
+    if (t->kv_q8 && !tc_usable(t)) return TALKER_EINVAL;
+    if (t->kv_q8 || (T >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t))) {   // Q8_0: always this path
         TRY(ensure_tc(t, T));
         TRY(enqueue_tc(t, t->st, T, rm, emb, 1, out, &nk));
     } else {
@@ -795,8 +807,10 @@ talker_status talker_create(const talker_config *cfg, const talker_weight_ptrs *
     t->G = t->nq / t->nkv;
     t->w_bf16 = cfg->weight_dtype == TALKER_DTYPE_BF16;
     t->kv_bf16 = cfg->kv_dtype == TALKER_DTYPE_BF16;
+    t->kv_q8 = cfg->kv_dtype == TALKER_DTYPE_Q8_0;
+    t->kv_kind = t->kv_q8 ? 2 : (t->kv_bf16 ? 1 : 0);
     t->wsz = t->w_bf16 ? 2 : 4;
-    t->kvsz = t->kv_bf16 ? 2 : 4;
+    t->kvsz = t->kv_q8 ? 1 : (t->kv_bf16 ? 2 : 4);   // bytes per pool unit
     talker_status s = from_cuda(cudaGetDevice(&t->dev));
     if (s == TALKER_OK) s = from_cuda(cudaDeviceGetAttribute(&t->n_sm, cudaDevAttrMultiProcessorCount, t->dev));
     if (s == TALKER_OK) s = from_cuda(prepare_kernels());
@@ -835,7 +849,10 @@ talker_status talker_kv_init_batched(talker_t *t, int n_streams, int max_seq_len
     drop_graphs(t);
     free_cache(t);
     const int pps = (max_seq_len + kPageRows - 1) / kPageRows;
-    const size_t page_elems = (size_t)t->c.n_layers * t->nkv * kPageRows * t->hd;
+    // pool units per page: elements, or bytes for Q8_0 tiles ([64][hd] codes + [64][hd/32] fp16 scales)
+    const size_t tile_units = t->kv_q8 ? (size_t)kPageRows * t->hd + (size_t)kPageRows * (t->hd / 32) * 2
+                                       : (size_t)kPageRows * t->hd;
+    const size_t page_elems = (size_t)t->c.n_layers * t->nkv * tile_units;
     const size_t n_pages = (size_t)n_streams * pps;
     const size_t pool_bytes = n_pages * page_elems * t->kvsz;
     TRY_CUDA(cudaMalloc(&t->kpool, pool_bytes));

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libtalker_gb300.so")
 
 STATUS = {0: "TALKER_OK", 1: "TALKER_EINVAL", 2: "TALKER_EOVERFLOW", 3: "TALKER_ENOMEM", 4: "TALKER_ECUDA",
           5: "TALKER_ESTATE", 6: "TALKER_EDEVICE"}
-DTYPE = {"f32": 0, "bf16": 1}
+DTYPE = {"f32": 0, "bf16": 1, "q8_0": 2}
 LAYER_FIELDS = ("input_norm", "q_proj", "k_proj", "v_proj", "q_norm", "k_norm", "o_proj", "post_norm",
                 "gate_proj", "up_proj", "down_proj")
 

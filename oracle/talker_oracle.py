@@ -211,7 +211,11 @@ def q8_0_quantize(x):
     safe = np.where(d > 0, d, np.float32(1.0))
     inv = np.where(d > 0, np.float32(1.0) / safe, np.float32(0.0)).astype(np.float32)
     t = (b * inv).astype(np.float32)
-    q = np.sign(t) * np.floor(np.abs(t) + np.float32(0.5))
+    # half away from zero; the fractional part of an f32 below 2^23 is exact, so no add-then-floor
+    # rounding error can move a value across the .5 boundary
+    a = np.abs(t)
+    fl = np.floor(a)
+    q = np.sign(t) * np.where(a - fl >= np.float32(0.5), fl + 1, fl)
     return q.astype(np.int8).reshape(shp), d[..., 0].astype(np.float16)
 
 

@@ -504,3 +504,13 @@ def test_q8_cache_attends_own_row_exactly(tiny):
     kp, _ = cp.kv_export(0, L + 1)
     np.testing.assert_array_equal(kq[:, :, L], q8_0_roundtrip(kp[:, :, L]))
     assert not np.array_equal(kp[:, :, L], kq[:, :, L])   # the plain cache keeps it exact
+
+
+def test_q8_0_rounding_just_below_half():
+    """x * (1/d) = 0.5 - 2^-25 must round to 0 (adding 0.5 in f32 would give 1.0)."""
+    from oracle import q8_0_quantize
+    x = np.zeros(32, np.float32)
+    x[0] = 127.0
+    x[1] = np.float32(0.5) - np.float32(2.0 ** -25)
+    q, d = q8_0_quantize(x)
+    assert float(d[0]) == 1.0 and q[1] == 0
