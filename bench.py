@@ -358,7 +358,40 @@ def long_context(tk, g, torch, st, hbm, tc):
         kvb = step_bytes(g, L + steps // 2)[1]
         res["decode"].append({"L": L, "ms_per_step": s * 1e3, "steps_per_s": 1.0 / s,
                               "hbm_frac": (wbytes + kvb) / s / 1e9 / hbm})
+    res["decode_q8_0_kv"] = long_context_q8(torch, lc, hbm)
     return res
+
+
+def long_context_q8(torch, lc, hbm):
+    """Single-stream decode at 8K/16K/32K cached rows with the Q8_0 KV storage (136 of 256 bytes per head row)."""
+    from dataclasses import replace
+    from kv_cached_qwen3_gb300.talker import Talker
+    g = replace(lc.geometry, kv_dtype="q8_0")
+    tk = Talker(g, inputs.make_weights(g, lc.seed))
+    tk.kv_init_batched(1, max(lc.long_lengths) + 8)
+    e1 = torch.randn(1, g.hidden, device="cuda")
+    lg = torch.empty(1, g.vocab, device="cuda")
+    wbytes = g.n_linear_params() * 2 + 4 * (g.n_layers * (2 * g.hidden + 2 * g.head_dim) + g.hidden)
+    row = 2 * g.n_layers * g.n_kv_heads * (g.head_dim + g.head_dim // 32 * 2)   # K and V, codes + scales
+    out = []
+    for L in lc.long_lengths:
+        kk = torch.randn(g.n_layers, g.n_kv_heads, L, g.head_dim, device="cuda")
+        vv = torch.randn(g.n_layers, g.n_kv_heads, L, g.head_dim, device="cuda")
+        tk.kv_import(0, kk, vv, L)
+        del kk, vv
+        steps = 5
+
+        def run():
+            tk.rewind(0, L)
+            for _ in range(steps):
+                tk.decode(e1, lg)
+        run()
+        torch.cuda.synchronize()
+        s = timed(torch, tk.stream, run, 2) / steps
+        out.append({"L": L, "ms_per_step": s * 1e3, "steps_per_s": 1.0 / s,
+                    "hbm_frac": (wbytes + row * (L + steps // 2 + 1)) / s / 1e9 / hbm})
+    tk.close()
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle arms

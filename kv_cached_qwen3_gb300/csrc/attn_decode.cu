@@ -293,6 +293,17 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
         // decode rows: row `newest` of this page is this step's row, read from knew / vnew (the
         // copied page may predate it); prefill rows were all written before the page was copied
         const int newest = (p.raw != nullptr) ? pos - pg * kPage : -1;
+        if constexpr (!kQ8) {   // bf16 / f32 tiles hold the fresh row exactly as stored: patch it in
+            if (newest >= 0 && newest < kPage) {
+                KT *kt = reinterpret_cast<KT *>(kbuf + buf * kTileBytes) + newest * HD;
+                KT *vt = reinterpret_cast<KT *>(vbuf + buf * kTileBytes) + newest * HD;
+                for (int i = tid; i < HD; i += kAttnThreads) {
+                    Elem<KT>::store(kt, i, knew[i]);
+                    Elem<KT>::store(vt, i, vnew[i]);
+                }
+                __syncthreads();
+            }
+        }
 
         // scores: warp w takes key rows w, w + 8, ...; lanes split the head dimension. All of a
         // warp's rows and heads are reduced in one interleaved butterfly (latency paid once).
@@ -305,7 +316,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const int j = warp + NWARP * i;
-                    kv[i][e] = (j == newest) ? knew[lane * E + e] : Tile::load(Ks, j, lane * E + e);
+                    if constexpr (kQ8) kv[i][e] = (j == newest) ? knew[lane * E + e] : Tile::load(Ks, j, lane * E + e);
+                    else kv[i][e] = Tile::load(Ks, j, lane * E + e);
                 }
             for (int gi0 = 0; gi0 < G; gi0 += 2) {   // two heads per pass keeps the register count bounded
                 float dv[RPW][2];
@@ -370,15 +382,18 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(const AttnParams p
                 // four independent chains over the page's rows
                 float a0 = o_acc[o] * al_s[gi], a1 = 0.f, a2 = 0.f, a3 = 0.f;
                 const float *pj = sc + gi * kPage;
-                auto vload = [&](int j) { return (j == newest) ? vnew[d] : Tile::load(Vs, j, d); };
+                // the fresh row, when this page holds it, is the page's last valid row: it is
+                // added from vnew after the branch-free loop over the copied rows
+                const int vmain = (newest >= 0 && newest < valid) ? valid - 1 : valid;
                 int j = 0;
-                for (; j + 4 <= valid; j += 4) {
-                    a0 = fmaf(pj[j], vload(j), a0);
-                    a1 = fmaf(pj[j + 1], vload(j + 1), a1);
-                    a2 = fmaf(pj[j + 2], vload(j + 2), a2);
-                    a3 = fmaf(pj[j + 3], vload(j + 3), a3);
+                for (; j + 4 <= vmain; j += 4) {
+                    a0 = fmaf(pj[j], Tile::load(Vs, j, d), a0);
+                    a1 = fmaf(pj[j + 1], Tile::load(Vs, j + 1, d), a1);
+                    a2 = fmaf(pj[j + 2], Tile::load(Vs, j + 2, d), a2);
+                    a3 = fmaf(pj[j + 3], Tile::load(Vs, j + 3, d), a3);
                 }
-                for (; j < valid; ++j) a0 = fmaf(pj[j], vload(j), a0);
+                for (; j < vmain; ++j) a0 = fmaf(pj[j], Tile::load(Vs, j, d), a0);
+                if (vmain < valid) a0 = fmaf(pj[vmain], vnew[d], a0);
                 o_acc[o] = (a0 + a1) + (a2 + a3);
             }
         }
