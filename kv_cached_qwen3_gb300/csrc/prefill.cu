@@ -20,27 +20,37 @@ using namespace talker_dev;
 
 namespace talker_k {
 
-// One warp per row.
+// One CTA per row: every thread stages its float4s of the row (one round trip), the sum of
+// squares is reduced across the CTA, then the scaled bf16 row is written.
 __global__ void k_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H,
                                __nv_bfloat16 *out) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= rows) return;
-    const float *xr = x + (size_t)warp * ld;
+    __shared__ float red[32];
+    const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float *xr = x + (size_t)row * ld;
+    constexpr int MAXV = 4;   // float4s per thread (H <= 4 * 4 * blockDim.x)
+    float4 v[MAXV];
     float ss = 0.f;
-    for (int k = lane * 4; k < H; k += 128) {
-        const float4 v = *reinterpret_cast<const float4 *>(xr + k);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+        const int k = (threadIdx.x + i * blockDim.x) * 4;
+        v[i] = k < H ? *reinterpret_cast<const float4 *>(xr + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
     }
     ss = warp_sum(ss);
-    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
-    __nv_bfloat16 *o = out + (size_t)warp * H;
-    for (int k = lane * 4; k < H; k += 128) {
-        const float4 v = *reinterpret_cast<const float4 *>(xr + k);
-        const float4 g = *reinterpret_cast<const float4 *>(w + k);
-        __nv_bfloat162 a = __floats2bfloat162_rn(v.x * inv * g.x, v.y * inv * g.y);
-        __nv_bfloat162 b = __floats2bfloat162_rn(v.z * inv * g.z, v.w * inv * g.w);
-        *reinterpret_cast<__nv_bfloat162 *>(o + k) = a;
-        *reinterpret_cast<__nv_bfloat162 *>(o + k + 2) = b;
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
+    const float inv = 1.0f / sqrtf(t / (float)H + eps);
+    __nv_bfloat16 *o = out + (size_t)row * H;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+        const int k = (threadIdx.x + i * blockDim.x) * 4;
+        if (k < H) {
+            const float4 g = *reinterpret_cast<const float4 *>(w + k);
+            *reinterpret_cast<__nv_bfloat162 *>(o + k) = __floats2bfloat162_rn(v[i].x * inv * g.x, v[i].y * inv * g.y);
+            *reinterpret_cast<__nv_bfloat162 *>(o + k + 2) = __floats2bfloat162_rn(v[i].z * inv * g.z, v[i].w * inv * g.w);
+        }
     }
 }
 
@@ -156,9 +166,9 @@ __global__ void k_swiglu_bf16(const float *gu, int rows, int I, __nv_bfloat16 *o
 
 cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H, void *out,
                                 cudaStream_t st) {
-    const int warps_per_block = 8;
-    k_rmsnorm_bf16<<<(rows + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, st>>>(
-        x, ld, w, eps, rows, H, static_cast<__nv_bfloat16 *>(out));
+    const int threads = 256;
+    if (H % 4 || H > 4 * 4 * threads) return cudaErrorInvalidValue;
+    k_rmsnorm_bf16<<<rows, threads, 0, st>>>(x, ld, w, eps, rows, H, static_cast<__nv_bfloat16 *>(out));
     return cudaGetLastError();
 }
 

@@ -937,7 +937,13 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
     int max_len = 0;
     for (int b = 0; b < B; ++b) max_len = std::max(max_len, t->len[b]);
     const int cluster = (B <= 2 && max_len + 1 <= kAttnClusterMax * kPageRows) ? 1 : 0;
-    const int splits = cluster ? kAttnClusterMax : decode_splits(t, B);
+    // enough splits to fill the GPU in one wave; with several streams (ragged lengths) also
+    // enough that a split walks about four pages of the longest stream, which balances the
+    // waves (captured steps are keyed by the split count)
+    const int pages_max = (max_len + 1 + kPageRows - 1) / kPageRows;
+    const int splits = cluster  ? kAttnClusterMax
+                       : B == 1 ? decode_splits(t, B)
+                                : std::min(64, std::max(decode_splits(t, B), (pages_max + 3) / 4));
     TRY(ensure_capacity(t, B, splits));
     if (kind == 1) TRY(ensure_tc(t, B));
     GraphEntry *ge = nullptr;
