@@ -149,6 +149,16 @@ talker_status talker_prefill_append(talker_t *t, int stream, const float *emb, i
 talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits, float *hidden,
                             int32_t *argmax);
 
+/* Batched prefill ("talker-forward.h", talker_forward_prefill for streams 0..B-1
+ * at once): rewind streams 0..B-1 and run T rows each; emb is [B, T, H] f32
+ * (stream-major). Outputs for the last row of every stream: hidden_last [B, H]
+ * (may be NULL), logits_last [B, vocab] (required), argmax_last [B] (may be
+ * NULL). Runs on the tensor-core path (bf16 weights). Errors: EINVAL (B < 1 or
+ * > n_streams, T < 1, null pointers, f32 weights), EOVERFLOW (T > max_seq_len),
+ * ESTATE, ECUDA. */
+talker_status talker_prefill_batched(talker_t *t, int B, const float *emb, int T, float *hidden_last,
+                                     float *logits_last, int32_t *argmax_last);
+
 /* TTS loop output ("qwen3-tts" talker prefill and step, codebook-0 selection):
  * before every head's argmax (prefill, append, decode), the logits of token
  * indices [vocab - vocab_tail, vocab) other than eos_id are set to -inf, in

@@ -27,9 +27,9 @@ namespace talker_k {
 
 constexpr int kMaxGroup = 8;
 
-__device__ __forceinline__ int attn_row_stream(const RowMap &m, int r) { return m.mode == 0 ? r : m.stream0; }
+__device__ __forceinline__ int attn_row_stream(const RowMap &m, int r) { return rowmap_stream(m, r); }
 __device__ __forceinline__ int attn_row_pos(const RowMap &m, int r) {
-    return m.mode == 0 ? m.cur_len[r] : m.pos0 + r;
+    return rowmap_pos(m, r);
 }
 
 // One (page, layer, KV head) tile of the cache as it sits in the pool and in shared memory.

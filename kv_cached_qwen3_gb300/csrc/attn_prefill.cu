@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const
                                                                int stream, int n_q, int group, int layer,
                                                                float scale_log2, CacheView cache,
                                                                const __nv_bfloat16 *dense_k,
-                                                               const __nv_bfloat16 *dense_v) {
+                                                               const __nv_bfloat16 *dense_v, int n_streams) {
     constexpr int NKS = HD / 16;        // k-steps of S = Q K^T
     constexpr int NNO = HD / 8;         // n-tiles of O
     constexpr int TILE = kPage * HD;    // elements of one K (or V) page of one head
@@ -86,7 +86,13 @@ __global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const
     constexpr int NTH = kWarpsPerHead * HPC * 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, t4 = lane & 3;
-    const int qt = gridDim.x - 1 - blockIdx.x;   // longest tiles first
+    // n_streams streams of T rows each (stream s = rows s*T .. s*T + T - 1); the longest tiles
+    // of every stream go first
+    const int tiles_ps = (T + kBM - 1) / kBM;
+    const int qt = tiles_ps - 1 - (int)(blockIdx.x / n_streams);
+    const int sb = blockIdx.x % n_streams;
+    const size_t rbase = (size_t)sb * T;   // this stream's first row in q, out and the dense copy
+    stream += sb;
     const int h = blockIdx.y * HPC + warp / kWarpsPerHead;
     const int kvh = (blockIdx.y * HPC) / group;
     const int qd = n_q * HD;
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const
             const int r = row0 + g8 + 8 * half;
             float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
             if (r < T) {
-                const float *src = q + (size_t)r * qd + (size_t)h * HD + ks * 16 + 2 * t4;
+                const float *src = q + (rbase + r) * qd + (size_t)h * HD + ks * 16 + 2 * t4;
                 lo = *reinterpret_cast<const float2 *>(src);
                 hi = *reinterpret_cast<const float2 *>(src + 8);
             }
@@ -125,8 +131,8 @@ __global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const
         const __nv_bfloat16 *ks, *vs;
         size_t rs;   // row stride (elements)
         if (dense_k != nullptr) {   // the call's own rows (Q8_0 storage; pos0 = 0)
-            ks = dense_k + ((size_t)kb * kPage * cache.n_kv + kvh) * HD;
-            vs = dense_v + ((size_t)kb * kPage * cache.n_kv + kvh) * HD;
+            ks = dense_k + ((rbase + (size_t)kb * kPage) * cache.n_kv + kvh) * HD;
+            vs = dense_v + ((rbase + (size_t)kb * kPage) * cache.n_kv + kvh) * HD;
             rs = (size_t)cache.n_kv * HD;
         } else {
             const size_t off = (size_t)ptab[kb] * cache.page_elems + head_off;
@@ -256,10 +262,10 @@ __global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const
     for (int n = 0; n < NNO; ++n) {
         const int d = n * 8 + 2 * t4;
         if (r0 < T)
-            *reinterpret_cast<uint32_t *>(out + (size_t)r0 * qd + (size_t)h * HD + d) =
+            *reinterpret_cast<uint32_t *>(out + (rbase + r0) * qd + (size_t)h * HD + d) =
                 pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
         if (r1 < T)
-            *reinterpret_cast<uint32_t *>(out + (size_t)r1 * qd + (size_t)h * HD + d) =
+            *reinterpret_cast<uint32_t *>(out + (rbase + r1) * qd + (size_t)h * HD + d) =
                 pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
     }
 }
@@ -271,11 +277,14 @@ constexpr size_t ap_smem() {   // (independent of the heads per CTA)
 
 template <int HD, int HPC>
 static cudaError_t launch_ap(const AttnParams &a, int T, cudaStream_t st) {
-    const dim3 grid((T + kBM - 1) / kBM, a.n_q / HPC);
+    // rows_per_stream > 0: n_streams = T / rows_per_stream streams of rows_per_stream rows
+    const int rps = a.rowmap.rows_per_stream > 0 ? a.rowmap.rows_per_stream : T;
+    const int ns = T / rps;
+    const dim3 grid(ns * ((rps + kBM - 1) / kBM), a.n_q / HPC);
     const float scale_log2 = a.scale * 1.4426950408889634f;
     k_attn_prefill<HD, HPC><<<grid, kWarpsPerHead * HPC * 32, ap_smem<HD>(), st>>>(
-        a.q, static_cast<__nv_bfloat16 *>(a.out), T, a.rowmap.pos0, a.rowmap.stream0, a.n_q, a.group, a.layer,
-        scale_log2, a.cache, a.dense_k, a.dense_v);
+        a.q, static_cast<__nv_bfloat16 *>(a.out), rps, a.rowmap.pos0, a.rowmap.stream0, a.n_q, a.group, a.layer,
+        scale_log2, a.cache, a.dense_k, a.dense_v, ns);
     return cudaGetLastError();
 }
 
@@ -299,6 +308,7 @@ bool attn_prefill_supported(int kv_kind, int head_dim) {
 
 cudaError_t launch_attn_prefill(int head_dim, const AttnParams &a, int T, cudaStream_t st) {
     if (a.rowmap.mode != 1 || !a.out_bf16) return cudaErrorInvalidValue;
+    if (a.rowmap.rows_per_stream > 0 && T % a.rowmap.rows_per_stream) return cudaErrorInvalidValue;
     if ((a.dense_k != nullptr) != (a.dense_v != nullptr) || (a.dense_k != nullptr && a.rowmap.pos0 != 0))
         return cudaErrorInvalidValue;
     if (a.cache.kv_q8 && a.dense_k == nullptr) return cudaErrorInvalidValue;

@@ -35,8 +35,8 @@ __device__ __forceinline__ size_t cache_offset(const CacheView &c, int stream, i
     return (size_t)page * c.page_elems + ((size_t)(layer * c.n_kv + head) * kPage + (pos % kPage)) * c.head_dim;
 }
 
-__device__ __forceinline__ int row_stream(const RowMap &m, int r) { return m.mode == 0 ? r : m.stream0; }
-__device__ __forceinline__ int row_pos(const RowMap &m, int r) { return m.mode == 0 ? m.cur_len[r] : m.pos0 + r; }
+__device__ __forceinline__ int row_stream(const RowMap &m, int r) { return rowmap_stream(m, r); }
+__device__ __forceinline__ int row_pos(const RowMap &m, int r) { return rowmap_pos(m, r); }
 
 // QK-norm + NEOX RoPE + KV append for one completed head over the rows of a
 // row block ("talker-forward.h", talker_layer_forward: per-head QK-norm, RoPE

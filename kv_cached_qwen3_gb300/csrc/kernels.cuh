@@ -19,12 +19,22 @@ enum Epilogue : int {
 // Which stream and position each activation row belongs to.
 //   mode 0 (decode):  row r is stream r at position cur_len[r]
 //   mode 1 (prefill): row r is stream `stream0` at position pos0 + r
+// Where row r of a launch sits. mode 0 (decode): stream r at position cur_len[r].
+// mode 1 (prefill): stream stream0 + r / rows_per_stream at position pos0 + r % rows_per_stream
+// (rows_per_stream = 0: every row in stream0).
 struct RowMap {
     int mode;
     int stream0;
     int pos0;
     const int *cur_len;
+    int rows_per_stream;
 };
+__device__ __forceinline__ int rowmap_stream(const RowMap &m, int r) {
+    return m.mode == 0 ? r : (m.rows_per_stream > 0 ? m.stream0 + r / m.rows_per_stream : m.stream0);
+}
+__device__ __forceinline__ int rowmap_pos(const RowMap &m, int r) {
+    return m.mode == 0 ? m.cur_len[r] : m.pos0 + (m.rows_per_stream > 0 ? r % m.rows_per_stream : r);
+}
 
 // The paged KV cache. Page = [n_layers][n_kv][kPage][head_dim] elements; the
 // position p of stream s lives in page page_table[s * pages_per_stream + p / kPage].

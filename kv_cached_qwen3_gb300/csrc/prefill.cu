@@ -74,8 +74,8 @@ __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd
         a[t] = (i < half) ? src[i] : 0.f;
         b[t] = (i < half) ? src[i + half] : 0.f;
     }
-    const int pos = rm.mode == 0 ? rm.cur_len[r] : rm.pos0 + r;
-    const int stream = rm.mode == 0 ? r : rm.stream0;
+    const int pos = rowmap_pos(rm, r);
+    const int stream = rowmap_stream(rm, r);
     if (pos < 0 || pos >= cache.max_seq) {
         if (lane == 0) atomicOr(status, ST_BAD_POSITION);
         return;

@@ -356,6 +356,7 @@ struct ForwardOut {
     int32_t *argmax;
     bool head_all_rows;  // logits/hidden for every row, else the last row only
     int inc_len;         // decode: bump cur_len[r] for every row after the step
+    int rows_per_stream = 0;   // batched prefill: the last row of every stream (rows of T each)
 };
 
 // Enqueue the whole forward for `rows` rows: per layer QKV (+QK-norm, RoPE, KV
@@ -707,14 +708,15 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         ++nk;
         TRY(tc_gemm(t, st, t->gb, T, t->I, d.down, t->H, t->x, t->H, true, &nk));
     }
-    const int hrows = out.head_all_rows ? T : 1;
+    const int rps = out.rows_per_stream;
+    const int hrows = out.head_all_rows ? T : (rps > 0 ? T / rps : 1);
     GemvParams h{};
     h.eps = t->c.rms_eps;
     h.rows = hrows;
     h.status = t->d_status;
     h.W = t->head;
-    h.act = out.head_all_rows ? t->x : t->x + (size_t)(T - 1) * t->H;
-    h.act_ld = t->H;
+    h.act = out.head_all_rows ? t->x : t->x + (size_t)((rps > 0 ? rps : T) - 1) * t->H;
+    h.act_ld = (!out.head_all_rows && rps > 0) ? rps * t->H : t->H;
     h.norm_w = t->fnorm;
     h.K = t->H;
     h.n_out = t->V;
@@ -916,6 +918,27 @@ talker_status talker_prefill_all_rows(talker_t *t, int stream, const float *emb,
 talker_status talker_prefill_append(talker_t *t, int stream, const float *emb, int T, float *hidden_last,
                                     float *logits_last, int32_t *argmax_last) {
     return prefill_impl(t, stream, emb, T, hidden_last, logits_last, argmax_last, false, true);
+}
+
+talker_status talker_prefill_batched(talker_t *t, int B, const float *emb, int T, float *hidden_last,
+                                     float *logits_last, int32_t *argmax_last) {
+    if (!t) return TALKER_EINVAL;
+    if (t->n_streams == 0) return TALKER_ESTATE;
+    if (!emb || !logits_last || B < 1 || B > t->n_streams || T < 1) return TALKER_EINVAL;
+    if (T > t->max_seq) return TALKER_EOVERFLOW;
+    if (!tc_usable(t) || (long long)B * T > (1 << 30)) return TALKER_EINVAL;   // tensor-core path only
+    TRY_CUDA(cudaSetDevice(t->dev));
+    const int rows = B * T;
+    TRY(ensure_capacity(t, rows, 1));
+    TRY(ensure_tc(t, rows));
+    RowMap rm{1, 0, 0, t->d_len, T};
+    ForwardOut out{logits_last, hidden_last, argmax_last, false, 0, T};
+    int nk = 0;
+    TRY(enqueue_tc(t, t->st, rows, rm, emb, 1, out, &nk));
+    for (int s = 0; s < B; ++s) TRY_CUDA(launch_set_len(t->d_len, s, T, t->st));
+    t->launches += nk + B;
+    for (int s = 0; s < B; ++s) t->len[s] = T;
+    return TALKER_OK;
 }
 
 talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits, float *hidden, int32_t *argmax) {

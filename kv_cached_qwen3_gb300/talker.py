@@ -69,6 +69,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_cur_len": (st, [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
         "talker_prefill": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
         "talker_prefill_append": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
+        "talker_prefill_batched": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
         "talker_set_logit_suppression": (st, [vp, ctypes.c_int, ctypes.c_int]),
         "talker_set_code_tables": (st, [vp, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_int), ctypes.c_int,
                                         ctypes.c_int]),
@@ -196,6 +197,16 @@ class Talker:
         am = self._out(1, dtype=self.torch.int32) if argmax else None
         self._check(self.lib.talker_prefill_append(self.h, stream, _ptr(emb), T, _ptr(hd), _ptr(lg), _ptr(am)),
                     "talker_prefill_append")
+        return hd, lg, am
+
+    def prefill_batched(self, emb, hidden=True, argmax=True):
+        """emb [B, T, H] f32 cuda: streams 0..B-1 prefilled with T rows each. Returns per-stream last rows."""
+        B, T = emb.shape[0], emb.shape[1]
+        lg = self._out(B, self.g.vocab)
+        hd = self._out(B, self.g.hidden) if hidden else None
+        am = self._out(B, dtype=self.torch.int32) if argmax else None
+        self._check(self.lib.talker_prefill_batched(self.h, B, _ptr(emb), T, _ptr(hd), _ptr(lg), _ptr(am)),
+                    "talker_prefill_batched")
         return hd, lg, am
 
     def prefill_all_rows(self, stream: int, emb, hidden=True):

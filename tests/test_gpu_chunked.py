@@ -93,3 +93,29 @@ def test_append_overflow_changes_nothing(cuda):
     assert tk.cur_len(0) == 40
     assert tk.sync_status() == 0
     tk.close()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "q8_0"])
+def test_batched_prefill_streams(cuda, kv):
+    """Streams 0..B-1 prefilled in one call (T rows each, across page boundaries), then a decode step."""
+    from kv_cached_qwen3_gb300.talker import Talker
+    g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 2, "kv_dtype": kv})
+    w = inputs.make_weights(g, 57)
+    B, T = 3, 70
+    emb = np.stack([inputs.make_embeddings(g, 57, 0, T + 1, stream=s) for s in range(B)])   # [B, T+1, H]
+    tk = Talker(g, w)
+    tk.kv_init_batched(B, T + 2)
+    oc = OracleCache(Oracle(g, w), B, T + 2, kv_q8=(kv == "q8_0"))
+    hd, lg, am = tk.prefill_batched(dev(emb[:, :T]))
+    for s in range(B):
+        rh, rl = oc.prefill(s, emb[s, :T])
+        check_rows(host(hd)[s], rh[None], bf16=True, what="stream %d hidden" % s)
+        check_rows(host(lg)[s], rl[None], bf16=True, what="stream %d logits" % s)
+        assert int(host(am)[s]) == int(np.argmax(host(lg)[s]))
+        assert tk.cur_len(s) == T
+    lgd = torch.empty(B, g.vocab, device="cuda")
+    tk.decode(dev(emb[:, T]), lgd)
+    _, rl = oc.decode(emb[:, T])
+    check_rows(host(lgd), rl, bf16=True, what="decode after batched prefill")
+    assert tk.sync_status() == 0
+    tk.close()
