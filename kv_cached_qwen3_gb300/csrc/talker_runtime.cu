@@ -116,6 +116,11 @@ struct talker {
     EmbedTables codes{};                        // caller-owned codebook tables (codes.n = 0: none)
     float *code_emb = nullptr;                  // [code_emb_rows, H] rows built from codebook ids
     int code_emb_rows = 0;
+    // whole-frame graph (prefill + steps fed by the previous step's code, on the device)
+    cudaGraphExec_t frame_exec = nullptr;
+    std::vector<const void *> frame_key;        // the inputs the captured frame is valid for
+    int frame_T0 = 0, frame_steps = 0, frame_kernels = 0;
+    float *frame_logits = nullptr;              // [V] scratch when the caller wants no logits
 };
 
 namespace {
@@ -123,6 +128,9 @@ namespace {
 void drop_graphs(talker *t) {
     for (auto &g : t->graphs) cudaGraphExecDestroy(g.exec);
     t->graphs.clear();
+    if (t->frame_exec) cudaGraphExecDestroy(t->frame_exec);
+    t->frame_exec = nullptr;
+    t->frame_key.clear();
 }
 
 void free_ptr(void *p) {
@@ -130,7 +138,8 @@ void free_ptr(void *p) {
 }
 
 void free_workspaces(talker *t) {
-    float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->attn_ws, &t->head_val, &t->code_emb};
+    float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->attn_ws, &t->head_val, &t->code_emb,
+                    &t->frame_logits};
     t->code_emb_rows = 0;
     for (auto pp : fl) {
         free_ptr(*pp);
@@ -634,6 +643,7 @@ bool tc_usable(talker *t) {
 talker_status ensure_tc(talker *t, int rows) {
     if (rows <= t->cap_tc_rows) return TALKER_OK;
     TRY_CUDA(cudaStreamSynchronize(t->st));
+    drop_graphs(t);   // captured steps hold the old buffers
     free_tc(t);
     const int cap = std::max(rows, 128);
     TRY_CUDA(cudaMalloc(&t->hb, (size_t)cap * t->H * 2));
@@ -1098,6 +1108,90 @@ talker_status talker_set_code_tables(talker_t *t, const void *const *tables, con
     e.n = n_tables;
     e.bf16 = dtype == TALKER_DTYPE_BF16;
     t->codes = e;
+    if (t->frame_exec) cudaGraphExecDestroy(t->frame_exec);   // a captured frame reads the old tables
+    t->frame_exec = nullptr;
+    t->frame_key.clear();
+    return TALKER_OK;
+}
+
+talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, const int *table_of_step,
+                           int32_t *codes, float *logits) {
+    if (!t) return TALKER_EINVAL;
+    if (t->n_streams == 0 || t->codes.n == 0) return TALKER_ESTATE;
+    if (!emb || !codes || T0 < 1 || n_steps < 0 || (n_steps > 0 && !table_of_step)) return TALKER_EINVAL;
+    for (int i = 0; i < n_steps; ++i)
+        if (table_of_step[i] < 0 || table_of_step[i] >= t->codes.n) return TALKER_EINVAL;
+    if (T0 > t->max_seq || n_steps > t->max_seq - T0) return TALKER_EOVERFLOW;
+    TRY_CUDA(cudaSetDevice(t->dev));
+    const bool tc_pre = t->kv_q8 || (T0 >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t));
+    if (t->kv_q8 && !tc_usable(t)) return TALKER_EINVAL;
+    // every buffer the frame touches, sized before capture (growing drops captured graphs)
+    const int splits_max = std::max(kAttnClusterMax, decode_splits(t, 1));
+    TRY(ensure_capacity(t, T0, splits_max));
+    if (tc_pre) TRY(ensure_tc(t, T0));
+    if (t->code_emb_rows < 1 || !t->frame_logits) {
+        drop_graphs(t);
+        if (t->code_emb_rows < 1) {
+            free_ptr(t->code_emb);
+            TRY_CUDA(cudaMalloc(&t->code_emb, (size_t)t->n_streams * t->H * sizeof(float)));
+            t->code_emb_rows = t->n_streams;
+        }
+        if (!t->frame_logits) TRY_CUDA(cudaMalloc(&t->frame_logits, (size_t)t->V * sizeof(float)));
+    }
+    std::vector<const void *> key = {emb, codes, logits};
+    for (int i = 0; i < n_steps; ++i) key.push_back(t->codes.table[table_of_step[i]]);
+    if (!(t->frame_exec && t->frame_T0 == T0 && t->frame_steps == n_steps && t->frame_key == key)) {
+        if (t->frame_exec) cudaGraphExecDestroy(t->frame_exec);
+        t->frame_exec = nullptr;
+        int nk = 0;
+        cudaGraph_t graph = nullptr;
+        TRY_CUDA(cudaStreamBeginCapture(t->cap_st, cudaStreamCaptureModeThreadLocal));
+        talker_status st = TALKER_OK;
+        {   // prefill of stream 0 from position 0; code 0 = its argmax
+            RowMap rm{1, 0, 0, t->d_len};
+            ForwardOut out{logits ? logits : t->frame_logits, nullptr, codes, false, 0};
+            st = tc_pre ? enqueue_tc(t, t->cap_st, T0, rm, emb, 1, out, &nk)
+                        : enqueue_forward(t, t->cap_st, T0, rm, emb, 1, out, &nk);
+            if (st == TALKER_OK) st = from_cuda(launch_set_len(t->d_len, 0, T0, t->cap_st));
+            ++nk;
+        }
+        for (int i = 0; i < n_steps && st == TALKER_OK; ++i) {
+            // step i: the row of code i in its table, then one decode step; code i + 1 = its argmax
+            const int g = table_of_step[i];
+            EmbedTables e{};
+            e.table[0] = t->codes.table[g];
+            e.vocab[0] = t->codes.vocab[g];
+            e.n = 1;
+            e.bf16 = t->codes.bf16;
+            st = from_cuda(launch_embed_codes(e, codes + i, nullptr, 1, t->H, t->code_emb, t->d_status, t->cap_st));
+            ++nk;
+            const int len = T0 + i;   // cache length before the step
+            t->attn_cluster = (len + 1 <= kAttnClusterMax * kPageRows) ? 1 : 0;
+            const int splits = t->attn_cluster ? kAttnClusterMax : decode_splits(t, 1);
+            RowMap rm{0, 0, 0, t->d_len};
+            ForwardOut out{logits ? logits + (size_t)(i + 1) * t->V : t->frame_logits, nullptr, codes + i + 1, false, 1};
+            if (st == TALKER_OK) st = enqueue_forward(t, t->cap_st, 1, rm, t->code_emb, splits, out, &nk);
+        }
+        cudaError_t e = cudaStreamEndCapture(t->cap_st, &graph);
+        if (st != TALKER_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return st;
+        }
+        if (e != cudaSuccess) return from_cuda(e);
+        e = cudaGraphInstantiate(&t->frame_exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) {
+            t->frame_exec = nullptr;
+            return from_cuda(e);
+        }
+        t->frame_T0 = T0;
+        t->frame_steps = n_steps;
+        t->frame_key = key;
+        t->frame_kernels = nk;
+    }
+    TRY_CUDA(cudaGraphLaunch(t->frame_exec, t->st));
+    t->launches += t->frame_kernels;
+    t->len[0] = T0 + n_steps;
     return TALKER_OK;
 }
 

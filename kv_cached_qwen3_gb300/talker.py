@@ -69,6 +69,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_cur_len": (st, [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
         "talker_prefill": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
         "talker_prefill_append": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
+        "talker_frame": (st, [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int), vp, vp]),
         "talker_prefill_batched": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
         "talker_set_logit_suppression": (st, [vp, ctypes.c_int, ctypes.c_int]),
         "talker_set_code_tables": (st, [vp, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_int), ctypes.c_int,
@@ -246,6 +247,14 @@ class Talker:
         self._check(self.lib.talker_decode_codes(self.h, _ptr(ids), _ptr(overlay), B, _ptr(logits), _ptr(hidden),
                                                  _ptr(argmax)), "talker_decode_codes")
         return logits, hidden, argmax
+
+    def frame(self, emb, table_of_step, codes, logits=None):
+        """emb [T0, H] f32 cuda; table_of_step: list of table indices (one per step); codes int32 cuda
+        [n_steps + 1]; logits f32 cuda [n_steps + 1, V] or None."""
+        n = len(table_of_step)
+        arr = (ctypes.c_int * max(1, n))(*table_of_step)
+        self._check(self.lib.talker_frame(self.h, _ptr(emb), emb.shape[0], n, arr, _ptr(codes), _ptr(logits)),
+                    "talker_frame")
 
     def set_decode_mode(self, mode: int):
         """0 automatic, 1 persistent decode kernel, 2 multi-kernel CUDA graph."""

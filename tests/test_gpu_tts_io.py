@@ -133,3 +133,54 @@ def test_decode_from_codebook_ids(cuda, bf16):
     tk.decode_codes(dev(bad, np.int32), None, lg, hd)
     assert tk.sync_status() & ST_BAD_ARG
     tk.close()
+
+
+@pytest.mark.parametrize("suppress", [False, True])
+def test_whole_frame_graph_predictor(cuda, suppress):
+    """Prefill T=2 + 15 device-fed steps in one graph on the predictor geometry, replayed for a
+    second frame. The oracle follows the GPU's codes (teacher forcing): every step's logits
+    against the oracle, every code = argmax of the GPU's own logits, top-1 agreement."""
+    from kv_cached_qwen3_gb300.talker import Talker
+    pl = inputs.WORKLOADS["predictor_loop"]
+    g = pl.geometry
+    w = inputs.make_weights(g, pl.seed)
+    rng = np.random.Generator(np.random.PCG64(64))
+    n_tables = 15
+    tables = [inputs.round_to_bf16(rng.standard_normal((g.vocab, g.hidden)).astype(np.float32))
+              for _ in range(n_tables)]
+    tdev = [dev(t).to(torch.bfloat16) for t in tables]
+    T0, n = pl.prefill_T, pl.decode_steps
+    steps = list(range(n))                       # step i reads table i
+    tk = Talker(g, w)
+    tk.set_code_tables(tdev, True)
+    if suppress:
+        tk.set_logit_suppression(1024, 2047)
+    tk.kv_init_batched(1, T0 + n + 1)
+    emb_dev = torch.empty(T0, g.hidden, device="cuda")
+    codes = torch.empty(n + 1, device="cuda", dtype=torch.int32)
+    lg = torch.empty(n + 1, g.vocab, device="cuda")
+    o = Oracle(g, w)
+    agree = []
+    for frame in range(2):
+        emb = inputs.make_embeddings(g, pl.seed, 0, T0, stream=frame)
+        emb_dev.copy_(dev(emb))
+        tk.frame(emb_dev, steps, codes, lg)
+        assert tk.cur_len(0) == T0 + n
+        c, L = host(codes).astype(np.int64), host(lg)
+        np.testing.assert_array_equal(c, np.argmax(L, axis=-1))
+        oc = OracleCache(o, 1, T0 + n + 1)
+        _, rl = oc.prefill(0, emb)
+        ref = [rl]
+        for i in range(n):
+            _, r = oc.decode(tables[steps[i]][c[i]][None])
+            ref.append(r[0])
+        ref = np.stack(ref)
+        if suppress:
+            check_suppressed(L, suppress_logits(ref, 1024, 2047), True, "frame %d" % frame)
+            ref = suppress_logits(ref, 1024, 2047)
+        else:
+            check_rows(L, ref, bf16=True, what="frame %d logits" % frame)
+        agree.append(np.argmax(ref, axis=-1) == c)
+    assert np.mean(np.concatenate(agree)) >= 0.93      # near-ties may differ; the GPU's own argmax is exact
+    assert tk.sync_status() == 0
+    tk.close()
