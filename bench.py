@@ -303,9 +303,21 @@ def predictor_loop(torch, hbm):
     wbytes, _ = step_bytes(g, 0)
     kv = sum(step_bytes(g, L)[1] for L in range(T0, T0 + n))
     per_frame = (n + 1) * wbytes + kv
+    # the same frame as one CUDA graph, each step's input gathered on the device from the previous
+    # step's code (15 random bf16 code tables [V, H])
+    tables = [torch.randn(g.vocab, g.hidden, device="cuda").to(torch.bfloat16) for _ in range(n)]
+    tk.set_code_tables(tables, True)
+    codes = torch.empty(n + 1, device="cuda", dtype=torch.int32)
+    steps = list(range(n))
+    for _ in range(3):
+        tk.frame(pre, steps, codes)
+    torch.cuda.synchronize()
+    sg = timed(torch, tk.stream, lambda: tk.frame(pre, steps, codes), frames)
     tk.close()
     return {"frames_per_s": 1.0 / s, "ms_per_frame": s * 1e3, "passes_per_frame": n + 1,
-            "hbm_frac": per_frame / s / 1e9 / hbm}
+            "hbm_frac": per_frame / s / 1e9 / hbm,
+            "frame_graph": {"frames_per_s": 1.0 / sg, "ms_per_frame": sg * 1e3,
+                            "hbm_frac": per_frame / sg / 1e9 / hbm}}
 
 
 def timed(torch, st, fn, reps):
