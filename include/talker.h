@@ -250,6 +250,15 @@ talker_status talker_set_prefill_mode(talker_t *t, int mode);
 talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, int N, float *out, int accumulate,
                                     int splits, void *cuda_stream);
 
+/* Test support: the prefill's gate/up GEMM with its SwiGLU epilogue ("qwentts.cpp/src/
+ * talker-forward.h", talker_layer_forward MLP: silu(gate) * up). B [N, K] bf16 holds the
+ * gate and up rows interleaved (row 2j = gate_j, row 2j + 1 = up_j); out_bf16 [M, N/2]
+ * receives bf16(silu(A B[2j]^T) * (A B[2j+1]^T)), silu(z) = z / (1 + exp(-z)). Device
+ * pointers; N % 128 == 0, K % 64 == 0, out 16-byte aligned. Synchronises the stream.
+ * Errors: EINVAL, ECUDA, EDEVICE (a wait in the kernel gave up). */
+talker_status talker_test_gemm_swiglu_bf16(const void *A, int M, int K, const void *B, int N, void *out_bf16,
+                                           void *cuda_stream);
+
 /* Tuning / test support: cap the number of CTAs that share one (stream, KV
  * group) along the sequence in the persistent decode kernel (0 = no cap).
  * Errors: EINVAL. */

@@ -2,14 +2,18 @@
 //   C[M, N] (+)= A[M, K] * B[N, K]^T,  A = activations, B = weights, both bf16,
 //   K-major ("[out, in]" row-major weights, as ggml_mul_mat reads them), fp32 accumulation.
 //
-// One CTA computes a 128 x BN tile over a range of K blocks (split-K over gridDim.z):
+// Persistent kernel, one CTA per SM over a list of 128 x BN output tiles (BN = 256 where
+// N allows, else 128), each optionally one K range of a split-K:
 //   warp 0, one lane: TMA producer - 2-D tiled bulk tensor copies of 128x64 (A) and
 //                     BNx64 (B) bf16 tiles with 128-byte swizzle into a STAGES-deep ring;
-//   warp 1:           allocates the TMEM accumulator (128 lanes x BN fp32 columns); one
-//                     lane issues tcgen05.mma (kind::f16, M=128, N=BN, K=16) from shared
-//                     memory descriptors and commits each stage back to the producer;
-//   warps 2..5:       epilogue - tcgen05.ld of their 32-lane quadrant, then plain stores
-//                     or vector reductions (red.add) into the fp32 output.
+//   warp 1:           allocates two TMEM accumulators (128 lanes x BN fp32 columns each);
+//                     one lane issues tcgen05.mma (kind::f16, M=128, N=BN, K=16) from
+//                     shared memory descriptors and commits each stage back to the producer;
+//   warps 2..5:       epilogue - tcgen05.ld of their 32-lane quadrant (one row per lane),
+//                     staged through a per-warp shared block so that each instruction
+//                     stores or reduce-adds (red.add) whole 128-byte row segments of the fp32
+//                     output, or (gate/up projection) silu(gate) * up of interleaved column
+//                     pairs, stored as bf16.
 // Every mbarrier wait is bounded; a wait that gives up sets the device status word.
 #include <cuda.h>
 
@@ -89,125 +93,52 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
                  : "memory");
 }
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const GemmParams p) {
-    constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
-    constexpr uint32_t IDESC = instr_desc(BM, BN);
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte alignment for the swizzled tiles
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *sA = smem;
-    unsigned char *sB = smem + STAGES * A_BYTES;
-    __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
-    __shared__ uint32_t tmem_base_s;
-    __shared__ int fail_s;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
-    const int nk_total = p.K / BK;
-    const int per = (nk_total + gridDim.z - 1) / gridDim.z;
-    const int kb0 = blockIdx.z * per;
-    const int nk = max(0, min(per, nk_total - kb0));
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_init(&done, 1);
-        fail_s = 0;
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_s)),
-                     "r"((uint32_t)BN)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        tc_fence_before();
-    }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_base_s;
-
-    if (nk > 0) {
-        if (warp == 0 && lane == 0) {
-            // ---- TMA producer
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % STAGES;
-                if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, p.status)) {
-                    fail_s = 1;
-                    break;
-                }
-                mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
-                tma_load_2d(sA + s * A_BYTES, &map_a, (kb0 + i) * BK, m0, &full[s]);
-                tma_load_2d(sB + s * B_BYTES, &map_b, (kb0 + i) * BK, n0, &full[s]);
-            }
-            // let the last copies land before the CTA can exit (no-op when they were consumed)
-            for (int i = max(0, nk - STAGES); i < nk; ++i) mbar_wait(&full[i % STAGES], (i / STAGES) & 1, p.status);
-        } else if (warp == 1 && lane == 0) {
-            // ---- MMA issuer
-            bool ok = true;
-            for (int i = 0; i < nk && ok; ++i) {
-                const int s = i % STAGES;
-                if (!mbar_wait(&full[s], (i / STAGES) & 1, p.status)) {
-                    ok = false;
-                    fail_s = 1;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(sA + s * A_BYTES), b0 = smem_u32(sB + s * B_BYTES);
-#pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    umma_bf16(tmem, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), IDESC, (i > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&empty[s]);
-            }
-            umma_commit(&done);   // arrives once every MMA issued so far has completed
-        } else if (warp >= 2) {
-            // ---- epilogue: TMEM quadrant (warp % 4) holds tile rows 32*(warp%4) .. +31
-            const bool ok = mbar_wait(&done, 0, p.status);
-            tc_fence_after();
-            const int q = warp & 3;
-            const int row = m0 + q * 32 + lane;
-            if (ok && !fail_s) {
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), v);
-                    if (row < p.M) {
-                        float *o = p.out + (size_t)row * p.ld_out + n0 + c * 32;
-                        if (p.accumulate) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4) red_add_v4(o + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4)
-                                *reinterpret_cast<float4 *>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                        }
-                    }
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)BN) : "memory");
-    }
+// Multicast form of the tile load: the box lands at the same shared-memory offset in
+// every CTA of the cluster named in `mask`, and completes bytes on the mbarrier at the
+// same offset in each of them.
+__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+// Commit that arrives on the mbarrier at this offset in every CTA of `mask`.
+__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
-// Persistent variant: one CTA per SM walks the tile list (tile t = blockIdx.x, +gridDim.x,
-// ...; each tile is (row block, column block, K split)). The accumulator is double
-// buffered in TMEM (2 x BN columns): while warps 2..5 drain tile j from buffer j & 1,
-// the MMA thread already accumulates tile j + 1 into the other buffer, and the producer
-// keeps the shared-memory ring full across tile boundaries.
-template <int BN, int STAGES>
+// One CTA per SM walks the tile list; each tile is (row block, column block, K split).
+// With CM > 1 the CTAs form clusters of CM along M: a cluster takes CM consecutive row
+// blocks of one column block, each CTA loads its own 128 x 64 A box and one BN/CM-row
+// slice of the shared B box, multicast to all CM CTAs, so every SM reads 1/CM of the
+// weight tile from L2. A ring slot is free again only when all CM CTAs have consumed it
+// (each MMA commit arrives on the slot's empty barrier in every CTA of the cluster).
+// The accumulator is double buffered in TMEM (2 x BN columns): while warps 2..5 drain
+// tile j from buffer j & 1, the MMA thread already accumulates tile j + 1 into the other
+// buffer, and the producer keeps the shared-memory ring full across tile boundaries.
+template <int BN, int STAGES, int CM>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_tc_persist(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                       const GemmParams p, int splits) {
     constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
+    constexpr uint32_t B_SLICE = B_BYTES / CM;
     constexpr uint32_t IDESC = instr_desc(BM, BN);
+    constexpr uint16_t MASK = (uint16_t)((1u << CM) - 1u);
+    static_assert((BN / CM) % 8 == 0, "a B slice must hold whole 8-row swizzle groups");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem;
@@ -217,7 +148,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __shared__ int fail_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_n = p.N / BN, tiles_m = (p.M + BM - 1) / BM;
+    const int rank = CM > 1 ? (int)cluster_rank() : 0;
+    const int cid = blockIdx.x / CM, n_clusters = gridDim.x / CM;
+    const int tiles_n = p.N / BN;
+    const int tiles_m = ((p.M + BM - 1) / BM + CM - 1) / CM;   // in cluster row blocks of CM x 128 rows
     const int n_tiles = tiles_m * tiles_n * splits;
     const int nk_total = p.K / BK;
     const int per = (nk_total + splits - 1) / splits;
@@ -225,7 +159,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], CM);   // one commit from each CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -242,13 +176,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
     }
     __syncthreads();
+    if (CM > 1) cluster_sync();   // peers' barriers are initialised before any multicast lands
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    // tile t -> (row block, column block, split); column blocks vary fastest
+    // tile t -> (row block of this CTA, column block, split); column blocks vary fastest
     auto tile_of = [&](int t, int &m0, int &n0, int &kb0, int &nk) {
         const int sp = t / (tiles_m * tiles_n), rem = t - sp * tiles_m * tiles_n;
-        m0 = (rem / tiles_n) * BM;
+        m0 = ((rem / tiles_n) * CM + rank) * BM;
         n0 = (rem % tiles_n) * BN;
         kb0 = sp * per;
         nk = max(0, min(per, nk_total - kb0));
@@ -258,7 +193,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- TMA producer: one ring across all tiles of this CTA
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        for (int t = cid; t < n_tiles && ok; t += n_clusters) {
             int m0, n0, kb0, nk;
             tile_of(t, m0, n0, kb0, nk);
             for (int i = 0; i < nk; ++i, ++it) {
@@ -270,18 +205,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
                 tma_load_2d(sA + s * A_BYTES, &map_a, (kb0 + i) * BK, m0, &full[s]);
-                tma_load_2d(sB + s * B_BYTES, &map_b, (kb0 + i) * BK, n0, &full[s]);
+                if (CM > 1)
+                    tma_load_2d_mc(sB + s * B_BYTES + rank * B_SLICE, &map_b, (kb0 + i) * BK, n0 + rank * (BN / CM),
+                                   &full[s], MASK);
+                else
+                    tma_load_2d(sB + s * B_BYTES, &map_b, (kb0 + i) * BK, n0, &full[s]);
             }
         }
-        // let the last copies land before the CTA can exit (no-op when they were consumed)
+        // Tail: every slot's last use is consumed by all CTAs of the cluster, so no copy or
+        // commit from a peer can still target this CTA's shared memory when it exits.
         for (uint32_t j = (it > (uint32_t)STAGES ? it - STAGES : 0); j < it; ++j)
-            mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.status);
+            mbar_wait(&empty[j % STAGES], (j / STAGES) & 1, p.status);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         uint32_t it = 0;
         int j = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++j) {
+        for (int t = cid; t < n_tiles && ok; t += n_clusters, ++j) {
             int m0, n0, kb0, nk;
             tile_of(t, m0, n0, kb0, nk);
             const int b = j & 1;
@@ -303,38 +243,80 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
                     umma_bf16(acc, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), IDESC, (i > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&empty[s]);
+                if (CM > 1)
+                    umma_commit_mc(&empty[s], MASK);
+                else
+                    umma_commit(&empty[s]);
             }
             umma_commit(&tfull[b]);   // arrives once this tile's MMAs have completed
         }
     } else if (warp >= 2) {
         // ---- epilogue: TMEM lane quadrant (warp % 4) holds tile rows 32*(warp%4) .. +31
         const int q = warp & 3;
+        float *stg = reinterpret_cast<float *>(sB + STAGES * B_BYTES) + q * 32 * 32;   // this warp's staging block
         int j = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+        for (int t = cid; t < n_tiles; t += n_clusters, ++j) {
             int m0, n0, kb0, nk;
             tile_of(t, m0, n0, kb0, nk);
             const int b = j & 1;
             const bool ok = mbar_wait(&tfull[b], (j >> 1) & 1, p.status);
             tc_fence_after();
             if (!ok || fail_s) break;
-            const int row = m0 + q * 32 + lane;
             if (nk > 0) {
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), v);
-                    if (row < p.M) {
-                        float *o = p.out + (size_t)row * p.ld_out + n0 + c * 32;
-                        if (p.accumulate) {
+                    if (p.swiglu_out != nullptr) {
+                        // columns (2j, 2j + 1) = (gate_j, up_j): 16 bf16 outputs = 32 bytes of this lane's
+                        // row, staged as [32 rows][2 x 16 B] with the halves swapped on every other group of
+                        // 4 rows (conflict-free), then written 16 rows x 32 bytes per instruction
+                        uint32_t h[8];
 #pragma unroll
-                            for (int i = 0; i < 32; i += 4) red_add_v4(o + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
-                        } else {
+                        for (int i = 0; i < 8; ++i) {
+                            const float g0 = v[4 * i], u0 = v[4 * i + 1], g1 = v[4 * i + 2], u1 = v[4 * i + 3];
+                            const __nv_bfloat16 lo = __float2bfloat16_rn(g0 / (1.0f + expf(-g0)) * u0);
+                            const __nv_bfloat16 hi = __float2bfloat16_rn(g1 / (1.0f + expf(-g1)) * u1);
+                            h[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+                        }
+                        uint4 *w = reinterpret_cast<uint4 *>(stg);
+                        const int sw = (lane >> 2) & 1;
+                        w[lane * 2 + sw] = make_uint4(h[0], h[1], h[2], h[3]);
+                        w[lane * 2 + (sw ^ 1)] = make_uint4(h[4], h[5], h[6], h[7]);
+                        __syncwarp();
 #pragma unroll
-                            for (int i = 0; i < 32; i += 4)
-                                *reinterpret_cast<float4 *>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        for (int it = 0; it < 2; ++it) {
+                            const int r = it * 16 + (lane >> 1), half = lane & 1;
+                            const uint4 x = w[r * 2 + (half ^ ((r >> 2) & 1))];
+                            const int grow = m0 + q * 32 + r;
+                            if (grow < p.M)
+                                *reinterpret_cast<uint4 *>(p.swiglu_out + (size_t)grow * p.ld_swiglu + (n0 + c * 32) / 2 +
+                                                           half * 8) = x;
+                        }
+                    } else {
+                        // this lane's 32 values of its row go to the warp's 32 x 32 block (16-byte chunks
+                        // XOR-swizzled by row, conflict-free), then each instruction stores or reduce-adds
+                        // 4 rows x 128 contiguous bytes
+                        float4 *w = reinterpret_cast<float4 *>(stg);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[lane * 8 + (i ^ (lane & 7))] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int r = it * 4 + (lane >> 3), ch = lane & 7;
+                            const float4 x = w[r * 8 + (ch ^ (r & 7))];
+                            const int grow = m0 + q * 32 + r;
+                            if (grow < p.M) {
+                                float *o = p.out + (size_t)grow * p.ld_out + n0 + c * 32 + ch * 4;
+                                if (p.accumulate)
+                                    red_add_v4(o, x.x, x.y, x.z, x.w);
+                                else
+                                    *reinterpret_cast<float4 *>(o) = x;
+                            }
                         }
                     }
+                    __syncwarp();   // the block is rewritten by the next chunk
                 }
             }
             tc_fence_before();
@@ -344,12 +326,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (CM > 1) cluster_sync();   // no CTA leaves while a peer may still address its shared memory
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)(2 * BN))
                      : "memory");
     }
 }
+
 
 }  // namespace tc
 }  // namespace talker_k
@@ -388,27 +372,33 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kBN = 128, kStages = 6;
-constexpr size_t kGemmSmem = (size_t)kStages * (tc::BM + kBN) * tc::BK * 2 + 1024;
+// Two tile widths: 128 x 256 tiles (M=128, N=256 MMAs, 4-stage ring) wherever N allows,
+// which halves the operand bytes per FLOP of the 128 x 128 tiles (6-stage ring) that
+// remain for other widths. TMEM holds two accumulators of BN columns either way.
+constexpr int kBNNarrow = 128, kStagesNarrow = 6;
+constexpr int kBNWide = 256, kStagesWide = 4;
+// ring + the epilogue's staging blocks (4 warps x 32 x 32 f32) + alignment slack
+constexpr size_t smem_for(int bn, int stages) {
+    return (size_t)stages * (tc::BM + bn) * tc::BK * 2 + 4 * 32 * 32 * 4 + 1024;
+}
+
+int tile_n_for(int N) { return N % kBNWide == 0 ? kBNWide : kBNNarrow; }
+
+// CTAs per cluster along M (B tile multicast); used once there are enough row blocks that
+// the padding to a multiple of the cluster wastes little.
+constexpr int kClusterM = 2;
+int cluster_m_for(int M) { return (M + tc::BM - 1) / tc::BM >= 8 ? kClusterM : 1; }
 
 }  // namespace
 
-bool gemm_tc_supported(int N, int K) { return N % kBN == 0 && K % tc::BK == 0 && K >= tc::BK; }
+bool gemm_tc_supported(int N, int K) { return N % kBNNarrow == 0 && K % tc::BK == 0 && K >= tc::BK; }
 
 int gemm_tc_splits(int M, int N, int K, int n_sm) {
-    const int tiles = ((M + tc::BM - 1) / tc::BM) * (N / kBN);
+    const int tiles = ((M + tc::BM - 1) / tc::BM) * (N / tile_n_for(N));
     const int nk = K / tc::BK;
     int s = (n_sm + tiles - 1) / tiles;
     s = std::min(s, std::max(1, nk / 4));   // keep at least 4 K blocks per split
     return std::max(1, s);
-}
-
-cudaError_t prepare_gemm_tc() {
-    cudaError_t e = cudaFuncSetAttribute(tc::k_gemm_tc<kBN, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kGemmSmem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tc::k_gemm_tc_persist<kBN, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kGemmSmem);
 }
 
 namespace {
@@ -422,11 +412,72 @@ int sm_count_current() {
 }
 }  // namespace
 
+template <int BN, int STAGES, int CM>
+static cudaError_t raise_smem() {
+    return cudaFuncSetAttribute(tc::k_gemm_tc_persist<BN, STAGES, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_for(BN, STAGES));
+}
+
+cudaError_t prepare_gemm_tc() {
+    cudaError_t e = raise_smem<kBNNarrow, kStagesNarrow, 1>();
+    e = e ? e : raise_smem<kBNNarrow, kStagesNarrow, kClusterM>();
+    e = e ? e : raise_smem<kBNWide, kStagesWide, 1>();
+    return e ? e : raise_smem<kBNWide, kStagesWide, kClusterM>();
+}
+
+namespace {
+// Persistent launch: as many CTAs (clusters of CM) as fit on the GPU at once, at most one
+// per cluster tile.
+template <int BN, int STAGES, int CM>
+cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &p, int splits, int n_sm,
+                       cudaStream_t st) {
+    const int tiles = (((p.M + tc::BM - 1) / tc::BM + CM - 1) / CM) * (p.N / BN) * splits;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(tc::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem_for(BN, STAGES);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CM > 1 ? 1 : 0;
+    static int max_clusters = 0;   // per instantiation; one device per process
+    if (max_clusters == 0) {
+        int n = 0;
+        cfg.gridDim = dim3(CM * (n_sm / CM), 1, 1);
+        if (CM > 1 && cudaOccupancyMaxActiveClusters(&n, tc::k_gemm_tc_persist<BN, STAGES, CM>, &cfg) == cudaSuccess &&
+            n > 0)
+            max_clusters = std::min(n, n_sm / CM);
+        else
+            max_clusters = n_sm / CM;
+        (void)cudaGetLastError();
+    }
+    cfg.gridDim = dim3(CM * std::min(tiles, max_clusters), 1, 1);
+    return cudaLaunchKernelEx(&cfg, tc::k_gemm_tc_persist<BN, STAGES, CM>, ma, mb, p, splits);
+}
+
+cudaError_t launch_persist(const void *A, const void *B, GemmParams &p, int splits, cudaStream_t st) {
+    const int M = p.M, N = p.N, K = p.K;
+    if (!gemm_tc_supported(N, K) || M < 1) return cudaErrorInvalidValue;
+    const int bn = tile_n_for(N), cm = cluster_m_for(M);
+    CUtensorMap ma, mb;   // with a cluster, each CTA copies (and multicasts) a BN/CM-row slice of B
+    if (!make_map(&ma, A, M, K, tc::BM) || !make_map(&mb, B, N, K, bn / cm)) return cudaErrorInvalidValue;
+    const int s = std::max(1, splits);
+    const int n_sm = sm_count_current();
+    if (n_sm <= 0) return cudaErrorInvalidDevice;
+    if (cm > 1) {
+        if (bn == kBNWide) return launch_cfg<kBNWide, kStagesWide, kClusterM>(ma, mb, p, s, n_sm, st);
+        return launch_cfg<kBNNarrow, kStagesNarrow, kClusterM>(ma, mb, p, s, n_sm, st);
+    }
+    if (bn == kBNWide) return launch_cfg<kBNWide, kStagesWide, 1>(ma, mb, p, s, n_sm, st);
+    return launch_cfg<kBNNarrow, kStagesNarrow, 1>(ma, mb, p, s, n_sm, st);
+}
+}  // namespace
+
 cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, float *out, int ld_out, int accumulate,
                            int splits, int *status, cudaStream_t st) {
-    if (!gemm_tc_supported(N, K) || M < 1) return cudaErrorInvalidValue;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, A, M, K, tc::BM) || !make_map(&mb, B, N, K, kBN)) return cudaErrorInvalidValue;
     GemmParams p{};
     p.M = M;
     p.N = N;
@@ -435,13 +486,21 @@ cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, fl
     p.ld_out = ld_out;
     p.accumulate = (accumulate || splits > 1) ? 1 : 0;
     p.status = status;
-    const int s = std::max(1, splits);
-    const int n_tiles = (N / kBN) * ((M + tc::BM - 1) / tc::BM) * s;
-    const int n_sm = sm_count_current();
-    if (n_sm <= 0) return cudaErrorInvalidDevice;
-    // persistent: one CTA per SM over the tile list, TMEM accumulators double buffered
-    tc::k_gemm_tc_persist<kBN, kStages><<<std::min(n_tiles, n_sm), tc::NTHREADS, kGemmSmem, st>>>(ma, mb, p, s);
-    return cudaGetLastError();
+    return launch_persist(A, B, p, splits, st);
+}
+
+cudaError_t launch_gemm_tc_swiglu(const void *A, int M, int K, const void *B, int N, __nv_bfloat16 *out_bf16, int ld,
+                                  int *status, cudaStream_t st) {
+    if (out_bf16 == nullptr || N % 32 != 0 || ld % 8 != 0 || (reinterpret_cast<uintptr_t>(out_bf16) & 15u) != 0)
+        return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.status = status;
+    p.swiglu_out = out_bf16;
+    p.ld_swiglu = ld;
+    return launch_persist(A, B, p, 1, st);
 }
 
 }  // namespace talker_k

@@ -170,6 +170,11 @@ struct GemmParams {
     int ld_out;
     int accumulate;   // 1: reduce-add into out (residual stream or split-K), 0: store
     int *status;
+    // SwiGLU epilogue (no split-K): with B the row-interleaved [gate; up] weights, output
+    // columns 2j and 2j+1 are gate_j and up_j; instead of out, write
+    // swiglu_out[row, j] = bf16(silu(gate_j) * up_j) with row stride ld_swiglu.
+    __nv_bfloat16 *swiglu_out;
+    int ld_swiglu;
 };
 
 constexpr int kGemvWarps = 8;
@@ -210,6 +215,9 @@ cudaError_t prepare_gemm_tc();
 // result is reduce-added, so out must hold zeros (or the residual stream).
 cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, float *out, int ld_out, int accumulate,
                            int splits, int *status, cudaStream_t st);
+// The same GEMM with the SwiGLU epilogue: out_bf16 [M, N/2] (row stride ld), one K pass.
+cudaError_t launch_gemm_tc_swiglu(const void *A, int M, int K, const void *B, int N, __nv_bfloat16 *out_bf16, int ld,
+                                  int *status, cudaStream_t st);
 
 // Element-wise stages of the tensor-core prefill path (prefill.cu).
 cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H, void *out,

@@ -713,9 +713,15 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         TRY(tc_gemm(t, st, t->ab, T, t->qd, d.o, t->H, t->x, t->H, true, &nk));
         TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.post_norm, t->c.rms_eps, T, t->H, t->hb, st));
         ++nk;
-        TRY(tc_gemm(t, st, t->hb, T, t->H, d.gu, 2 * t->I, t->gu, 2 * t->I, false, &nk));
-        TRY_CUDA(launch_swiglu_bf16(t->gu, T, t->I, t->gb, st));
-        ++nk;
+        if (gemm_tc_splits(T, 2 * t->I, t->H, t->n_sm) == 1) {   // one K pass: SwiGLU in the GEMM epilogue
+            TRY_CUDA(launch_gemm_tc_swiglu(t->hb, T, t->H, d.gu, 2 * t->I, static_cast<__nv_bfloat16 *>(t->gb), t->I,
+                                                 t->d_status, st));
+            ++nk;
+        } else {
+            TRY(tc_gemm(t, st, t->hb, T, t->H, d.gu, 2 * t->I, t->gu, 2 * t->I, false, &nk));
+            TRY_CUDA(launch_swiglu_bf16(t->gu, T, t->I, t->gb, st));
+            ++nk;
+        }
         TRY(tc_gemm(t, st, t->gb, T, t->I, d.down, t->H, t->x, t->H, true, &nk));
     }
     const int rps = out.rows_per_stream;
@@ -1075,6 +1081,23 @@ talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, 
     TRY_CUDA(prepare_gemm_tc());
     TRY_CUDA(launch_gemm_tc(A, M, K, B, N, out, N, accumulate, splits, d_status,
                             static_cast<cudaStream_t>(cuda_stream)));
+    TRY_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)));
+    int h = 0;
+    TRY_CUDA(cudaMemcpy(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost));
+    return h ? TALKER_EDEVICE : TALKER_OK;
+}
+
+talker_status talker_test_gemm_swiglu_bf16(const void *A, int M, int K, const void *B, int N, void *out_bf16,
+                                           void *cuda_stream) {
+    if (!A || !B || !out_bf16 || M < 1 || N % 2 || !gemm_tc_supported(N, K)) return TALKER_EINVAL;
+    static int *d_status = nullptr;
+    if (!d_status) {
+        TRY_CUDA(cudaMalloc(&d_status, sizeof(int)));
+        TRY_CUDA(cudaMemset(d_status, 0, sizeof(int)));
+    }
+    TRY_CUDA(prepare_gemm_tc());
+    TRY_CUDA(launch_gemm_tc_swiglu(A, M, K, B, N, static_cast<__nv_bfloat16 *>(out_bf16), N / 2, d_status,
+                                   static_cast<cudaStream_t>(cuda_stream)));
     TRY_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)));
     int h = 0;
     TRY_CUDA(cudaMemcpy(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost));

@@ -91,6 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                             vp]),
         "talker_test_gemm_bf16": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
                                        ctypes.c_int, vp]),
+        "talker_test_gemm_swiglu_bf16": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp]),
         "talker_trace_slots": (ctypes.c_int, []),
     }
     for name, (res, args) in proto.items():
@@ -280,6 +281,20 @@ class Talker:
 
     def kernel_launches(self) -> int:
         return int(self.lib.talker_kernel_launches(self.h))
+
+
+def test_gemm_swiglu_bf16(A, B, out):
+    """Test support: out[M, N/2] = bf16(silu(A @ B[0::2].T) * (A @ B[1::2].T)) on the tensor-core
+    GEMM's SwiGLU epilogue (A [M,K], B [N,K] bf16 with gate/up rows interleaved; out bf16)."""
+    import torch
+    lib = load_library()
+    M, K = A.shape
+    N = B.shape[0]
+    st = lib.talker_test_gemm_swiglu_bf16(_ptr(A), M, K, _ptr(B), N, _ptr(out),
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if st != 0:
+        raise TalkerError(st, "talker_test_gemm_swiglu_bf16")
+    return out
 
 
 def test_gemm_bf16(A, B, out, accumulate=False, splits=1):

@@ -1,4 +1,8 @@
-"""GPU: the tensor-core (tcgen05/TMEM) GEMM against a float64 matmul of the same bf16 inputs."""
+"""GPU: the tensor-core (tcgen05/TMEM) GEMM against a float64 matmul of the same bf16 inputs.
+
+Shapes cover both tile widths (N % 256 == 0 or not), split-K, ragged M, and M of eight or
+more row blocks, where CTA pairs share the weight tile through cluster multicast (an odd
+row-block count leaves the second CTA of the last pair wholly past M)."""
 import numpy as np
 import pytest
 
@@ -16,7 +20,8 @@ def cuda():
 
 
 @pytest.mark.parametrize("M,N,K,splits", [(1, 128, 64, 1), (96, 4096, 1024, 1), (96, 1024, 3072, 12),
-                                          (130, 256, 128, 1), (300, 384, 2048, 4), (4096, 1024, 1024, 1)])
+                                          (130, 256, 128, 1), (300, 384, 2048, 4), (4096, 1024, 1024, 1),
+                                          (1100, 384, 256, 1), (1030, 768, 1024, 2), (2048, 6144, 1024, 1)])
 def test_gemm_matches_fp64(cuda, M, N, K, splits):
     from kv_cached_qwen3_gb300.talker import test_gemm_bf16
     g = torch.Generator(device="cpu").manual_seed(M * 7 + N + K)
@@ -39,3 +44,22 @@ def test_gemm_accumulates_into_output(cuda):
     test_gemm_bf16(A, B, out, accumulate=True)
     ref = base.double().cpu() + A.double().cpu() @ B.double().cpu().T
     assert float((out.cpu().double() - ref).norm() / ref.norm()) < 1e-5
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (130, 256, 128), (300, 6144, 1024), (1024, 384, 192),
+                                   (1100, 6144, 1024)])
+def test_gemm_swiglu_epilogue(cuda, M, N, K):
+    """silu(gate) * up from interleaved gate/up rows, rounded to bf16 (both tile widths, ragged M)."""
+    from kv_cached_qwen3_gb300.talker import test_gemm_swiglu_bf16
+    g = torch.Generator(device="cpu").manual_seed(M + 3 * N + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = (0.05 * torch.randn(N, K, generator=g)).to(torch.bfloat16)
+    gu = A.double() @ B.double().T
+    gate, up = gu[:, 0::2], gu[:, 1::2]
+    ref = gate / (1.0 + torch.exp(-gate)) * up
+    out = torch.zeros(M, N // 2, dtype=torch.bfloat16, device="cuda")
+    test_gemm_swiglu_bf16(A.cuda(), B.cuda(), out)
+    got = out.cpu().double()
+    err = (got - ref).norm() / ref.norm()
+    assert float(err) < 4e-3, float(err)          # bf16 output rounding (2^-9 relative per element)
+    assert float((got - ref).abs().max()) <= float(ref.abs().max()) * 2 ** -7
