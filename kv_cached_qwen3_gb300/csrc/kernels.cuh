@@ -208,6 +208,13 @@ cudaError_t launch_embed_codes(const EmbedTables &t, const int32_t *ids, const f
                                float *out, int *status, cudaStream_t st);
 cudaError_t prepare_kernels();  // raise dynamic shared-memory limits once per process
 
+// tcgen05 causal prefill attention (head_dim 128, one stream from position 0): dense K and
+// V^T copies (kd, vt: n_kv * attn_prefill_tc_lpad(T) * 128 bf16 each), then the tiles.
+bool attn_prefill_tc_supported(const AttnParams &a, int T);
+int attn_prefill_tc_lpad(int nkeys);
+cudaError_t prepare_attn_prefill_tc();
+cudaError_t launch_attn_prefill_tc(const AttnParams &a, int T, __nv_bfloat16 *kd, __nv_bfloat16 *vt, cudaStream_t st);
+
 bool gemm_tc_supported(int N, int K);
 int gemm_tc_splits(int M, int N, int K, int n_sm);
 cudaError_t prepare_gemm_tc();

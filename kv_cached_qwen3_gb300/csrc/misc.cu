@@ -111,6 +111,8 @@ cudaError_t launch_embed_codes(const EmbedTables &t, const int32_t *ids, const f
 cudaError_t prepare_kernels() {
     cudaError_t e = prepare_gemv();
     if (e != cudaSuccess) return e;
+    e = prepare_attn_prefill_tc();
+    if (e != cudaSuccess) return e;
     e = prepare_attn_prefill();
     if (e != cudaSuccess) return e;
     return prepare_attn();

@@ -102,13 +102,16 @@ struct talker {
     size_t ll_words = 0;
     uint32_t epoch = 0;                  // step counter for the persistent kernel's flags
     int max_splits = 0;                  // cap on the persistent kernel's attention splits (0 = none)
-    int prefill_mode = 0;                // 0 automatic, 2 always the GEMV kernels
+    int prefill_mode = 0;                // 0 automatic, 2 always the GEMV kernels, 3 tensor-core GEMMs with
+                                         // the mma.sync attention
     int persist_ok[2] = {-1, -1};        // per R template (1, 4): -1 unknown, 0 unusable, 1 usable
     unsigned long long *trace = nullptr; // optional phase stamps of the persistent kernel (caller-owned)
     // tensor-core prefill buffers (bf16 GEMM operands and the f32 gate/up projection)
     int cap_tc_rows = 0;
     void *hb = nullptr, *ab = nullptr, *gb = nullptr;
     __nv_bfloat16 *kv_dense = nullptr;   // Q8_0 storage: the prefill's own k / v rows, [2][rows][n_kv][hd]
+    __nv_bfloat16 *kd_tc = nullptr;      // tcgen05 prefill attention: K [n_kv][L][hd] and V^T [n_kv][hd][L]
+    __nv_bfloat16 *vt_tc = nullptr;
     float *gu = nullptr;
     int tc_ok = -1;                      // tensor-core prefill usable for this geometry (-1 unknown)
     // TTS loop input / output
@@ -156,7 +159,8 @@ void free_workspaces(talker *t) {
 }
 
 void free_tc(talker *t) {
-    void **bl[] = {&t->hb, &t->ab, &t->gb, reinterpret_cast<void **>(&t->gu), reinterpret_cast<void **>(&t->kv_dense)};
+    void **bl[] = {&t->hb, &t->ab, &t->gb, reinterpret_cast<void **>(&t->gu), reinterpret_cast<void **>(&t->kv_dense),
+                   reinterpret_cast<void **>(&t->kd_tc), reinterpret_cast<void **>(&t->vt_tc)};
     for (auto pp : bl) {
         free_ptr(*pp);
         *pp = nullptr;
@@ -651,6 +655,11 @@ talker_status ensure_tc(talker *t, int rows) {
     TRY_CUDA(cudaMalloc(&t->gb, (size_t)cap * t->I * 2));
     TRY_CUDA(cudaMalloc(&t->gu, (size_t)cap * 2 * t->I * sizeof(float)));
     if (t->kv_q8) TRY_CUDA(cudaMalloc(&t->kv_dense, (size_t)2 * cap * t->nkv * t->hd * 2));
+    if (t->hd == 128) {
+        const size_t lp = (size_t)attn_prefill_tc_lpad(cap);
+        TRY_CUDA(cudaMalloc(&t->kd_tc, lp * t->nkv * t->hd * 2));
+        TRY_CUDA(cudaMalloc(&t->vt_tc, lp * t->nkv * t->hd * 2));
+    }
     t->cap_tc_rows = cap;
     return TALKER_OK;
 }
@@ -705,11 +714,16 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
             a.dense_k = t->kv_dense;
             a.dense_v = t->kv_dense + (size_t)T * t->nkv * t->hd;
         }
-        if (rm.mode == 1 && attn_prefill_supported(t->kv_kind, t->hd))
-            TRY_CUDA(launch_attn_prefill(t->hd, a, T, st));   // causal tiles on the tensor cores
-        else
+        if (rm.mode == 1 && t->prefill_mode != 3 && t->kd_tc != nullptr && attn_prefill_tc_supported(a, T)) {
+            TRY_CUDA(launch_attn_prefill_tc(a, T, t->kd_tc, t->vt_tc, st));   // dense K, V^T + tcgen05 tiles
+            nk += 2;
+        } else if (rm.mode == 1 && attn_prefill_supported(t->kv_kind, t->hd)) {
+            TRY_CUDA(launch_attn_prefill(t->hd, a, T, st));   // causal tiles on mma.sync
+            ++nk;
+        } else {
             TRY_CUDA(launch_attn(t->kv_kind, t->hd, a, T, st, false));
-        ++nk;
+            ++nk;
+        }
         TRY(tc_gemm(t, st, t->ab, T, t->qd, d.o, t->H, t->x, t->H, true, &nk));
         TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.post_norm, t->c.rms_eps, T, t->H, t->hb, st));
         ++nk;
@@ -1241,7 +1255,7 @@ talker_status talker_decode_codes(talker_t *t, const int32_t *ids, const float *
 }
 
 talker_status talker_set_prefill_mode(talker_t *t, int mode) {
-    if (!t || (mode != 0 && mode != 2)) return TALKER_EINVAL;
+    if (!t || (mode != 0 && mode != 2 && mode != 3)) return TALKER_EINVAL;
     t->prefill_mode = mode;
     return TALKER_OK;
 }
