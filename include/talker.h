@@ -239,10 +239,11 @@ talker_status talker_set_decode_mode(talker_t *t, int mode);
 
 /* Choose how prefill runs: 0 = automatic (tensor-core GEMMs when the weights
  * are bf16, T >= 16 and every projection shape is a multiple of the GEMM tile;
- * otherwise the GEMV kernels; the causal attention of a head_dim-128 prefill from
- * position 0 of one stream on tcgen05, else on mma.sync), 2 = always the GEMV
- * kernels, 3 = as 0 but the attention always on mma.sync (comparison and test
- * support). Errors: EINVAL. */
+ * otherwise the GEMV kernels; the causal attention of a head_dim-128 prefill of
+ * T >= 256 rows from position 0 of one stream on tcgen05, else on mma.sync),
+ * 2 = always the GEMV kernels, 3 / 4 = as 0 but the attention on mma.sync /
+ * on tcgen05 (where supported) at any T (comparison and test support).
+ * Errors: EINVAL. */
 talker_status talker_set_prefill_mode(talker_t *t, int mode);
 
 /* Test support: the tensor-core GEMM of the prefill path on its own,

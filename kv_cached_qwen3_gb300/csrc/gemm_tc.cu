@@ -293,9 +293,9 @@ bool make_map(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows) {
     return make_map_bf16_2d(m, ptr, (uint64_t)rows, (uint64_t)K, (uint64_t)K * 2, tc::BK, box_rows);
 }
 
-// Two tile widths: 128 x 256 tiles (M=128, N=256 MMAs, 4-stage ring) wherever N allows,
-// which halves the operand bytes per FLOP of the 128 x 128 tiles (6-stage ring) that
-// remain for other widths. TMEM holds two accumulators of BN columns either way.
+// Two tile widths: 128 x 256 tiles (M=128, N=256 MMAs, 4-stage ring) for tall products
+// where N allows, which halves the operand bytes per FLOP, and 128 x 128 tiles (6-stage
+// ring) otherwise. TMEM holds two accumulators of BN columns either way.
 constexpr int kBNNarrow = 128, kStagesNarrow = 6;
 constexpr int kBNWide = 256, kStagesWide = 4;
 // ring + the epilogue's staging blocks (4 warps x 32 x 32 f32) + alignment slack
@@ -303,19 +303,23 @@ constexpr size_t smem_for(int bn, int stages) {
     return (size_t)stages * (tc::BM + bn) * tc::BK * 2 + 4 * 32 * 32 * 4 + 1024;
 }
 
-int tile_n_for(int N) { return N % kBNWide == 0 ? kBNWide : kBNNarrow; }
+// Wide tiles and CTA pairs only for tall activations (8 or more row blocks). A short M
+// (small prefills, decode batches) streams the weights once, and there the narrow tiles
+// give twice as many CTAs pulling them from HBM.
+constexpr int kWideMinRowBlocks = 8;
+bool tall(int M) { return (M + tc::BM - 1) / tc::BM >= kWideMinRowBlocks; }
+int tile_n_for(int M, int N) { return (tall(M) && N % kBNWide == 0) ? kBNWide : kBNNarrow; }
 
-// CTAs per cluster along M (B tile multicast); used once there are enough row blocks that
-// the padding to a multiple of the cluster wastes little.
+// CTAs per cluster along M (B tile multicast).
 constexpr int kClusterM = 2;
-int cluster_m_for(int M) { return (M + tc::BM - 1) / tc::BM >= 8 ? kClusterM : 1; }
+int cluster_m_for(int M) { return tall(M) ? kClusterM : 1; }
 
 }  // namespace
 
 bool gemm_tc_supported(int N, int K) { return N % kBNNarrow == 0 && K % tc::BK == 0 && K >= tc::BK; }
 
 int gemm_tc_splits(int M, int N, int K, int n_sm) {
-    const int tiles = ((M + tc::BM - 1) / tc::BM) * (N / tile_n_for(N));
+    const int tiles = ((M + tc::BM - 1) / tc::BM) * (N / tile_n_for(M, N));
     const int nk = K / tc::BK;
     int s = (n_sm + tiles - 1) / tiles;
     s = std::min(s, std::max(1, nk / 4));   // keep at least 4 K blocks per split
@@ -382,7 +386,7 @@ cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, const GemmP
 cudaError_t launch_persist(const void *A, const void *B, GemmParams &p, int splits, cudaStream_t st) {
     const int M = p.M, N = p.N, K = p.K;
     if (!gemm_tc_supported(N, K) || M < 1) return cudaErrorInvalidValue;
-    const int bn = tile_n_for(N), cm = cluster_m_for(M);
+    const int bn = tile_n_for(M, N), cm = cluster_m_for(M);
     CUtensorMap ma, mb;   // with a cluster, each CTA copies (and multicasts) a BN/CM-row slice of B
     if (!make_map(&ma, A, M, K, tc::BM) || !make_map(&mb, B, N, K, bn / cm)) return cudaErrorInvalidValue;
     const int s = std::max(1, splits);

@@ -102,8 +102,8 @@ struct talker {
     size_t ll_words = 0;
     uint32_t epoch = 0;                  // step counter for the persistent kernel's flags
     int max_splits = 0;                  // cap on the persistent kernel's attention splits (0 = none)
-    int prefill_mode = 0;                // 0 automatic, 2 always the GEMV kernels, 3 tensor-core GEMMs with
-                                         // the mma.sync attention
+    int prefill_mode = 0;                // 0 automatic, 2 always the GEMV kernels, 3 / 4 tensor-core GEMMs
+                                         // with the mma.sync / the tcgen05 attention at any T
     int persist_ok[2] = {-1, -1};        // per R template (1, 4): -1 unknown, 0 unusable, 1 usable
     unsigned long long *trace = nullptr; // optional phase stamps of the persistent kernel (caller-owned)
     // tensor-core prefill buffers (bf16 GEMM operands and the f32 gate/up projection)
@@ -632,6 +632,8 @@ talker_status decode_persistent(talker *t, const float *emb, int B, float *logit
 
 
 constexpr int kTcMinRows = 16;        // prefills shorter than this stay on the GEMV kernels
+constexpr int kAttnTcMinRows = 256;   // tcgen05 prefill attention from two 128-row query tiles up (below,
+                                      // its extra dense-copy launch and TMEM setup outweigh the tiles)
 constexpr int kTcMinDecodeRows = 4;   // decode batches at least this wide use the tensor-core GEMMs
 
 bool tc_usable(talker *t) {
@@ -714,7 +716,8 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
             a.dense_k = t->kv_dense;
             a.dense_v = t->kv_dense + (size_t)T * t->nkv * t->hd;
         }
-        if (rm.mode == 1 && t->prefill_mode != 3 && t->kd_tc != nullptr && attn_prefill_tc_supported(a, T)) {
+        const bool attn_tc = t->prefill_mode == 4 || (t->prefill_mode != 3 && T >= kAttnTcMinRows);
+        if (rm.mode == 1 && attn_tc && t->kd_tc != nullptr && attn_prefill_tc_supported(a, T)) {
             TRY_CUDA(launch_attn_prefill_tc(a, T, t->kd_tc, t->vt_tc, st));   // dense K, V^T + tcgen05 tiles
             nk += 2;
         } else if (rm.mode == 1 && attn_prefill_supported(t->kv_kind, t->hd)) {
@@ -1255,7 +1258,7 @@ talker_status talker_decode_codes(talker_t *t, const int32_t *ids, const float *
 }
 
 talker_status talker_set_prefill_mode(talker_t *t, int mode) {
-    if (!t || (mode != 0 && mode != 2 && mode != 3)) return TALKER_EINVAL;
+    if (!t || (mode != 0 && mode != 2 && mode != 3 && mode != 4)) return TALKER_EINVAL;
     t->prefill_mode = mode;
     return TALKER_OK;
 }

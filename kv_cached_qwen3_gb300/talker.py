@@ -262,7 +262,8 @@ class Talker:
         self._check(self.lib.talker_set_decode_mode(self.h, mode), "talker_set_decode_mode")
 
     def set_prefill_mode(self, mode: int):
-        """0 automatic (tensor cores for bf16 weights and T >= 16), 2 GEMV kernels."""
+        """0 automatic (tensor cores for bf16 weights and T >= 16), 2 GEMV kernels, 3 / 4 tensor
+        cores with the mma.sync / tcgen05 prefill attention at any T."""
         self._check(self.lib.talker_set_prefill_mode(self.h, mode), "talker_set_prefill_mode")
 
     def set_attn_splits(self, n: int):
