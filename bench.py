@@ -53,6 +53,17 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of a list of floats over the ranks of the default process group
+    (one all-reduce; device "cuda" under NCCL, "cpu" under gloo). world == 1: unchanged."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -186,10 +197,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_secs = ev0.elapsed_time(ev1) / 1e3
 
-    secs_t = torch.tensor([secs, e2e_secs], device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(secs_t, op=torch.distributed.ReduceOp.MAX)
-    secs, e2e_secs = [float(x) for x in secs_t.cpu()]
+    secs, e2e_secs = max_over_ranks([secs, e2e_secs], world, "cuda")
 
     wbytes, _ = step_bytes(g, 0)
     kv_total = sum(step_bytes(g, T0 + t + 1)[1] for t in range(K))
