@@ -77,3 +77,32 @@ def test_calls_on_null_handle_are_rejected(lib):
     assert lib.talker_decode(None, None, 1, None, None, None) == 1
     assert lib.talker_sync_status(None, None) == 1
     lib.talker_destroy(None)
+
+
+def test_later_entry_points_reject_null_handles_and_off_grid_shapes(lib):
+    """Every entry point added for chunked / batched prefill, the TTS loop and the test
+    GEMMs validates its arguments on the host first (EINVAL = 1, no device work)."""
+    vp = ctypes.c_void_p
+    assert lib.talker_prefill_append(None, 0, None, 1, None, None, None) == 1
+    assert lib.talker_prefill_batched(None, 1, None, 1, None, None, None) == 1
+    assert lib.talker_prefill_all_rows(None, 0, None, 1, None, None) == 1
+    assert lib.talker_set_logit_suppression(None, 0, 0) == 1
+    assert lib.talker_set_code_tables(None, None, None, 0, 0) == 1
+    assert lib.talker_decode_codes(None, None, None, 1, None, None, None) == 1
+    assert lib.talker_frame(None, None, 2, 1, None, None, None) == 1
+    assert lib.talker_set_attn_splits(None, 0) == 1
+    assert lib.talker_set_trace(None, None) == 1
+    assert lib.talker_kv_import(None, 0, None, None, 0) == 1
+    assert lib.talker_kv_export(None, 0, None, None, 0) == 1
+    for mode in (0, 2, 3, 4, 1, 5, -1):
+        assert lib.talker_set_prefill_mode(None, mode) == 1
+    assert lib.talker_set_decode_mode(None, 0) == 1
+    # test GEMMs: null operands, or shapes off the tile grid (N % 128, K % 64)
+    buf = vp(1 << 20)   # never dereferenced: the shape check fails first
+    assert lib.talker_test_gemm_bf16(None, 1, 64, None, 128, None, 0, 1, None) == 1
+    assert lib.talker_test_gemm_bf16(buf, 1, 64, buf, 96, buf, 0, 1, None) == 1
+    assert lib.talker_test_gemm_bf16(buf, 1, 48, buf, 128, buf, 0, 1, None) == 1
+    assert lib.talker_test_gemm_bf16(buf, 1, 64, buf, 128, buf, 0, 0, None) == 1
+    assert lib.talker_test_gemm_swiglu_bf16(None, 1, 64, None, 128, None, None) == 1
+    assert lib.talker_test_gemm_swiglu_bf16(buf, 1, 64, buf, 192, buf, None) == 1
+    assert lib.talker_head_argmax_noalloc(None, 1, 64, None, 256, 1, None, None, None) == 1
