@@ -29,7 +29,7 @@ from kv_cached_qwen3_gb300 import inputs  # noqa: E402
 
 METRIC = "decode steps/s (B=1, B=16) + prefill tok/s; % of HBM / bf16 TC roofline"
 # DRAM read + write of one decode step (all kernels of the graph) from one ncu capture of the current
-# kernels (profiles/decode_step_graph_talker_b1.md); set to None whenever a decode kernel changes.
+# decode kernels (the launch-list summary under profiles/); None whenever a decode kernel changes.
 STEP_TRAFFIC = {"bytes": 907574016,
                 "note": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the 141 kernels of one decode "
                         "step at cache length 100, where the algorithmic bytes are 898.8 MB"}

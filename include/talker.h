@@ -163,8 +163,8 @@ talker_status talker_prefill_batched(talker_t *t, int B, const float *emb, int T
  * before every head's argmax (prefill, append, decode), the logits of token
  * indices [vocab - vocab_tail, vocab) other than eos_id are set to -inf, in
  * the returned logits too. vocab_tail = 0 turns it off (the default). Steps
- * captured before the call are dropped and captured again. The persistent
- * decode kernel does not run while it is on. Errors: EINVAL (vocab_tail < 0). */
+ * captured before the call are dropped and captured again. Errors: EINVAL
+ * (vocab_tail < 0). */
 talker_status talker_set_logit_suppression(talker_t *t, int vocab_tail, int eos_id);
 
 /* TTS loop input ("talker-forward.h", batched forward "input_embed"): register
@@ -230,11 +230,9 @@ const char *talker_last_error(void);
 
 /* Choose how talker_decode runs a step: 0 = automatic (B >= 4 with bf16
  * weights: the CUDA graph of tensor-core GEMMs; otherwise the CUDA graph of
- * GEMV kernels), 1 = the persistent kernel (one cooperative CTA per SM; needs
- * B <= 4, a GQA group <= 8, weight rows and KV page pairs within
- * one 32 KB ring slot), 2 = always the GEMV graph, 3 = always the tensor-core
- * graph (talker_decode returns EINVAL where the chosen path cannot run).
- * Errors: EINVAL. */
+ * GEMV kernels), 2 = always the GEMV graph, 3 = always the tensor-core graph
+ * (talker_decode returns EINVAL where the chosen path cannot run).
+ * Errors: EINVAL (any other mode). */
 talker_status talker_set_decode_mode(talker_t *t, int mode);
 
 /* Choose how prefill runs: 0 = automatic (tensor-core GEMMs when the weights
@@ -263,26 +261,15 @@ talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, 
 talker_status talker_test_gemm_swiglu_bf16(const void *A, int M, int K, const void *B, int N, void *out_bf16,
                                            void *cuda_stream);
 
-/* Tuning / test support: cap the number of CTAs that share one (stream, KV
- * group) along the sequence in the persistent decode kernel (0 = no cap).
- * Errors: EINVAL. */
-talker_status talker_set_attn_splits(talker_t *t, int max_splits);
-
-/* Test support: when buf is not NULL, every persistent-kernel decode step
- * writes globaltimer stamps (ns) of its consumer phases into
- * buf[cta * talker_trace_slots() + event] (15 events per layer, then 3 for the
- * head); buf is a caller-owned device buffer of n_SM * talker_trace_slots()
- * uint64 values. NULL turns tracing off. Errors: EINVAL. */
-talker_status talker_set_trace(talker_t *t, unsigned long long *buf);
-int talker_trace_slots(void);
-
 /* Allocation-free codec_head + argmax, for callers that cannot allocate device
  * memory (a real-time audio thread where cudaMalloc would stall, a host that
  * hands the library fixed buffers only, a process whose allocator belongs to
  * another framework). The pages have no counterpart: this is a packaging of
  * the head kernel, not part of the method.
  *   logits[r][v] = hidden[r] . W[v] (f32 accumulation), argmax[r] = the index of
- *   the largest logit of row r, the lowest index on ties; 0 <= r < rows.
+ *   the largest logit of row r, the lowest index on ties; 0 <= r < rows. A NaN
+ *   logit ranks as -inf, so a row whose logits are all NaN (or all -inf) gets
+ *   index 0; argmax is always a valid vocabulary index.
  * hidden: device f32 [rows, hidden_size]; W: device [vocab, hidden_size] in
  * weight_dtype (talker_dtype); logits: device f32 [rows, vocab]; argmax: device
  * int32 [rows]; cuda_stream: cudaStream_t (NULL = legacy stream). No handle.

@@ -32,24 +32,16 @@ constexpr int BM = 128;
 constexpr int BK = 64;                 // 64 bf16 = one 128-byte swizzle row
 constexpr int NTHREADS = 192;
 
-// One CTA per SM walks the tile list; each tile is (row block, column block, K split).
-// With CM > 1 the CTAs form clusters of CM along M: a cluster takes CM consecutive row
-// blocks of one column block, each CTA loads its own 128 x 64 A box and one BN/CM-row
-// slice of the shared B box, multicast to all CM CTAs, so every SM reads 1/CM of the
-// weight tile from L2. A ring slot is free again only when all CM CTAs have consumed it
-// (each MMA commit arrives on the slot's empty barrier in every CTA of the cluster).
-// The accumulator is double buffered in TMEM (2 x BN columns): while warps 2..5 drain
-// tile j from buffer j & 1, the MMA thread already accumulates tile j + 1 into the other
+// One CTA per SM walks the tile list; each tile is (row block, column block, K split),
+// and every CTA loads its own A and B boxes. The accumulator is double buffered in TMEM
+// (2 x BN columns): while warps 2..5 drain tile j from buffer j & 1, the MMA thread already accumulates tile j + 1 into the other
 // buffer, and the producer keeps the shared-memory ring full across tile boundaries.
-template <int BN, int STAGES, int CM>
+template <int BN, int STAGES>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_gemm_tc_persist(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                       const GemmParams p, int splits) {
     constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
-    constexpr uint32_t B_SLICE = B_BYTES / CM;
     constexpr uint32_t IDESC = instr_desc(BM, BN);
-    constexpr uint16_t MASK = (uint16_t)((1u << CM) - 1u);
-    static_assert((BN / CM) % 8 == 0, "a B slice must hold whole 8-row swizzle groups");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem;
@@ -59,10 +51,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __shared__ int fail_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = CM > 1 ? (int)cluster_rank() : 0;
-    const int cid = blockIdx.x / CM, n_clusters = gridDim.x / CM;
+    const int cid = blockIdx.x, n_ctas = gridDim.x;
     const int tiles_n = p.N / BN;
-    const int tiles_m = ((p.M + BM - 1) / BM + CM - 1) / CM;   // in cluster row blocks of CM x 128 rows
+    const int tiles_m = (p.M + BM - 1) / BM;
     const int n_tiles = tiles_m * tiles_n * splits;
     const int nk_total = p.K / BK;
     const int per = (nk_total + splits - 1) / splits;
@@ -70,7 +61,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CM);   // one commit from each CTA of the cluster
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -87,14 +78,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
     }
     __syncthreads();
-    if (CM > 1) cluster_sync();   // peers' barriers are initialised before any multicast lands
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
     // tile t -> (row block of this CTA, column block, split); column blocks vary fastest
     auto tile_of = [&](int t, int &m0, int &n0, int &kb0, int &nk) {
         const int sp = t / (tiles_m * tiles_n), rem = t - sp * tiles_m * tiles_n;
-        m0 = ((rem / tiles_n) * CM + rank) * BM;
+        m0 = (rem / tiles_n) * BM;
         n0 = (rem % tiles_n) * BN;
         kb0 = sp * per;
         nk = max(0, min(per, nk_total - kb0));
@@ -104,7 +94,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- TMA producer: one ring across all tiles of this CTA
         uint32_t it = 0;
         bool ok = true;
-        for (int t = cid; t < n_tiles && ok; t += n_clusters) {
+        for (int t = cid; t < n_tiles && ok; t += n_ctas) {
             int m0, n0, kb0, nk;
             tile_of(t, m0, n0, kb0, nk);
             for (int i = 0; i < nk; ++i, ++it) {
@@ -116,15 +106,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
                 tma_load_2d(sA + s * A_BYTES, &map_a, (kb0 + i) * BK, m0, &full[s]);
-                if (CM > 1)
-                    tma_load_2d_mc(sB + s * B_BYTES + rank * B_SLICE, &map_b, (kb0 + i) * BK, n0 + rank * (BN / CM),
-                                   &full[s], MASK);
-                else
-                    tma_load_2d(sB + s * B_BYTES, &map_b, (kb0 + i) * BK, n0, &full[s]);
+                tma_load_2d(sB + s * B_BYTES, &map_b, (kb0 + i) * BK, n0, &full[s]);
             }
         }
-        // Tail: every slot's last use is consumed by all CTAs of the cluster, so no copy or
-        // commit from a peer can still target this CTA's shared memory when it exits.
+        // Tail: wait until the MMAs have consumed every slot still in flight, so no copy
+        // lands in shared memory after the CTA has moved on.
         for (uint32_t j = (it > (uint32_t)STAGES ? it - STAGES : 0); j < it; ++j)
             mbar_wait(&empty[j % STAGES], (j / STAGES) & 1, p.status);
     } else if (warp == 1 && lane == 0) {
@@ -132,7 +118,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t it = 0;
         int j = 0;
         bool ok = true;
-        for (int t = cid; t < n_tiles && ok; t += n_clusters, ++j) {
+        for (int t = cid; t < n_tiles && ok; t += n_ctas, ++j) {
             int m0, n0, kb0, nk;
             tile_of(t, m0, n0, kb0, nk);
             const int b = j & 1;
@@ -154,10 +140,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
                     umma_bf16(acc, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), IDESC, (i > 0 || k > 0) ? 1u : 0u);
-                if (CM > 1)
-                    umma_commit_mc(&empty[s], MASK);
-                else
-                    umma_commit(&empty[s]);
+                umma_commit(&empty[s]);
             }
             umma_commit(&tfull[b]);   // arrives once this tile's MMAs have completed
         }
@@ -166,7 +149,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int q = warp & 3;
         float *stg = reinterpret_cast<float *>(sB + STAGES * B_BYTES) + q * 32 * 32;   // this warp's staging block
         int j = 0;
-        for (int t = cid; t < n_tiles; t += n_clusters, ++j) {
+        for (int t = cid; t < n_tiles; t += n_ctas, ++j) {
             int m0, n0, kb0, nk;
             tile_of(t, m0, n0, kb0, nk);
             const int b = j & 1;
@@ -237,7 +220,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CM > 1) cluster_sync();   // no CTA leaves while a peer may still address its shared memory
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)(2 * BN))
@@ -303,16 +285,12 @@ constexpr size_t smem_for(int bn, int stages) {
     return (size_t)stages * (tc::BM + bn) * tc::BK * 2 + 4 * 32 * 32 * 4 + 1024;
 }
 
-// Wide tiles and CTA pairs only for tall activations (8 or more row blocks). A short M
+// Wide tiles only for tall activations (8 or more row blocks). A short M
 // (small prefills, decode batches) streams the weights once, and there the narrow tiles
 // give twice as many CTAs pulling them from HBM.
 constexpr int kWideMinRowBlocks = 8;
 bool tall(int M) { return (M + tc::BM - 1) / tc::BM >= kWideMinRowBlocks; }
 int tile_n_for(int M, int N) { return (tall(M) && N % kBNWide == 0) ? kBNWide : kBNNarrow; }
-
-// CTAs per cluster along M (B tile multicast).
-constexpr int kClusterM = 2;
-int cluster_m_for(int M) { return tall(M) ? kClusterM : 1; }
 
 }  // namespace
 
@@ -337,67 +315,43 @@ int sm_count_current() {
 }
 }  // namespace
 
-template <int BN, int STAGES, int CM>
+template <int BN, int STAGES>
 static cudaError_t raise_smem() {
-    return cudaFuncSetAttribute(tc::k_gemm_tc_persist<BN, STAGES, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(tc::k_gemm_tc_persist<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)smem_for(BN, STAGES));
 }
 
 cudaError_t prepare_gemm_tc() {
-    cudaError_t e = raise_smem<kBNNarrow, kStagesNarrow, 1>();
-    e = e ? e : raise_smem<kBNNarrow, kStagesNarrow, kClusterM>();
-    e = e ? e : raise_smem<kBNWide, kStagesWide, 1>();
-    return e ? e : raise_smem<kBNWide, kStagesWide, kClusterM>();
+    cudaError_t e = raise_smem<kBNNarrow, kStagesNarrow>();
+    return e ? e : raise_smem<kBNWide, kStagesWide>();
 }
 
 namespace {
-// Persistent launch: as many CTAs (clusters of CM) as fit on the GPU at once, at most one
-// per cluster tile.
-template <int BN, int STAGES, int CM>
+// Persistent launch: one CTA per SM (the shared-memory ring allows no more), at most one
+// per tile.
+template <int BN, int STAGES>
 cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &p, int splits, int n_sm,
                        cudaStream_t st) {
-    const int tiles = (((p.M + tc::BM - 1) / tc::BM + CM - 1) / CM) * (p.N / BN) * splits;
+    const int tiles = ((p.M + tc::BM - 1) / tc::BM) * (p.N / BN) * splits;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(tc::NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = smem_for(BN, STAGES);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CM;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = CM > 1 ? 1 : 0;
-    static int max_clusters = 0;   // per instantiation; one device per process
-    if (max_clusters == 0) {
-        int n = 0;
-        cfg.gridDim = dim3(CM * (n_sm / CM), 1, 1);
-        if (CM > 1 && cudaOccupancyMaxActiveClusters(&n, tc::k_gemm_tc_persist<BN, STAGES, CM>, &cfg) == cudaSuccess &&
-            n > 0)
-            max_clusters = std::min(n, n_sm / CM);
-        else
-            max_clusters = n_sm / CM;
-        (void)cudaGetLastError();
-    }
-    cfg.gridDim = dim3(CM * std::min(tiles, max_clusters), 1, 1);
-    return cudaLaunchKernelEx(&cfg, tc::k_gemm_tc_persist<BN, STAGES, CM>, ma, mb, p, splits);
+    cfg.gridDim = dim3(std::min(tiles, n_sm), 1, 1);
+    return cudaLaunchKernelEx(&cfg, tc::k_gemm_tc_persist<BN, STAGES>, ma, mb, p, splits);
 }
 
 cudaError_t launch_persist(const void *A, const void *B, GemmParams &p, int splits, cudaStream_t st) {
     const int M = p.M, N = p.N, K = p.K;
     if (!gemm_tc_supported(N, K) || M < 1) return cudaErrorInvalidValue;
-    const int bn = tile_n_for(M, N), cm = cluster_m_for(M);
-    CUtensorMap ma, mb;   // with a cluster, each CTA copies (and multicasts) a BN/CM-row slice of B
-    if (!make_map(&ma, A, M, K, tc::BM) || !make_map(&mb, B, N, K, bn / cm)) return cudaErrorInvalidValue;
+    const int bn = tile_n_for(M, N);
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A, M, K, tc::BM) || !make_map(&mb, B, N, K, bn)) return cudaErrorInvalidValue;
     const int s = std::max(1, splits);
     const int n_sm = sm_count_current();
     if (n_sm <= 0) return cudaErrorInvalidDevice;
-    if (cm > 1) {
-        if (bn == kBNWide) return launch_cfg<kBNWide, kStagesWide, kClusterM>(ma, mb, p, s, n_sm, st);
-        return launch_cfg<kBNNarrow, kStagesNarrow, kClusterM>(ma, mb, p, s, n_sm, st);
-    }
-    if (bn == kBNWide) return launch_cfg<kBNWide, kStagesWide, 1>(ma, mb, p, s, n_sm, st);
-    return launch_cfg<kBNNarrow, kStagesNarrow, 1>(ma, mb, p, s, n_sm, st);
+    if (bn == kBNWide) return launch_cfg<kBNWide, kStagesWide>(ma, mb, p, s, n_sm, st);
+    return launch_cfg<kBNNarrow, kStagesNarrow>(ma, mb, p, s, n_sm, st);
 }
 }  // namespace
 

@@ -300,11 +300,11 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
             float best = -INFINITY;
             int bi = 0x7fffffff;
             for (int w = 0; w < kGemvWarps; ++w) {
-                const float v = hv_s[w][r];
+                float v = hv_s[w][r];
                 const int i = hi_s[w][r];
-                if (isnan(v)) {
+                if (isnan(v)) {   // reported, and ranked as -inf: the argmax stays a valid index
                     atomicOr(p.status, ST_NAN_LOGIT);
-                    continue;
+                    v = -INFINITY;
                 }
                 if (v > best || (v == best && i < bi)) {
                     best = v;

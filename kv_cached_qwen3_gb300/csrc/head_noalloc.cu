@@ -9,6 +9,8 @@
 // array of a fixed size that every GPU loading the library keeps until exit.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "talker.h"
 
@@ -29,9 +31,15 @@ struct NoAllocScratch {
 // The scratch; its name in host code is a host-side stand-in, not a device address.
 static __device__ __align__(256) NoAllocScratch g_na_scratch;
 
+constexpr int kNaRowTile = 8;      // rows that share one pass over a weight row
+
+// A NaN logit ranks as -inf in the argmax, so a row whose logits are all NaN (or all
+// -inf) selects index 0, and the result never depends on the order of the CTAs.
+__device__ __forceinline__ float rank_value(float x) { return isnan(x) ? -INFINITY : x; }
+
 // logits[r][v] = hidden[r] . W[v] for v < V, argmax[r] (lowest index on ties).
-// One warp per vocabulary row for all rows of the call; the CTA that arrives
-// last reduces the per-CTA partials in CTA order.
+// One warp per vocabulary row; the warp reads its weight row once per tile of 8
+// input rows. The CTA that arrives last reduces the per-CTA partials.
 template <typename WT>
 __global__ void __launch_bounds__(kNaWarps * 32) k_head_argmax_noalloc(const float *hidden, int rows, int H,
                                                                         const WT *W, int V, float *logits,
@@ -41,15 +49,26 @@ __global__ void __launch_bounds__(kNaWarps * 32) k_head_argmax_noalloc(const flo
     __shared__ int last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int v = blockIdx.x * kNaWarps + warp;
-    for (int r = 0; r < rows; ++r) {
-        float acc = 0.f;
+    for (int r0 = 0; r0 < rows; r0 += kNaRowTile) {
+        const int nr = min(kNaRowTile, rows - r0);
+        float acc[kNaRowTile];
+#pragma unroll
+        for (int j = 0; j < kNaRowTile; ++j) acc[j] = 0.f;
         if (v < V)
-            for (int k = lane; k < H; k += 32) acc = fmaf(Elem<WT>::load(W, (size_t)v * H + k), hidden[(size_t)r * H + k], acc);
-        acc = warp_sum(acc);
-        if (lane == 0) {
-            if (v < V) logits[(size_t)r * V + v] = acc;
-            bv[warp][r] = (v < V) ? acc : -INFINITY;
-            bi[warp][r] = v;
+            for (int k = lane; k < H; k += 32) {
+                const float w = Elem<WT>::load(W, (size_t)v * H + k);
+#pragma unroll
+                for (int j = 0; j < kNaRowTile; ++j)
+                    if (j < nr) acc[j] = fmaf(w, hidden[(size_t)(r0 + j) * H + k], acc[j]);
+            }
+#pragma unroll
+        for (int j = 0; j < kNaRowTile; ++j) {
+            const float a = warp_sum(acc[j]);
+            if (lane == 0 && j < nr) {
+                if (v < V) logits[(size_t)(r0 + j) * V + v] = a;
+                bv[warp][r0 + j] = (v < V) ? rank_value(a) : -INFINITY;
+                bi[warp][r0 + j] = v;
+            }
         }
     }
     __syncthreads();
@@ -87,25 +106,29 @@ __global__ void __launch_bounds__(kNaWarps * 32) k_head_argmax_noalloc(const flo
 }
 
 // Device address of the scratch, looked up once per device (with that device current).
+// Two host threads making their first call at once both look it up and store the same
+// value; the slots are atomics, so that is not a data race.
 NoAllocScratch *scratch_for_current_device(talker_status *st) {
-    static NoAllocScratch *addr[64] = {nullptr};
+    static std::atomic<NoAllocScratch *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
         *st = TALKER_ECUDA;
         return nullptr;
     }
-    if (addr[dev] == nullptr) {
+    NoAllocScratch *p = addr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_na_scratch) != cudaSuccess || ptr == nullptr) {
             cudaGetLastError();
             *st = TALKER_ECUDA;
             return nullptr;
         }
-        addr[dev] = static_cast<NoAllocScratch *>(ptr);
+        p = static_cast<NoAllocScratch *>(ptr);
+        addr[dev].store(p, std::memory_order_relaxed);
     }
     *st = TALKER_OK;
-    return addr[dev];
+    return p;
 }
 
 }  // namespace

@@ -16,9 +16,6 @@ enum Epilogue : int {
     EPI_HEAD = 3     // logits, final hidden, argmax (last CTA), decode length bump
 };
 
-// Which stream and position each activation row belongs to.
-//   mode 0 (decode):  row r is stream r at position cur_len[r]
-//   mode 1 (prefill): row r is stream `stream0` at position pos0 + r
 // Where row r of a launch sits. mode 0 (decode): stream r at position cur_len[r].
 // mode 1 (prefill): stream stream0 + r / rows_per_stream at position pos0 + r % rows_per_stream
 // (rows_per_stream = 0: every row in stream0).
@@ -115,54 +112,6 @@ struct AttnParams {
 };
 constexpr int kAttnClusterMax = 8;   // portable cluster size
 
-// One layer's weights as the persistent decode kernel reads them (device array).
-struct PersistLayer {
-    const float *in_norm, *post_norm, *q_norm, *k_norm;
-    const void *qkv, *o, *gu, *down;
-};
-
-constexpr int kMaxSplits = 16;        // attention splits per (row, KV group) in the persistent kernel
-
-struct PersistParams {
-    int n_layers, H, nq, nkv, hd, I, V, G;
-    float eps, scale;
-    int rows;                         // streams 0..rows-1, one row each
-    uint32_t flag_base;               // step epoch * 256 (never 0): flags of this step's words
-    int splits;                       // attention splits per (row, KV group), <= kMaxSplits
-    const PersistLayer *layers;       // device array [n_layers]
-    const float *final_norm;
-    const void *head;
-    CacheView cache;
-    const float2 *rope;
-    int *cur_len;
-    const float *emb;                 // [rows, H]
-    float *logits;                    // [rows, V]
-    float *hidden_out;                // [rows, H] or null
-    int *argmax_out;                  // [rows] or null
-    // flag words (value | flag << 32), single-buffered, rows of the 4-row template:
-    unsigned long long *x_ll;         // [4][H]      residual stream after o_proj / after down
-    unsigned long long *raw_ll;       // [4][qkv_n]  raw q|k|v
-    unsigned long long *o_ll;         // [4][nq*hd]  attention output
-    unsigned long long *act_ll;       // [4][I]      silu(gate) * up
-    unsigned long long *part_ll;      // [4][nq][kMaxSplits][hd + 2]  split partials (m, l, o)
-    float *head_val;                  // [grid][4] per-CTA argmax partials
-    int *head_idx;
-    int *sync;                        // [0] argmax arrival counter, [2] abort flag; zero between launches
-    int *status;
-    unsigned long long *trace;        // optional: [grid][kTraceSlots] globaltimer stamps
-};
-
-// Trace stamps per CTA: [0, 512) consumer phase events (15 per layer + 3 for the head),
-// [512, 1280) time the producer issued ring chunk k, [1280, 2048) time the consumers got chunk k.
-// [2048, 2816) time chunk k's dot products were done (consumer thread 0), [2816, 3584) its epilogue.
-constexpr int kTraceSlots = 4096;
-constexpr int kTraceProducer = 512;
-constexpr int kTraceAcquire = 1280;
-constexpr int kTraceDots = 2048;
-constexpr int kTraceEpi = 2816;
-constexpr int kTraceChunks = 768;
-constexpr int kTracePerLayer = 16;
-
 // Tensor-core GEMM C[M, N] (+)= A[M, K] B[N, K]^T, bf16 inputs, fp32 output.
 struct GemmParams {
     int M, N, K;
@@ -235,14 +184,5 @@ cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int h
                             int layer, const RowMap &rm, int *status, cudaStream_t st,
                             __nv_bfloat16 *dense_kv = nullptr);
 cudaError_t launch_swiglu_bf16(const float *gu, int rows, int I, void *out, cudaStream_t st);
-
-// Persistent decode kernel (one cooperative launch per decode step, one CTA per SM).
-size_t persist_smem(int R, int head_dim, int kv_bf16, int kmax, int group, int splits);
-int persist_threads();
-int persist_slot_bytes();
-int persist_sync_words(int n_heads);
-cudaError_t setup_persistent(int w_bf16, int head_dim, int R, size_t smem, int *blocks_per_sm);
-cudaError_t launch_persistent(int w_bf16, int head_dim, int R, const PersistParams &p, int grid, size_t smem,
-                              cudaStream_t st);
 
 }  // namespace talker_k

@@ -91,21 +91,10 @@ struct talker {
     int *d_status = nullptr;
     int64_t launches = 0;
     std::vector<GraphEntry> graphs;
-    // persistent decode kernel
-    int decode_mode = 0;                 // 0 auto, 1 persistent kernel, 2 multi-kernel CUDA graph
+    int decode_mode = 0;                 // 0 auto, 2 GEMV graph, 3 tensor-core graph
     int attn_cluster = 0;   // decode attention: splits combine inside a thread-block cluster
-    PersistLayer *d_layers = nullptr;    // device copy of the layer pointer table
-    int *d_sync = nullptr;               // counter words of the persistent kernel
-    unsigned long long *ll = nullptr;    // flag-word buffers of the persistent kernel (one allocation)
-    float *pk_head_val = nullptr;        // per-CTA argmax partials of the persistent kernel
-    int *pk_head_idx = nullptr;
-    size_t ll_words = 0;
-    uint32_t epoch = 0;                  // step counter for the persistent kernel's flags
-    int max_splits = 0;                  // cap on the persistent kernel's attention splits (0 = none)
     int prefill_mode = 0;                // 0 automatic, 2 always the GEMV kernels, 3 / 4 tensor-core GEMMs
                                          // with the mma.sync / the tcgen05 attention at any T
-    int persist_ok[2] = {-1, -1};        // per R template (1, 4): -1 unknown, 0 unusable, 1 usable
-    unsigned long long *trace = nullptr; // optional phase stamps of the persistent kernel (caller-owned)
     // tensor-core prefill buffers (bf16 GEMM operands and the f32 gate/up projection)
     int cap_tc_rows = 0;
     void *hb = nullptr, *ab = nullptr, *gb = nullptr;
@@ -166,20 +155,6 @@ void free_tc(talker *t) {
         *pp = nullptr;
     }
     t->cap_tc_rows = 0;
-}
-
-void free_persist(talker *t) {
-    free_ptr(t->d_layers);
-    free_ptr(t->d_sync);
-    free_ptr(t->ll);
-    free_ptr(t->pk_head_val);
-    free_ptr(t->pk_head_idx);
-    t->pk_head_val = nullptr;
-    t->pk_head_idx = nullptr;
-    t->d_layers = nullptr;
-    t->d_sync = nullptr;
-    t->ll = nullptr;
-    t->ll_words = 0;
 }
 
 void free_cache(talker *t) {
@@ -514,123 +489,6 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
     return TALKER_OK;
 }
 
-int persist_rows_tmpl(int B) { return B <= 1 ? 1 : 4; }
-
-int persist_splits(const talker *t, int B) {
-    int s = std::max(1, std::min(kMaxSplits, t->n_sm / (B * t->nkv)));
-    if (t->max_splits > 0) s = std::min(s, t->max_splits);
-    return s;
-}
-
-
-
-int kmax_of(const talker *t) { return std::max(std::max(t->H, t->qd), t->I); }
-
-// Can the persistent kernel run this geometry with B rows? (one CTA per SM must fit,
-// every weight row group and KV page pair must fit one ring slot)
-bool persist_usable(talker *t, int B) {
-    if (B > 4 || t->w_bf16 != t->kv_bf16 || t->suppress_tail > 0) return false;
-    const int R = persist_rows_tmpl(B);
-    int &ok = t->persist_ok[R == 1 ? 0 : 1];
-    if (ok >= 0) return ok == 1;
-    ok = 0;
-    const size_t slot = (size_t)persist_slot_bytes();
-    const size_t wsz = t->wsz;
-    if ((size_t)t->H * wsz > slot || (size_t)t->qd * wsz > slot || (size_t)2 * t->H * wsz > slot ||
-        (size_t)t->I * wsz > slot || (size_t)2 * 64 * t->hd * t->kvsz > slot)
-        return false;
-    if (kmax_of(t) > 3072 || (t->H + t->n_sm - 1) / t->n_sm > 64 || t->G > 8) return false;
-    // 32-bit span arithmetic in the kernel: every (units x grid) product below 2^32
-    if ((uint64_t)std::max(std::max(t->qkv_n, t->V), t->I) * (uint64_t)(t->n_sm + 1) >= (1ull << 32)) return false;
-    // shared memory is largest at the smallest B of the row template (most attention splits)
-    const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t), t->G, persist_splits(t, R == 1 ? 1 : 2));
-    if (smem > 227 * 1024 - 8 * 1024) return false;
-    int per_sm = 0;
-    if (setup_persistent(t->w_bf16, t->hd, R, smem, &per_sm) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    if (per_sm < 1) return false;
-    ok = 1;
-    return true;
-}
-
-talker_status ensure_persist(talker *t) {
-    const int n_heads = t->nq + 2 * t->nkv;
-    if (!t->d_layers) {
-        std::vector<PersistLayer> h(t->c.n_layers);
-        for (int l = 0; l < t->c.n_layers; ++l) {
-            const LayerDev &d = t->L[l];
-            h[l] = PersistLayer{d.in_norm, d.post_norm, d.q_norm, d.k_norm, d.qkv, d.o, d.gu, d.down};
-        }
-        TRY_CUDA(cudaMalloc(&t->d_layers, h.size() * sizeof(PersistLayer)));
-        TRY_CUDA(cudaMemcpy(t->d_layers, h.data(), h.size() * sizeof(PersistLayer), cudaMemcpyHostToDevice));
-        const size_t words = 8 + n_heads;
-        TRY_CUDA(cudaMalloc(&t->d_sync, words * sizeof(int)));
-        TRY_CUDA(cudaMemset(t->d_sync, 0, words * sizeof(int)));
-        // flag words for 4 rows: x, raw, o, act, split partials; zero flags never match a step's flags
-        const size_t words_ll = 4 * ((size_t)t->H + t->qkv_n + t->qd + t->I) +
-                                4 * (size_t)t->nq * kMaxSplits * (t->hd + 2);
-        TRY_CUDA(cudaMalloc(&t->ll, words_ll * 8));
-        TRY_CUDA(cudaMemset(t->ll, 0, words_ll * 8));
-        t->ll_words = words_ll;
-        TRY_CUDA(cudaMalloc(&t->pk_head_val, (size_t)t->n_sm * 4 * sizeof(float)));
-        TRY_CUDA(cudaMalloc(&t->pk_head_idx, (size_t)t->n_sm * 4 * sizeof(int)));
-    }
-    return TALKER_OK;
-}
-
-talker_status decode_persistent(talker *t, const float *emb, int B, float *logits, float *hidden, int32_t *argmax) {
-    TRY(ensure_persist(t));
-    const int R = persist_rows_tmpl(B);
-    if (++t->epoch >= (1u << 24)) t->epoch = 1;
-    PersistParams p{};
-    p.n_layers = t->c.n_layers;
-    p.H = t->H;
-    p.nq = t->nq;
-    p.nkv = t->nkv;
-    p.hd = t->hd;
-    p.I = t->I;
-    p.V = t->V;
-    p.G = t->G;
-    p.eps = t->c.rms_eps;
-    p.scale = 1.0f / sqrtf((float)t->hd);
-    p.rows = B;
-    p.flag_base = t->epoch << 8;
-    p.splits = persist_splits(t, B);
-    p.layers = t->d_layers;
-    p.final_norm = t->fnorm;
-    p.head = t->head;
-    p.cache = cache_view(t);
-    p.rope = t->d_rope;
-    p.cur_len = t->d_len;
-    p.emb = emb;
-    p.logits = logits;
-    p.hidden_out = hidden;
-    p.argmax_out = argmax;
-    unsigned long long *q = t->ll;
-    p.x_ll = q;
-    q += 4 * (size_t)t->H;
-    p.raw_ll = q;
-    q += 4 * (size_t)t->qkv_n;
-    p.o_ll = q;
-    q += 4 * (size_t)t->qd;
-    p.act_ll = q;
-    q += 4 * (size_t)t->I;
-    p.part_ll = q;
-    p.head_val = t->pk_head_val;
-    p.head_idx = t->pk_head_idx;
-    p.sync = t->d_sync;
-    p.status = t->d_status;
-    p.trace = t->trace;
-    const size_t smem = persist_smem(R, t->hd, t->kv_bf16, kmax_of(t), t->G, p.splits);
-    TRY_CUDA(launch_persistent(t->w_bf16, t->hd, R, p, t->n_sm, smem, t->st));
-    t->launches += 1;
-    for (int b = 0; b < B; ++b) t->len[b] += 1;
-    return TALKER_OK;
-}
-
-
 constexpr int kTcMinRows = 16;        // prefills shorter than this stay on the GEMV kernels
 constexpr int kAttnTcMinRows = 256;   // tcgen05 prefill attention from two 128-row query tiles up (below,
                                       // its extra dense-copy launch and TMEM setup outweigh the tiles)
@@ -870,7 +728,6 @@ void talker_destroy(talker_t *t) {
     free_workspaces(t);
     free_cache(t);
     free_ptr(t->wstore);
-    free_persist(t);
     free_tc(t);
     free_ptr(t->d_status);
     if (t->cap_st) cudaStreamDestroy(t->cap_st);
@@ -981,10 +838,6 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
     for (int b = 0; b < B; ++b)
         if (t->len[b] + 1 > t->max_seq) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));
-    // The persistent kernel runs on request only: on GB300 the graph of per-phase kernels
-    // is faster at every batch and length measured.
-    if (t->decode_mode == 1 && persist_usable(t, B)) return decode_persistent(t, emb, B, logits, hidden, argmax);
-    if (t->decode_mode == 1) return TALKER_EINVAL;
     const int kind = (t->decode_mode == 3 || (t->decode_mode == 0 && B >= kTcMinDecodeRows)) && tc_usable(t) ? 1 : 0;
     if (t->decode_mode == 3 && kind == 0) return TALKER_EINVAL;
     // One or two short streams: the splits of a (row, KV group) form one thread-block cluster
@@ -1079,14 +932,6 @@ int64_t talker_kernel_launches(const talker_t *t) { return t ? t->launches : 0; 
 
 const char *talker_last_error(void) { return g_last_error; }
 
-talker_status talker_set_trace(talker_t *t, unsigned long long *buf) {
-    if (!t) return TALKER_EINVAL;
-    t->trace = buf;
-    return TALKER_OK;
-}
-
-int talker_trace_slots(void) { return kTraceSlots; }
-
 talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, int N, float *out, int accumulate,
                                     int splits, void *cuda_stream) {
     if (!A || !B || !out || M < 1 || splits < 1 || !gemm_tc_supported(N, K)) return TALKER_EINVAL;
@@ -1119,12 +964,6 @@ talker_status talker_test_gemm_swiglu_bf16(const void *A, int M, int K, const vo
     int h = 0;
     TRY_CUDA(cudaMemcpy(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost));
     return h ? TALKER_EDEVICE : TALKER_OK;
-}
-
-talker_status talker_set_attn_splits(talker_t *t, int max_splits) {
-    if (!t || max_splits < 0) return TALKER_EINVAL;
-    t->max_splits = max_splits;
-    return TALKER_OK;
 }
 
 talker_status talker_set_logit_suppression(talker_t *t, int vocab_tail, int eos_id) {
@@ -1264,7 +1103,7 @@ talker_status talker_set_prefill_mode(talker_t *t, int mode) {
 }
 
 talker_status talker_set_decode_mode(talker_t *t, int mode) {
-    if (!t || mode < 0 || mode > 3) return TALKER_EINVAL;
+    if (!t || (mode != 0 && mode != 2 && mode != 3)) return TALKER_EINVAL;
     t->decode_mode = mode;
     return TALKER_OK;
 }

@@ -1,7 +1,6 @@
 // tcgen05 / TMA building blocks shared by the tensor-core kernels (sm_103a): tiled bulk
 // tensor loads into 128-byte-swizzled shared memory, shared-memory matrix descriptors,
-// kind::f16 MMAs with TMEM accumulators, commits to mbarriers, TMEM loads, and the
-// cluster primitives of the multicast GEMM.
+// kind::f16 MMAs with TMEM accumulators, commits to mbarriers and TMEM loads.
 #pragma once
 
 #include <cuda.h>
@@ -94,34 +93,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
-}
-
-// Multicast form of the tile load: the box lands at the same shared-memory offset in
-// every CTA of the cluster named in `mask`, and completes bytes on the mbarrier at the
-// same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-// Commit that arrives on the mbarrier at this offset in every CTA of `mask`.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
 }
 
 // Generic-proxy writes to shared memory (st.shared) made visible to the tensor core

@@ -84,15 +84,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_kernel_launches": (i64, [vp]),
         "talker_last_error": (ctypes.c_char_p, []),
         "talker_set_decode_mode": (st, [vp, ctypes.c_int]),
-        "talker_set_trace": (st, [vp, vp]),
-        "talker_set_attn_splits": (st, [vp, ctypes.c_int]),
         "talker_set_prefill_mode": (st, [vp, ctypes.c_int]),
         "talker_head_argmax_noalloc": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, vp, vp,
                                             vp]),
         "talker_test_gemm_bf16": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
                                        ctypes.c_int, vp]),
         "talker_test_gemm_swiglu_bf16": (st, [vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp]),
-        "talker_trace_slots": (ctypes.c_int, []),
     }
     for name, (res, args) in proto.items():
         fn = getattr(lib, name)
@@ -258,20 +255,13 @@ class Talker:
                     "talker_frame")
 
     def set_decode_mode(self, mode: int):
-        """0 automatic, 1 persistent decode kernel, 2 multi-kernel CUDA graph."""
+        """0 automatic, 2 the GEMV graph, 3 the tensor-core graph."""
         self._check(self.lib.talker_set_decode_mode(self.h, mode), "talker_set_decode_mode")
 
     def set_prefill_mode(self, mode: int):
         """0 automatic (tensor cores for bf16 weights and T >= 16), 2 GEMV kernels, 3 / 4 tensor
         cores with the mma.sync / tcgen05 prefill attention at any T."""
         self._check(self.lib.talker_set_prefill_mode(self.h, mode), "talker_set_prefill_mode")
-
-    def set_attn_splits(self, n: int):
-        self._check(self.lib.talker_set_attn_splits(self.h, n), "talker_set_attn_splits")
-
-    def set_trace(self, buf):
-        """buf: int64 cuda tensor [n_sm * trace_slots] or None (persistent decode phase stamps)."""
-        self._check(self.lib.talker_set_trace(self.h, _ptr(buf)), "talker_set_trace")
 
     def sync_status(self) -> int:
         code = ctypes.c_int32(0)

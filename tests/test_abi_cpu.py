@@ -90,8 +90,6 @@ def test_later_entry_points_reject_null_handles_and_off_grid_shapes(lib):
     assert lib.talker_set_code_tables(None, None, None, 0, 0) == 1
     assert lib.talker_decode_codes(None, None, None, 1, None, None, None) == 1
     assert lib.talker_frame(None, None, 2, 1, None, None, None) == 1
-    assert lib.talker_set_attn_splits(None, 0) == 1
-    assert lib.talker_set_trace(None, None) == 1
     assert lib.talker_kv_import(None, 0, None, None, 0) == 1
     assert lib.talker_kv_export(None, 0, None, None, 0) == 1
     for mode in (0, 2, 3, 4, 1, 5, -1):

@@ -91,7 +91,7 @@ def poisoned_cache(g, seed, L, extra, n_layers):
 
 
 @pytest.mark.parametrize("L", [0, 1, 63, 64, 65, 128, 150])
-@pytest.mark.parametrize("mode", [pytest.param(1, id="persistent"), pytest.param(2, id="graph")])
+@pytest.mark.parametrize("mode", [pytest.param(0, id="auto"), pytest.param(2, id="graph")])
 def test_stale_rows_past_length_never_read_fp32(cuda, tiny, L, mode):
     """NaN rows beyond the rewound length (same page and next pages) leave decode unchanged."""
     from kv_cached_qwen3_gb300.talker import Talker
@@ -118,8 +118,7 @@ def test_stale_rows_past_length_never_read_fp32(cuda, tiny, L, mode):
     tk.close()
 
 
-@pytest.mark.parametrize("mode", [pytest.param(1, id="persistent"), pytest.param(2, id="graph"),
-                                  pytest.param(3, id="tensor-core-graph")])
+@pytest.mark.parametrize("mode", [pytest.param(2, id="graph"), pytest.param(3, id="tensor-core-graph")])
 def test_stale_rows_past_length_never_read_bf16(cuda, mode):
     """The same on a 2-layer bf16 Talker geometry, with a rewound length inside a page."""
     from kv_cached_qwen3_gb300.talker import Talker

@@ -1,8 +1,7 @@
 """GPU: the tensor-core (tcgen05/TMEM) GEMM against a float64 matmul of the same bf16 inputs.
 
-Shapes cover both tile widths (N % 256 == 0 or not), split-K, ragged M, and M of eight or
-more row blocks, where CTA pairs share the weight tile through cluster multicast (an odd
-row-block count leaves the second CTA of the last pair wholly past M)."""
+Shapes cover both tile widths (N % 256 == 0 or not), split-K, ragged M, and tall M (eight
+or more row blocks, the wide-tile range) with a ragged last row block."""
 import numpy as np
 import pytest
 

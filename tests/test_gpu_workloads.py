@@ -46,7 +46,7 @@ def predictor():
     return wl, g, w, Oracle(g, w)
 
 
-@pytest.mark.parametrize("mode", [pytest.param(1, id="persistent"), pytest.param(2, id="graph")])
+@pytest.mark.parametrize("mode", [pytest.param(2, id="graph"), pytest.param(3, id="tensor-core-graph")])
 def test_predictor_loop_frames(cuda, predictor, mode):
     """Four frames of prefill T=2 + 15 decodes on one cache; each frame against a fresh oracle forward."""
     from kv_cached_qwen3_gb300.talker import Talker
@@ -117,7 +117,7 @@ def test_long_context_decode(cuda, talker_long, L):
     lg = torch.empty(1, g.vocab, device="cuda")
     hdn = torch.empty(1, g.hidden, device="cuda")
     am = torch.empty(1, device="cuda", dtype=torch.int32)
-    for mode in (1, 2, 3):
+    for mode in (2, 3):
         tk.set_decode_mode(mode)
         tk.rewind(0, L)
         tk.decode(dev(emb), lg, hdn, am)

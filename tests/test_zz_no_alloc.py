@@ -78,3 +78,70 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(cuda):
     with pytest.raises(TalkerError):
         head_argmax_noalloc(hidden[:1], W2, torch.empty(1, 8200, device="cuda"),
                             torch.empty(1, dtype=torch.int32, device="cuda"), "f32")
+
+
+def _noalloc(hidden, W, wdt):
+    from kv_cached_qwen3_gb300.talker import head_argmax_noalloc
+    rows, V = hidden.shape[0], W.shape[0]
+    out = torch.full((rows, V), float("nan"), device="cuda")
+    arg = torch.full((rows,), -1, device="cuda", dtype=torch.int32)
+    head_argmax_noalloc(hidden.contiguous(), W.contiguous(), out, arg, wdt)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64), arg.cpu().numpy()
+
+
+@pytest.mark.parametrize("rows,H,V,wdt", [(64, 1024, 8192, "bf16"), (3, 37, 8189, "f32"), (1, 1024, 3072, "bf16"),
+                                          (64, 37, 8, "f32")])
+def test_noalloc_head_matches_fp64_product(cuda, rows, H, V, wdt):
+    """logits against an fp64 hidden @ W.T of the same stored values, at the size limits
+    (64 rows, vocab 8192), with a vocab that is not a multiple of 8 (idle warps in the
+    last CTA) and a hidden size that is not a multiple of 32; calls of different grid
+    sizes run back to back, so the arrival counter must be back at zero after each."""
+    g = torch.Generator(device="cpu").manual_seed(rows * 1000 + V)
+    hidden = torch.randn(rows, H, generator=g)
+    W = 0.05 * torch.randn(V, H, generator=g)
+    if wdt == "bf16":
+        W = W.to(torch.bfloat16)
+    ref = hidden.double() @ W.double().T
+    for _ in range(2):
+        got, arg = _noalloc(hidden.cuda(), W.cuda(), wdt)
+        for r in range(rows):
+            assert rel_l2(got[r], ref[r].numpy()) <= TOL_F32
+        np.testing.assert_array_equal(arg, np.argmax(got, axis=-1))
+
+
+def test_noalloc_small_grid_after_large_grid(cuda):
+    """A one-CTA call right after a 1024-CTA call reduces only its own partials."""
+    W_big = (0.05 * torch.randn(8192, 64)).cuda()
+    W_small = (0.05 * torch.randn(8, 64)).cuda()
+    x = torch.randn(4, 64).cuda()
+    _noalloc(x, W_big, "f32")
+    got, arg = _noalloc(x, W_small, "f32")
+    ref = x.double().cpu() @ W_small.double().cpu().T
+    np.testing.assert_array_equal(arg, np.argmax(ref.numpy(), axis=-1))
+    _noalloc(x, W_big, "f32")
+    got2, arg2 = _noalloc(x, W_small, "f32")
+    np.testing.assert_array_equal(arg2, arg)
+
+
+def test_noalloc_ties_and_nan_rows(cuda):
+    """Equal maxima resolve to the lowest index (also when they sit in different CTAs);
+    NaN logits rank as -inf, so an all-NaN row returns index 0, a valid index."""
+    V, H = 64, 8
+    W = torch.zeros(V, H)
+    W[5, 0] = 1.0          # rows 5 and 40 give the same logit for hidden = e0
+    W[40, 0] = 1.0
+    W[50, 1] = 2.0         # the maximum for hidden = e1, unless that row is NaN
+    hidden = torch.zeros(4, H)
+    hidden[0, 0] = 1.0                      # tie between 5 and 40 (CTAs 0 and 5) -> 5
+    hidden[1, :] = float("nan")             # every logit NaN -> 0
+    hidden[2, 1] = 1.0                      # plain maximum -> 50
+    # row 3 all zero: every logit 0.0, a 64-way tie -> 0
+    got, arg = _noalloc(hidden.cuda(), W.cuda(), "f32")
+    assert list(arg) == [5, 0, 50, 0]
+    assert np.all(np.isnan(got[1]))
+    W2 = W.clone()
+    W2[50, 1] = float("nan")                # a NaN logit never wins: row 2 falls to the zeros -> 0
+    W2[7, 1] = -1.0
+    got, arg = _noalloc(hidden[2:3].cuda(), W2.cuda(), "f32")
+    assert list(arg) == [0]
