@@ -156,10 +156,15 @@ class Oracle:
         a = silu(h2 @ w["gate_proj"].T) * (h2 @ w["up_proj"].T)
         return x + a @ w["down_proj"].T
 
-    def head(self, x):
-        """Final RMSNorm and codec_head (talker_forward_core). Returns (hidden, logits)."""
+    def head(self, x, head_w=None):
+        """Final RMSNorm and codec_head (talker_forward_core). Returns (hidden, logits).
+
+        head_w [V, H] replaces codec_head: the code predictor of the rightkit-qts page
+        ("tts_transformer.rs", forward_code_pred_prefill_cached / forward_code_pred_step_cached)
+        projects its prefill with heads[0] and generation step g with heads[g]."""
         y = rms_norm(x, self.final_norm, self.g.rms_eps)
-        return y, y @ self.codec_head.T
+        W = self.codec_head if head_w is None else np.asarray(head_w, F64)
+        return y, y @ W.T
 
     # -- mode A: uncached full-sequence forward ---------------------------------
     def forward_full(self, emb, return_layers=False):
@@ -279,8 +284,9 @@ class OracleCache:
     def kv_export(self, s, length):
         return self.K[s][:, :, :length].copy(), self.V[s][:, :, :length].copy()
 
-    def append_rows(self, s, emb):
-        """talker_forward_core with n_past = cur_len[s]: T rows appended, all rows' outputs."""
+    def append_rows(self, s, emb, head_w=None):
+        """talker_forward_core with n_past = cur_len[s]: T rows appended, all rows' outputs.
+        head_w: another output head (see Oracle.head), else codec_head."""
         o, g = self.o, self.o.g
         x = np.asarray(emb, F64)
         T = x.shape[0]
@@ -304,21 +310,22 @@ class OracleCache:
                 sc = np.where(vis, sc, -np.inf)
                 attn[:, h, :] = softmax(sc, axis=-1) @ Vc[kv, :n_past + T]
             x = o.post_attention(l, x, attn.reshape(T, -1))
-        hid, logits = o.head(x)
+        hid, logits = o.head(x, head_w)
         self.cur_len[s] = n_past + T
         return hid, logits
 
-    def prefill(self, s, emb):
+    def prefill(self, s, emb, head_w=None):
         """talker_forward_prefill: rewind to 0, append T rows, return the last row (hidden, logits)."""
         T = np.asarray(emb).shape[0]
         if T < 1 or T > self.max_seq_len:
             raise ValueError("prefill length out of range")
         self.cur_len[s] = 0
-        hid, logits = self.append_rows(s, emb)
+        hid, logits = self.append_rows(s, emb, head_w)
         return hid[-1], logits[-1]
 
-    def decode(self, embs):
-        """talker_forward_decode over streams 0..B-1, one row each. Returns (hidden [B,H], logits [B,V])."""
+    def decode(self, embs, head_w=None):
+        """talker_forward_decode over streams 0..B-1, one row each. Returns (hidden [B,H], logits [B,V]).
+        head_w: another output head (see Oracle.head), else codec_head."""
         o, g = self.o, self.o.g
         x = np.asarray(embs, F64)
         B = x.shape[0]
@@ -335,7 +342,7 @@ class OracleCache:
                 self._store(s, l, pos[s:s + 1], k[s:s + 1], v[s:s + 1])
                 attn[s] = attend_one(q[s], Ks, Vs, pos[s] + 1)
             x = o.post_attention(l, x, attn.reshape(B, -1))
-        hid, logits = o.head(x)
+        hid, logits = o.head(x, head_w)
         for s in range(B):
             self.cur_len[s] += 1
         return hid, logits
@@ -380,6 +387,25 @@ def embed_codes(tables, ids, overlay=None):
     if overlay is not None:
         x += np.asarray(overlay, F64)
     return x
+
+
+def code_predictor_frame(cache, emb, tables, table_of_step, heads, codes=None):
+    """One frame of the code predictor on stream 0 of `cache` (rightkit-qts "tts_transformer.rs",
+    predict_remaining_codebooks_kv_with_cache): prefill with emb [T0, H] and take the greedy code
+    of its last row through heads[0]; then step i (generation step i + 1) reads row code_i of
+    tables[table_of_step[i]], is decoded, and its code i + 1 is the greedy token of heads[i + 1].
+    heads: len(table_of_step) + 1 arrays [V, H]. codes: optional codes to feed instead of the
+    oracle's own (teacher forcing: codes[i] is the input of step i).
+    Returns (logits [n_steps + 1, V], the oracle's greedy codes [n_steps + 1])."""
+    _, lg = cache.prefill(0, emb, heads[0])
+    logits, own = [lg], [argmax_low(lg)]
+    for i, tab in enumerate(table_of_step):
+        prev = own[i] if codes is None else int(codes[i])
+        x = np.asarray(tables[tab], F64)[prev][None]
+        _, lg = cache.decode(x, heads[i + 1])
+        logits.append(lg[0])
+        own.append(argmax_low(lg[0]))
+    return np.stack(logits), np.array(own)
 
 
 def suppress_logits(logits, vocab_tail, eos_id):

@@ -447,6 +447,71 @@ def test_suppress_logits_tail_keeps_eos():
     assert argmax_low(small) == 3 and np.isinf(small).sum() == 9
 
 
+def test_argmax_low_breaks_ties_by_lowest_index():
+    """The greedy token of a row with equal maxima is the lowest of their indices (the
+    reading taken where the pages leave ties open), including an all-equal row and rows of
+    -inf where suppression removed every other candidate."""
+    from oracle import argmax_low
+    assert argmax_low([1.0, 3.0, 3.0, 2.0]) == 1
+    assert argmax_low([0.0, 0.0, 0.0]) == 0
+    assert argmax_low([-np.inf, 2.5, -np.inf, 2.5]) == 1
+    assert argmax_low([-np.inf, -np.inf]) == 0
+    assert argmax_low([-1.0, -3.0, -1.0]) == 0
+    v = np.full(3072, -0.5)
+    v[[17, 900, 3071]] = 4.0
+    assert argmax_low(v) == 17
+
+
+def test_code_predictor_frame_heads_per_generation_step(tiny):
+    """The frame projects its prefill with heads[0] and step i with heads[i + 1] (generation
+    step i + 1 on the rightkit-qts page). Head g is zero except rows 7g (+1) and 7g + 1 (-1), so
+    its greedy code is 7g or 7g + 1 whatever the hidden state: code j // 7 must equal j."""
+    from oracle import OracleCache, code_predictor_frame
+    w, o = tiny
+    g = TINY
+    n = 15
+    rng = np.random.Generator(np.random.PCG64(5))
+    tables = [rng.standard_normal((g.vocab, g.hidden)) for _ in range(n)]
+    heads = []
+    for j in range(n + 1):
+        h = np.zeros((g.vocab, g.hidden))
+        h[7 * j] = 1.0
+        h[7 * j + 1] = -1.0
+        heads.append(h)
+    emb = rng.standard_normal((2, g.hidden))
+    lg, codes = code_predictor_frame(OracleCache(o, 1, 20), emb, tables, list(range(n)), heads)
+    assert list(codes // 7) == list(range(n + 1))
+    assert lg.shape == (n + 1, g.vocab)
+
+
+def test_code_predictor_frame_matches_plain_steps(tiny):
+    """With every head = codec_head, the frame equals a prefill followed by decode steps whose
+    input is the table row of the previous greedy code; another head equals an oracle built
+    with that head as codec_head."""
+    from oracle import Oracle, OracleCache, code_predictor_frame, argmax_low
+    w, o = tiny
+    g = TINY
+    n = 4
+    rng = np.random.Generator(np.random.PCG64(6))
+    tables = [rng.standard_normal((g.vocab, g.hidden)) for _ in range(n)]
+    emb = rng.standard_normal((3, g.hidden))
+    lg, codes = code_predictor_frame(OracleCache(o, 1, 10), emb, tables, [2, 0, 3, 1], [o.codec_head] * (n + 1))
+    oc = OracleCache(o, 1, 10)
+    _, r = oc.prefill(0, emb)
+    ref, c = [r], [argmax_low(r)]
+    for i, tab in enumerate([2, 0, 3, 1]):
+        _, r = oc.decode(tables[tab][c[i]][None])
+        ref.append(r[0])
+        c.append(argmax_low(r[0]))
+    np.testing.assert_array_equal(lg, np.stack(ref))
+    assert list(codes) == c
+    W2 = rng.standard_normal((g.vocab, g.hidden))
+    o2 = Oracle(g, {**w, "codec_head": W2})
+    _, a = OracleCache(o, 1, 10).prefill(0, emb, W2)
+    _, b = OracleCache(o2, 1, 10).prefill(0, emb)
+    np.testing.assert_array_equal(a, b)
+
+
 def test_q8_0_hand_block():
     """Block 0..31: d = 31/127 -> fp16 0.244140625; codes round(x * 127/31) half away from zero."""
     from oracle import q8_0_quantize, q8_0_dequantize
