@@ -312,15 +312,18 @@ def predictor_loop(torch, hbm):
     kv = sum(step_bytes(g, L)[1] for L in range(T0, T0 + n))
     per_frame = (n + 1) * wbytes + kv
     # the same frame as one CUDA graph, each step's input gathered on the device from the previous
-    # step's code (15 random bf16 code tables [V, H])
+    # step's code (15 random bf16 code tables [V, H]) and each code taken through its own output
+    # head (15 random bf16 heads [V, H], code j through head j mod 15)
     tables = [torch.randn(g.vocab, g.hidden, device="cuda").to(torch.bfloat16) for _ in range(n)]
+    heads = [(0.02 * torch.randn(g.vocab, g.hidden, device="cuda")).to(torch.bfloat16) for _ in range(15)]
+    step_heads = [heads[j % 15] for j in range(n + 1)]
     tk.set_code_tables(tables, True)
     codes = torch.empty(n + 1, device="cuda", dtype=torch.int32)
     steps = list(range(n))
     for _ in range(3):
-        tk.frame(pre, steps, codes)
+        tk.frame(pre, steps, codes, heads=step_heads)
     torch.cuda.synchronize()
-    sg = timed(torch, tk.stream, lambda: tk.frame(pre, steps, codes), frames)
+    sg = timed(torch, tk.stream, lambda: tk.frame(pre, steps, codes, heads=step_heads), frames)
     tk.close()
     return {"frames_per_s": 1.0 / s, "ms_per_frame": s * 1e3, "passes_per_frame": n + 1,
             "hbm_frac": per_frame / s / 1e9 / hbm,

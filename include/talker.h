@@ -184,21 +184,25 @@ talker_status talker_set_code_tables(talker_t *t, const void *const *tables, con
 talker_status talker_decode_codes(talker_t *t, const int32_t *ids, const float *overlay, int B, float *logits,
                                   float *hidden, int32_t *argmax);
 
-/* Whole frame of the code-predictor loop as one CUDA graph (the qwen3-tts code
- * predictor: a prefill, then steps whose input is the previous step's code):
- * prefill stream 0 with T0 rows emb [T0, H] f32 (e.g. the talker's final hidden
- * row written on the device through talker_decode's `hidden`, and a code row),
- * code 0 = greedy argmax of its last row; then n_steps decode steps, step i
- * reading the row code_i of the registered table table_of_step[i] (host int
- * array) and producing code i+1 = its argmax. The codes never leave the
- * device. Outputs: codes [n_steps + 1] int32 (required), logits
+/* Whole frame of the code-predictor loop as one CUDA graph (rightkit-qts
+ * "tts_transformer.rs", predict_remaining_codebooks_kv_with_cache: a prefill,
+ * then steps whose input is the previous step's code): prefill stream 0 with T0
+ * rows emb [T0, H] f32 (e.g. the talker's final hidden row written on the
+ * device through talker_decode's `hidden`, and a code row); code 0 = the
+ * greedy token of its last row through heads[0]; then n_steps decode steps,
+ * step i (generation step i + 1 on the page) reading row code_i of the
+ * registered table table_of_step[i] (host int array) and producing code i + 1
+ * = the greedy token of heads[i + 1]. heads is a HOST array of n_steps + 1
+ * device pointers [vocab, H] in weight_dtype (the predictor's per-codebook
+ * output heads), or NULL to use codec_head for every code. The codes never
+ * leave the device. Outputs: codes [n_steps + 1] int32 (required), logits
  * [n_steps + 1, vocab] f32 (may be NULL). Afterwards stream 0's length is
  * T0 + n_steps. The graph is captured once and replayed while T0, n_steps,
- * the pointers and the tables stay the same. Errors: EINVAL (bad sizes or
- * table index), EOVERFLOW (T0 + n_steps > max_seq_len), ESTATE (no cache or no
- * code tables), ECUDA. */
+ * the pointers, the tables and the heads stay the same. Errors: EINVAL (bad
+ * sizes, table index or a NULL head), EOVERFLOW (T0 + n_steps > max_seq_len),
+ * ESTATE (no cache or no code tables), ECUDA. */
 talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, const int *table_of_step,
-                           int32_t *codes, float *logits);
+                           const void *const *heads, int32_t *codes, float *logits);
 
 /* Test support: the prefill above, but writing every row's outputs:
  * hidden [T, H] (may be NULL) and logits [T, vocab] (required). */

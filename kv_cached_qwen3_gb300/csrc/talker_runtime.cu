@@ -345,6 +345,7 @@ struct ForwardOut {
     bool head_all_rows;  // logits/hidden for every row, else the last row only
     int inc_len;         // decode: bump cur_len[r] for every row after the step
     int rows_per_stream = 0;   // batched prefill: the last row of every stream (rows of T each)
+    const void *head_w = nullptr;   // output head [V, H] in place of codec_head (predictor steps)
 };
 
 // Enqueue the whole forward for `rows` rows: per layer QKV (+QK-norm, RoPE, KV
@@ -466,7 +467,7 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
     h.eps = t->c.rms_eps;
     h.rows = hrows;
     h.status = t->d_status;
-    h.W = t->head;
+    h.W = out.head_w ? out.head_w : t->head;
     h.act = out.head_all_rows ? t->x : t->x + (size_t)(rows - 1) * t->H;
     h.act_ld = t->H;
     h.norm_w = t->fnorm;
@@ -605,7 +606,7 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
     h.eps = t->c.rms_eps;
     h.rows = hrows;
     h.status = t->d_status;
-    h.W = t->head;
+    h.W = out.head_w ? out.head_w : t->head;
     h.act = out.head_all_rows ? t->x : t->x + (size_t)((rps > 0 ? rps : T) - 1) * t->H;
     h.act_ld = (!out.head_all_rows && rps > 0) ? rps * t->H : t->H;
     h.norm_w = t->fnorm;
@@ -994,12 +995,16 @@ talker_status talker_set_code_tables(talker_t *t, const void *const *tables, con
 }
 
 talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, const int *table_of_step,
-                           int32_t *codes, float *logits) {
+                           const void *const *heads, int32_t *codes, float *logits) {
     if (!t) return TALKER_EINVAL;
     if (t->n_streams == 0 || t->codes.n == 0) return TALKER_ESTATE;
     if (!emb || !codes || T0 < 1 || n_steps < 0 || (n_steps > 0 && !table_of_step)) return TALKER_EINVAL;
     for (int i = 0; i < n_steps; ++i)
         if (table_of_step[i] < 0 || table_of_step[i] >= t->codes.n) return TALKER_EINVAL;
+    if (heads)
+        for (int i = 0; i <= n_steps; ++i)
+            if (!heads[i]) return TALKER_EINVAL;
+    auto head_of = [&](int i) -> const void * { return heads ? heads[i] : t->head; };
     if (T0 > t->max_seq || n_steps > t->max_seq - T0) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));
     const bool tc_pre = t->kv_q8 || (T0 >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t));
@@ -1019,6 +1024,7 @@ talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, c
     }
     std::vector<const void *> key = {emb, codes, logits};
     for (int i = 0; i < n_steps; ++i) key.push_back(t->codes.table[table_of_step[i]]);
+    for (int i = 0; i <= n_steps; ++i) key.push_back(head_of(i));
     if (!(t->frame_exec && t->frame_T0 == T0 && t->frame_steps == n_steps && t->frame_key == key)) {
         if (t->frame_exec) cudaGraphExecDestroy(t->frame_exec);
         t->frame_exec = nullptr;
@@ -1029,6 +1035,7 @@ talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, c
         {   // prefill of stream 0 from position 0; code 0 = its argmax
             RowMap rm{1, 0, 0, t->d_len};
             ForwardOut out{logits ? logits : t->frame_logits, nullptr, codes, false, 0};
+            out.head_w = head_of(0);
             st = tc_pre ? enqueue_tc(t, t->cap_st, T0, rm, emb, 1, out, &nk)
                         : enqueue_forward(t, t->cap_st, T0, rm, emb, 1, out, &nk);
             if (st == TALKER_OK) st = from_cuda(launch_set_len(t->d_len, 0, T0, t->cap_st));
@@ -1049,6 +1056,7 @@ talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, c
             const int splits = t->attn_cluster ? kAttnClusterMax : decode_splits(t, 1);
             RowMap rm{0, 0, 0, t->d_len};
             ForwardOut out{logits ? logits + (size_t)(i + 1) * t->V : t->frame_logits, nullptr, codes + i + 1, false, 1};
+            out.head_w = head_of(i + 1);
             if (st == TALKER_OK) st = enqueue_forward(t, t->cap_st, 1, rm, t->code_emb, splits, out, &nk);
         }
         cudaError_t e = cudaStreamEndCapture(t->cap_st, &graph);

@@ -69,7 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "talker_cur_len": (st, [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
         "talker_prefill": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
         "talker_prefill_append": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
-        "talker_frame": (st, [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int), vp, vp]),
+        "talker_frame": (st, [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(vp),
+                              vp, vp]),
         "talker_prefill_batched": (st, [vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]),
         "talker_set_logit_suppression": (st, [vp, ctypes.c_int, ctypes.c_int]),
         "talker_set_code_tables": (st, [vp, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_int), ctypes.c_int,
@@ -246,12 +247,19 @@ class Talker:
                                                  _ptr(argmax)), "talker_decode_codes")
         return logits, hidden, argmax
 
-    def frame(self, emb, table_of_step, codes, logits=None):
+    def frame(self, emb, table_of_step, codes, logits=None, heads=None):
         """emb [T0, H] f32 cuda; table_of_step: list of table indices (one per step); codes int32 cuda
-        [n_steps + 1]; logits f32 cuda [n_steps + 1, V] or None."""
+        [n_steps + 1]; logits f32 cuda [n_steps + 1, V] or None; heads: None (codec_head for every
+        code) or a list of n_steps + 1 cuda tensors [V, H] in the weight dtype (heads[0] for the
+        prefill's code, heads[i + 1] for step i's)."""
         n = len(table_of_step)
         arr = (ctypes.c_int * max(1, n))(*table_of_step)
-        self._check(self.lib.talker_frame(self.h, _ptr(emb), emb.shape[0], n, arr, _ptr(codes), _ptr(logits)),
+        hp = None
+        if heads is not None:
+            if len(heads) != n + 1:
+                raise ValueError("frame: need n_steps + 1 heads")
+            hp = (ctypes.c_void_p * (n + 1))(*[h.data_ptr() for h in heads])
+        self._check(self.lib.talker_frame(self.h, _ptr(emb), emb.shape[0], n, arr, hp, _ptr(codes), _ptr(logits)),
                     "talker_frame")
 
     def set_decode_mode(self, mode: int):

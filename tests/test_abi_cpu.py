@@ -89,7 +89,7 @@ def test_later_entry_points_reject_null_handles_and_off_grid_shapes(lib):
     assert lib.talker_set_logit_suppression(None, 0, 0) == 1
     assert lib.talker_set_code_tables(None, None, None, 0, 0) == 1
     assert lib.talker_decode_codes(None, None, None, 1, None, None, None) == 1
-    assert lib.talker_frame(None, None, 2, 1, None, None, None) == 1
+    assert lib.talker_frame(None, None, 2, 1, None, None, None, None) == 1
     assert lib.talker_kv_import(None, 0, None, None, 0) == 1
     assert lib.talker_kv_export(None, 0, None, None, 0) == 1
     for mode in (0, 2, 3, 4, 1, 5, -1):

@@ -167,3 +167,44 @@ def test_export_round_trip_and_prefill_rewinds(cuda, tiny):
     check_rows(host(lg), rl, bf16=False, what="second prefill logits")
     assert tk.sync_status() == 0
     tk.close()
+
+
+@pytest.mark.parametrize("wdt", ["f32", "bf16"])
+def test_fused_argmax_tie_goes_to_lowest_index(cuda, wdt):
+    """Two codec_head rows made identical (in different CTAs of the head kernel) give bit-equal
+    maximal logits; the fused argmax of prefill and decode must return the lower index."""
+    from kv_cached_qwen3_gb300.talker import Talker
+    g = inputs.Geometry(**{**inputs.TINY.__dict__, "weight_dtype": wdt, "kv_dtype": wdt})
+    w = inputs.make_weights(g, 47)
+    emb = inputs.make_embeddings(g, 47, 0, 20)
+    hid, ref_logits = Oracle(g, w).forward_full(emb[:17])
+    lo, hi = 3, 200
+    # rows lo and hi both = a * y15 + b * y16 with y the final hidden rows of the prefill's last
+    # row (15) and of the decode row (16), solved so that both logits are 3x the largest other
+    # logit at both steps: the two rows win by a wide margin and are equal bit for bit
+    y15, y16 = hid[15], hid[16]
+    target = 3.0 * float(np.abs(ref_logits[15:17]).max())
+    G = np.array([[y15 @ y15, y16 @ y15], [y15 @ y16, y16 @ y16]])
+    a, b = np.linalg.solve(G, [target, target])
+    big = (a * y15 + b * y16).astype(np.float32)
+    if wdt == "bf16":
+        big = inputs.round_to_bf16(big)
+    head = np.array(w["codec_head"], copy=True)
+    head[lo] = big
+    head[hi] = big
+    w2 = dict(w)
+    w2["codec_head"] = head
+    tk = Talker(g, w2)
+    tk.kv_init_batched(1, 32)
+    _, lg, am = tk.prefill(0, dev(emb[:16]))
+    lgh = host(lg)
+    assert lgh[lo] == lgh[hi] and lgh[lo] == lgh.max()
+    assert int(host(am)[0]) == lo
+    out_l = torch.empty(1, g.vocab, device="cuda")
+    out_a = torch.empty(1, device="cuda", dtype=torch.int32)
+    tk.decode(dev(emb[16:17]), out_l, None, out_a)
+    d = host(out_l)[0]
+    assert d[lo] == d[hi] and d[lo] == d.max()
+    assert int(out_a.cpu()[0]) == lo
+    assert tk.sync_status() == 0
+    tk.close()

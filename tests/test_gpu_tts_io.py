@@ -9,8 +9,8 @@ import numpy as np
 import pytest
 
 from kv_cached_qwen3_gb300 import inputs
-from oracle import Oracle, OracleCache, embed_codes, suppress_logits
-from parity_util import check_rows
+from oracle import Oracle, OracleCache, code_predictor_frame, embed_codes, suppress_logits
+from parity_util import TOL_TOP1, check_rows
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -135,11 +135,22 @@ def test_decode_from_codebook_ids(cuda, bf16):
     tk.close()
 
 
+def top2_margin(row):
+    """Gap between the largest and the second largest finite logit of a row."""
+    f = np.sort(row[np.isfinite(row)])
+    return float(f[-1] - f[-2])
+
+
 @pytest.mark.parametrize("suppress", [False, True])
 def test_whole_frame_graph_predictor(cuda, suppress):
-    """Prefill T=2 + 15 device-fed steps in one graph on the predictor geometry, replayed for a
-    second frame. The oracle follows the GPU's codes (teacher forcing): every step's logits
-    against the oracle, every code = argmax of the GPU's own logits, top-1 agreement."""
+    """Prefill T=2 + 15 device-fed steps in one graph on the predictor geometry, replayed for
+    8 frames, with a separate output head per code (head j mod 15 for code j: the predictor's
+    per-codebook heads). The oracle follows the GPU's codes (teacher forcing): every step's
+    logits against the oracle, every code = the argmax of the GPU's own logits, and top-1
+    agreement >= 99% over the steps that the logits tolerance decides. A step is undecided
+    when the oracle's top-2 margin is at most twice the step's largest logit error
+    max |L_gpu - L_oracle|: only there can two logits within that error swap order. Undecided
+    steps are counted and the margin distribution is printed."""
     from kv_cached_qwen3_gb300.talker import Talker
     pl = inputs.WORKLOADS["predictor_loop"]
     g = pl.geometry
@@ -148,9 +159,13 @@ def test_whole_frame_graph_predictor(cuda, suppress):
     n_tables = 15
     tables = [inputs.round_to_bf16(rng.standard_normal((g.vocab, g.hidden)).astype(np.float32))
               for _ in range(n_tables)]
+    heads = [inputs.round_to_bf16((0.02 * rng.standard_normal((g.vocab, g.hidden))).astype(np.float32))
+             for _ in range(15)]
     tdev = [dev(t).to(torch.bfloat16) for t in tables]
+    hdev = [dev(h).to(torch.bfloat16) for h in heads]
     T0, n = pl.prefill_T, pl.decode_steps
     steps = list(range(n))                       # step i reads table i
+    head_of = [j % 15 for j in range(n + 1)]     # code j through head j mod 15
     tk = Talker(g, w)
     tk.set_code_tables(tdev, True)
     if suppress:
@@ -160,27 +175,33 @@ def test_whole_frame_graph_predictor(cuda, suppress):
     codes = torch.empty(n + 1, device="cuda", dtype=torch.int32)
     lg = torch.empty(n + 1, g.vocab, device="cuda")
     o = Oracle(g, w)
-    agree = []
-    for frame in range(2):
+    agree, decided, margins = [], [], []
+    for frame in range(8):
         emb = inputs.make_embeddings(g, pl.seed, 0, T0, stream=frame)
         emb_dev.copy_(dev(emb))
-        tk.frame(emb_dev, steps, codes, lg)
+        tk.frame(emb_dev, steps, codes, lg, heads=[hdev[j] for j in head_of])
         assert tk.cur_len(0) == T0 + n
         c, L = host(codes).astype(np.int64), host(lg)
         np.testing.assert_array_equal(c, np.argmax(L, axis=-1))
-        oc = OracleCache(o, 1, T0 + n + 1)
-        _, rl = oc.prefill(0, emb)
-        ref = [rl]
-        for i in range(n):
-            _, r = oc.decode(tables[steps[i]][c[i]][None])
-            ref.append(r[0])
-        ref = np.stack(ref)
+        ref, _ = code_predictor_frame(OracleCache(o, 1, T0 + n + 1), emb, tables, steps,
+                                      [heads[j] for j in head_of], codes=c)
         if suppress:
             check_suppressed(L, suppress_logits(ref, 1024, 2047), True, "frame %d" % frame)
             ref = suppress_logits(ref, 1024, 2047)
         else:
             check_rows(L, ref, bf16=True, what="frame %d logits" % frame)
-        agree.append(np.argmax(ref, axis=-1) == c)
-    assert np.mean(np.concatenate(agree)) >= 0.93      # near-ties may differ; the GPU's own argmax is exact
+        for j in range(n + 1):
+            fin = np.isfinite(ref[j])
+            err = float(np.abs(L[j][fin] - ref[j][fin]).max())
+            m = top2_margin(ref[j])
+            margins.append(m)
+            decided.append(m > 2.0 * err)
+            agree.append(int(np.argmax(ref[j])) == c[j])
+    agree, decided, margins = np.array(agree), np.array(decided), np.array(margins)
+    print("frame top-1: %d/%d agree overall, %d undecided steps; oracle top-2 margin min %.2e median %.2e"
+          % (agree.sum(), agree.size, (~decided).sum(), margins.min(), np.median(margins)))
+    assert decided.sum() >= 0.9 * decided.size
+    assert np.mean(agree[decided]) >= TOL_TOP1
+    assert np.all(agree[decided])             # within the error no decided step can flip
     assert tk.sync_status() == 0
     tk.close()

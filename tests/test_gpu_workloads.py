@@ -147,3 +147,62 @@ def test_long_context_prefill_4096_tensor_cores(cuda, talker_long):
     check_rows(hid, rh, bf16=True, what="prefill 4096 hidden")
     check_rows(lg, rl, bf16=True, what="prefill 4096 logits")
     assert top1_agreement(lg, rl) >= TOL_TOP1
+
+
+def stream_cache(g, seed, s, L):
+    """Stream s's pre-filled cache of L rows, fp32 [n_layers, n_kv, L, hd] (bf16-valued)."""
+    ks, vs = zip(*(inputs.make_kv_layer(g, seed, l, L, stream=s) for l in range(g.n_layers)))
+    return np.stack(ks), np.stack(vs)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", [pytest.param(0, id="auto"), pytest.param(2, id="gemv-graph")])
+def test_batched16_full_size(cuda, mode):
+    """The 16-stream batched decode at its own size: the 28-layer Talker, start lengths drawn
+    U{128..2048} (the workload's seed), per-stream causal windows, 8 decode steps. Every stream
+    against the oracle (its own cache and rows) at the bf16 tolerances; top-1 >= 99% over all
+    stream-steps; lengths advance exactly."""
+    from kv_cached_qwen3_gb300.talker import Talker
+    from oracle import OracleCache
+    wl = inputs.WORKLOADS["batched16"]
+    g, seed, B = wl.geometry, wl.seed, wl.n_streams
+    w = inputs.make_weights(g, seed)
+    lens = inputs.make_start_lengths(seed, B, *wl.start_len_range)
+    steps = 8
+    max_seq = int(lens.max()) + steps + 1
+    tk = Talker(g, w)
+    tk.set_decode_mode(mode)
+    tk.kv_init_batched(B, max_seq)
+    for s in range(B):
+        K, V = stream_cache(g, seed, s, int(lens[s]))
+        tk.kv_import(s, torch.from_numpy(K).to(torch.bfloat16).cuda(), torch.from_numpy(V).to(torch.bfloat16).cuda(),
+                     int(lens[s]))
+        del K, V
+    embs = [inputs.make_embeddings(g, seed, int(lens[s]), int(lens[s]) + steps, stream=s) for s in range(B)]
+    lg = torch.empty(B, g.vocab, device="cuda")
+    hd = torch.empty(B, g.hidden, device="cuda")
+    am = torch.empty(B, device="cuda", dtype=torch.int32)
+    got_h, got_l = [], []
+    for t in range(steps):
+        tk.decode(dev(np.stack([embs[s][t] for s in range(B)])), lg, hd, am)
+        got_h.append(host(hd))
+        got_l.append(host(lg))
+        np.testing.assert_array_equal(host(am).astype(np.int64), np.argmax(got_l[-1], axis=-1))
+    assert tk.sync_status() == 0
+    assert [tk.cur_len(s) for s in range(B)] == [int(L) + steps for L in lens]
+    tk.close()
+    got_h, got_l = np.stack(got_h), np.stack(got_l)      # [steps, B, *]
+    o = Oracle(g, w)
+    ref_l = np.empty_like(got_l, dtype=np.float64)
+    for s in range(B):
+        oc = OracleCache(o, 1, max_seq)
+        K, V = stream_cache(g, seed, s, int(lens[s]))
+        oc.kv_import(0, K, V, int(lens[s]))
+        del K, V
+        for t in range(steps):
+            rh, rl = oc.decode(embs[s][t:t + 1])
+            ref_l[t, s] = rl[0]
+            check_rows(got_h[t, s], rh[0], bf16=True, what="stream %d (L=%d) step %d hidden" % (s, lens[s], t))
+            check_rows(got_l[t, s], rl[0], bf16=True, what="stream %d (L=%d) step %d logits" % (s, lens[s], t))
+    agree = top1_agreement(got_l.reshape(-1, g.vocab), ref_l.reshape(-1, g.vocab))
+    assert agree >= TOL_TOP1, agree
