@@ -10,7 +10,7 @@ import pytest
 
 from kv_cached_qwen3_gb300 import inputs
 from oracle import Oracle, decode_row_lazy_cache
-from parity_util import check_rows, top1_agreement, TOL_TOP1
+from parity_util import assert_top1, check_rows, top1_agreement, TOL_TOP1
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -161,7 +161,8 @@ def test_batched16_full_size(cuda, mode):
     """The 16-stream batched decode at its own size: the 28-layer Talker, start lengths drawn
     U{128..2048} (the workload's seed), per-stream causal windows, 8 decode steps. Every stream
     against the oracle (its own cache and rows) at the bf16 tolerances; top-1 >= 99% over all
-    stream-steps; lengths advance exactly."""
+    stream-steps that the logits tolerance decides (the near-tie rule of parity_util);
+    lengths advance exactly."""
     from kv_cached_qwen3_gb300.talker import Talker
     from oracle import OracleCache
     wl = inputs.WORKLOADS["batched16"]
@@ -204,5 +205,4 @@ def test_batched16_full_size(cuda, mode):
             ref_l[t, s] = rl[0]
             check_rows(got_h[t, s], rh[0], bf16=True, what="stream %d (L=%d) step %d hidden" % (s, lens[s], t))
             check_rows(got_l[t, s], rl[0], bf16=True, what="stream %d (L=%d) step %d logits" % (s, lens[s], t))
-    agree = top1_agreement(got_l.reshape(-1, g.vocab), ref_l.reshape(-1, g.vocab))
-    assert agree >= TOL_TOP1, agree
+    assert_top1(got_l.reshape(-1, g.vocab), ref_l.reshape(-1, g.vocab), "batched16 full size")
