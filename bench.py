@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="profiling aid: run `--steps` prefills of T rows on the Talker geometry and print their time")
+    ap.add_argument("--batched-only", action="store_true",
+                    help="profiling aid: run `--steps` 16-stream decode steps (start lengths U{128..2048}) and "
+                         "print their time")
     return ap.parse_args()
 
 
@@ -472,6 +475,30 @@ def prefill_only(T, steps, warmup):
     return out
 
 
+def batched_only(steps, warmup):
+    """16-stream decode steps on the Talker geometry (the batched workload's start lengths)."""
+    import torch
+    from kv_cached_qwen3_gb300.talker import Talker
+    b = inputs.WORKLOADS["batched16"]
+    g = b.geometry
+    lens = inputs.make_start_lengths(b.seed, b.n_streams, *b.start_len_range)
+    tk = Talker(g, inputs.make_weights(g, b.seed))
+    tk.kv_init_batched(b.n_streams, int(lens.max()) + steps + warmup + 1)
+    for s_ in range(b.n_streams):
+        kk = torch.randn(g.n_layers, g.n_kv_heads, int(lens[s_]), g.head_dim, device="cuda").to(torch.bfloat16)
+        tk.kv_import(s_, kk, kk, int(lens[s_]))
+        del kk
+    eb = torch.randn(b.n_streams, g.hidden, device="cuda")
+    lg = torch.empty(b.n_streams, g.vocab, device="cuda")
+    for _ in range(warmup):
+        tk.decode(eb, lg)
+    torch.cuda.synchronize()
+    s = timed(torch, tk.stream, lambda: tk.decode(eb, lg), steps)
+    out = {"batched_only": {"streams": int(b.n_streams), "ms_per_step": s * 1e3, "status": tk.sync_status()}}
+    tk.close()
+    return out
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
@@ -488,6 +515,9 @@ def main():
         return
     if args.prefill_only:
         print(json.dumps(prefill_only(args.prefill_only, max(1, args.steps), max(1, args.warmup))))
+        return
+    if args.batched_only:
+        print(json.dumps(batched_only(max(1, args.steps), max(1, args.warmup))))
         return
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:

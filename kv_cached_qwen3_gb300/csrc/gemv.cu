@@ -112,12 +112,31 @@ __device__ void finish_head(const GemvParams &p, int hidx, int row0, int nrows) 
     }
 }
 
+__device__ __forceinline__ float4 ld_cluster_v4(const float *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// EPI_SWIGLU_DOWN: CTAs whose down-projection partials are summed on chip, and the widest
+// down output a CTA's threads cover (four outputs per thread).
+constexpr int kFuseCluster = 8;
+constexpr int kFuseMaxOut2 = 4 * kGemvThreads;
+
 // VPL: 16-byte weight vectors a lane holds in flight per weight row (sized to K at
 // launch, so that short rows leave registers free and more CTAs fit on an SM).
 template <typename WT, int ROWS, int EPI, int VPL>
 __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
     constexpr int EPV = Elem<WT>::kPerVec;
-    constexpr int NW = (EPI == EPI_SWIGLU) ? 2 : 1;
+    constexpr bool FUSED = (EPI == EPI_SWIGLU_DOWN);
+    constexpr int NW = (EPI == EPI_SWIGLU || FUSED) ? 2 : 1;
     constexpr int MAXC = VPL;
     constexpr bool NORM = (EPI != EPI_RESID);
     extern __shared__ __align__(16) float act_s[];
@@ -137,6 +156,19 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
     const WT *wrow = static_cast<const WT *>(p.W) + (size_t)(NW * (fvalid ? f : 0)) * K;
 
     pdl_launch_dependents();
+
+    // FUSED: this thread's down-projection weights W2[j][f0 .. f0 + 7] (j = tid + 256 i), 16 bytes
+    // each; the cluster's 8 CTAs cover 128 contiguous bytes of every row j
+    uint4 wd[FUSED ? 4 : 1];
+    if constexpr (FUSED) {
+        const int f0 = blockIdx.x * kGemvWarps;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = threadIdx.x + kGemvThreads * i;
+            wd[i] = (j < p.n_out2) ? ldg_stream(static_cast<const __nv_bfloat16 *>(p.W2) + (size_t)j * p.n_out + f0)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 
     float acc[NW][ROWS];
 #pragma unroll
@@ -260,12 +292,71 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
             hv_s[warp][r] = (fvalid && r < nrows) ? v0 : -INFINITY;
             hi_s[warp][r] = f;
         }
-        if (lane == r && r < nrows && fvalid) {
+        if (FUSED) {
+            if (lane == r) hv_s[warp][r] = (r < nrows && fvalid) ? silu_f(v0) * v1 : 0.f;
+        } else if (lane == r && r < nrows && fvalid) {
             float *o = p.out + (size_t)(row0 + r) * p.out_ld + f;
-            if (EPI == EPI_RESID) *o = resid + v0;
-            else if (EPI == EPI_SWIGLU) *o = silu_f(v0) * v1;
-            else *o = v0;
+            if (EPI == EPI_RESID) {
+                *o = resid + v0;
+                if (p.out2 != nullptr) p.out2[(size_t)(row0 + r) * p.out_ld + f] = resid + v0;
+            } else if (EPI == EPI_SWIGLU) {
+                *o = silu_f(v0) * v1;
+            } else {
+                *o = v0;
+            }
         }
+    }
+
+    if constexpr (FUSED) {
+        // partial down products of this CTA's 8 activations a[f0 .. f0 + 7] for every output j
+        // ("talker-forward.h", talker_layer_forward MLP: down(silu(gate) * up)), kept in shared
+        // memory; the cluster's 8 CTAs then sum them (rank k owns outputs [k n2/8, (k+1) n2/8))
+        // and reduce-add the sums into red_out, which holds the residual stream
+        __syncthreads();
+        const int n2 = p.n_out2;
+        float *part_s = act_s + ROWS * K;   // [ROWS][n2]
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            if (r < nrows) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = threadIdx.x + kGemvThreads * i;
+                    if (j < n2) {
+                        const uint4 u = wd[i];
+                        float t = bf16lo(u.x) * hv_s[0][r];
+                        t = fmaf(bf16hi(u.x), hv_s[1][r], t);
+                        t = fmaf(bf16lo(u.y), hv_s[2][r], t);
+                        t = fmaf(bf16hi(u.y), hv_s[3][r], t);
+                        t = fmaf(bf16lo(u.z), hv_s[4][r], t);
+                        t = fmaf(bf16hi(u.z), hv_s[5][r], t);
+                        t = fmaf(bf16lo(u.w), hv_s[6][r], t);
+                        t = fmaf(bf16hi(u.w), hv_s[7][r], t);
+                        part_s[r * n2 + j] = t;
+                    }
+                }
+            }
+        }
+        cluster_sync_all();
+        uint32_t rank;
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+        const int per = n2 / kFuseCluster, per4 = per / 4;
+        for (int idx = threadIdx.x; idx < nrows * per4; idx += kGemvThreads) {
+            const int r = idx / per4, j = (int)rank * per + (idx - r * per4) * 4;
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < kFuseCluster; ++c) {
+                const float4 v = ld_cluster_v4(part_s + r * n2 + j, (uint32_t)c);
+                t.x += v.x;
+                t.y += v.y;
+                t.z += v.z;
+                t.w += v.w;
+            }
+            float *o = p.red_out + (size_t)(row0 + r) * n2 + j;
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(o), "f"(t.x), "f"(t.y), "f"(t.z),
+                         "f"(t.w)
+                         : "memory");
+        }
+        cluster_sync_all();   // peers read this CTA's partials: keep its shared memory until they are done
     }
 
     if (EPI == EPI_QKV && p.q_out != nullptr) {
@@ -382,11 +473,22 @@ static cudaError_t launch_vpl(const GemvParams &p, cudaStream_t st, bool pdl) {
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
     cfg.dynamicSmemBytes = gemv_smem_bytes(ROWS, p.K);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (EPI == EPI_SWIGLU_DOWN) {
+        if (grid.x % kFuseCluster || p.n_out % kGemvWarps || p.n_out2 % (4 * kFuseCluster) ||
+            p.n_out2 > kFuseMaxOut2 || p.W2 == nullptr || p.red_out == nullptr)
+            return cudaErrorInvalidValue;
+        cfg.dynamicSmemBytes += (size_t)ROWS * p.n_out2 * sizeof(float);
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = kFuseCluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, k_gemv<WT, ROWS, EPI, VPL>, p);
 }
 
@@ -413,6 +515,9 @@ static cudaError_t launch_rows(int epi, const GemvParams &p, cudaStream_t st, bo
         case EPI_RESID: return launch_one<WT, ROWS, EPI_RESID>(p, st, pdl);
         case EPI_SWIGLU: return launch_one<WT, ROWS, EPI_SWIGLU>(p, st, pdl);
         case EPI_HEAD: return launch_one<WT, ROWS, EPI_HEAD>(p, st, pdl);
+        case EPI_SWIGLU_DOWN:
+            if constexpr (sizeof(WT) == 2) return launch_one<WT, ROWS, EPI_SWIGLU_DOWN>(p, st, pdl);
+            return cudaErrorInvalidValue;
     }
     return cudaErrorInvalidValue;
 }
@@ -441,6 +546,9 @@ static cudaError_t raise_vpl() {
     e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_SWIGLU, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      bytes);
     e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_HEAD, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if constexpr (sizeof(WT) == 2)
+        e = e ? e : cudaFuncSetAttribute(k_gemv<WT, ROWS, EPI_SWIGLU_DOWN, VPL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     return e;
 }
 

@@ -13,7 +13,8 @@ enum Epilogue : int {
     EPI_QKV = 0,     // raw q|k|v rows; the CTA that completes a head applies QK-norm, RoPE, KV append
     EPI_RESID = 1,   // out[r][f] += acc (residual stream)
     EPI_SWIGLU = 2,  // rows 2j (gate) and 2j+1 (up): out[r][j] = silu(gate) * up
-    EPI_HEAD = 3     // logits, final hidden, argmax (last CTA), decode length bump
+    EPI_HEAD = 3,    // logits, final hidden, argmax (last CTA), decode length bump
+    EPI_SWIGLU_DOWN = 4   // SwiGLU, then this CTA's share of the down projection reduce-added into red_out
 };
 
 // Where row r of a launch sits. mode 0 (decode): stream r at position cur_len[r].
@@ -61,6 +62,10 @@ struct GemvParams {
     float *out;          // epilogue destination, row stride out_ld
     int out_ld;
     float *copy_x;       // optional: CTA column 0 copies the raw input rows here (residual init)
+    float *out2;         // EPI_RESID: optional second destination of the same sums
+    const void *W2;      // EPI_SWIGLU_DOWN: down weights [n_out2][n_out] (bf16)
+    float *red_out;      // EPI_SWIGLU_DOWN: [rows][n_out2], reduce-added (holds the residual)
+    int n_out2;
     // EPI_QKV
     int layer, n_q, n_kv, head_dim;
     const float *q_norm, *k_norm;

@@ -82,6 +82,7 @@ struct talker {
     // activations, sized for cap_rows rows
     int cap_rows = 0;
     float *x = nullptr, *raw = nullptr, *q = nullptr, *attn = nullptr, *act = nullptr;
+    float *x2 = nullptr;   // GEMV decode with the fused MLP: the residual stream (x: its post-attention copy)
     // workspaces
     size_t cap_attn_ws = 0, cap_head_part = 0;
     float *attn_ws = nullptr, *head_val = nullptr;
@@ -131,7 +132,7 @@ void free_ptr(void *p) {
 
 void free_workspaces(talker *t) {
     float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->attn_ws, &t->head_val, &t->code_emb,
-                    &t->frame_logits};
+                    &t->frame_logits, &t->x2};
     t->code_emb_rows = 0;
     for (auto pp : fl) {
         free_ptr(*pp);
@@ -197,9 +198,9 @@ talker_status ensure_capacity(talker *t, int rows, int splits) {
     drop_graphs(t);
     if (grow_rows) {
         const int cap = std::max(rows, 16);
-        float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act};
-        const int widths[] = {t->H, t->qkv_n, t->qd, t->qd, t->I};
-        for (int i = 0; i < 5; ++i) {
+        float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->x2};
+        const int widths[] = {t->H, t->qkv_n, t->qd, t->qd, t->I, t->H};
+        for (int i = 0; i < 6; ++i) {
             free_ptr(*fl[i]);
             *fl[i] = nullptr;
             TRY_CUDA(cudaMalloc(fl[i], (size_t)cap * widths[i] * sizeof(float)));
@@ -348,9 +349,13 @@ struct ForwardOut {
     const void *head_w = nullptr;   // output head [V, H] in place of codec_head (predictor steps)
 };
 
-// Enqueue the whole forward for `rows` rows: per layer QKV (+QK-norm, RoPE, KV
-// append), attention, o_proj + residual, gate/up SwiGLU, down + residual; then
-// the final norm + codec_head (+argmax). Returns the number of kernels enqueued
+// The GEMV path folds the down projection into the gate/up kernel (clusters of 8 CTAs sum their
+// partial products on chip) where the geometry allows: bf16 weights, I / 8 CTAs in whole
+// clusters, H a multiple of 32 and at most 1024 (four down outputs per thread).
+bool fuse_mlp_ok(const talker *t) {
+    return t->w_bf16 && t->x2 != nullptr && t->I % 64 == 0 && t->H % 32 == 0 && t->H <= 1024;
+}
+
 // Decode attention reads the raw q|k|v projections and finishes the heads itself.
 void set_raw_heads(const talker *t, const LayerDev &d, AttnParams &a) {
     a.raw = t->raw;
@@ -361,13 +366,20 @@ void set_raw_heads(const talker *t, const LayerDev &d, AttnParams &a) {
     a.eps = t->c.rms_eps;
 }
 
-// through *n_kernels.
+// Enqueue the whole forward for `rows` rows on the GEMV kernels: per layer QKV (+QK-norm,
+// RoPE, KV append), attention, o_proj + residual, gate/up SwiGLU, down + residual (the last
+// two in one kernel where fuse_mlp_ok); then the final norm + codec_head (+argmax). Returns
+// the number of kernels enqueued through *n_kernels.
 talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap &rm, const float *emb,
                               int splits, const ForwardOut &out, int *n_kernels) {
     const CacheView cv = cache_view(t);
     const int nh = t->c.n_layers;
     int nk = 0;
     bool pdl = false;  // the first kernel waits on everything before it in the stream
+    // Fused MLP (bf16 weights): the residual stream lives in x2; o_proj writes it to x too, and
+    // the gate/up kernel normalises x and reduce-adds its share of the down projection into x2.
+    const bool fuse = fuse_mlp_ok(t);
+    float *X = fuse ? t->x2 : t->x;
     for (int l = 0; l < nh; ++l) {
         const LayerDev &d = t->L[l];
         GemvParams p{};
@@ -376,14 +388,14 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
         p.status = t->d_status;
         // 1) RMSNorm -> [Wq;Wk;Wv] -> QK-norm, RoPE, KV append
         p.W = d.qkv;
-        p.act = (l == 0) ? emb : t->x;
+        p.act = (l == 0) ? emb : X;
         p.act_ld = t->H;
         p.norm_w = d.in_norm;
         p.K = t->H;
         p.n_out = t->qkv_n;
         p.out = t->raw;
         p.out_ld = t->qkv_n;
-        p.copy_x = (l == 0) ? t->x : nullptr;
+        p.copy_x = (l == 0) ? X : nullptr;
         p.layer = l;
         p.n_q = t->nq;
         p.n_kv = t->nkv;
@@ -428,10 +440,30 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
         o.act_ld = t->qd;
         o.K = t->qd;
         o.n_out = t->H;
-        o.out = t->x;
+        o.out = X;
+        o.out2 = fuse ? t->x : nullptr;
         o.out_ld = t->H;
         TRY_CUDA(launch_gemv(EPI_RESID, t->w_bf16, pick_rows(rows, t->qd), o, st, pdl));
         ++nk;
+        if (fuse) {
+            // 4+5) post-norm -> [Wg;Wu] -> SwiGLU -> down, partials summed per cluster into x2
+            GemvParams m{};
+            m.rows = rows;
+            m.status = t->d_status;
+            m.eps = t->c.rms_eps;
+            m.W = d.gu;
+            m.act = t->x;
+            m.act_ld = t->H;
+            m.norm_w = d.post_norm;
+            m.K = t->H;
+            m.n_out = t->I;
+            m.W2 = d.down;
+            m.n_out2 = t->H;
+            m.red_out = t->x2;
+            TRY_CUDA(launch_gemv(EPI_SWIGLU_DOWN, t->w_bf16, pick_rows(rows, t->H), m, st, pdl));
+            ++nk;
+            continue;
+        }
         // 4) post-norm -> [Wg;Wu] -> silu(gate) * up
         GemvParams m{};
         m.rows = rows;
@@ -468,7 +500,7 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
     h.rows = hrows;
     h.status = t->d_status;
     h.W = out.head_w ? out.head_w : t->head;
-    h.act = out.head_all_rows ? t->x : t->x + (size_t)(rows - 1) * t->H;
+    h.act = out.head_all_rows ? X : X + (size_t)(rows - 1) * t->H;
     h.act_ld = t->H;
     h.norm_w = t->fnorm;
     h.K = t->H;
