@@ -506,6 +506,7 @@ static cudaError_t launch_attn_t(const AttnParams &p, int rows, cudaStream_t st,
 }
 
 cudaError_t launch_attn(int kv_kind, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
+    if (attn_dec_keys_supported(kv_kind, head_dim, p)) return launch_attn_dec_keys(head_dim, p, rows, st, pdl);
     if (kv_kind == 2) {   // Q8_0 storage
         switch (head_dim) {
             case 64: return launch_attn_t<int8_t, 64>(p, rows, st, pdl);
@@ -543,7 +544,7 @@ cudaError_t prepare_attn() {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     e = e ? e : cudaFuncSetAttribute(k_attn_decode<int8_t, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     e = e ? e : cudaFuncSetAttribute(k_attn_decode<int8_t, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    return e;
+    return e ? e : prepare_attn_dec_keys();
 }
 
 }  // namespace talker_k

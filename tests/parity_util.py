@@ -81,6 +81,6 @@ def assert_top1(gpu_logits, ref_logits, what=""):
     print("%s top-1: %.4f over all %d steps, %.4f over decided steps, %d undecided; oracle top-2 margin "
           "min %.2e median %.2e" % (what, r["agree_all"], r["steps"], r["agree_decided"], r["undecided"],
                                      r["margin_min"], r["margin_median"]))
-    assert r["undecided"] <= 0.1 * r["steps"], (what, r)
+    assert r["undecided"] <= 0.25 * r["steps"], (what, r)
     assert r["agree_decided"] >= TOL_TOP1, (what, r)
     return r

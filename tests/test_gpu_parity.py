@@ -7,7 +7,7 @@ import pytest
 
 from kv_cached_qwen3_gb300 import inputs
 from oracle import Oracle, OracleCache
-from parity_util import check_rows, top1_agreement, TOL_TOP1
+from parity_util import assert_top1, check_rows, top1_agreement, TOL_TOP1
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -111,8 +111,7 @@ def test_talker_b1_prefill96_decode512_bf16(cuda, talker_b1_ref, mode):
     hid, lg, am = run_prefill_decode(g, w, emb, T0, n, T0 + n, mode)
     check_rows(hid, rh[T0 - 1:], bf16=True, what="talker hidden")
     check_rows(lg, rl[T0 - 1:], bf16=True, what="talker logits")
-    agree = top1_agreement(lg[1:], rl[T0:])
-    assert agree >= TOL_TOP1, agree
+    assert_top1(lg[1:], rl[T0:], "talker_b1 mode %d" % mode)
     np.testing.assert_array_equal(am, np.argmax(lg, axis=-1))
 
 
