@@ -90,8 +90,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         nk = max(0, min(per, nk_total - kb0));
     };
 
+    pdl_launch_dependents();
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer: one ring across all tiles of this CTA
+        // ---- TMA producer: one ring across all tiles of this CTA. The weight boxes of the
+        // first STAGES slots do not depend on the previous kernel: they are requested before
+        // the dependency wait, the activation boxes after it.
+        uint32_t pre = 0;
+        for (int t = cid; t < n_tiles && pre < (uint32_t)STAGES; t += n_ctas) {
+            int m0, n0, kb0, nk;
+            tile_of(t, m0, n0, kb0, nk);
+            for (int i = 0; i < nk && pre < (uint32_t)STAGES; ++i, ++pre) {
+                mbar_arrive_expect_tx(&full[pre], A_BYTES + B_BYTES);
+                tma_load_2d(sB + pre * B_BYTES, &map_b, (kb0 + i) * BK, n0, &full[pre]);
+            }
+        }
+        pdl_wait();
         uint32_t it = 0;
         bool ok = true;
         for (int t = cid; t < n_tiles && ok; t += n_ctas) {
@@ -99,6 +112,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tile_of(t, m0, n0, kb0, nk);
             for (int i = 0; i < nk; ++i, ++it) {
                 const int s = it % STAGES;
+                if (it < pre) {   // weights already requested
+                    tma_load_2d(sA + s * A_BYTES, &map_a, (kb0 + i) * BK, m0, &full[s]);
+                    continue;
+                }
                 if (it >= (uint32_t)STAGES && !mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, p.status)) {
                     fail_s = 1;
                     ok = false;
@@ -145,7 +162,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             umma_commit(&tfull[b]);   // arrives once this tile's MMAs have completed
         }
     } else if (warp >= 2) {
-        // ---- epilogue: TMEM lane quadrant (warp % 4) holds tile rows 32*(warp%4) .. +31
+        // ---- epilogue: TMEM lane quadrant (warp % 4) holds tile rows 32*(warp%4) .. +31;
+        // it writes (or reduce-adds into) buffers of the previous kernels: wait for them first
+        pdl_wait();
         const int q = warp & 3;
         float *stg = reinterpret_cast<float *>(sB + STAGES * B_BYTES) + q * 32 * 32;   // this warp's staging block
         int j = 0;
@@ -338,6 +357,11 @@ cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, const GemmP
     cfg.dynamicSmemBytes = smem_for(BN, STAGES);
     cfg.stream = st;
     cfg.gridDim = dim3(std::min(tiles, n_sm), 1, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, tc::k_gemm_tc_persist<BN, STAGES>, ma, mb, p, splits);
 }
 

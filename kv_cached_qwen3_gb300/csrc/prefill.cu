@@ -20,12 +20,30 @@ using namespace talker_dev;
 
 namespace talker_k {
 
+// Launch with programmatic dependent launch: the kernel starts while its predecessor drains
+// and waits for it (griddepcontrol.wait) before touching the predecessor's outputs.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // One CTA per row: every thread stages its float4s of the row (one round trip), the sum of
 // squares is reduced across the CTA, then the scaled bf16 row is written.
 __global__ void k_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H,
                                __nv_bfloat16 *out) {
     __shared__ float red[32];
     const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
     const float *xr = x + (size_t)row * ld;
     constexpr int MAXV = 4;   // float4s per thread (H <= 4 * 4 * blockDim.x)
     float4 v[MAXV];
@@ -61,6 +79,8 @@ __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd
                            RowMap rm, int *status, __nv_bfloat16 *dense_kv) {
     const int n_heads = n_q + 2 * n_kv;
     const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
     if (item >= rows * n_heads) return;
     const int r = item / n_heads, h = item - r * n_heads;
     const int half = hd >> 1;
@@ -157,6 +177,8 @@ __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd
 
 __global__ void k_swiglu_bf16(const float *gu, int rows, int I, __nv_bfloat16 *out) {
     const size_t n = (size_t)rows * I;
+    pdl_launch_dependents();
+    pdl_wait();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const size_t r = i / I, j = i - r * I;
         const float2 v = *reinterpret_cast<const float2 *>(gu + r * 2 * I + 2 * j);
@@ -168,8 +190,8 @@ cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float ep
                                 cudaStream_t st) {
     const int threads = 256;
     if (H % 4 || H > 4 * 4 * threads) return cudaErrorInvalidValue;
-    k_rmsnorm_bf16<<<rows, threads, 0, st>>>(x, ld, w, eps, rows, H, static_cast<__nv_bfloat16 *>(out));
-    return cudaGetLastError();
+    return launch_pdl(k_rmsnorm_bf16, dim3(rows), dim3(threads), st, x, ld, w, eps, rows, H,
+                      static_cast<__nv_bfloat16 *>(out));
 }
 
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
@@ -178,16 +200,14 @@ cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int h
     if (cache.kv_q8 && dense_kv == nullptr) return cudaErrorInvalidValue;
     const long long items = (long long)rows * (n_q + 2 * n_kv);
     const int per_block = 8;
-    k_qkv_post<<<(unsigned)((items + per_block - 1) / per_block), per_block * 32, 0, st>>>(
-        raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, rm, status, dense_kv);
-    return cudaGetLastError();
+    return launch_pdl(k_qkv_post, dim3((unsigned)((items + per_block - 1) / per_block)), dim3(per_block * 32), st,
+                      raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, rm, status, dense_kv);
 }
 
 cudaError_t launch_swiglu_bf16(const float *gu, int rows, int I, void *out, cudaStream_t st) {
     const size_t n = (size_t)rows * I;
     const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
-    k_swiglu_bf16<<<blocks, 256, 0, st>>>(gu, rows, I, static_cast<__nv_bfloat16 *>(out));
-    return cudaGetLastError();
+    return launch_pdl(k_swiglu_bf16, dim3(blocks), dim3(256), st, gu, rows, I, static_cast<__nv_bfloat16 *>(out));
 }
 
 }  // namespace talker_k

@@ -24,6 +24,13 @@ struct LayerDev {
     const void *qkv, *o, *gu, *down;
 };
 
+// A captured prefill (or batched prefill): replayed while every input of the key is the same.
+struct PrefillGraph {
+    std::vector<long long> key;
+    cudaGraphExec_t exec;
+    int n_kernels;
+};
+
 struct GraphEntry {
     int kind;   // 0: GEMV kernels, 1: tensor-core GEMMs
     int B;
@@ -92,6 +99,7 @@ struct talker {
     int *d_status = nullptr;
     int64_t launches = 0;
     std::vector<GraphEntry> graphs;
+    std::vector<PrefillGraph> pgraphs;
     int decode_mode = 0;                 // 0 auto, 2 GEMV graph, 3 tensor-core graph
     int attn_cluster = 0;   // decode attention: splits combine inside a thread-block cluster
     int prefill_mode = 0;                // 0 automatic, 2 always the GEMV kernels, 3 / 4 tensor-core GEMMs
@@ -121,6 +129,8 @@ namespace {
 void drop_graphs(talker *t) {
     for (auto &g : t->graphs) cudaGraphExecDestroy(g.exec);
     t->graphs.clear();
+    for (auto &g : t->pgraphs) cudaGraphExecDestroy(g.exec);
+    t->pgraphs.clear();
     if (t->frame_exec) cudaGraphExecDestroy(t->frame_exec);
     t->frame_exec = nullptr;
     t->frame_key.clear();
@@ -668,6 +678,41 @@ talker_status check_stream(const talker *t, int stream) {
     return TALKER_OK;
 }
 
+// Run `enqueue(stream, &n_kernels)` as a CUDA graph captured once per key and replayed
+// afterwards (the host then issues one launch instead of a few hundred, and the tensor maps
+// of the GEMMs are encoded once, at capture). Keeps the last kMaxGraphs prefill graphs.
+template <typename F>
+talker_status run_graph(talker *t, const std::vector<long long> &key, F enqueue) {
+    PrefillGraph *pg = nullptr;
+    for (auto &g : t->pgraphs)
+        if (g.key == key) pg = &g;
+    if (!pg) {
+        if ((int)t->pgraphs.size() >= kMaxGraphs) {
+            cudaGraphExecDestroy(t->pgraphs.front().exec);
+            t->pgraphs.erase(t->pgraphs.begin());
+        }
+        int nk = 0;
+        cudaGraph_t graph = nullptr;
+        TRY_CUDA(cudaStreamBeginCapture(t->cap_st, cudaStreamCaptureModeThreadLocal));
+        talker_status s = enqueue(t->cap_st, &nk);
+        cudaError_t e = cudaStreamEndCapture(t->cap_st, &graph);
+        if (s != TALKER_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return s;
+        }
+        if (e != cudaSuccess) return from_cuda(e);
+        cudaGraphExec_t exec = nullptr;
+        e = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return from_cuda(e);
+        t->pgraphs.push_back(PrefillGraph{key, exec, nk});
+        pg = &t->pgraphs.back();
+    }
+    TRY_CUDA(cudaGraphLaunch(pg->exec, t->st));
+    t->launches += pg->n_kernels;
+    return TALKER_OK;
+}
+
 // Prefill rows at positions pos0 .. pos0 + T - 1 of `stream` (pos0 = 0: talker_prefill;
 // pos0 = cur_len: talker_prefill_append).
 talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float *hidden, float *logits,
@@ -681,16 +726,19 @@ talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float
     TRY(ensure_capacity(t, T, 1));
     RowMap rm{1, stream, pos0, t->d_len};
     ForwardOut out{logits, hidden, all_rows ? nullptr : argmax, all_rows, 0};
-    int nk = 0;
     if (t->kv_q8 && !tc_usable(t)) return TALKER_EINVAL;
-    if (t->kv_q8 || (T >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t))) {   // Q8_0: always this path
-        TRY(ensure_tc(t, T));
-        TRY(enqueue_tc(t, t->st, T, rm, emb, 1, out, &nk));
-    } else {
-        TRY(enqueue_forward(t, t->st, T, rm, emb, 1, out, &nk));
-    }
-    TRY_CUDA(launch_set_len(t->d_len, stream, pos0 + T, t->st));
-    t->launches += nk + 1;
+    const bool tc = t->kv_q8 || (T >= kTcMinRows && t->prefill_mode != 2 && tc_usable(t));   // Q8_0: always tc
+    if (tc) TRY(ensure_tc(t, T));
+    const std::vector<long long> key = {0, tc, T, stream, pos0, all_rows, t->prefill_mode,
+                                        (long long)(uintptr_t)emb, (long long)(uintptr_t)hidden,
+                                        (long long)(uintptr_t)logits, (long long)(uintptr_t)out.argmax};
+    TRY(run_graph(t, key, [&](cudaStream_t st, int *nk) -> talker_status {
+        if (tc) TRY(enqueue_tc(t, st, T, rm, emb, 1, out, nk));
+        else TRY(enqueue_forward(t, st, T, rm, emb, 1, out, nk));
+        TRY_CUDA(launch_set_len(t->d_len, stream, pos0 + T, st));
+        ++*nk;
+        return TALKER_OK;
+    }));
     t->len[stream] = pos0 + T;
     return TALKER_OK;
 }
@@ -856,10 +904,15 @@ talker_status talker_prefill_batched(talker_t *t, int B, const float *emb, int T
     TRY(ensure_tc(t, rows));
     RowMap rm{1, 0, 0, t->d_len, T};
     ForwardOut out{logits_last, hidden_last, argmax_last, false, 0, T};
-    int nk = 0;
-    TRY(enqueue_tc(t, t->st, rows, rm, emb, 1, out, &nk));
-    for (int s = 0; s < B; ++s) TRY_CUDA(launch_set_len(t->d_len, s, T, t->st));
-    t->launches += nk + B;
+    const std::vector<long long> key = {1, B, T, t->prefill_mode, (long long)(uintptr_t)emb,
+                                        (long long)(uintptr_t)hidden_last, (long long)(uintptr_t)logits_last,
+                                        (long long)(uintptr_t)argmax_last};
+    TRY(run_graph(t, key, [&](cudaStream_t st, int *nk) -> talker_status {
+        TRY(enqueue_tc(t, st, rows, rm, emb, 1, out, nk));
+        for (int s = 0; s < B; ++s) TRY_CUDA(launch_set_len(t->d_len, s, T, st));
+        *nk += B;
+        return TALKER_OK;
+    }));
     for (int s = 0; s < B; ++s) t->len[s] = T;
     return TALKER_OK;
 }
