@@ -1,12 +1,13 @@
 // Causal prefill attention on the fifth-generation tensor cores, head_dim 128
-// ("qwentts.cpp/src/talker-forward.h", talker_layer_forward, attention step: query row r at
-// position r attends keys [0, r]; softmax of the scaled dot products, weighted sum of the
-// values). Used for a prefill from position 0 of one stream; other cases take the
-// mma.sync kernel.
+// ("qwentts.cpp/src/talker-forward.h", talker_layer_forward / talker_forward_core with
+// n_past: query row r of a call starting at position pos0 attends keys [0, pos0 + r]; softmax
+// of the scaled dot products, weighted sum of the values). One stream per launch: a prefill
+// from position 0, an appended chunk (pos0 > 0, the earlier keys read from the cache), or one
+// stream of a batched prefill.
 //
 // Per layer, k_kv_dense_tc first writes the KV group's keys densely, K [n_kv][L][128], and
-// its values transposed, V^T [n_kv][128][L] (L = keys rounded up to 128, zero rows past
-// the stream's length), so that both products read K-major operands.
+// its values transposed, V^T [n_kv][128][L] (L = pos0 + T keys rounded up to 128, zero rows
+// past them), so that both products read K-major operands.
 //
 // k_attn_prefill_tc: one CTA per 128 query rows of one q head (longest tiles first),
 // walking key blocks of 128:
@@ -67,6 +68,7 @@ struct Params {
     const float *q;        // [T][n_q * HD] f32, QK-normed and rotated, unscaled
     __nv_bfloat16 *out;    // [T][n_q * HD] bf16
     int T, n_q, group, Lpad;
+    int pos0;              // position of row 0 (keys [0, pos0 + T) are in the dense copy)
     float scale_log2;
     int *status;
 };
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int qt = n_qt - 1 - (int)blockIdx.x;
     const int h = blockIdx.y, kvh = h / p.group;
     const int last_row = min(p.T, (qt + 1) * BM) - 1;
-    const int nb = last_row / BN + 1;
+    const int nb = (p.pos0 + last_row) / BN + 1;
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -171,7 +173,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // takes keys 0..63 of each block and O columns 0..63, half 1 the other 64
         const int q4 = warp & 3, half = (warp - 2) >> 2;
         const int r = q4 * 32 + lane;
-        const int grow = qt * BM + r;   // row index = position (prefill from 0)
+        const int grow = qt * BM + r;   // row of the call
+        const int qpos = p.pos0 + grow;  // its position
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
         const int qd = p.n_q * HD;
         // exchange point of the warp pair: both warps' shared-memory writes before it are
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             tc::tc_fence_after();
             const int key0 = j * BN + half * 64;                 // first key of this half
-            const bool masked = j * BN + BN - 1 > qt * BM;       // the block reaches past the tile's first row
+            const bool masked = j * BN + BN - 1 > p.pos0 + qt * BM;   // the block reaches past the tile's first row
             const uint32_t sb = lane_base + (uint32_t)(b * 128 + half * 64);
             // pass 1: this half's row max over the keys this row may see (key <= position)
             float mx = -INFINITY;
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (masked) {
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
-                        if (key0 + c * 32 + t <= grow) mx = fmaxf(mx, v[t]);
+                        if (key0 + c * 32 + t <= qpos) mx = fmaxf(mx, v[t]);
                 } else {
 #pragma unroll
                     for (int t = 0; t < 32; ++t) mx = fmaxf(mx, v[t]);
@@ -276,8 +279,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int k = key0 + c * 32 + 2 * t;
                     float p0 = fast_exp2(v[2 * t] - m), p1 = fast_exp2(v[2 * t + 1] - m);
                     if (masked) {
-                        p0 = (k <= grow) ? p0 : 0.f;
-                        p1 = (k + 1 <= grow) ? p1 : 0.f;
+                        p0 = (k <= qpos) ? p0 : 0.f;
+                        p1 = (k + 1 <= qpos) ? p1 : 0.f;
                     }
                     ps += p0 + p1;
                     pk[t] = pack2(p0, p1);
@@ -379,8 +382,10 @@ int attn_prefill_tc_lpad(int nkeys) { return (nkeys + atc::BN - 1) / atc::BN * a
 
 bool attn_prefill_tc_supported(const AttnParams &a, int T) {
     const bool one_stream = a.rowmap.rows_per_stream == 0 || a.rowmap.rows_per_stream == T;
-    return a.rowmap.mode == 1 && a.rowmap.pos0 == 0 && one_stream && a.out_bf16 && a.cache.head_dim == atc::HD &&
-           (a.cache.kv_bf16 || (a.cache.kv_q8 && a.dense_k != nullptr)) && T >= 1;
+    // bf16 cache: any start position (the dense copy reads every key from the pages); Q8_0: the
+    // call's own rows from position 0 only (the dense bf16 copy of the call)
+    return a.rowmap.mode == 1 && one_stream && a.out_bf16 && a.cache.head_dim == atc::HD && T >= 1 &&
+           (a.cache.kv_bf16 || (a.cache.kv_q8 && a.dense_k != nullptr && a.rowmap.pos0 == 0));
 }
 
 cudaError_t prepare_attn_prefill_tc() {
@@ -390,7 +395,7 @@ cudaError_t prepare_attn_prefill_tc() {
 cudaError_t launch_attn_prefill_tc(const AttnParams &a, int T, __nv_bfloat16 *kd, __nv_bfloat16 *vt,
                                    cudaStream_t st) {
     if (!attn_prefill_tc_supported(a, T) || kd == nullptr || vt == nullptr) return cudaErrorInvalidValue;
-    const int nkeys = T, Lpad = attn_prefill_tc_lpad(nkeys);
+    const int nkeys = a.rowmap.pos0 + T, Lpad = attn_prefill_tc_lpad(nkeys);
     const int n_kv = a.cache.n_kv;
     atc::k_kv_dense_tc<<<dim3(Lpad / 64, n_kv), 256, 0, st>>>(a.cache, a.layer, a.rowmap.stream0, nkeys, Lpad,
                                                                a.dense_k, a.dense_v, kd, vt);
@@ -407,6 +412,7 @@ cudaError_t launch_attn_prefill_tc(const AttnParams &a, int T, __nv_bfloat16 *kd
     p.n_q = a.n_q;
     p.group = a.group;
     p.Lpad = Lpad;
+    p.pos0 = a.rowmap.pos0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.status = a.status;
     const dim3 grid((T + atc::BM - 1) / atc::BM, a.n_q);

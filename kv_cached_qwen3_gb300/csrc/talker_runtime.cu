@@ -106,6 +106,7 @@ struct talker {
                                          // with the mma.sync / the tcgen05 attention at any T
     // tensor-core prefill buffers (bf16 GEMM operands and the f32 gate/up projection)
     int cap_tc_rows = 0;
+    int cap_kd_keys = 0;                 // keys kd_tc / vt_tc hold per KV head
     void *hb = nullptr, *ab = nullptr, *gb = nullptr;
     __nv_bfloat16 *kv_dense = nullptr;   // Q8_0 storage: the prefill's own k / v rows, [2][rows][n_kv][hd]
     __nv_bfloat16 *kd_tc = nullptr;      // tcgen05 prefill attention: K [n_kv][L][hd] and V^T [n_kv][hd][L]
@@ -166,6 +167,7 @@ void free_tc(talker *t) {
         *pp = nullptr;
     }
     t->cap_tc_rows = 0;
+    t->cap_kd_keys = 0;
 }
 
 void free_cache(talker *t) {
@@ -558,10 +560,11 @@ talker_status ensure_tc(talker *t, int rows) {
     TRY_CUDA(cudaMalloc(&t->gb, (size_t)cap * t->I * 2));
     TRY_CUDA(cudaMalloc(&t->gu, (size_t)cap * 2 * t->I * sizeof(float)));
     if (t->kv_q8) TRY_CUDA(cudaMalloc(&t->kv_dense, (size_t)2 * cap * t->nkv * t->hd * 2));
-    if (t->hd == 128) {
-        const size_t lp = (size_t)attn_prefill_tc_lpad(cap);
+    if (t->hd == 128) {   // keys of a call: up to the whole cache (an appended chunk reads every earlier key)
+        const size_t lp = (size_t)attn_prefill_tc_lpad(std::max(cap, t->max_seq));
         TRY_CUDA(cudaMalloc(&t->kd_tc, lp * t->nkv * t->hd * 2));
         TRY_CUDA(cudaMalloc(&t->vt_tc, lp * t->nkv * t->hd * 2));
+        t->cap_kd_keys = (int)lp;
     }
     t->cap_tc_rows = cap;
     return TALKER_OK;
@@ -617,10 +620,28 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
             a.dense_k = t->kv_dense;
             a.dense_v = t->kv_dense + (size_t)T * t->nkv * t->hd;
         }
-        const bool attn_tc = t->prefill_mode == 4 || (t->prefill_mode != 3 && T >= kAttnTcMinRows);
-        if (rm.mode == 1 && attn_tc && t->kd_tc != nullptr && attn_prefill_tc_supported(a, T)) {
-            TRY_CUDA(launch_attn_prefill_tc(a, T, t->kd_tc, t->vt_tc, st));   // dense K, V^T + tcgen05 tiles
-            nk += 2;
+        // rows of one stream: all T, or T / B in a batched prefill (B streams of rows_per_stream rows)
+        const int Ts = rm.rows_per_stream > 0 ? rm.rows_per_stream : T;
+        const int n_str = T / Ts;
+        const bool attn_tc = t->prefill_mode == 4 || (t->prefill_mode != 3 && Ts >= kAttnTcMinRows);
+        AttnParams a1 = a;   // the first stream's rows as a one-stream call
+        a1.rowmap.rows_per_stream = 0;
+        if (rm.mode == 1 && attn_tc && t->kd_tc != nullptr && rm.pos0 + Ts <= t->cap_kd_keys &&
+            attn_prefill_tc_supported(a1, Ts)) {
+            // dense K, V^T + tcgen05 tiles, one stream after the other (the dense copy is reused)
+            const size_t qrows = (size_t)Ts * t->qd, kvrows = (size_t)Ts * t->nkv * t->hd;
+            for (int s = 0; s < n_str; ++s) {
+                AttnParams as = a1;
+                as.rowmap.stream0 = rm.stream0 + s;
+                as.q = t->q + s * qrows;
+                as.out = static_cast<__nv_bfloat16 *>(t->ab) + s * qrows;
+                if (a.dense_k != nullptr) {
+                    as.dense_k = a.dense_k + s * kvrows;
+                    as.dense_v = a.dense_v + s * kvrows;
+                }
+                TRY_CUDA(launch_attn_prefill_tc(as, Ts, t->kd_tc, t->vt_tc, st));
+                nk += 2;
+            }
         } else if (rm.mode == 1 && attn_prefill_supported(t->kv_kind, t->hd)) {
             TRY_CUDA(launch_attn_prefill(t->hd, a, T, st));   // causal tiles on mma.sync
             ++nk;

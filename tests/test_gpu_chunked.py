@@ -33,11 +33,12 @@ def host(t):
     return t.detach().float().cpu().numpy()
 
 
-def run_chunks(g, w, chunks, n_dec, seed, bf16):
+def run_chunks(g, w, chunks, n_dec, seed, bf16, prefill_mode=0):
     from kv_cached_qwen3_gb300.talker import Talker
     total = sum(chunks) + n_dec
     emb = inputs.make_embeddings(g, seed, 0, total)
     tk = Talker(g, w)
+    tk.set_prefill_mode(prefill_mode)
     tk.kv_init_batched(1, total + 3)
     oc = OracleCache(Oracle(g, w), 1, total + 3)
     at = 0
@@ -72,9 +73,22 @@ def test_chunked_prefill_fp32_gemv_path(cuda):
     run_chunks(g, inputs.make_weights(g, 51), [20, 1, 7, 30, 40], 3, 52, bf16=False)
 
 
-def test_chunked_prefill_bf16_both_paths(cuda):
+@pytest.mark.parametrize("mode", [pytest.param(0, id="auto"), pytest.param(3, id="mma-sync-attention"),
+                                  pytest.param(4, id="tcgen05-attention")])
+def test_chunked_prefill_bf16_both_paths(cuda, mode):
+    """Chunks on the GEMV path (T < 16) and the tensor-core path; modes 3 / 4 pin the causal
+    attention of the tensor-core chunks to the mma.sync / tcgen05 kernel (the latter reads the
+    earlier keys of the stream through its dense copy and masks on positions pos0 + r)."""
     g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 4})
-    run_chunks(g, inputs.make_weights(g, 53), [100, 70, 5, 16, 64], 2, 54, bf16=True)
+    run_chunks(g, inputs.make_weights(g, 53), [100, 70, 5, 16, 64], 2, 54, bf16=True, prefill_mode=mode)
+
+
+@pytest.mark.parametrize("mode", [pytest.param(0, id="auto"), pytest.param(4, id="tcgen05-attention")])
+def test_chunked_prefill_long_chunks(cuda, mode):
+    """Chunks of several 128-row query tiles whose start positions are not multiples of the
+    128-key block (300, then 260 after 300, then 40 after 560)."""
+    g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 2})
+    run_chunks(g, inputs.make_weights(g, 56), [300, 260, 40], 1, 58, bf16=True, prefill_mode=mode)
 
 
 def test_append_overflow_changes_nothing(cuda):
@@ -95,15 +109,18 @@ def test_append_overflow_changes_nothing(cuda):
     tk.close()
 
 
+@pytest.mark.parametrize("mode", [pytest.param(3, id="mma-sync-attention"), pytest.param(4, id="tcgen05-attention")])
 @pytest.mark.parametrize("kv", ["bf16", "q8_0"])
-def test_batched_prefill_streams(cuda, kv):
-    """Streams 0..B-1 prefilled in one call (T rows each, across page boundaries), then a decode step."""
+def test_batched_prefill_streams(cuda, kv, mode):
+    """Streams 0..B-1 prefilled in one call (T rows each, across page boundaries), then a decode
+    step; the causal attention pinned to either kernel (tcgen05: one launch pair per stream)."""
     from kv_cached_qwen3_gb300.talker import Talker
     g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 2, "kv_dtype": kv})
     w = inputs.make_weights(g, 57)
     B, T = 3, 70
     emb = np.stack([inputs.make_embeddings(g, 57, 0, T + 1, stream=s) for s in range(B)])   # [B, T+1, H]
     tk = Talker(g, w)
+    tk.set_prefill_mode(mode)
     tk.kv_init_batched(B, T + 2)
     oc = OracleCache(Oracle(g, w), B, T + 2, kv_q8=(kv == "q8_0"))
     hd, lg, am = tk.prefill_batched(dev(emb[:, :T]))
