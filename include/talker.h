@@ -171,16 +171,20 @@ talker_status talker_set_logit_suppression(talker_t *t, int vocab_tail, int eos_
  * n_tables codebook embedding tables [vocab[g], hidden] (device pointers in
  * dtype TALKER_DTYPE_F32 or _BF16, table 0 = codec_embedding, then the acoustic
  * tables). The tables stay owned by the caller and must outlive their use.
- * n_tables = 0 unregisters. Errors: EINVAL (n_tables > 32, null table, vocab < 1). */
+ * n_tables = 0 unregisters. Synchronises the stream (captured steps read the
+ * registered pointers when they run) and drops captured steps.
+ * Errors: EINVAL (n_tables > 32, null table, vocab < 1), ECUDA. */
 talker_status talker_set_code_tables(talker_t *t, const void *const *tables, const int *vocab, int n_tables,
                                      int dtype);
 
 /* Decode from codebook ids: row b of the step's input is
  *   sum_g table_g[ids[g * B + b]] + overlay[b]
  * (ids: device int32 [n_tables][B], group-major; overlay: device f32 [B, hidden]
- * or NULL), built by one kernel into a library buffer, then talker_decode.
- * An id outside its table sets the device status word (ST bad argument) and
- * contributes nothing. Errors: as talker_decode; ESTATE without tables. */
+ * or NULL), summed inside the step's first kernel (the first layer's RMSNorm +
+ * QKV projection reads the table rows directly), then the step as
+ * talker_decode. An id outside its table sets the device status word (ST bad
+ * argument) and contributes nothing. Errors: as talker_decode; ESTATE without
+ * tables. */
 talker_status talker_decode_codes(talker_t *t, const int32_t *ids, const float *overlay, int B, float *logits,
                                   float *hidden, int32_t *argmax);
 

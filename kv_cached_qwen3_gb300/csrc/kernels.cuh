@@ -50,6 +50,45 @@ struct CacheView {
     size_t page_elems;
 };
 
+// Decode input rows gathered from codebook tables ("talker-forward.h", batched decode graph
+// input: the codebook rows summed, plus an overlay row): row b = sum_g tables[g][ids[g * ids_stride
+// + b]] + overlay[b]. An id outside [0, vocab[g]) sets ST_BAD_ARG and adds nothing.
+struct CodeGather {
+    const void *const *tables;   // device array of n table pointers, each [vocab[g], H]
+    const int *vocab;            // device array of n vocabulary sizes
+    int n;                       // 0: no gather (rows come from the input buffer)
+    int bf16;                    // tables are bf16 (else f32)
+    const int32_t *ids;          // device [n][ids_stride], group-major
+    int ids_stride;
+    const float *overlay;        // device [rows][H] or null
+};
+// Four consecutive elements [k, k + 4) of gathered row b (H % 4 == 0).
+__device__ __forceinline__ float4 gather_row4(const CodeGather &c, int b, int k, int H, int *status) {
+    float4 s = c.overlay ? *reinterpret_cast<const float4 *>(c.overlay + (size_t)b * H + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < c.n; ++g) {
+        const int id = c.ids[(size_t)g * c.ids_stride + b];
+        if (id < 0 || id >= c.vocab[g]) {
+            if (k == 0) atomicOr(status, 1 << 3);   // ST_BAD_ARG
+            continue;
+        }
+        const size_t i = (size_t)id * H + k;
+        if (c.bf16) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(c.tables[g]) + i);
+            s.x += __uint_as_float(u.x << 16);
+            s.y += __uint_as_float(u.x & 0xffff0000u);
+            s.z += __uint_as_float(u.y << 16);
+            s.w += __uint_as_float(u.y & 0xffff0000u);
+        } else {
+            const float4 v = *reinterpret_cast<const float4 *>(static_cast<const float *>(c.tables[g]) + i);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+    }
+    return s;
+}
+
 struct GemvParams {
     const void *W;       // [rows_w, K] weight_dtype (rows_w = n_out, or 2*n_out for SWIGLU)
     const float *act;    // [rows, act_ld] f32 input activations
@@ -62,6 +101,7 @@ struct GemvParams {
     float *out;          // epilogue destination, row stride out_ld
     int out_ld;
     float *copy_x;       // optional: CTA column 0 copies the raw input rows here (residual init)
+    CodeGather gather;   // gather.n > 0: the input rows come from codebook tables, not act
     float *out2;         // EPI_RESID: optional second destination of the same sums
     const void *W2;      // EPI_SWIGLU_DOWN: down weights [n_out2][n_out] (bf16)
     float *red_out;      // EPI_SWIGLU_DOWN: [rows][n_out2], reduce-added (holds the residual)
@@ -156,16 +196,6 @@ cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *
 // mode 1, bf16 output).
 bool attn_prefill_supported(int kv_bf16, int head_dim);
 cudaError_t launch_attn_prefill(int head_dim, const AttnParams &a, int T, cudaStream_t st);
-// Decode input rows from codebook ids: out[b] = sum_g table_g[ids[g * B + b]] + overlay[b]
-// (tables bf16 or f32 [V_g, H]); an id outside [0, V_g) sets ST_BAD_ARG and adds nothing.
-struct EmbedTables {
-    const void *table[32];
-    int vocab[32];
-    int n;
-    int bf16;
-};
-cudaError_t launch_embed_codes(const EmbedTables &t, const int32_t *ids, const float *overlay, int B, int H,
-                               float *out, int *status, cudaStream_t st);
 cudaError_t prepare_kernels();  // raise dynamic shared-memory limits once per process
 
 // tcgen05 causal prefill attention (head_dim 128, one stream from position 0): dense K and
@@ -187,8 +217,9 @@ cudaError_t launch_gemm_tc_swiglu(const void *A, int M, int K, const void *B, in
                                   int *status, cudaStream_t st);
 
 // Element-wise stages of the tensor-core prefill path (prefill.cu).
-cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H, void *out,
-                                cudaStream_t st);
+// With gather.n > 0 the rows are first gathered from codebook tables and also written to x.
+cudaError_t launch_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int rows, int H, void *out,
+                                cudaStream_t st, const CodeGather *gather = nullptr, int *status = nullptr);
 // dense_kv (Q8_0 storage only, else null): the rows' k / v also go to bf16 [2][rows][n_kv][hd]
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
                             const float *k_norm, const float2 *rope, float eps, float *q_out, const CacheView &cache,

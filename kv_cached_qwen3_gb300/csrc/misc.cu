@@ -81,33 +81,6 @@ cudaError_t launch_kv_copy(const CacheView &c, int stream, void *dense_k, void *
     return cudaGetLastError();
 }
 
-// One CTA per slot b: the sum over the codebooks of the rows the slot's ids select, plus
-// the slot's overlay row (qwen3-tts talker batch input, "input_embed").
-__global__ void k_embed_codes(const EmbedTables t, const int32_t *ids, const float *overlay, int B, int H,
-                              float *out, int *status) {
-    const int b = blockIdx.x;
-    for (int k = threadIdx.x; k < H; k += blockDim.x) {
-        float acc = overlay ? overlay[(size_t)b * H + k] : 0.f;
-        for (int g = 0; g < t.n; ++g) {
-            const int id = ids[(size_t)g * B + b];
-            if (id < 0 || id >= t.vocab[g]) {
-                if (k == 0) atomicOr(status, ST_BAD_ARG);
-                continue;
-            }
-            const size_t i = (size_t)id * H + k;
-            acc += t.bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(t.table[g])[i])
-                          : static_cast<const float *>(t.table[g])[i];
-        }
-        out[(size_t)b * H + k] = acc;
-    }
-}
-
-cudaError_t launch_embed_codes(const EmbedTables &t, const int32_t *ids, const float *overlay, int B, int H,
-                               float *out, int *status, cudaStream_t st) {
-    k_embed_codes<<<B, 256, 0, st>>>(t, ids, overlay, B, H, out, status);
-    return cudaGetLastError();
-}
-
 cudaError_t prepare_kernels() {
     cudaError_t e = prepare_gemv();
     if (e != cudaSuccess) return e;

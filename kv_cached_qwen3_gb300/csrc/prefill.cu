@@ -38,8 +38,8 @@ static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, c
 
 // One CTA per row: every thread stages its float4s of the row (one round trip), the sum of
 // squares is reduced across the CTA, then the scaled bf16 row is written.
-__global__ void k_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H,
-                               __nv_bfloat16 *out) {
+__global__ void k_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int rows, int H,
+                               __nv_bfloat16 *out, CodeGather gather, int *status) {
     __shared__ float red[32];
     const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
@@ -51,7 +51,12 @@ __global__ void k_rmsnorm_bf16(const float *x, int ld, const float *w, float eps
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
         const int k = (threadIdx.x + i * blockDim.x) * 4;
-        v[i] = k < H ? *reinterpret_cast<const float4 *>(xr + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (gather.n > 0) {   // the row from codebook tables, kept as the residual stream
+            v[i] = k < H ? gather_row4(gather, row, k, H, status) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < H) *reinterpret_cast<float4 *>(x + (size_t)row * ld + k) = v[i];
+        } else {
+            v[i] = k < H ? *reinterpret_cast<const float4 *>(xr + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
     }
     ss = warp_sum(ss);
@@ -186,12 +191,14 @@ __global__ void k_swiglu_bf16(const float *gu, int rows, int I, __nv_bfloat16 *o
     }
 }
 
-cudaError_t launch_rmsnorm_bf16(const float *x, int ld, const float *w, float eps, int rows, int H, void *out,
-                                cudaStream_t st) {
+cudaError_t launch_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int rows, int H, void *out,
+                                cudaStream_t st, const CodeGather *gather, int *status) {
     const int threads = 256;
-    if (H % 4 || H > 4 * 4 * threads) return cudaErrorInvalidValue;
+    if (H % 4 || H > 4 * 4 * threads || (gather != nullptr && gather->n > 0 && status == nullptr))
+        return cudaErrorInvalidValue;
+    const CodeGather none{};
     return launch_pdl(k_rmsnorm_bf16, dim3(rows), dim3(threads), st, x, ld, w, eps, rows, H,
-                      static_cast<__nv_bfloat16 *>(out));
+                      static_cast<__nv_bfloat16 *>(out), gather ? *gather : none, status);
 }
 
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,

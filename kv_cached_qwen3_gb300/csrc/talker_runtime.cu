@@ -38,6 +38,8 @@ struct GraphEntry {
     const float *emb;
     float *logits, *hidden;
     int32_t *argmax;
+    const int32_t *ids;     // codebook ids of a step whose input rows are gathered (else null)
+    const float *overlay;
     cudaGraphExec_t exec;
     int n_kernels;
 };
@@ -115,9 +117,11 @@ struct talker {
     int tc_ok = -1;                      // tensor-core prefill usable for this geometry (-1 unknown)
     // TTS loop input / output
     int suppress_tail = 0, suppress_eos = -1;   // head: logits [V - tail, V) except eos become -inf
-    EmbedTables codes{};                        // caller-owned codebook tables (codes.n = 0: none)
-    float *code_emb = nullptr;                  // [code_emb_rows, H] rows built from codebook ids
-    int code_emb_rows = 0;
+    std::vector<const void *> code_tables;      // caller-owned codebook tables (empty: none)
+    std::vector<int> code_vocab;
+    int code_bf16 = 0;
+    const void **d_code_tables = nullptr;       // device copies of the table pointers and vocab sizes,
+    int *d_code_vocab = nullptr;                // read by the kernels that gather input rows
     // whole-frame graph (prefill + steps fed by the previous step's code, on the device)
     cudaGraphExec_t frame_exec = nullptr;
     std::vector<const void *> frame_key;        // the inputs the captured frame is valid for
@@ -142,9 +146,8 @@ void free_ptr(void *p) {
 }
 
 void free_workspaces(talker *t) {
-    float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->attn_ws, &t->head_val, &t->code_emb,
-                    &t->frame_logits, &t->x2};
-    t->code_emb_rows = 0;
+    float **fl[] = {&t->x, &t->raw, &t->q, &t->attn, &t->act, &t->attn_ws, &t->head_val, &t->frame_logits,
+                    &t->x2};
     for (auto pp : fl) {
         free_ptr(*pp);
         *pp = nullptr;
@@ -383,7 +386,7 @@ void set_raw_heads(const talker *t, const LayerDev &d, AttnParams &a) {
 // two in one kernel where fuse_mlp_ok); then the final norm + codec_head (+argmax). Returns
 // the number of kernels enqueued through *n_kernels.
 talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap &rm, const float *emb,
-                              int splits, const ForwardOut &out, int *n_kernels) {
+                              int splits, const ForwardOut &out, int *n_kernels, const CodeGather *gather = nullptr) {
     const CacheView cv = cache_view(t);
     const int nh = t->c.n_layers;
     int nk = 0;
@@ -408,6 +411,7 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
         p.out = t->raw;
         p.out_ld = t->qkv_n;
         p.copy_x = (l == 0) ? X : nullptr;
+        if (l == 0 && gather != nullptr) p.gather = *gather;   // rows summed from codebook tables
         p.layer = l;
         p.n_q = t->nq;
         p.n_kv = t->nkv;
@@ -585,13 +589,16 @@ talker_status tc_gemm(talker *t, cudaStream_t st, const void *A, int M, int K, c
 // into the residual stream, RMSNorm -> bf16, [Wg;Wu] GEMM, SwiGLU -> bf16, down GEMM
 // reduce-added into the residual stream; then the final norm + codec_head GEMV.
 talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, const float *emb, int attn_splits,
-                         const ForwardOut &out, int *n_kernels) {
+                         const ForwardOut &out, int *n_kernels, const CodeGather *gather = nullptr) {
     const CacheView cv = cache_view(t);
     int nk = 0;
-    TRY_CUDA(cudaMemcpyAsync(t->x, emb, (size_t)T * t->H * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    // the input rows: copied in, or (gather) summed from codebook tables by layer 0's RMSNorm
+    if (gather == nullptr)
+        TRY_CUDA(cudaMemcpyAsync(t->x, emb, (size_t)T * t->H * sizeof(float), cudaMemcpyDeviceToDevice, st));
     for (int l = 0; l < t->c.n_layers; ++l) {
         const LayerDev &d = t->L[l];
-        TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.in_norm, t->c.rms_eps, T, t->H, t->hb, st));
+        TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.in_norm, t->c.rms_eps, T, t->H, t->hb, st,
+                                     l == 0 ? gather : nullptr, t->d_status));
         ++nk;
         TRY(tc_gemm(t, st, t->hb, T, t->H, d.qkv, t->qkv_n, t->raw, t->qkv_n, false, &nk));
         if (rm.mode != 0) {   // prefill rows; decode rows are finished inside the attention kernel
@@ -832,6 +839,8 @@ void talker_destroy(talker_t *t) {
     free_ptr(t->wstore);
     free_tc(t);
     free_ptr(t->d_status);
+    free_ptr(t->d_code_tables);
+    free_ptr(t->d_code_vocab);
     if (t->cap_st) cudaStreamDestroy(t->cap_st);
     delete t;
 }
@@ -938,10 +947,13 @@ talker_status talker_prefill_batched(talker_t *t, int B, const float *emb, int T
     return TALKER_OK;
 }
 
-talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits, float *hidden, int32_t *argmax) {
+// One decode step of streams 0..B-1 as a replayed CUDA graph; the input rows come from emb, or
+// (gather != null) are summed from codebook tables inside the step's first kernel.
+static talker_status decode_impl(talker *t, const float *emb, const CodeGather *gather, int B, float *logits,
+                                 float *hidden, int32_t *argmax) {
     if (!t) return TALKER_EINVAL;
     if (t->n_streams == 0) return TALKER_ESTATE;
-    if (!emb || !logits || B < 1 || B > t->n_streams) return TALKER_EINVAL;
+    if ((!emb && !gather) || !logits || B < 1 || B > t->n_streams) return TALKER_EINVAL;
     for (int b = 0; b < B; ++b)
         if (t->len[b] + 1 > t->max_seq) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));
@@ -963,9 +975,11 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
     TRY(ensure_capacity(t, B, splits));
     if (kind == 1) TRY(ensure_tc(t, B));
     GraphEntry *ge = nullptr;
+    const int32_t *ids = gather ? gather->ids : nullptr;
+    const float *overlay = gather ? gather->overlay : nullptr;
     for (auto &g : t->graphs)
         if (g.kind == kind && g.B == B && g.splits == splits && g.cluster == cluster && g.emb == emb &&
-            g.logits == logits && g.hidden == hidden && g.argmax == argmax)
+            g.logits == logits && g.hidden == hidden && g.argmax == argmax && g.ids == ids && g.overlay == overlay)
             ge = &g;
     if (!ge) {
         if ((int)t->graphs.size() >= kMaxGraphs) {
@@ -978,8 +992,8 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
         cudaGraph_t graph = nullptr;
         t->attn_cluster = cluster;
         TRY_CUDA(cudaStreamBeginCapture(t->cap_st, cudaStreamCaptureModeThreadLocal));
-        talker_status s = kind == 1 ? enqueue_tc(t, t->cap_st, B, rm, emb, splits, out, &nk)
-                                    : enqueue_forward(t, t->cap_st, B, rm, emb, splits, out, &nk);
+        talker_status s = kind == 1 ? enqueue_tc(t, t->cap_st, B, rm, emb, splits, out, &nk, gather)
+                                    : enqueue_forward(t, t->cap_st, B, rm, emb, splits, out, &nk, gather);
         cudaError_t e = cudaStreamEndCapture(t->cap_st, &graph);
         if (s != TALKER_OK) {
             if (graph) cudaGraphDestroy(graph);
@@ -990,13 +1004,17 @@ talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits,
         e = cudaGraphInstantiate(&exec, graph, 0);
         cudaGraphDestroy(graph);
         if (e != cudaSuccess) return from_cuda(e);
-        t->graphs.push_back(GraphEntry{kind, B, splits, cluster, emb, logits, hidden, argmax, exec, nk});
+        t->graphs.push_back(GraphEntry{kind, B, splits, cluster, emb, logits, hidden, argmax, ids, overlay, exec, nk});
         ge = &t->graphs.back();
     }
     TRY_CUDA(cudaGraphLaunch(ge->exec, t->st));
     t->launches += ge->n_kernels;
     for (int b = 0; b < B; ++b) t->len[b] += 1;
     return TALKER_OK;
+}
+
+talker_status talker_decode(talker_t *t, const float *emb, int B, float *logits, float *hidden, int32_t *argmax) {
+    return decode_impl(t, emb, nullptr, B, logits, hidden, argmax);
 }
 
 talker_status talker_kv_import(talker_t *t, int stream, const void *k, const void *v, int len) {
@@ -1085,28 +1103,34 @@ talker_status talker_set_code_tables(talker_t *t, const void *const *tables, con
                                      int dtype) {
     if (!t || n_tables < 0 || n_tables > 32 || (n_tables > 0 && (!tables || !vocab))) return TALKER_EINVAL;
     if (dtype != TALKER_DTYPE_F32 && dtype != TALKER_DTYPE_BF16) return TALKER_EINVAL;
-    EmbedTables e{};
-    for (int g = 0; g < n_tables; ++g) {
+    for (int g = 0; g < n_tables; ++g)
         if (!tables[g] || vocab[g] < 1) return TALKER_EINVAL;
-        e.table[g] = tables[g];
-        e.vocab[g] = vocab[g];
+    TRY_CUDA(cudaSetDevice(t->dev));
+    if (!t->d_code_tables) {
+        TRY_CUDA(cudaMalloc(&t->d_code_tables, 32 * sizeof(void *)));
+        TRY_CUDA(cudaMalloc(&t->d_code_vocab, 32 * sizeof(int)));
     }
-    e.n = n_tables;
-    e.bf16 = dtype == TALKER_DTYPE_BF16;
-    t->codes = e;
-    if (t->frame_exec) cudaGraphExecDestroy(t->frame_exec);   // a captured frame reads the old tables
-    t->frame_exec = nullptr;
-    t->frame_key.clear();
+    // captured steps read these device copies when they run: let queued work finish first
+    TRY_CUDA(cudaStreamSynchronize(t->st));
+    if (n_tables > 0) {
+        TRY_CUDA(cudaMemcpy(t->d_code_tables, tables, n_tables * sizeof(void *), cudaMemcpyHostToDevice));
+        TRY_CUDA(cudaMemcpy(t->d_code_vocab, vocab, n_tables * sizeof(int), cudaMemcpyHostToDevice));
+    }
+    t->code_tables.assign(tables, tables + n_tables);
+    t->code_vocab.assign(vocab, vocab + n_tables);
+    t->code_bf16 = dtype == TALKER_DTYPE_BF16;
+    drop_graphs(t);   // captured steps bake the table count and type in
     return TALKER_OK;
 }
 
 talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, const int *table_of_step,
                            const void *const *heads, int32_t *codes, float *logits) {
     if (!t) return TALKER_EINVAL;
-    if (t->n_streams == 0 || t->codes.n == 0) return TALKER_ESTATE;
+    const int n_tables = (int)t->code_tables.size();
+    if (t->n_streams == 0 || n_tables == 0) return TALKER_ESTATE;
     if (!emb || !codes || T0 < 1 || n_steps < 0 || (n_steps > 0 && !table_of_step)) return TALKER_EINVAL;
     for (int i = 0; i < n_steps; ++i)
-        if (table_of_step[i] < 0 || table_of_step[i] >= t->codes.n) return TALKER_EINVAL;
+        if (table_of_step[i] < 0 || table_of_step[i] >= n_tables) return TALKER_EINVAL;
     if (heads)
         for (int i = 0; i <= n_steps; ++i)
             if (!heads[i]) return TALKER_EINVAL;
@@ -1119,17 +1143,12 @@ talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, c
     const int splits_max = std::max(kAttnClusterMax, decode_splits(t, 1));
     TRY(ensure_capacity(t, T0, splits_max));
     if (tc_pre) TRY(ensure_tc(t, T0));
-    if (t->code_emb_rows < 1 || !t->frame_logits) {
+    if (!t->frame_logits) {
         drop_graphs(t);
-        if (t->code_emb_rows < 1) {
-            free_ptr(t->code_emb);
-            TRY_CUDA(cudaMalloc(&t->code_emb, (size_t)t->n_streams * t->H * sizeof(float)));
-            t->code_emb_rows = t->n_streams;
-        }
-        if (!t->frame_logits) TRY_CUDA(cudaMalloc(&t->frame_logits, (size_t)t->V * sizeof(float)));
+        TRY_CUDA(cudaMalloc(&t->frame_logits, (size_t)t->V * sizeof(float)));
     }
     std::vector<const void *> key = {emb, codes, logits};
-    for (int i = 0; i < n_steps; ++i) key.push_back(t->codes.table[table_of_step[i]]);
+    for (int i = 0; i < n_steps; ++i) key.push_back(t->code_tables[table_of_step[i]]);
     for (int i = 0; i <= n_steps; ++i) key.push_back(head_of(i));
     if (!(t->frame_exec && t->frame_T0 == T0 && t->frame_steps == n_steps && t->frame_key == key)) {
         if (t->frame_exec) cudaGraphExecDestroy(t->frame_exec);
@@ -1148,22 +1167,23 @@ talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, c
             ++nk;
         }
         for (int i = 0; i < n_steps && st == TALKER_OK; ++i) {
-            // step i: the row of code i in its table, then one decode step; code i + 1 = its argmax
+            // step i: one decode step whose input row is the row of code i in its table, gathered
+            // by the step's first kernel; code i + 1 = its argmax
             const int g = table_of_step[i];
-            EmbedTables e{};
-            e.table[0] = t->codes.table[g];
-            e.vocab[0] = t->codes.vocab[g];
-            e.n = 1;
-            e.bf16 = t->codes.bf16;
-            st = from_cuda(launch_embed_codes(e, codes + i, nullptr, 1, t->H, t->code_emb, t->d_status, t->cap_st));
-            ++nk;
+            CodeGather cg{};
+            cg.tables = t->d_code_tables + g;
+            cg.vocab = t->d_code_vocab + g;
+            cg.n = 1;
+            cg.bf16 = t->code_bf16;
+            cg.ids = codes + i;
+            cg.ids_stride = 1;
             const int len = T0 + i;   // cache length before the step
             t->attn_cluster = (len + 1 <= kAttnClusterMax * kPageRows) ? 1 : 0;
             const int splits = t->attn_cluster ? kAttnClusterMax : decode_splits(t, 1);
             RowMap rm{0, 0, 0, t->d_len};
             ForwardOut out{logits ? logits + (size_t)(i + 1) * t->V : t->frame_logits, nullptr, codes + i + 1, false, 1};
             out.head_w = head_of(i + 1);
-            if (st == TALKER_OK) st = enqueue_forward(t, t->cap_st, 1, rm, t->code_emb, splits, out, &nk);
+            if (st == TALKER_OK) st = enqueue_forward(t, t->cap_st, 1, rm, nullptr, splits, out, &nk, &cg);
         }
         cudaError_t e = cudaStreamEndCapture(t->cap_st, &graph);
         if (st != TALKER_OK) {
@@ -1191,23 +1211,17 @@ talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, c
 talker_status talker_decode_codes(talker_t *t, const int32_t *ids, const float *overlay, int B, float *logits,
                                   float *hidden, int32_t *argmax) {
     if (!t) return TALKER_EINVAL;
-    if (t->n_streams == 0) return TALKER_ESTATE;
-    if (t->codes.n == 0) return TALKER_ESTATE;
-    if (!ids || !logits || B < 1 || B > t->n_streams) return TALKER_EINVAL;
-    for (int b = 0; b < B; ++b)
-        if (t->len[b] + 1 > t->max_seq) return TALKER_EOVERFLOW;
-    TRY_CUDA(cudaSetDevice(t->dev));
-    if (t->code_emb_rows < t->n_streams) {
-        drop_graphs(t);   // captured steps read the old buffer
-        free_ptr(t->code_emb);
-        t->code_emb = nullptr;
-        t->code_emb_rows = 0;
-        TRY_CUDA(cudaMalloc(&t->code_emb, (size_t)t->n_streams * t->H * sizeof(float)));
-        t->code_emb_rows = t->n_streams;
-    }
-    TRY_CUDA(launch_embed_codes(t->codes, ids, overlay, B, t->H, t->code_emb, t->d_status, t->st));
-    t->launches += 1;
-    return talker_decode(t, t->code_emb, B, logits, hidden, argmax);
+    if (t->n_streams == 0 || t->code_tables.empty()) return TALKER_ESTATE;
+    if (!ids) return TALKER_EINVAL;
+    CodeGather cg{};
+    cg.tables = t->d_code_tables;
+    cg.vocab = t->d_code_vocab;
+    cg.n = (int)t->code_tables.size();
+    cg.bf16 = t->code_bf16;
+    cg.ids = ids;
+    cg.ids_stride = B;
+    cg.overlay = overlay;
+    return decode_impl(t, nullptr, &cg, B, logits, hidden, argmax);
 }
 
 talker_status talker_set_prefill_mode(talker_t *t, int mode) {
