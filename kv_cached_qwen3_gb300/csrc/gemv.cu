@@ -200,8 +200,11 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
             for (int r = 0; r < ROWS; ++r) ss[r] = 0.f;
             for (int idx = threadIdx.x; idx < nrows * K4; idx += kGemvThreads) {
                 const int r = idx / K4, k = (idx - r * K4) * 4;
-                const float4 v = p.gather.n > 0 ? gather_row4(p.gather, row0 + r, k, K, p.status)
-                                                : *reinterpret_cast<const float4 *>(p.act + (size_t)(row0 + r) * p.act_ld + k);
+                float4 v;
+                if (EPI == EPI_QKV && p.gather.n > 0)   // only the first layer's QKV projection gathers
+                    v = gather_row4(p.gather, row0 + r, k, K, p.status);
+                else
+                    v = *reinterpret_cast<const float4 *>(p.act + (size_t)(row0 + r) * p.act_ld + k);
                 if (do_copy) *reinterpret_cast<float4 *>(p.copy_x + (size_t)(row0 + r) * K + k) = v;
                 *reinterpret_cast<float4 *>(act_s + act_index<EPV>(r, k, K)) = v;
                 if (NORM) {
