@@ -506,7 +506,7 @@ static cudaError_t launch_attn_t(const AttnParams &p, int rows, cudaStream_t st,
 }
 
 cudaError_t launch_attn(int kv_kind, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
-    if (attn_dec_keys_supported(kv_kind, head_dim, p)) return launch_attn_dec_keys(head_dim, p, rows, st, pdl);
+    if (attn_dec_keys_supported(kv_kind, head_dim, p)) return launch_attn_dec_keys(kv_kind, head_dim, p, rows, st, pdl);
     if (kv_kind == 2) {   // Q8_0 storage
         switch (head_dim) {
             case 64: return launch_attn_t<int8_t, 64>(p, rows, st, pdl);

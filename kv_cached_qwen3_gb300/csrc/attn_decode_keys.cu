@@ -33,7 +33,8 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlots = 2;                    // page slots (K + V tiles) per CTA
+constexpr int kSlotsBf16 = 2;                // page slots (K + V tiles) per CTA: bf16 tiles
+constexpr int kSlotsQ8 = 4;                  // Q8_0 tiles (about half the bytes)
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void cluster_barrier() {
@@ -62,6 +63,24 @@ __device__ __forceinline__ int rot(int i, int key, int quarter) {
     else return (i + (key & 1)) & 1;
 }
 
+// Rotation of the two 16-byte halves of a lane's 32 Q8_0 codes (head_dim 128): the 8 lanes of a
+// phase (two keys x four quarters) then hit distinct banks.
+template <int HD>
+__device__ __forceinline__ int rot_q8(int i, int key) {
+    if constexpr (HD == 128) return (i + (key & 1)) & 1;
+    else return i;
+}
+
+// The four signed codes of a 32-bit word as floats: each biased byte goes under the exponent
+// of 2^23 (byte_perm), and subtracting 2^23 + 128 leaves the code exactly.
+__device__ __forceinline__ void q8x4(uint32_t w, float *f) {
+    const uint32_t v = w ^ 0x80808080u;
+    f[0] = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7440)) - 8388736.0f;
+    f[1] = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7441)) - 8388736.0f;
+    f[2] = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7442)) - 8388736.0f;
+    f[3] = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7443)) - 8388736.0f;
+}
+
 template <int G>
 __device__ __forceinline__ void dot8(const uint4 u, const float (&q)[G][8], float (&s)[G]) {
 #pragma unroll
@@ -81,19 +100,22 @@ __device__ __forceinline__ void dot8(const uint4 u, const float (&q)[G][8], floa
 
 }  // namespace
 
-size_t attn_dec_keys_smem_bytes(int head_dim, int group) {
-    const size_t tile = (size_t)kPage * head_dim * 2;
+// bf16 tile: [64][hd] values; Q8_0 tile: [64][hd] codes, then [64][hd / 32] fp16 scales.
+size_t attn_dec_keys_smem_bytes(int head_dim, int group, bool q8) {
+    const size_t tile = q8 ? (size_t)kPage * head_dim + (size_t)kPage * (head_dim / 32) * 2 : (size_t)kPage * head_dim * 2;
     const size_t gh = (size_t)group * head_dim;
-    return 2 * kSlots * tile + gh * 4 + 2 * (size_t)head_dim * 4 + kWarps * gh * 4 +
+    return 2 * (q8 ? kSlotsQ8 : kSlotsBf16) * tile + gh * 4 + 2 * (size_t)head_dim * 4 + kWarps * gh * 4 +
            kAttnClusterMax * (gh + 2 * group) * 4;
 }
 
-template <int HD, int G>
+template <int HD, int G, bool Q8>
 __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams p) {
-    constexpr int QD = HD / 4;         // dims of a key that one lane scores
-    constexpr int NSUB = QD / 8;       // 16-byte loads per lane per key
-    constexpr int PD = HD / 32;        // output dims per lane in P.V
-    constexpr uint32_t kTile = kPage * HD * 2;
+    constexpr int QD = HD / 4;                 // dims of a key that one lane scores
+    constexpr int EPL = Q8 ? 16 : 8;           // elements per 16-byte load
+    constexpr int NSUB = QD / EPL;             // 16-byte loads per lane per key
+    constexpr int PD = HD / 32;                // output dims per lane in P.V
+    constexpr uint32_t kTile = Q8 ? kPage * HD + kPage * (HD / 32) * 2 : kPage * HD * 2;
+    constexpr int kSlots = Q8 ? kSlotsQ8 : kSlotsBf16;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *kbuf = smem_raw;                                   // [kSlots][tile]
     unsigned char *vbuf = kbuf + kSlots * kTile;                      // [kSlots][tile]
@@ -129,10 +151,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
     if (!has && !clustered) return;
 
     const int *ptab = p.cache.page_table + (size_t)r * p.cache.pages_per_stream;
-    const size_t head_off = (size_t)(p.layer * p.cache.n_kv + g) * kPage * HD;   // elements
-    const __nv_bfloat16 *kpool = static_cast<const __nv_bfloat16 *>(p.cache.k);
-    const __nv_bfloat16 *vpool = static_cast<const __nv_bfloat16 *>(p.cache.v);
-    auto tile_of = [&](const __nv_bfloat16 *pool, int page) { return pool + (size_t)page * p.cache.page_elems + head_off; };
+    // a (page, layer, head) tile is kTile contiguous bytes; page_elems counts pool units (bf16
+    // elements, or bytes for Q8_0)
+    const size_t head_off = (size_t)(p.layer * p.cache.n_kv + g) * kTile;
+    const size_t page_bytes = p.cache.page_elems * (Q8 ? 1 : 2);
+    unsigned char *kpool = static_cast<unsigned char *>(p.cache.k);
+    unsigned char *vpool = static_cast<unsigned char *>(p.cache.v);
+    auto tile_of = [&](unsigned char *pool, int page) { return pool + (size_t)page * page_bytes + head_off; };
 
     uint32_t rank = 0;
     if (clustered) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
@@ -200,16 +225,31 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
                 q_s[hh * HD + i] = a[j] * qscale;
                 q_s[hh * HD + i + half] = b[j] * qscale;
             } else {
+                // the row as this step attends it: exact with Q8_0 storage (a call attends its own
+                // rows unquantized), else as stored
                 float *d = hh == G ? knew : vnew;
-                d[i] = Elem<__nv_bfloat16>::round(a[j]);
-                d[i + half] = Elem<__nv_bfloat16>::round(b[j]);
-                if (sidx == 0) {
-                    __nv_bfloat16 *c = const_cast<__nv_bfloat16 *>(tile_of(hh == G ? kpool : vpool, ptab[pos / kPage])) +
+                d[i] = Q8 ? a[j] : Elem<__nv_bfloat16>::round(a[j]);
+                d[i + half] = Q8 ? b[j] : Elem<__nv_bfloat16>::round(b[j]);
+                if (!Q8 && sidx == 0) {
+                    __nv_bfloat16 *c = reinterpret_cast<__nv_bfloat16 *>(tile_of(hh == G ? kpool : vpool, ptab[pos / kPage])) +
                                        (size_t)(pos % kPage) * HD;
                     c[i] = __float2bfloat16_rn(a[j]);
                     c[i + half] = __float2bfloat16_rn(b[j]);
                 }
             }
+        }
+        if (Q8 && hh >= G && sidx == 0) {
+            // Q8_0 row for later steps: each valid register of the warp is one block of 32 dims
+            unsigned char *t = tile_of(hh == G ? kpool : vpool, ptab[pos / kPage]);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int d0 = 32 * j + u * half;   // first dim of this register's block
+                    if (32 * j >= half) continue;
+                    q8_store_block(t, (pos % kPage) * HD + d0, kPage * HD + ((pos % kPage) * (HD / 32) + d0 / 32) * 2,
+                                   u ? b[j] : a[j], lane);
+                }
         }
     }
     __syncthreads();
@@ -227,14 +267,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
     bool failed = false;
     int fail_it = 0;
     if (has) {
-        float qr[G][NSUB][8];   // q over this lane's quarter, in the lane's load order
+        float qr[G][NSUB][EPL];   // q over this lane's quarter, in the lane's load order
+        auto sub_of = [&](int i) { return Q8 ? rot_q8<HD>(i, kk) : rot<HD>(i, kk, quarter); };
 #pragma unroll
         for (int gi = 0; gi < G; ++gi)
 #pragma unroll
             for (int i = 0; i < NSUB; ++i) {
-                const float *qs = q_s + gi * HD + quarter * QD + rot<HD>(i, kk, quarter) * 8;
+                const float *qs = q_s + gi * HD + quarter * QD + sub_of(i) * EPL;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) qr[gi][i][e] = qs[e];
+                for (int e = 0; e < EPL; ++e) qr[gi][i][e] = qs[e];
             }
         for (int pg = pb, it = 0; pg < pe; ++pg, ++it) {
             const int slot = it % kSlots;
@@ -248,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
             unsigned char *Vs = vbuf + slot * kTile;
             const int valid = min(kPage, nvis - pg * kPage);
             const int newest = pos - pg * kPage;   // the fresh row, when this page holds it
-            if (newest >= 0 && newest < kPage && (newest >> 3) == warp) {
+            if (!Q8 && newest >= 0 && newest < kPage && (newest >> 3) == warp) {
                 // only this warp reads that row: patch the stored values in (the copy may predate them)
                 __nv_bfloat16 *kr = reinterpret_cast<__nv_bfloat16 *>(Ks) + newest * HD;
                 __nv_bfloat16 *vr = reinterpret_cast<__nv_bfloat16 *>(Vs) + newest * HD;
@@ -262,16 +303,47 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
             float sc[G];
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) sc[gi] = 0.f;
-            const uint32_t krow = smem_u32(Ks) + (uint32_t)(kk * HD + quarter * QD) * 2;
+            if constexpr (!Q8) {
+                const uint32_t krow = smem_u32(Ks) + (uint32_t)(kk * HD + quarter * QD) * 2;
 #pragma unroll
-            for (int i = 0; i < NSUB; ++i) {
-                const uint4 u = lds_u4(krow + rot<HD>(i, kk, quarter) * 16);
-                float qv[G][8];
+                for (int i = 0; i < NSUB; ++i) {
+                    const uint4 u = lds_u4(krow + rot<HD>(i, kk, quarter) * 16);
+                    float qv[G][8];
 #pragma unroll
-                for (int gi = 0; gi < G; ++gi)
+                    for (int gi = 0; gi < G; ++gi)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) qv[gi][e] = qr[gi][i][e];
-                dot8<G>(u, qv, sc);
+                        for (int e = 0; e < 8; ++e) qv[gi][e] = qr[gi][i][e];
+                    dot8<G>(u, qv, sc);
+                }
+            } else if (kk == newest) {   // this step's own row, exact
+#pragma unroll
+                for (int i = 0; i < NSUB; ++i)
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) {
+                        const float x = knew[quarter * QD + sub_of(i) * EPL + e];
+#pragma unroll
+                        for (int gi = 0; gi < G; ++gi) sc[gi] = fmaf(qr[gi][i][e], x, sc[gi]);
+                    }
+            } else {   // codes times q, then the block's scale
+                const uint32_t krow = smem_u32(Ks) + (uint32_t)(kk * HD + quarter * QD);
+#pragma unroll
+                for (int i = 0; i < NSUB; ++i) {
+                    const uint4 u = lds_u4(krow + sub_of(i) * 16);
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int wq = 0; wq < 4; ++wq) {
+                        float c4[4];
+                        q8x4(w4[wq], c4);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+#pragma unroll
+                            for (int gi = 0; gi < G; ++gi) sc[gi] = fmaf(qr[gi][i][wq * 4 + e], c4[e], sc[gi]);
+                    }
+                }
+                const float sd = __half2float(*reinterpret_cast<const __half *>(
+                    Ks + kPage * HD + (kk * (HD / 32) + (quarter * QD) / 32) * 2));
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi) sc[gi] *= sd;
             }
             const bool kval = kk < valid;
             float pk[G];
@@ -299,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
             }
             // P.V over the warp's 8 keys (rows past the window are skipped: their contents are
             // never read into the arithmetic)
-            const uint32_t vbase = smem_u32(Vs) + (uint32_t)(lane * PD) * 2;
+            const uint32_t vbase = smem_u32(Vs) + (uint32_t)(lane * PD) * (Q8 ? 1 : 2);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int key = warp * 8 + j;
@@ -308,7 +380,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
                 for (int gi = 0; gi < G; ++gi) pj[gi] = __shfl_sync(0xffffffffu, pk[gi], j * 4);
                 if (key < valid) {
                     float v[PD];
-                    if constexpr (PD == 4) {
+                    if constexpr (Q8) {
+                        if (key == newest) {   // this step's own row, exact
+#pragma unroll
+                            for (int d = 0; d < PD; ++d) v[d] = vnew[lane * PD + d];
+                        } else {
+                            float c4[4];
+                            uint32_t w;
+                            if constexpr (PD == 4) asm("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(vbase + (uint32_t)key * HD));
+                            else w = lds_u16(vbase + (uint32_t)key * HD);
+                            q8x4(w, c4);
+                            const float sd = __half2float(*reinterpret_cast<const __half *>(
+                                Vs + kPage * HD + (key * (HD / 32) + (lane * PD) / 32) * 2));
+#pragma unroll
+                            for (int d = 0; d < PD; ++d) v[d] = c4[d] * sd;
+                        }
+                    } else if constexpr (PD == 4) {
                         const uint2 u = lds_u2(vbase + (uint32_t)key * HD * 2);
                         v[0] = bf16lo(u.x);
                         v[1] = bf16hi(u.x);
@@ -482,16 +569,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
 }
 
 bool attn_dec_keys_supported(int kv_kind, int head_dim, const AttnParams &p) {
-    return kv_kind == 1 && (head_dim == 64 || head_dim == 128) && (p.group == 1 || p.group == 2) &&
+    return (kv_kind == 1 || kv_kind == 2) && (head_dim == 64 || head_dim == 128) && (p.group == 1 || p.group == 2) &&
            p.rowmap.mode == 0 && p.raw != nullptr && (!p.cluster || p.splits <= kAttnClusterMax);
 }
 
-template <int HD, int G>
+template <int HD, int G, bool Q8>
 static cudaError_t launch_keys_t(const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits, p.n_kv, rows);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = attn_dec_keys_smem_bytes(HD, G);
+    cfg.dynamicSmemBytes = attn_dec_keys_smem_bytes(HD, G, Q8);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -505,21 +592,34 @@ static cudaError_t launch_keys_t(const AttnParams &p, int rows, cudaStream_t st,
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, k_attn_dec_keys<HD, G>, p);
+    return cudaLaunchKernelEx(&cfg, k_attn_dec_keys<HD, G, Q8>, p);
 }
 
-cudaError_t launch_attn_dec_keys(int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
-    if (head_dim == 128) return p.group == 2 ? launch_keys_t<128, 2>(p, rows, st, pdl) : launch_keys_t<128, 1>(p, rows, st, pdl);
-    if (head_dim == 64) return p.group == 2 ? launch_keys_t<64, 2>(p, rows, st, pdl) : launch_keys_t<64, 1>(p, rows, st, pdl);
+template <bool Q8>
+static cudaError_t launch_keys_q(int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
+    if (head_dim == 128)
+        return p.group == 2 ? launch_keys_t<128, 2, Q8>(p, rows, st, pdl) : launch_keys_t<128, 1, Q8>(p, rows, st, pdl);
+    if (head_dim == 64)
+        return p.group == 2 ? launch_keys_t<64, 2, Q8>(p, rows, st, pdl) : launch_keys_t<64, 1, Q8>(p, rows, st, pdl);
     return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_attn_dec_keys(int kv_kind, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
+    return kv_kind == 2 ? launch_keys_q<true>(head_dim, p, rows, st, pdl) : launch_keys_q<false>(head_dim, p, rows, st, pdl);
+}
+
+template <bool Q8>
+static cudaError_t raise_keys() {
+    const int bytes = (int)attn_dec_keys_smem_bytes(128, 2, Q8);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_dec_keys<128, 2, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_dec_keys<128, 1, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = e ? e : cudaFuncSetAttribute(k_attn_dec_keys<64, 2, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e ? e : cudaFuncSetAttribute(k_attn_dec_keys<64, 1, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 cudaError_t prepare_attn_dec_keys() {
-    const int bytes = (int)attn_dec_keys_smem_bytes(128, 2);
-    cudaError_t e = cudaFuncSetAttribute(k_attn_dec_keys<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    e = e ? e : cudaFuncSetAttribute(k_attn_dec_keys<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    e = e ? e : cudaFuncSetAttribute(k_attn_dec_keys<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    return e ? e : cudaFuncSetAttribute(k_attn_dec_keys<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaError_t e = raise_keys<false>();
+    return e ? e : raise_keys<true>();
 }
 
 }  // namespace talker_k

@@ -182,11 +182,12 @@ size_t attn_smem_bytes(int kv_bf16, int head_dim, int group);
 
 cudaError_t launch_gemv(int epi, int w_bf16, int rows_tmpl, const GemvParams &p, cudaStream_t st, bool pdl);
 // Decode / prefill-row attention over the paged cache (kv_kind 0 f32, 1 bf16, 2 Q8_0). Decode rows
-// that finish their heads from the raw projections on a bf16 cache (head_dim 64 or 128, GQA group
-// of 1 or 2) run the key-parallel kernel (attn_decode_keys.cu), every other case the split kernel.
+// that finish their heads from the raw projections on a bf16 or Q8_0 cache (head_dim 64 or 128,
+// GQA group of 1 or 2) run the key-parallel kernel (attn_decode_keys.cu), every other case the
+// split kernel.
 cudaError_t launch_attn(int kv_kind, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl);
 bool attn_dec_keys_supported(int kv_kind, int head_dim, const AttnParams &p);
-cudaError_t launch_attn_dec_keys(int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl);
+cudaError_t launch_attn_dec_keys(int kv_kind, int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl);
 cudaError_t prepare_attn_dec_keys();
 cudaError_t launch_set_len(int *cur_len, int stream, int value, cudaStream_t st);
 // Copy len rows of a stream between a dense [n_layers][n_kv][len][hd] buffer and the cache.
