@@ -30,9 +30,9 @@ from kv_cached_qwen3_gb300 import inputs  # noqa: E402
 METRIC = "decode steps/s (B=1, B=16) + prefill tok/s; % of HBM / bf16 TC roofline"
 # DRAM read + write of one decode step (all kernels of the graph) from one ncu capture of the current
 # decode kernels (the launch-list summary under profiles/); None whenever a decode kernel changes.
-STEP_TRAFFIC = {"bytes": 907574016,
-                "note": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the 141 kernels of one decode "
-                        "step at cache length 100, where the algorithmic bytes are 898.8 MB"}
+STEP_TRAFFIC = {"bytes": 906716160,
+                "note": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the 113 kernels of one decode "
+                        "step at cache length about 100, where the algorithmic bytes are 898.8 MB"}
 UNIT = "steps/s"
 
 
@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="profiling aid: run `--steps` prefills of T rows on the Talker geometry and print their time")
+    ap.add_argument("--decode-only", type=int, default=0, metavar="L",
+                    help="profiling aid: run `--steps` single-stream decode steps against L imported cache rows "
+                         "(Talker widths, --layers layers, --kv storage) and print their time")
+    ap.add_argument("--layers", type=int, default=0, help="with --decode-only: layers (default: the Talker's 28)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "q8_0"], help="with --decode-only: KV storage")
     ap.add_argument("--batched-only", action="store_true",
                     help="profiling aid: run `--steps` 16-stream decode steps (start lengths U{128..2048}) and "
                          "print their time")
@@ -475,6 +480,31 @@ def prefill_only(T, steps, warmup):
     return out
 
 
+def decode_only(L, layers, kv, steps, warmup):
+    """Single-stream decode steps at cache length L (rewound before every timed pass)."""
+    import torch
+    from dataclasses import replace
+    from kv_cached_qwen3_gb300.talker import Talker
+    lc = inputs.WORKLOADS["long_context"]
+    g = replace(lc.geometry, kv_dtype=kv, n_layers=layers or lc.geometry.n_layers)
+    tk = Talker(g, inputs.make_weights(g, lc.seed))
+    tk.kv_init_batched(1, L + steps + warmup + 1)
+    kvd = torch.bfloat16 if kv == "bf16" else torch.float32
+    kk = torch.randn(g.n_layers, g.n_kv_heads, L, g.head_dim, device="cuda").to(kvd)
+    tk.kv_import(0, kk, kk, L)
+    del kk
+    e1 = torch.randn(1, g.hidden, device="cuda")
+    lg = torch.empty(1, g.vocab, device="cuda")
+    for _ in range(warmup):
+        tk.decode(e1, lg)
+    tk.rewind(0, L)
+    torch.cuda.synchronize()
+    s = timed(torch, tk.stream, lambda: tk.decode(e1, lg), steps)
+    out = {"decode_only": {"L": L, "layers": g.n_layers, "kv": kv, "ms_per_step": s * 1e3, "status": tk.sync_status()}}
+    tk.close()
+    return out
+
+
 def batched_only(steps, warmup):
     """16-stream decode steps on the Talker geometry (the batched workload's start lengths)."""
     import torch
@@ -515,6 +545,9 @@ def main():
         return
     if args.prefill_only:
         print(json.dumps(prefill_only(args.prefill_only, max(1, args.steps), max(1, args.warmup))))
+        return
+    if args.decode_only:
+        print(json.dumps(decode_only(args.decode_only, args.layers, args.kv, max(1, args.steps), max(1, args.warmup))))
         return
     if args.batched_only:
         print(json.dumps(batched_only(max(1, args.steps), max(1, args.warmup))))
