@@ -26,7 +26,10 @@ holding bf16 values, widened exactly). The forward follows these page sections:
     projections, "NeoX rotate_half" RoPE, GQA by repeat_interleave of the KV
     heads, i.e. q head h reads KV head h // (n_q / n_kv)).
   rightkit-qts "tts_transformer.rs": the explicit SwiGLU form silu(gate) * up;
-    the uncached "recompute" path that re-runs the full sequence (mode A here).
+    the uncached "recompute" path that re-runs the full sequence (mode A here);
+    the code predictor's frame (predict_remaining_codebooks_kv_with_cache), whose
+    prefill projects with heads[0] and generation step g with heads[g], the
+    step's input being the previous code's row of its embedding table.
 
 Readings taken where the pages leave a step open (each is listed in the design
 notes): RoPE angle for pair i at position p is p * theta**(-2 i / hd), pairing
