@@ -551,17 +551,37 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
     __syncthreads();
     if (!flag_s) return;
     __threadfence();
+    // Eight splits' partials are requested at a time (independent loads in flight), so the
+    // combine costs a few L2 round trips, not one per split.
+    constexpr int CB = 8;
     for (int idx = tid; idx < G * HD; idx += kThreads) {
         const int gi = idx / HD, d = idx - gi * HD;
         const float *w0 = p.ws + (((size_t)r * p.n_q + hq0 + gi) * p.splits) * WS;
         float M = -INFINITY;
-        for (int c = 0; c < nact; ++c) M = fmaxf(M, __ldcg(w0 + (size_t)c * WS));
+        for (int c0 = 0; c0 < nact; c0 += CB) {
+            float mv[CB];
+#pragma unroll
+            for (int c = 0; c < CB; ++c) mv[c] = c0 + c < nact ? __ldcg(w0 + (size_t)(c0 + c) * WS) : -INFINITY;
+#pragma unroll
+            for (int c = 0; c < CB; ++c) M = fmaxf(M, mv[c]);
+        }
         float L = 0.f, O = 0.f;
-        for (int c = 0; c < nact; ++c) {
-            const float mc = __ldcg(w0 + (size_t)c * WS);
-            const float e = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-            L = fmaf(__ldcg(w0 + (size_t)c * WS + 1), e, L);
-            O = fmaf(__ldcg(w0 + (size_t)c * WS + 4 + d), e, O);
+        for (int c0 = 0; c0 < nact; c0 += CB) {
+            float mv[CB], lv[CB], ov[CB];
+#pragma unroll
+            for (int c = 0; c < CB; ++c) {
+                const bool in = c0 + c < nact;
+                const float *wc = w0 + (size_t)(c0 + c) * WS;
+                mv[c] = in ? __ldcg(wc) : -INFINITY;
+                lv[c] = in ? __ldcg(wc + 1) : 0.f;
+                ov[c] = in ? __ldcg(wc + 4 + d) : 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < CB; ++c) {
+                const float e = (mv[c] == -INFINITY) ? 0.f : exp2f(mv[c] - M);
+                L = fmaf(lv[c], e, L);
+                O = fmaf(ov[c], e, O);
+            }
         }
         store(idx, O / L);
     }
