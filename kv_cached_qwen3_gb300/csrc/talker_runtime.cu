@@ -199,6 +199,27 @@ int decode_splits(const talker *t, int B) {
     return std::max(1, std::min(64, want));
 }
 
+// Attention splits of a decode step (CTAs per (row, KV group) along the cache) and whether they
+// combine inside a thread-block cluster, from the longest stream's length before the step
+// (captured steps are keyed by both). Measured on GB300: one or two short streams run one CTA
+// per KV group up to 2 pages (no combine at all), then a cluster of 8 (one or two pages per
+// split, combined on chip) up to 16 pages; longer or more streams fill the GPU in one wave,
+// combined through L2, and with several ragged streams a split walks about four pages of the
+// longest one, which balances the waves.
+void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster) {
+    const int pages_max = (max_len + 1 + kPageRows - 1) / kPageRows;
+    if (B <= 2 && pages_max <= 2) {
+        *splits = 1;
+        *cluster = 0;
+    } else if (B <= 2 && pages_max <= 2 * kAttnClusterMax) {
+        *splits = kAttnClusterMax;
+        *cluster = 1;
+    } else {
+        *cluster = 0;
+        *splits = B == 1 ? decode_splits(t, B) : std::min(64, std::max(decode_splits(t, B), (pages_max + 3) / 4));
+    }
+}
+
 // Grow activation buffers and workspaces to cover `rows` rows with `splits`
 // attention splits. Growing invalidates captured graphs (their pointers move).
 talker_status ensure_capacity(talker *t, int rows, int splits) {
@@ -959,19 +980,10 @@ static talker_status decode_impl(talker *t, const float *emb, const CodeGather *
     TRY_CUDA(cudaSetDevice(t->dev));
     const int kind = (t->decode_mode == 3 || (t->decode_mode == 0 && B >= kTcMinDecodeRows)) && tc_usable(t) ? 1 : 0;
     if (t->decode_mode == 3 && kind == 0) return TALKER_EINVAL;
-    // One or two short streams: the splits of a (row, KV group) form one thread-block cluster
-    // (one page per split) and combine on chip; otherwise more splits, combined through L2
-    // (measured faster there on GB300).
     int max_len = 0;
     for (int b = 0; b < B; ++b) max_len = std::max(max_len, t->len[b]);
-    const int cluster = (B <= 2 && max_len + 1 <= kAttnClusterMax * kPageRows) ? 1 : 0;
-    // enough splits to fill the GPU in one wave; with several streams (ragged lengths) also
-    // enough that a split walks about four pages of the longest stream, which balances the
-    // waves (captured steps are keyed by the split count)
-    const int pages_max = (max_len + 1 + kPageRows - 1) / kPageRows;
-    const int splits = cluster  ? kAttnClusterMax
-                       : B == 1 ? decode_splits(t, B)
-                                : std::min(64, std::max(decode_splits(t, B), (pages_max + 3) / 4));
+    int splits = 0, cluster = 0;
+    attn_config(t, B, max_len, &splits, &cluster);
     TRY(ensure_capacity(t, B, splits));
     if (kind == 1) TRY(ensure_tc(t, B));
     GraphEntry *ge = nullptr;
@@ -1178,8 +1190,8 @@ talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, c
             cg.ids = codes + i;
             cg.ids_stride = 1;
             const int len = T0 + i;   // cache length before the step
-            t->attn_cluster = (len + 1 <= kAttnClusterMax * kPageRows) ? 1 : 0;
-            const int splits = t->attn_cluster ? kAttnClusterMax : decode_splits(t, 1);
+            int splits = 0;
+            attn_config(t, 1, len, &splits, &t->attn_cluster);
             RowMap rm{0, 0, 0, t->d_len};
             ForwardOut out{logits ? logits + (size_t)(i + 1) * t->V : t->frame_logits, nullptr, codes + i + 1, false, 1};
             out.head_w = head_of(i + 1);
