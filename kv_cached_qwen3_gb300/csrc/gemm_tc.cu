@@ -247,6 +247,146 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 
+
+// Short products (M <= 128 activation rows: decode batches, small prefills) with the weights as
+// the MMA's M operand: D^T[f, r] = sum_k W[f, k] X[r, k] for one tile of 128 weight rows
+// (output features) and all rows at once (N = M rounded up to 16), a K range per CTA.
+// The shared-memory ring holds 128 x 64 weight boxes and only N x 64 activation boxes, so
+// a CTA fits next to the previous kernel's CTAs and streams its first weight boxes before the
+// dependency wait. Epilogue: TMEM lane = feature, column = row; each warp turns 16 rows x its
+// 32 features around in shared memory and stores or reduce-adds (split-K, the residual) 4 rows
+// x 128 bytes per instruction, or writes silu(gate) * up of the interleaved feature pairs as bf16.
+constexpr int kSwapStages = 4;
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_gemm_tc_swap(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+                   const GemmParams p, int splits) {
+    constexpr uint32_t W_BYTES = BM * BK * 2;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int ncol = (p.M + 15) / 16 * 16;                 // MMA N: rows rounded up to 16
+    const uint32_t X_BYTES = (uint32_t)ncol * BK * 2;      // a multiple of 2048
+    unsigned char *sW = smem;
+    unsigned char *sX = smem + kSwapStages * W_BYTES;
+    __shared__ __align__(8) uint64_t full[kSwapStages], empty[kSwapStages], tfull;
+    __shared__ uint32_t tmem_base_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x / splits, sp = blockIdx.x - tile * splits;
+    const int f0 = tile * BM;
+    const int nk_total = p.K / BK;
+    const int kb0 = sp * nk_total / splits, kb1 = (sp + 1) * nk_total / splits;
+    const int nk = kb1 - kb0;
+    uint32_t tcols = 32;
+    while ((int)tcols < ncol) tcols <<= 1;
+    const uint32_t idesc = instr_desc(BM, ncol);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSwapStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&tfull, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_s)),
+                     "r"(tcols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    pdl_launch_dependents();
+
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer: weight boxes of the first stages before the dependency wait
+        const int pre = nk < kSwapStages ? nk : kSwapStages;
+        for (int i = 0; i < pre; ++i) {
+            mbar_arrive_expect_tx(&full[i], W_BYTES + X_BYTES);
+            tma_load_2d(sW + i * W_BYTES, &map_w, (kb0 + i) * BK, f0, &full[i]);
+        }
+        pdl_wait();
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % kSwapStages;
+            if (i >= pre) {
+                if (!mbar_wait(&empty[s], ((i / kSwapStages) - 1) & 1, p.status)) break;
+                mbar_arrive_expect_tx(&full[s], W_BYTES + X_BYTES);
+                tma_load_2d(sW + s * W_BYTES, &map_w, (kb0 + i) * BK, f0, &full[s]);
+            }
+            tma_load_2d(sX + s * X_BYTES, &map_x, (kb0 + i) * BK, 0, &full[s]);
+        }
+        for (int j = (nk > kSwapStages ? nk - kSwapStages : 0); j < nk; ++j)
+            mbar_wait(&empty[j % kSwapStages], (j / kSwapStages) & 1, p.status);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % kSwapStages;
+            if (!mbar_wait(&full[s], (i / kSwapStages) & 1, p.status)) break;
+            tc_fence_after();
+            const uint32_t w0 = smem_u32(sW + s * W_BYTES), x0 = smem_u32(sX + s * X_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+                umma_bf16(tmem, smem_desc(w0 + k * 32), smem_desc(x0 + k * 32), idesc, (i > 0 || k > 0) ? 1u : 0u);
+            umma_commit(&empty[s]);
+        }
+        umma_commit(&tfull);
+    } else if (warp >= 2) {
+        // ---- epilogue: warp q holds features f0 + 32 q + lane (its TMEM lane quadrant)
+        pdl_wait();
+        const int q = warp & 3;
+        const int f = f0 + q * 32 + lane;
+        float *stg = reinterpret_cast<float *>(sX + kSwapStages * X_BYTES) + q * 16 * 32;
+        const bool ok = mbar_wait(&tfull, 0, p.status);
+        tc_fence_after();
+        if (ok) {
+            for (int c0 = 0; c0 < ncol; c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+                if (p.swiglu_out != nullptr) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        // features 2i (gate) and 2i + 1 (up) sit in neighbouring lanes
+                        const int r = c0 + j;
+                        const float u = __shfl_xor_sync(0xffffffffu, v[j], 1);
+                        if (r < p.M && (lane & 1) == 0) {
+                            const float g = v[j];
+                            p.swiglu_out[(size_t)r * p.ld_swiglu + f / 2] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+                        }
+                    }
+                } else {
+                    // through the warp's 16 x 32 staging block: lane = feature on the way in, then
+                    // each instruction stores or reduce-adds 4 rows x 128 contiguous bytes
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = v[j];
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int rr = it * 4 + (lane >> 3), ch = lane & 7;
+                        const float4 x = reinterpret_cast<const float4 *>(stg)[rr * 8 + ch];
+                        const int r = c0 + rr;
+                        if (r < p.M) {
+                            float *o = p.out + (size_t)r * p.ld_out + f0 + q * 32 + ch * 4;
+                            if (p.accumulate)
+                                red_add_v4(o, x.x, x.y, x.z, x.w);
+                            else
+                                *reinterpret_cast<float4 *>(o) = x;
+                        }
+                    }
+                    __syncwarp();   // the block is rewritten by the next chunk
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tcols) : "memory");
+    }
+}
 }  // namespace tc
 }  // namespace talker_k
 
@@ -316,6 +456,7 @@ int tile_n_for(int M, int N) { return (tall(M) && N % kBNWide == 0) ? kBNWide : 
 bool gemm_tc_supported(int N, int K) { return N % kBNNarrow == 0 && K % tc::BK == 0 && K >= tc::BK; }
 
 int gemm_tc_splits(int M, int N, int K, int n_sm) {
+    if (gemm_tc_swap_ok(M, N, K)) return gemm_tc_swap_splits(M, N, K, n_sm);
     const int tiles = ((M + tc::BM - 1) / tc::BM) * (N / tile_n_for(M, N));
     const int nk = K / tc::BK;
     int s = (n_sm + tiles - 1) / tiles;
@@ -340,9 +481,67 @@ static cudaError_t raise_smem() {
                                 (int)smem_for(BN, STAGES));
 }
 
+namespace {
+// The swapped kernel's shared memory: weight and activation boxes of each stage, the
+// epilogue's staging blocks (4 warps x 16 x 32 f32) and alignment slack.
+size_t smem_swap(int M) {
+    const size_t ncol = (size_t)(M + 15) / 16 * 16;
+    return (size_t)tc::kSwapStages * (tc::BM + ncol) * tc::BK * 2 + 4 * 16 * 32 * 4 + 1024;
+}
+constexpr int kSwapMaxRows = 128;
+}  // namespace
+
 cudaError_t prepare_gemm_tc() {
     cudaError_t e = raise_smem<kBNNarrow, kStagesNarrow>();
-    return e ? e : raise_smem<kBNWide, kStagesWide>();
+    e = e ? e : raise_smem<kBNWide, kStagesWide>();
+    return e ? e : cudaFuncSetAttribute(tc::k_gemm_tc_swap, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem_swap(kSwapMaxRows));
+}
+
+bool gemm_tc_swap_ok(int M, int N, int K) {
+    return M >= 1 && M <= kSwapMaxRows && N % tc::BM == 0 && K % tc::BK == 0 && K >= tc::BK;
+}
+
+// K splits of the swapped kernel: one wave of CTAs (as many per SM as the shared memory of
+// this row count allows, at most two), at least two K blocks each.
+int gemm_tc_swap_splits(int M, int N, int K, int n_sm) {
+    const int tiles = N / tc::BM, nkb = K / tc::BK;
+    const int per_sm = std::max(1, std::min(2, (int)((228 * 1024) / (smem_swap(M) + 1024))));
+    const int s = std::max(1, n_sm * per_sm / tiles);
+    return std::max(1, std::min(s, nkb / 2));
+}
+
+cudaError_t launch_gemm_tc_swap(const void *X, int M, int K, const void *W, int N, float *out, int ld_out,
+                                int accumulate, int splits, __nv_bfloat16 *swiglu_out, int ld_swiglu, int *status,
+                                cudaStream_t st) {
+    if (!gemm_tc_swap_ok(M, N, K) || splits < 1 || splits > K / tc::BK || (swiglu_out != nullptr && splits != 1))
+        return cudaErrorInvalidValue;
+    if (swiglu_out == nullptr && (out == nullptr || ld_out % 4 != 0 || (reinterpret_cast<uintptr_t>(out) & 15u) != 0))
+        return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.out = out;
+    p.ld_out = ld_out;
+    p.accumulate = (accumulate || splits > 1) ? 1 : 0;
+    p.status = status;
+    p.swiglu_out = swiglu_out;
+    p.ld_swiglu = ld_swiglu;
+    CUtensorMap mw, mx;
+    const int ncol = (M + 15) / 16 * 16;
+    if (!make_map(&mw, W, N, K, tc::BM) || !make_map(&mx, X, M, K, ncol)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N / tc::BM) * splits, 1, 1);
+    cfg.blockDim = dim3(tc::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem_swap(M);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc::k_gemm_tc_swap, mw, mx, p, splits);
 }
 
 namespace {
@@ -381,6 +580,8 @@ cudaError_t launch_persist(const void *A, const void *B, GemmParams &p, int spli
 
 cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, float *out, int ld_out, int accumulate,
                            int splits, int *status, cudaStream_t st) {
+    if (gemm_tc_swap_ok(M, N, K) && splits <= K / tc::BK)
+        return launch_gemm_tc_swap(A, M, K, B, N, out, ld_out, accumulate, splits, nullptr, 0, status, st);
     GemmParams p{};
     p.M = M;
     p.N = N;
@@ -396,6 +597,8 @@ cudaError_t launch_gemm_tc_swiglu(const void *A, int M, int K, const void *B, in
                                   int *status, cudaStream_t st) {
     if (out_bf16 == nullptr || N % 32 != 0 || ld % 8 != 0 || (reinterpret_cast<uintptr_t>(out_bf16) & 15u) != 0)
         return cudaErrorInvalidValue;
+    if (gemm_tc_swap_ok(M, N, K))
+        return launch_gemm_tc_swap(A, M, K, B, N, nullptr, 0, 0, 1, out_bf16, ld, status, st);
     GemmParams p{};
     p.M = M;
     p.N = N;

@@ -209,6 +209,15 @@ cudaError_t launch_attn_prefill_tc(const AttnParams &a, int T, __nv_bfloat16 *kd
 bool gemm_tc_supported(int N, int K);
 int gemm_tc_splits(int M, int N, int K, int n_sm);
 cudaError_t prepare_gemm_tc();
+// Short products (M <= 128) with the weights as the MMA's M operand (k_gemm_tc_swap): X bf16
+// [M, K], W bf16 [N, K] (N % 128 == 0); out f32 [M, ld_out], reduce-added when accumulate or
+// splits > 1 (then out must hold zeros or the residual stream); or, with swiglu_out and one
+// split, bf16(silu(gate) * up) of interleaved weight rows into swiglu_out [M, N/2].
+bool gemm_tc_swap_ok(int M, int N, int K);
+int gemm_tc_swap_splits(int M, int N, int K, int n_sm);
+cudaError_t launch_gemm_tc_swap(const void *X, int M, int K, const void *W, int N, float *out, int ld_out,
+                                int accumulate, int splits, __nv_bfloat16 *swiglu_out, int ld_swiglu, int *status,
+                                cudaStream_t st);
 // A: bf16 [M, K], B: bf16 [N, K] (device); out: f32 [M, ld_out]. With splits > 1 the
 // result is reduce-added, so out must hold zeros (or the residual stream).
 cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, float *out, int ld_out, int accumulate,
