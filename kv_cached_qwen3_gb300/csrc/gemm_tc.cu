@@ -269,6 +269,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     unsigned char *sX = smem + kSwapStages * W_BYTES;
     __shared__ __align__(8) uint64_t full[kSwapStages], empty[kSwapStages], tfull;
     __shared__ uint32_t tmem_base_s;
+    __shared__ int last_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x / splits, sp = blockIdx.x - tile * splits;
@@ -340,12 +341,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float *stg = reinterpret_cast<float *>(sX + kSwapStages * X_BYTES) + q * 16 * 32;
         const bool ok = mbar_wait(&tfull, 0, p.status);
         tc_fence_after();
+        const bool direct_swiglu = p.swiglu_out != nullptr && p.fin_cnt == nullptr;
         if (ok) {
             for (int c0 = 0; c0 < ncol; c0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-#pragma unroll
-                if (p.swiglu_out != nullptr) {
+                if (direct_swiglu) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         // features 2i (gate) and 2i + 1 (up) sit in neighbouring lanes
@@ -377,6 +378,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     __syncwarp();   // the block is rewritten by the next chunk
                 }
+            }
+        }
+        if (p.fin_cnt != nullptr) {
+            // split-K SwiGLU: the CTA whose reduce-adds complete the tile finishes it (release by
+            // the fence before the count, acquire by the fence after it)
+            __threadfence();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (threadIdx.x == 64) last_s = atomicAdd(&p.fin_cnt[tile], 1) == splits - 1;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (last_s) {
+                __threadfence();
+                // 8 independent L2 reads in flight per thread, then their outputs
+                const int t = threadIdx.x - 64, n4 = p.M * 32;
+                for (int i0 = t; i0 < n4; i0 += 128 * 8) {
+                    float4 x[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int i = i0 + u * 128;
+                        if (i < n4)
+                            x[u] = __ldcg(reinterpret_cast<const float4 *>(p.out + (size_t)(i >> 5) * p.ld_out + f0 +
+                                                                           (i & 31) * 4));
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int i = i0 + u * 128;
+                        if (i < n4) {
+                            const int r = i >> 5, c = i & 31;
+                            __stcg(reinterpret_cast<float4 *>(p.out + (size_t)r * p.ld_out + f0 + c * 4),
+                                   make_float4(0.f, 0.f, 0.f, 0.f));
+                            *reinterpret_cast<__nv_bfloat162 *>(p.swiglu_out + (size_t)r * p.ld_swiglu + f0 / 2 + c * 2) =
+                                __floats2bfloat162_rn(x[u].x / (1.0f + expf(-x[u].x)) * x[u].y,
+                                                      x[u].z / (1.0f + expf(-x[u].z)) * x[u].w);
+                        }
+                    }
+                }
+                if (t == 0) p.fin_cnt[tile] = 0;
             }
         }
     }
@@ -513,11 +550,14 @@ int gemm_tc_swap_splits(int M, int N, int K, int n_sm) {
 
 cudaError_t launch_gemm_tc_swap(const void *X, int M, int K, const void *W, int N, float *out, int ld_out,
                                 int accumulate, int splits, __nv_bfloat16 *swiglu_out, int ld_swiglu, int *status,
-                                cudaStream_t st) {
-    if (!gemm_tc_swap_ok(M, N, K) || splits < 1 || splits > K / tc::BK || (swiglu_out != nullptr && splits != 1))
+                                cudaStream_t st, int *fin_cnt) {
+    if (!gemm_tc_swap_ok(M, N, K) || splits < 1 || splits > K / tc::BK ||
+        (swiglu_out != nullptr && fin_cnt == nullptr && splits != 1))
         return cudaErrorInvalidValue;
-    if (swiglu_out == nullptr && (out == nullptr || ld_out % 4 != 0 || (reinterpret_cast<uintptr_t>(out) & 15u) != 0))
+    if ((swiglu_out == nullptr || fin_cnt != nullptr) &&
+        (out == nullptr || ld_out % 4 != 0 || (reinterpret_cast<uintptr_t>(out) & 15u) != 0))
         return cudaErrorInvalidValue;
+    if (fin_cnt != nullptr && (swiglu_out == nullptr || ld_swiglu % 2 != 0)) return cudaErrorInvalidValue;
     GemmParams p{};
     p.M = M;
     p.N = N;
@@ -528,6 +568,8 @@ cudaError_t launch_gemm_tc_swap(const void *X, int M, int K, const void *W, int 
     p.status = status;
     p.swiglu_out = swiglu_out;
     p.ld_swiglu = ld_swiglu;
+    p.fin_cnt = fin_cnt;
+    if (fin_cnt != nullptr) p.accumulate = 1;
     CUtensorMap mw, mx;
     const int ncol = (M + 15) / 16 * 16;
     if (!make_map(&mw, W, N, K, tc::BM) || !make_map(&mx, X, M, K, ncol)) return cudaErrorInvalidValue;
@@ -542,6 +584,13 @@ cudaError_t launch_gemm_tc_swap(const void *X, int M, int K, const void *W, int 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, tc::k_gemm_tc_swap, mw, mx, p, splits);
+}
+
+cudaError_t launch_gemm_tc_swiglu_split(const void *A, int M, int K, const void *B, int N, float *acc,
+                                        __nv_bfloat16 *out_bf16, int ld, int *cnt, int splits, int *status,
+                                        cudaStream_t st) {
+    if (acc == nullptr || cnt == nullptr || out_bf16 == nullptr) return cudaErrorInvalidValue;
+    return launch_gemm_tc_swap(A, M, K, B, N, acc, N, 1, splits, out_bf16, ld, status, st, cnt);
 }
 
 namespace {

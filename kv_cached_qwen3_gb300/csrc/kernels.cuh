@@ -169,6 +169,10 @@ struct GemmParams {
     // swiglu_out[row, j] = bf16(silu(gate_j) * up_j) with row stride ld_swiglu.
     __nv_bfloat16 *swiglu_out;
     int ld_swiglu;
+    // Split-K SwiGLU (short-product kernel only): the K splits reduce-add [gate; up] into out,
+    // which holds zeros on entry; fin_cnt[tile] counts the splits that have landed, and the
+    // last one writes swiglu_out from the summed tile, zeroes the tile again and resets its counter.
+    int *fin_cnt;
 };
 
 constexpr int kGemvWarps = 8;
@@ -217,7 +221,13 @@ bool gemm_tc_swap_ok(int M, int N, int K);
 int gemm_tc_swap_splits(int M, int N, int K, int n_sm);
 cudaError_t launch_gemm_tc_swap(const void *X, int M, int K, const void *W, int N, float *out, int ld_out,
                                 int accumulate, int splits, __nv_bfloat16 *swiglu_out, int ld_swiglu, int *status,
-                                cudaStream_t st);
+                                cudaStream_t st, int *fin_cnt = nullptr);
+// Split-K gate/up with SwiGLU for M <= 128: acc f32 [M, N] must hold zeros and cnt [N / 128]
+// zeros on entry, and both hold zeros again when the kernel has finished; out_bf16 [M, N/2]
+// (row stride ld) receives bf16(silu(gate) * up).
+cudaError_t launch_gemm_tc_swiglu_split(const void *A, int M, int K, const void *B, int N, float *acc,
+                                        __nv_bfloat16 *out_bf16, int ld, int *cnt, int splits, int *status,
+                                        cudaStream_t st);
 // A: bf16 [M, K], B: bf16 [N, K] (device); out: f32 [M, ld_out]. With splits > 1 the
 // result is reduce-added, so out must hold zeros (or the residual stream).
 cudaError_t launch_gemm_tc(const void *A, int M, int K, const void *B, int N, float *out, int ld_out, int accumulate,
@@ -228,13 +238,18 @@ cudaError_t launch_gemm_tc_swiglu(const void *A, int M, int K, const void *B, in
 
 // Element-wise stages of the tensor-core prefill path (prefill.cu).
 // With gather.n > 0 the rows are first gathered from codebook tables and also written to x.
+// With zero != null the kernel also clears zero[0 .. zero_n) (zero_n % 4 == 0, 16-byte aligned):
+// the split-K accumulator of the GEMM that follows.
 cudaError_t launch_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int rows, int H, void *out,
-                                cudaStream_t st, const CodeGather *gather = nullptr, int *status = nullptr);
+                                cudaStream_t st, const CodeGather *gather = nullptr, int *status = nullptr,
+                                float *zero = nullptr, size_t zero_n = 0);
 // dense_kv (Q8_0 storage only, else null): the rows' k / v also go to bf16 [2][rows][n_kv][hd]
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
                             const float *k_norm, const float2 *rope, float eps, float *q_out, const CacheView &cache,
                             int layer, const RowMap &rm, int *status, cudaStream_t st,
                             __nv_bfloat16 *dense_kv = nullptr);
-cudaError_t launch_swiglu_bf16(const float *gu, int rows, int I, void *out, cudaStream_t st);
+// silu(gate) * up of a split-K [gate; up] sum; gu is zeroed behind the read (its split-K
+// accumulation always starts from zeros).
+cudaError_t launch_swiglu_bf16(float *gu, int rows, int I, void *out, cudaStream_t st);
 
 }  // namespace talker_k

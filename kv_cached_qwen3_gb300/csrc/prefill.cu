@@ -2,13 +2,15 @@
 // the tcgen05 GEMM):
 //   k_rmsnorm_bf16: x / sqrt(mean(x^2) + eps) * w, rounded to bf16 as the next
 //                   GEMM's A operand ("talker-forward.h", talker_layer_forward
-//                   pre-norm and MLP pre-norm);
+//                   pre-norm and MLP pre-norm); it also clears the split-K
+//                   accumulator of the GEMM that follows, when there is one;
 //   k_qkv_post:     per (row, head) of the raw projections: QK-RMSNorm with the
 //                   [hd] gain and NEOX RoPE at the row's position for q and k,
 //                   k and v appended to the cache at that position (set_rows),
 //                   q kept in f32 for attention;
 //   k_swiglu_bf16:  silu(gate) * up from the row-interleaved [gate; up]
-//                   projection (columns 2j, 2j+1), rounded to bf16.
+//                   projection (columns 2j, 2j+1), rounded to bf16; the f32 split-K
+//                   sum is zeroed behind the read, ready for the next accumulation.
 #include <math.h>
 
 #include <algorithm>
@@ -39,11 +41,16 @@ static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, c
 // One CTA per row: every thread stages its float4s of the row (one round trip), the sum of
 // squares is reduced across the CTA, then the scaled bf16 row is written.
 __global__ void k_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int rows, int H,
-                               __nv_bfloat16 *out, CodeGather gather, int *status) {
+                               __nv_bfloat16 *out, CodeGather gather, int *status, float4 *zero, size_t zero_n4) {
     __shared__ float red[32];
     const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
     pdl_wait();
+    if (zero != nullptr) {   // this CTA's share of the next GEMM's split-K accumulator
+        const size_t per = (zero_n4 + gridDim.x - 1) / gridDim.x;
+        const size_t b = (size_t)blockIdx.x * per, e = b + per < zero_n4 ? b + per : zero_n4;
+        for (size_t i = b + threadIdx.x; i < e; i += blockDim.x) zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const float *xr = x + (size_t)row * ld;
     constexpr int MAXV = 4;   // float4s per thread (H <= 4 * 4 * blockDim.x)
     float4 v[MAXV];
@@ -180,25 +187,30 @@ __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd
     }
 }
 
-__global__ void k_swiglu_bf16(const float *gu, int rows, int I, __nv_bfloat16 *out) {
+__global__ void k_swiglu_bf16(float *gu, int rows, int I, __nv_bfloat16 *out) {
     const size_t n = (size_t)rows * I;
     pdl_launch_dependents();
     pdl_wait();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const size_t r = i / I, j = i - r * I;
-        const float2 v = *reinterpret_cast<const float2 *>(gu + r * 2 * I + 2 * j);
+        float2 *src = reinterpret_cast<float2 *>(gu + r * 2 * I + 2 * j);
+        const float2 v = *src;
+        *src = make_float2(0.f, 0.f);
         out[i] = __float2bfloat16_rn(v.x / (1.0f + expf(-v.x)) * v.y);
     }
 }
 
 cudaError_t launch_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int rows, int H, void *out,
-                                cudaStream_t st, const CodeGather *gather, int *status) {
+                                cudaStream_t st, const CodeGather *gather, int *status, float *zero, size_t zero_n) {
     const int threads = 256;
     if (H % 4 || H > 4 * 4 * threads || (gather != nullptr && gather->n > 0 && status == nullptr))
         return cudaErrorInvalidValue;
+    if (zero != nullptr && (zero_n % 4 != 0 || (reinterpret_cast<uintptr_t>(zero) & 15u) != 0))
+        return cudaErrorInvalidValue;
     const CodeGather none{};
     return launch_pdl(k_rmsnorm_bf16, dim3(rows), dim3(threads), st, x, ld, w, eps, rows, H,
-                      static_cast<__nv_bfloat16 *>(out), gather ? *gather : none, status);
+                      static_cast<__nv_bfloat16 *>(out), gather ? *gather : none, status,
+                      reinterpret_cast<float4 *>(zero), zero != nullptr ? zero_n / 4 : (size_t)0);
 }
 
 cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd, const float *q_norm,
@@ -211,7 +223,7 @@ cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int h
                       raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, rm, status, dense_kv);
 }
 
-cudaError_t launch_swiglu_bf16(const float *gu, int rows, int I, void *out, cudaStream_t st) {
+cudaError_t launch_swiglu_bf16(float *gu, int rows, int I, void *out, cudaStream_t st) {
     const size_t n = (size_t)rows * I;
     const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
     return launch_pdl(k_swiglu_bf16, dim3(blocks), dim3(256), st, gu, rows, I, static_cast<__nv_bfloat16 *>(out));

@@ -113,7 +113,8 @@ struct talker {
     __nv_bfloat16 *kv_dense = nullptr;   // Q8_0 storage: the prefill's own k / v rows, [2][rows][n_kv][hd]
     __nv_bfloat16 *kd_tc = nullptr;      // tcgen05 prefill attention: K [n_kv][L][hd] and V^T [n_kv][hd][L]
     __nv_bfloat16 *vt_tc = nullptr;
-    float *gu = nullptr;
+    float *gu = nullptr;                 // split-K [gate; up] sums: all zeros between uses
+    int *gemm_cnt = nullptr;             // per-tile split counters of the split-K SwiGLU GEMM: zeros between uses
     int tc_ok = -1;                      // tensor-core prefill usable for this geometry (-1 unknown)
     // TTS loop input / output
     int suppress_tail = 0, suppress_eos = -1;   // head: logits [V - tail, V) except eos become -inf
@@ -164,7 +165,8 @@ void free_workspaces(talker *t) {
 
 void free_tc(talker *t) {
     void **bl[] = {&t->hb, &t->ab, &t->gb, reinterpret_cast<void **>(&t->gu), reinterpret_cast<void **>(&t->kv_dense),
-                   reinterpret_cast<void **>(&t->kd_tc), reinterpret_cast<void **>(&t->vt_tc)};
+                   reinterpret_cast<void **>(&t->kd_tc), reinterpret_cast<void **>(&t->vt_tc),
+                   reinterpret_cast<void **>(&t->gemm_cnt)};
     for (auto pp : bl) {
         free_ptr(*pp);
         *pp = nullptr;
@@ -562,7 +564,7 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
 constexpr int kTcMinRows = 16;        // prefills shorter than this stay on the GEMV kernels
 constexpr int kAttnTcMinRows = 256;   // tcgen05 prefill attention from two 128-row query tiles up (below,
                                       // its extra dense-copy launch and TMEM setup outweigh the tiles)
-constexpr int kTcMinDecodeRows = 4;   // decode batches at least this wide use the tensor-core GEMMs
+constexpr int kTcMinDecodeRows = 2;   // decode batches at least this wide use the tensor-core GEMMs
 
 bool tc_usable(talker *t) {
     if (t->tc_ok < 0) {
@@ -584,6 +586,9 @@ talker_status ensure_tc(talker *t, int rows) {
     TRY_CUDA(cudaMalloc(&t->ab, (size_t)cap * t->qd * 2));
     TRY_CUDA(cudaMalloc(&t->gb, (size_t)cap * t->I * 2));
     TRY_CUDA(cudaMalloc(&t->gu, (size_t)cap * 2 * t->I * sizeof(float)));
+    TRY_CUDA(cudaMemset(t->gu, 0, (size_t)cap * 2 * t->I * sizeof(float)));
+    TRY_CUDA(cudaMalloc(&t->gemm_cnt, (size_t)(2 * t->I / 128 + 1) * sizeof(int)));
+    TRY_CUDA(cudaMemset(t->gemm_cnt, 0, (size_t)(2 * t->I / 128 + 1) * sizeof(int)));
     if (t->kv_q8) TRY_CUDA(cudaMalloc(&t->kv_dense, (size_t)2 * cap * t->nkv * t->hd * 2));
     if (t->hd == 128) {   // keys of a call: up to the whole cache (an appended chunk reads every earlier key)
         const size_t lp = (size_t)attn_prefill_tc_lpad(std::max(cap, t->max_seq));
@@ -595,11 +600,11 @@ talker_status ensure_tc(talker *t, int rows) {
     return TALKER_OK;
 }
 
-// GEMM into `out`; with split-K into a non-residual output, zero it first.
+// GEMM into `out`: reduce-added into the residual stream, or (split-K into a non-residual
+// output) into zeros that an earlier kernel of the chain has written.
 talker_status tc_gemm(talker *t, cudaStream_t st, const void *A, int M, int K, const void *W, int N, float *out, int ld,
                       bool residual, int *nk) {
     const int splits = gemm_tc_splits(M, N, K, t->n_sm);
-    if (splits > 1 && !residual) TRY_CUDA(cudaMemsetAsync(out, 0, (size_t)M * ld * sizeof(float), st));
     TRY_CUDA(launch_gemm_tc(A, M, K, W, N, out, ld, residual ? 1 : 0, splits, t->d_status, st));
     ++*nk;
     return TALKER_OK;
@@ -618,8 +623,11 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         TRY_CUDA(cudaMemcpyAsync(t->x, emb, (size_t)T * t->H * sizeof(float), cudaMemcpyDeviceToDevice, st));
     for (int l = 0; l < t->c.n_layers; ++l) {
         const LayerDev &d = t->L[l];
+        // a split-K QKV projection accumulates into zeros: the RMSNorm clears raw first
+        const bool qkv_split = gemm_tc_splits(T, t->qkv_n, t->H, t->n_sm) > 1;
         TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.in_norm, t->c.rms_eps, T, t->H, t->hb, st,
-                                     l == 0 ? gather : nullptr, t->d_status));
+                                     l == 0 ? gather : nullptr, t->d_status, qkv_split ? t->raw : nullptr,
+                                     (size_t)T * t->qkv_n));
         ++nk;
         TRY(tc_gemm(t, st, t->hb, T, t->H, d.qkv, t->qkv_n, t->raw, t->qkv_n, false, &nk));
         if (rm.mode != 0) {   // prefill rows; decode rows are finished inside the attention kernel
@@ -680,9 +688,16 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         TRY(tc_gemm(t, st, t->ab, T, t->qd, d.o, t->H, t->x, t->H, true, &nk));
         TRY_CUDA(launch_rmsnorm_bf16(t->x, t->H, d.post_norm, t->c.rms_eps, T, t->H, t->hb, st));
         ++nk;
-        if (gemm_tc_splits(T, 2 * t->I, t->H, t->n_sm) == 1) {   // one K pass: SwiGLU in the GEMM epilogue
-            TRY_CUDA(launch_gemm_tc_swiglu(t->hb, T, t->H, d.gu, 2 * t->I, static_cast<__nv_bfloat16 *>(t->gb), t->I,
-                                                 t->d_status, st));
+        // gate/up + SwiGLU: in the GEMM epilogue (one K pass, or split-K finished by the last split
+        // of each tile), else split-K into the zeroed gu and a SwiGLU pass that zeroes it again
+        const int gu_splits = gemm_tc_splits(T, 2 * t->I, t->H, t->n_sm);
+        __nv_bfloat16 *gb = static_cast<__nv_bfloat16 *>(t->gb);
+        if (gu_splits == 1) {
+            TRY_CUDA(launch_gemm_tc_swiglu(t->hb, T, t->H, d.gu, 2 * t->I, gb, t->I, t->d_status, st));
+            ++nk;
+        } else if (gemm_tc_swap_ok(T, 2 * t->I, t->H)) {
+            TRY_CUDA(launch_gemm_tc_swiglu_split(t->hb, T, t->H, d.gu, 2 * t->I, t->gu, gb, t->I, t->gemm_cnt,
+                                                 gu_splits, t->d_status, st));
             ++nk;
         } else {
             TRY(tc_gemm(t, st, t->hb, T, t->H, d.gu, 2 * t->I, t->gu, 2 * t->I, false, &nk));
@@ -1095,10 +1110,40 @@ talker_status talker_test_gemm_swiglu_bf16(const void *A, int M, int K, const vo
         TRY_CUDA(cudaMemset(d_status, 0, sizeof(int)));
     }
     TRY_CUDA(prepare_gemm_tc());
-    TRY_CUDA(launch_gemm_tc_swiglu(A, M, K, B, N, static_cast<__nv_bfloat16 *>(out_bf16), N / 2, d_status,
-                                   static_cast<cudaStream_t>(cuda_stream)));
-    TRY_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)));
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    int n_sm = 0, dev = 0;
+    TRY_CUDA(cudaGetDevice(&dev));
+    TRY_CUDA(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+    const int splits = gemm_tc_splits(M, N, K, n_sm);
     int h = 0;
+    if (splits > 1 && gemm_tc_swap_ok(M, N, K)) {
+        // the runtime's split-K form: zeroed accumulator and counters, which must be zeros again after
+        const size_t acc_n = (size_t)M * N, cnt_n = (size_t)N / 128;
+        float *acc = nullptr;
+        int *cnt = nullptr;
+        TRY_CUDA(cudaMalloc(&acc, acc_n * sizeof(float)));
+        TRY_CUDA(cudaMalloc(&cnt, cnt_n * sizeof(int)));
+        TRY_CUDA(cudaMemsetAsync(acc, 0, acc_n * sizeof(float), st));
+        TRY_CUDA(cudaMemsetAsync(cnt, 0, cnt_n * sizeof(int), st));
+        TRY_CUDA(launch_gemm_tc_swiglu_split(A, M, K, B, N, acc, static_cast<__nv_bfloat16 *>(out_bf16), N / 2, cnt,
+                                             splits, d_status, st));
+        TRY_CUDA(cudaStreamSynchronize(st));
+        std::vector<float> a(acc_n);
+        std::vector<int> c(cnt_n);
+        TRY_CUDA(cudaMemcpy(a.data(), acc, acc_n * sizeof(float), cudaMemcpyDeviceToHost));
+        TRY_CUDA(cudaMemcpy(c.data(), cnt, cnt_n * sizeof(int), cudaMemcpyDeviceToHost));
+        cudaFree(acc);
+        cudaFree(cnt);
+        for (float v : a) h |= v != 0.f;
+        for (int v : c) h |= v != 0;
+        if (h) {
+            snprintf(g_last_error, sizeof(g_last_error), "split-K SwiGLU left its accumulator or counters non-zero");
+            return TALKER_EDEVICE;
+        }
+    } else {
+        TRY_CUDA(launch_gemm_tc_swiglu(A, M, K, B, N, static_cast<__nv_bfloat16 *>(out_bf16), N / 2, d_status, st));
+        TRY_CUDA(cudaStreamSynchronize(st));
+    }
     TRY_CUDA(cudaMemcpy(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost));
     return h ? TALKER_EDEVICE : TALKER_OK;
 }
