@@ -15,6 +15,13 @@
 //   scores: lane = (key, quarter of the head dimension); q for its quarter lives in registers;
 //           the four quarters are summed with two shuffles;
 //   P.V:    lane = HD/32 output dimensions; the warp's 8 probabilities come by shuffle.
+// With bf16 storage and head_dim 128 the tiles come through the pool's tensor maps instead
+// (128-byte swizzle, conflict-free 8 x 8 fragment loads) and a warp's 8 keys of a page go
+// through the tensor cores (mma.sync; the M = 16 operand rows carry the G query heads twice):
+//   scores: S[16 x 8 keys] = [hi(q); lo(q)] . K^T, m16n8k16 over the head dimension, with
+//           q split into two bf16 parts (hi + lo) whose products sum to the f32 score;
+//   P.V:    O[16 x 128] += [hi(p); lo(p)] . V, m16n8k8 over the warp's keys, V fragments by
+//           transposing 8 x 8 loads; the two row halves add up to the f32 product.
 // No CTA barrier separates the phases of a page; the warps meet only before a slot is
 // refilled and once at the end, where their partials are merged. Splits combine either
 // inside one thread-block cluster (every other rank pushes its partial into rank 0's shared
@@ -24,6 +31,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tcgen05.cuh"
 
 using namespace talker_dev;
 
@@ -81,6 +89,43 @@ __device__ __forceinline__ void q8x4(uint32_t w, float *f) {
     f[3] = __int_as_float(__byte_perm(v, 0x4B000000u, 0x7443)) - 8388736.0f;
 }
 
+// Byte offset of (row, dim) in a bf16 [64][128] tile loaded as two 64-dim boxes with the
+// 128-byte swizzle (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t sw128(int row, int dim) {
+    return (uint32_t)((dim >> 6) * 8192 + row * 128 + ((((dim & 63) >> 3) ^ (row & 7)) << 4) + (dim & 7) * 2);
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+// (lo, hi) as a bf16 pair, the first element in the low half
+__device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 lo, __nv_bfloat16 hi) {
+    return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
+// x = hi + lo with both parts bf16 (hi the rounded value, lo the rounded remainder)
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
+    hi = __float2bfloat16_rn(x);
+    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
 template <int G>
 __device__ __forceinline__ void dot8(const uint4 u, const float (&q)[G][8], float (&s)[G]) {
 #pragma unroll
@@ -101,15 +146,17 @@ __device__ __forceinline__ void dot8(const uint4 u, const float (&q)[G][8], floa
 }  // namespace
 
 // bf16 tile: [64][hd] values; Q8_0 tile: [64][hd] codes, then [64][hd / 32] fp16 scales.
-size_t attn_dec_keys_smem_bytes(int head_dim, int group, bool q8) {
+// The tensor-core form (mm) aligns its swizzled tiles to 1024 bytes.
+size_t attn_dec_keys_smem_bytes(int head_dim, int group, bool q8, bool mm) {
     const size_t tile = q8 ? (size_t)kPage * head_dim + (size_t)kPage * (head_dim / 32) * 2 : (size_t)kPage * head_dim * 2;
     const size_t gh = (size_t)group * head_dim;
     return 2 * (q8 ? kSlotsQ8 : kSlotsBf16) * tile + gh * 4 + 2 * (size_t)head_dim * 4 + kWarps * gh * 4 +
-           kAttnClusterMax * (gh + 2 * group) * 4;
+           kAttnClusterMax * (gh + 2 * group) * 4 + (mm ? 1024 : 0);
 }
 
-template <int HD, int G, bool Q8>
-__global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams p) {
+template <int HD, int G, bool Q8, bool MM>
+__global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams p, const __grid_constant__ KvMaps maps) {
+    static_assert(!MM || (!Q8 && HD == 128 && G <= 8), "tensor-core form: bf16 tiles, head_dim 128, G <= 8");
     constexpr int QD = HD / 4;                 // dims of a key that one lane scores
     constexpr int EPL = Q8 ? 16 : 8;           // elements per 16-byte load
     constexpr int NSUB = QD / EPL;             // 16-byte loads per lane per key
@@ -117,7 +164,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
     constexpr uint32_t kTile = Q8 ? kPage * HD + kPage * (HD / 32) * 2 : kPage * HD * 2;
     constexpr int kSlots = Q8 ? kSlotsQ8 : kSlotsBf16;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *kbuf = smem_raw;                                   // [kSlots][tile]
+    unsigned char *kbuf = MM ? reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                                 ~(uintptr_t)1023)
+                             : smem_raw;                              // [kSlots][tile]
     unsigned char *vbuf = kbuf + kSlots * kTile;                      // [kSlots][tile]
     float *q_s = reinterpret_cast<float *>(vbuf + kSlots * kTile);    // [G][HD], scaled
     float *knew = q_s + G * HD;                                       // this step's k, v row as stored
@@ -158,6 +207,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
     unsigned char *kpool = static_cast<unsigned char *>(p.cache.k);
     unsigned char *vpool = static_cast<unsigned char *>(p.cache.v);
     auto tile_of = [&](unsigned char *pool, int page) { return pool + (size_t)page * page_bytes + head_off; };
+    // tensor-map row of the tile's first key (tiles of all layers and heads of a page are consecutive)
+    const int rows_per_page = (int)(p.cache.page_elems / HD);
+    const int tile_row = (p.layer * p.cache.n_kv + g) * kPage;
+    auto issue = [&](int slot, int page) {
+        mbar_arrive_expect_tx(&bars[slot], 2 * kTile);
+        if constexpr (MM) {
+            const int y = page * rows_per_page + tile_row;
+            tc::tma_load_2d(kbuf + slot * kTile, &maps.k, 0, y, &bars[slot]);
+            tc::tma_load_2d(kbuf + slot * kTile + kTile / 2, &maps.k, 64, y, &bars[slot]);
+            tc::tma_load_2d(vbuf + slot * kTile, &maps.v, 0, y, &bars[slot]);
+            tc::tma_load_2d(vbuf + slot * kTile + kTile / 2, &maps.v, 64, y, &bars[slot]);
+        } else {
+            bulk_g2s(kbuf + slot * kTile, tile_of(kpool, page), kTile, &bars[slot]);
+            bulk_g2s(vbuf + slot * kTile, tile_of(vpool, page), kTile, &bars[slot]);
+        }
+    };
 
     uint32_t rank = 0;
     if (clustered) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
@@ -168,11 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
     }
     __syncthreads();
     if (tid == 0 && has) {
-        for (int b = 0; b < kSlots && pb + b < pe; ++b) {
-            mbar_arrive_expect_tx(&bars[b], 2 * kTile);
-            bulk_g2s(kbuf + b * kTile, tile_of(kpool, ptab[pb + b]), kTile, &bars[b]);
-            bulk_g2s(vbuf + b * kTile, tile_of(vpool, ptab[pb + b]), kTile, &bars[b]);
-        }
+        for (int b = 0; b < kSlots && pb + b < pe; ++b) issue(b, ptab[pb + b]);
     }
     if (clustered) {
         // rank 0's receive barrier is initialised before any rank can arrive on it; ranks without
@@ -254,204 +315,327 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_dec_keys(const AttnParams 
     }
     __syncthreads();
 
-    // per-warp online softmax state
-    float m[G], l[G], o[G][PD];
+    if constexpr (MM) {
+        // Lane (h = lane / 4, c = 2 (lane % 4)): S rows h (hi) and h + 8 (lo) of keys c, c + 1 of
+        // the warp's 8; the same lane holds O rows h, h + 8 of dims 8 n + c, c + 1 (n = 0..15).
+        const int h = lane >> 2, c2 = (lane & 3) * 2;
+        float mh = -INFINITY, lh = 0.f;
+        float o[16][4];
 #pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-        m[gi] = -INFINITY;
-        l[gi] = 0.f;
+        for (int n = 0; n < 16; ++n)
 #pragma unroll
-        for (int d = 0; d < PD; ++d) o[gi][d] = 0.f;
-    }
-    const int kk = warp * 8 + (lane >> 2), quarter = lane & 3;
-    bool failed = false;
-    int fail_it = 0;
-    if (has) {
-        float qr[G][NSUB][EPL];   // q over this lane's quarter, in the lane's load order
-        auto sub_of = [&](int i) { return Q8 ? rot_q8<HD>(i, kk) : rot<HD>(i, kk, quarter); };
+            for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
+        bool failed = false;
+        int fail_it = 0;
+        if (has) {
+            uint32_t qf[8][4];   // A fragments of [hi(q); lo(q)] per 16-dim step
 #pragma unroll
-        for (int gi = 0; gi < G; ++gi)
+            for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-            for (int i = 0; i < NSUB; ++i) {
-                const float *qs = q_s + gi * HD + quarter * QD + sub_of(i) * EPL;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) qr[gi][i][e] = qs[e];
-            }
-        for (int pg = pb, it = 0; pg < pe; ++pg, ++it) {
-            const int slot = it % kSlots;
-            const bool ok = mbar_wait(&bars[slot], (it / kSlots) & 1, p.status);
-            if (__syncthreads_or(!ok)) {
-                failed = true;
-                fail_it = it;
-                break;
-            }
-            unsigned char *Ks = kbuf + slot * kTile;
-            unsigned char *Vs = vbuf + slot * kTile;
-            const int valid = min(kPage, nvis - pg * kPage);
-            const int newest = pos - pg * kPage;   // the fresh row, when this page holds it
-            if (!Q8 && newest >= 0 && newest < kPage && (newest >> 3) == warp) {
-                // only this warp reads that row: patch the stored values in (the copy may predate them)
-                __nv_bfloat16 *kr = reinterpret_cast<__nv_bfloat16 *>(Ks) + newest * HD;
-                __nv_bfloat16 *vr = reinterpret_cast<__nv_bfloat16 *>(Vs) + newest * HD;
-                for (int i = lane; i < HD; i += 32) {
-                    kr[i] = __float2bfloat16_rn(knew[i]);
-                    vr[i] = __float2bfloat16_rn(vnew[i]);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int d = ks * 16 + hf * 8 + c2;
+                    const float x0 = h < G ? q_s[h * HD + d] : 0.f, x1 = h < G ? q_s[h * HD + d + 1] : 0.f;
+                    __nv_bfloat16 h0, l0, h1, l1;
+                    split_bf16(x0, h0, l0);
+                    split_bf16(x1, h1, l1);
+                    qf[ks][2 * hf] = pack_bf16(h0, h1);
+                    qf[ks][2 * hf + 1] = pack_bf16(l0, l1);
                 }
-                __syncwarp();
-            }
-            // scores of key kk for every head
-            float sc[G];
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi) sc[gi] = 0.f;
-            if constexpr (!Q8) {
-                const uint32_t krow = smem_u32(Ks) + (uint32_t)(kk * HD + quarter * QD) * 2;
-#pragma unroll
-                for (int i = 0; i < NSUB; ++i) {
-                    const uint4 u = lds_u4(krow + rot<HD>(i, kk, quarter) * 16);
-                    float qv[G][8];
-#pragma unroll
-                    for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) qv[gi][e] = qr[gi][i][e];
-                    dot8<G>(u, qv, sc);
+            const int lrow = warp * 8 + (lane & 7);   // the key row this lane addresses in 8 x 8 loads
+            const int key0 = warp * 8 + c2;
+            for (int pg = pb, it = 0; pg < pe; ++pg, ++it) {
+                const int slot = it % kSlots;
+                const bool ok = mbar_wait(&bars[slot], (it / kSlots) & 1, p.status);
+                if (__syncthreads_or(!ok)) {
+                    failed = true;
+                    fail_it = it;
+                    break;
                 }
-            } else if (kk == newest) {   // this step's own row, exact
-#pragma unroll
-                for (int i = 0; i < NSUB; ++i)
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) {
-                        const float x = knew[quarter * QD + sub_of(i) * EPL + e];
-#pragma unroll
-                        for (int gi = 0; gi < G; ++gi) sc[gi] = fmaf(qr[gi][i][e], x, sc[gi]);
+                unsigned char *Ks = kbuf + slot * kTile;
+                unsigned char *Vs = vbuf + slot * kTile;
+                const int valid = min(kPage, nvis - pg * kPage);
+                const int newest = pos - pg * kPage;
+                if (newest >= 0 && newest < kPage && (newest >> 3) == warp) {
+                    // only this warp reads that row: patch the stored values in (the copy may predate them)
+                    for (int i = lane; i < HD; i += 32) {
+                        *reinterpret_cast<__nv_bfloat16 *>(Ks + sw128(newest, i)) = __float2bfloat16_rn(knew[i]);
+                        *reinterpret_cast<__nv_bfloat16 *>(Vs + sw128(newest, i)) = __float2bfloat16_rn(vnew[i]);
                     }
-            } else {   // codes times q, then the block's scale
-                const uint32_t krow = smem_u32(Ks) + (uint32_t)(kk * HD + quarter * QD);
+                    __syncwarp();
+                }
+                const uint32_t kb = smem_u32(Ks), vb = smem_u32(Vs);
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < NSUB; ++i) {
-                    const uint4 u = lds_u4(krow + sub_of(i) * 16);
-                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                for (int kp = 0; kp < 4; ++kp) {   // 32 dims: two m16n8k16 steps
+                    uint32_t b[4];
+                    ldsm_x4(kb + sw128(lrow, kp * 32 + (lane >> 3) * 8), b);
+                    mma_16816(sc, qf[2 * kp], b[0], b[1]);
+                    mma_16816(sc, qf[2 * kp + 1], b[2], b[3]);
+                }
+                const bool v0 = h < G && key0 < valid, v1 = h < G && key0 + 1 < valid;
+                const float s0 = v0 ? sc[0] + sc[2] : -INFINITY, s1 = v1 ? sc[1] + sc[3] : -INFINITY;
+                float mx = fmaxf(s0, s1);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_new = fmaxf(mh, mx);
+                const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(mh - m_new);
+                const float p0 = v0 ? exp2f(s0 - m_new) : 0.f, p1 = v1 ? exp2f(s1 - m_new) : 0.f;
+                float ls = p0 + p1;
+                ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+                ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+                lh = lh * alpha + ls;
+                mh = m_new;
 #pragma unroll
-                    for (int wq = 0; wq < 4; ++wq) {
-                        float c4[4];
-                        q8x4(w4[wq], c4);
+                for (int n = 0; n < 16; ++n)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
+                    for (int e = 0; e < 4; ++e) o[n][e] *= alpha;
+                __nv_bfloat16 ph0, pl0, ph1, pl1;
+                split_bf16(p0, ph0, pl0);
+                split_bf16(p1, ph1, pl1);
+                const uint32_t pa0 = pack_bf16(ph0, ph1), pa1 = pack_bf16(pl0, pl1);
+                // keys past the window: their V values are never multiplied in (zeroed fragments)
+                const bool partial = valid < kPage;
+                const bool kv0 = key0 < valid, kv1 = key0 + 1 < valid;
+                const uint32_t vmask = (kv0 ? 0x0000ffffu : 0u) | (kv1 ? 0xffff0000u : 0u);
 #pragma unroll
-                            for (int gi = 0; gi < G; ++gi) sc[gi] = fmaf(qr[gi][i][wq * 4 + e], c4[e], sc[gi]);
+                for (int j = 0; j < 4; ++j) {   // 32 dims: four m16n8k8 steps
+                    uint32_t b[4];
+                    ldsm_x4_t(vb + sw128(lrow, (4 * j + (lane >> 3)) * 8), b);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) mma_1688(o[4 * j + u], pa0, pa1, partial ? b[u] & vmask : b[u]);
+                }
+                if (pg + kSlots < pe) {   // refill this slot once every warp is done with it
+                    __syncthreads();
+                    if (tid == 0) {
+                        fence_proxy_async();
+                        issue(slot, ptab[pg + kSlots]);
                     }
                 }
-                const float sd = __half2float(*reinterpret_cast<const __half *>(
-                    Ks + kPage * HD + (kk * (HD / 32) + (quarter * QD) / 32) * 2));
-#pragma unroll
-                for (int gi = 0; gi < G; ++gi) sc[gi] *= sd;
             }
-            const bool kval = kk < valid;
-            float pk[G];
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi) {
-                float s = sc[gi];
-                s += __shfl_xor_sync(0xffffffffu, s, 1);
-                s += __shfl_xor_sync(0xffffffffu, s, 2);
-                s = kval ? s : -INFINITY;
-                float mx = s;
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_new = fmaxf(m[gi], mx);
-                const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m[gi] - m_new);
-                pk[gi] = kval ? exp2f(s - m_new) : 0.f;
-                float ls = pk[gi];
-                ls += __shfl_xor_sync(0xffffffffu, ls, 4);
-                ls += __shfl_xor_sync(0xffffffffu, ls, 8);
-                ls += __shfl_xor_sync(0xffffffffu, ls, 16);
-                l[gi] = l[gi] * alpha + ls;
-                m[gi] = m_new;
-#pragma unroll
-                for (int d = 0; d < PD; ++d) o[gi][d] *= alpha;
-            }
-            // P.V over the warp's 8 keys (rows past the window are skipped: their contents are
-            // never read into the arithmetic)
-            const uint32_t vbase = smem_u32(Vs) + (uint32_t)(lane * PD) * (Q8 ? 1 : 2);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int key = warp * 8 + j;
-                float pj[G];
-#pragma unroll
-                for (int gi = 0; gi < G; ++gi) pj[gi] = __shfl_sync(0xffffffffu, pk[gi], j * 4);
-                if (key < valid) {
-                    float v[PD];
-                    if constexpr (Q8) {
-                        if (key == newest) {   // this step's own row, exact
-#pragma unroll
-                            for (int d = 0; d < PD; ++d) v[d] = vnew[lane * PD + d];
-                        } else {
-                            float c4[4];
-                            uint32_t w;
-                            if constexpr (PD == 4) asm("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(vbase + (uint32_t)key * HD));
-                            else w = lds_u16(vbase + (uint32_t)key * HD);
-                            q8x4(w, c4);
-                            const float sd = __half2float(*reinterpret_cast<const __half *>(
-                                Vs + kPage * HD + (key * (HD / 32) + (lane * PD) / 32) * 2));
-#pragma unroll
-                            for (int d = 0; d < PD; ++d) v[d] = c4[d] * sd;
-                        }
-                    } else if constexpr (PD == 4) {
-                        const uint2 u = lds_u2(vbase + (uint32_t)key * HD * 2);
-                        v[0] = bf16lo(u.x);
-                        v[1] = bf16hi(u.x);
-                        v[2] = bf16lo(u.y);
-                        v[3] = bf16hi(u.y);
-                    } else {
-                        uint32_t u;
-                        asm("ld.shared.u32 %0, [%1];" : "=r"(u) : "r"(vbase + (uint32_t)key * HD * 2));
-                        v[0] = bf16lo(u);
-                        v[1] = bf16hi(u);
-                    }
-#pragma unroll
-                    for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                        for (int d = 0; d < PD; ++d) o[gi][d] = fmaf(pj[gi], v[d], o[gi][d]);
-                }
-            }
-            if (pg + kSlots < pe) {   // refill this slot once every warp is done with it
+            if (failed) {
+                if (tid == 0)
+                    for (int j = fail_it; j < fail_it + kSlots && pb + j < pe; ++j)
+                        mbar_wait(&bars[j % kSlots], (j / kSlots) & 1, p.status);
                 __syncthreads();
-                if (tid == 0) {
-                    fence_proxy_async();
-                    mbar_arrive_expect_tx(&bars[slot], 2 * kTile);
-                    bulk_g2s(Ks, tile_of(kpool, ptab[pg + kSlots]), kTile, &bars[slot]);
-                    bulk_g2s(Vs, tile_of(vpool, ptab[pg + kSlots]), kTile, &bars[slot]);
+                mh = -INFINITY;
+                lh = 0.f;
+#pragma unroll
+                for (int n = 0; n < 16; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
+            }
+        }
+        // this warp's partial: lane 4h holds (m, l) of head h, rows h and h + 8 sum to O
+        if (h < G) {
+            if ((lane & 3) == 0) {
+                wm[warp][h] = mh;
+                wl[warp][h] = lh;
+            }
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                float *dst = ow + (warp * G + h) * HD + n * 8 + c2;
+                dst[0] = o[n][0] + o[n][2];
+                dst[1] = o[n][1] + o[n][3];
+            }
+        }
+    } else {
+        // per-warp online softmax state
+        float m[G], l[G], o[G][PD];
+    #pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+            m[gi] = -INFINITY;
+            l[gi] = 0.f;
+    #pragma unroll
+            for (int d = 0; d < PD; ++d) o[gi][d] = 0.f;
+        }
+        const int kk = warp * 8 + (lane >> 2), quarter = lane & 3;
+        bool failed = false;
+        int fail_it = 0;
+        if (has) {
+            float qr[G][NSUB][EPL];   // q over this lane's quarter, in the lane's load order
+            auto sub_of = [&](int i) { return Q8 ? rot_q8<HD>(i, kk) : rot<HD>(i, kk, quarter); };
+    #pragma unroll
+            for (int gi = 0; gi < G; ++gi)
+    #pragma unroll
+                for (int i = 0; i < NSUB; ++i) {
+                    const float *qs = q_s + gi * HD + quarter * QD + sub_of(i) * EPL;
+    #pragma unroll
+                    for (int e = 0; e < EPL; ++e) qr[gi][i][e] = qs[e];
+                }
+            for (int pg = pb, it = 0; pg < pe; ++pg, ++it) {
+                const int slot = it % kSlots;
+                const bool ok = mbar_wait(&bars[slot], (it / kSlots) & 1, p.status);
+                if (__syncthreads_or(!ok)) {
+                    failed = true;
+                    fail_it = it;
+                    break;
+                }
+                unsigned char *Ks = kbuf + slot * kTile;
+                unsigned char *Vs = vbuf + slot * kTile;
+                const int valid = min(kPage, nvis - pg * kPage);
+                const int newest = pos - pg * kPage;   // the fresh row, when this page holds it
+                if (!Q8 && newest >= 0 && newest < kPage && (newest >> 3) == warp) {
+                    // only this warp reads that row: patch the stored values in (the copy may predate them)
+                    __nv_bfloat16 *kr = reinterpret_cast<__nv_bfloat16 *>(Ks) + newest * HD;
+                    __nv_bfloat16 *vr = reinterpret_cast<__nv_bfloat16 *>(Vs) + newest * HD;
+                    for (int i = lane; i < HD; i += 32) {
+                        kr[i] = __float2bfloat16_rn(knew[i]);
+                        vr[i] = __float2bfloat16_rn(vnew[i]);
+                    }
+                    __syncwarp();
+                }
+                // scores of key kk for every head
+                float sc[G];
+    #pragma unroll
+                for (int gi = 0; gi < G; ++gi) sc[gi] = 0.f;
+                if constexpr (!Q8) {
+                    const uint32_t krow = smem_u32(Ks) + (uint32_t)(kk * HD + quarter * QD) * 2;
+    #pragma unroll
+                    for (int i = 0; i < NSUB; ++i) {
+                        const uint4 u = lds_u4(krow + rot<HD>(i, kk, quarter) * 16);
+                        float qv[G][8];
+    #pragma unroll
+                        for (int gi = 0; gi < G; ++gi)
+    #pragma unroll
+                            for (int e = 0; e < 8; ++e) qv[gi][e] = qr[gi][i][e];
+                        dot8<G>(u, qv, sc);
+                    }
+                } else if (kk == newest) {   // this step's own row, exact
+    #pragma unroll
+                    for (int i = 0; i < NSUB; ++i)
+    #pragma unroll
+                        for (int e = 0; e < EPL; ++e) {
+                            const float x = knew[quarter * QD + sub_of(i) * EPL + e];
+    #pragma unroll
+                            for (int gi = 0; gi < G; ++gi) sc[gi] = fmaf(qr[gi][i][e], x, sc[gi]);
+                        }
+                } else {   // codes times q, then the block's scale
+                    const uint32_t krow = smem_u32(Ks) + (uint32_t)(kk * HD + quarter * QD);
+    #pragma unroll
+                    for (int i = 0; i < NSUB; ++i) {
+                        const uint4 u = lds_u4(krow + sub_of(i) * 16);
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+    #pragma unroll
+                        for (int wq = 0; wq < 4; ++wq) {
+                            float c4[4];
+                            q8x4(w4[wq], c4);
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e)
+    #pragma unroll
+                                for (int gi = 0; gi < G; ++gi) sc[gi] = fmaf(qr[gi][i][wq * 4 + e], c4[e], sc[gi]);
+                        }
+                    }
+                    const float sd = __half2float(*reinterpret_cast<const __half *>(
+                        Ks + kPage * HD + (kk * (HD / 32) + (quarter * QD) / 32) * 2));
+    #pragma unroll
+                    for (int gi = 0; gi < G; ++gi) sc[gi] *= sd;
+                }
+                const bool kval = kk < valid;
+                float pk[G];
+    #pragma unroll
+                for (int gi = 0; gi < G; ++gi) {
+                    float s = sc[gi];
+                    s += __shfl_xor_sync(0xffffffffu, s, 1);
+                    s += __shfl_xor_sync(0xffffffffu, s, 2);
+                    s = kval ? s : -INFINITY;
+                    float mx = s;
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_new = fmaxf(m[gi], mx);
+                    const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m[gi] - m_new);
+                    pk[gi] = kval ? exp2f(s - m_new) : 0.f;
+                    float ls = pk[gi];
+                    ls += __shfl_xor_sync(0xffffffffu, ls, 4);
+                    ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+                    ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+                    l[gi] = l[gi] * alpha + ls;
+                    m[gi] = m_new;
+    #pragma unroll
+                    for (int d = 0; d < PD; ++d) o[gi][d] *= alpha;
+                }
+                // P.V over the warp's 8 keys (rows past the window are skipped: their contents are
+                // never read into the arithmetic)
+                const uint32_t vbase = smem_u32(Vs) + (uint32_t)(lane * PD) * (Q8 ? 1 : 2);
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int key = warp * 8 + j;
+                    float pj[G];
+    #pragma unroll
+                    for (int gi = 0; gi < G; ++gi) pj[gi] = __shfl_sync(0xffffffffu, pk[gi], j * 4);
+                    if (key < valid) {
+                        float v[PD];
+                        if constexpr (Q8) {
+                            if (key == newest) {   // this step's own row, exact
+    #pragma unroll
+                                for (int d = 0; d < PD; ++d) v[d] = vnew[lane * PD + d];
+                            } else {
+                                float c4[4];
+                                uint32_t w;
+                                if constexpr (PD == 4) asm("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(vbase + (uint32_t)key * HD));
+                                else w = lds_u16(vbase + (uint32_t)key * HD);
+                                q8x4(w, c4);
+                                const float sd = __half2float(*reinterpret_cast<const __half *>(
+                                    Vs + kPage * HD + (key * (HD / 32) + (lane * PD) / 32) * 2));
+    #pragma unroll
+                                for (int d = 0; d < PD; ++d) v[d] = c4[d] * sd;
+                            }
+                        } else if constexpr (PD == 4) {
+                            const uint2 u = lds_u2(vbase + (uint32_t)key * HD * 2);
+                            v[0] = bf16lo(u.x);
+                            v[1] = bf16hi(u.x);
+                            v[2] = bf16lo(u.y);
+                            v[3] = bf16hi(u.y);
+                        } else {
+                            uint32_t u;
+                            asm("ld.shared.u32 %0, [%1];" : "=r"(u) : "r"(vbase + (uint32_t)key * HD * 2));
+                            v[0] = bf16lo(u);
+                            v[1] = bf16hi(u);
+                        }
+    #pragma unroll
+                        for (int gi = 0; gi < G; ++gi)
+    #pragma unroll
+                            for (int d = 0; d < PD; ++d) o[gi][d] = fmaf(pj[gi], v[d], o[gi][d]);
+                    }
+                }
+                if (pg + kSlots < pe) {   // refill this slot once every warp is done with it
+                    __syncthreads();
+                    if (tid == 0) {
+                        fence_proxy_async();
+                        issue(slot, ptab[pg + kSlots]);
+                    }
+                }
+            }
+            if (failed) {
+                // give the copies still in flight a bounded chance to land before the CTA moves on
+                if (tid == 0)
+                    for (int j = fail_it; j < fail_it + kSlots && pb + j < pe; ++j)
+                        mbar_wait(&bars[j % kSlots], (j / kSlots) & 1, p.status);
+                __syncthreads();
+    #pragma unroll
+                for (int gi = 0; gi < G; ++gi) {
+                    m[gi] = -INFINITY;
+                    l[gi] = 0.f;
+    #pragma unroll
+                    for (int d = 0; d < PD; ++d) o[gi][d] = 0.f;
                 }
             }
         }
-        if (failed) {
-            // give the copies still in flight a bounded chance to land before the CTA moves on
-            if (tid == 0)
-                for (int j = fail_it; j < fail_it + kSlots && pb + j < pe; ++j)
-                    mbar_wait(&bars[j % kSlots], (j / kSlots) & 1, p.status);
-            __syncthreads();
-#pragma unroll
+
+        // merge the warps (one barrier): thread t takes output t, scaling each warp's partial by
+        // 2^(m_w - M) and adding them in warp order (deterministic)
+        if (lane == 0) {
+    #pragma unroll
             for (int gi = 0; gi < G; ++gi) {
-                m[gi] = -INFINITY;
-                l[gi] = 0.f;
-#pragma unroll
-                for (int d = 0; d < PD; ++d) o[gi][d] = 0.f;
+                wm[warp][gi] = m[gi];
+                wl[warp][gi] = l[gi];
             }
         }
+    #pragma unroll
+        for (int gi = 0; gi < G; ++gi)
+    #pragma unroll
+            for (int d = 0; d < PD; ++d) ow[(warp * G + gi) * HD + lane * PD + d] = o[gi][d];
     }
-
-    // merge the warps (one barrier): thread t takes output t, scaling each warp's partial by
-    // 2^(m_w - M) and adding them in warp order (deterministic)
-    if (lane == 0) {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            wm[warp][gi] = m[gi];
-            wl[warp][gi] = l[gi];
-        }
-    }
-#pragma unroll
-    for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-        for (int d = 0; d < PD; ++d) ow[(warp * G + gi) * HD + lane * PD + d] = o[gi][d];
     __syncthreads();
 
     const int hq0 = g * G;
@@ -593,12 +777,12 @@ bool attn_dec_keys_supported(int kv_kind, int head_dim, const AttnParams &p) {
            p.rowmap.mode == 0 && p.raw != nullptr && (!p.cluster || p.splits <= kAttnClusterMax);
 }
 
-template <int HD, int G, bool Q8>
+template <int HD, int G, bool Q8, bool MM>
 static cudaError_t launch_keys_t(const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits, p.n_kv, rows);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = attn_dec_keys_smem_bytes(HD, G, Q8);
+    cfg.dynamicSmemBytes = attn_dec_keys_smem_bytes(HD, G, Q8, MM);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -612,15 +796,22 @@ static cudaError_t launch_keys_t(const AttnParams &p, int rows, cudaStream_t st,
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, k_attn_dec_keys<HD, G, Q8>, p);
+    static const KvMaps none{};
+    return cudaLaunchKernelEx(&cfg, k_attn_dec_keys<HD, G, Q8, MM>, p, MM ? *p.cache.maps : none);
 }
 
 template <bool Q8>
 static cudaError_t launch_keys_q(int head_dim, const AttnParams &p, int rows, cudaStream_t st, bool pdl) {
-    if (head_dim == 128)
-        return p.group == 2 ? launch_keys_t<128, 2, Q8>(p, rows, st, pdl) : launch_keys_t<128, 1, Q8>(p, rows, st, pdl);
+    if (head_dim == 128) {
+        if (!Q8 && p.cache.maps != nullptr)   // bf16 tiles through the tensor maps, tensor-core scores and P.V
+            return p.group == 2 ? launch_keys_t<128, 2, false, true>(p, rows, st, pdl)
+                                : launch_keys_t<128, 1, false, true>(p, rows, st, pdl);
+        return p.group == 2 ? launch_keys_t<128, 2, Q8, false>(p, rows, st, pdl)
+                            : launch_keys_t<128, 1, Q8, false>(p, rows, st, pdl);
+    }
     if (head_dim == 64)
-        return p.group == 2 ? launch_keys_t<64, 2, Q8>(p, rows, st, pdl) : launch_keys_t<64, 1, Q8>(p, rows, st, pdl);
+        return p.group == 2 ? launch_keys_t<64, 2, Q8, false>(p, rows, st, pdl)
+                            : launch_keys_t<64, 1, Q8, false>(p, rows, st, pdl);
     return cudaErrorInvalidValue;
 }
 
@@ -628,18 +819,23 @@ cudaError_t launch_attn_dec_keys(int kv_kind, int head_dim, const AttnParams &p,
     return kv_kind == 2 ? launch_keys_q<true>(head_dim, p, rows, st, pdl) : launch_keys_q<false>(head_dim, p, rows, st, pdl);
 }
 
-template <bool Q8>
-static cudaError_t raise_keys() {
-    const int bytes = (int)attn_dec_keys_smem_bytes(128, 2, Q8);
-    cudaError_t e = cudaFuncSetAttribute(k_attn_dec_keys<128, 2, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    e = e ? e : cudaFuncSetAttribute(k_attn_dec_keys<128, 1, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    e = e ? e : cudaFuncSetAttribute(k_attn_dec_keys<64, 2, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    return e ? e : cudaFuncSetAttribute(k_attn_dec_keys<64, 1, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+template <int HD, int G, bool Q8, bool MM>
+static cudaError_t raise_one() {
+    return cudaFuncSetAttribute(k_attn_dec_keys<HD, G, Q8, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)attn_dec_keys_smem_bytes(HD, G, Q8, MM));
 }
 
 cudaError_t prepare_attn_dec_keys() {
-    cudaError_t e = raise_keys<false>();
-    return e ? e : raise_keys<true>();
+    cudaError_t e = raise_one<128, 2, false, false>();
+    e = e ? e : raise_one<128, 1, false, false>();
+    e = e ? e : raise_one<64, 2, false, false>();
+    e = e ? e : raise_one<64, 1, false, false>();
+    e = e ? e : raise_one<128, 2, true, false>();
+    e = e ? e : raise_one<128, 1, true, false>();
+    e = e ? e : raise_one<64, 2, true, false>();
+    e = e ? e : raise_one<64, 1, true, false>();
+    e = e ? e : raise_one<128, 2, false, true>();
+    return e ? e : raise_one<128, 1, false, true>();
 }
 
 }  // namespace talker_k

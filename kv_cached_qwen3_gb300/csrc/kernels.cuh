@@ -2,6 +2,7 @@
 // kernel translation units and by the host runtime (talker_runtime.cu).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -36,7 +37,19 @@ __device__ __forceinline__ int rowmap_pos(const RowMap &m, int r) {
 
 // The paged KV cache. Page = [n_layers][n_kv][kPage][head_dim] elements; the
 // position p of stream s lives in page page_table[s * pages_per_stream + p / kPage].
+// Tensor maps of a bf16 K and V pool with head_dim 128, viewed as [pool rows][128] (a
+// (page, layer, head) tile is 64 consecutive rows): boxes of 64 rows x 64 dims, 128-byte swizzle.
+struct KvMaps {
+    CUtensorMap k, v;
+};
+
+// Tensor map of a bf16 matrix [rows][cols] (row stride in bytes, a multiple of 16), boxes of
+// box_cols x box_rows with the 128-byte swizzle (box_cols * 2 == 128), zero fill (gemm_tc.cu).
+bool make_map_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint64_t row_stride_bytes,
+                      int box_cols, int box_rows);
+
 struct CacheView {
+    const KvMaps *maps;   // host copy of the pool's tensor maps (bf16 storage, head_dim 128), else null
     void *k;
     void *v;
     const int *page_table;

@@ -35,6 +35,7 @@ struct GraphEntry {
     int kind;   // 0: GEMV kernels, 1: tensor-core GEMMs
     int B;
     int splits, cluster;   // attention splits per (row, KV group); 1: splits combine inside a cluster
+    int mm;                // attention on the tensor cores (bf16 tiles through the tensor maps)
     const float *emb;
     float *logits, *hidden;
     int32_t *argmax;
@@ -84,6 +85,8 @@ struct talker {
     // KV cache
     int n_streams = 0, max_seq = 0, pps = 0;
     size_t page_elems = 0;
+    KvMaps kv_maps{};                    // tensor maps of the bf16 pools (head_dim 128)
+    bool kv_maps_ok = false;
     void *kpool = nullptr, *vpool = nullptr;
     int *d_pt = nullptr, *d_len = nullptr;
     float2 *d_rope = nullptr;
@@ -104,6 +107,7 @@ struct talker {
     std::vector<PrefillGraph> pgraphs;
     int decode_mode = 0;                 // 0 auto, 2 GEMV graph, 3 tensor-core graph
     int attn_cluster = 0;   // decode attention: splits combine inside a thread-block cluster
+    int attn_mm = 0;        // decode attention: bf16 tiles through the tensor maps, tensor-core scores and P.V
     int prefill_mode = 0;                // 0 automatic, 2 always the GEMV kernels, 3 / 4 tensor-core GEMMs
                                          // with the mma.sync / the tcgen05 attention at any T
     // tensor-core prefill buffers (bf16 GEMM operands and the f32 gate/up projection)
@@ -184,6 +188,7 @@ void free_cache(talker *t) {
     t->kpool = t->vpool = nullptr;
     t->d_pt = t->d_len = nullptr;
     t->d_rope = nullptr;
+    t->kv_maps_ok = false;
     t->n_streams = t->max_seq = t->pps = 0;
     t->len.clear();
 }
@@ -208,7 +213,9 @@ int decode_splits(const talker *t, int B) {
 // split, combined on chip) up to 16 pages; longer or more streams fill the GPU in one wave,
 // combined through L2, and with several ragged streams a split walks about four pages of the
 // longest one, which balances the waves.
-void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster) {
+constexpr int kAttnMmMinPages = 3;
+
+void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster, int *mm) {
     const int pages_max = (max_len + 1 + kPageRows - 1) / kPageRows;
     if (B <= 2 && pages_max <= 2) {
         *splits = 1;
@@ -220,6 +227,8 @@ void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster)
         *cluster = 0;
         *splits = B == 1 ? decode_splits(t, B) : std::min(64, std::max(decode_splits(t, B), (pages_max + 3) / 4));
     }
+    // the tensor-core form pays for its fragment setup from three pages per split on
+    *mm = t->kv_maps_ok && (pages_max + *splits - 1) / *splits >= kAttnMmMinPages ? 1 : 0;
 }
 
 // Grow activation buffers and workspaces to cover `rows` rows with `splits`
@@ -363,6 +372,7 @@ namespace {
 
 CacheView cache_view(const talker *t) {
     CacheView c{};
+    c.maps = t->kv_maps_ok ? &t->kv_maps : nullptr;
     c.k = t->kpool;
     c.v = t->vpool;
     c.page_table = t->d_pt;
@@ -456,6 +466,7 @@ talker_status enqueue_forward(talker *t, cudaStream_t st, int rows, const RowMap
         a.out = t->attn;
         a.out_bf16 = 0;
         a.cache = cv;
+        if (rm.mode != 0 || !t->attn_mm) a.cache.maps = nullptr;
         a.rowmap = rm;
         a.layer = l;
         a.n_q = t->nq;
@@ -640,6 +651,7 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         a.out = t->ab;
         a.out_bf16 = 1;
         a.cache = cv;
+        if (rm.mode != 0 || !t->attn_mm) a.cache.maps = nullptr;
         a.rowmap = rm;
         a.layer = l;
         a.n_q = t->nq;
@@ -917,6 +929,12 @@ talker_status talker_kv_init_batched(talker_t *t, int n_streams, int max_seq_len
     TRY_CUDA(cudaMalloc(&t->d_rope, rope.size() * sizeof(float2)));
     TRY_CUDA(cudaMemcpy(t->d_rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice));
     TRY_CUDA(cudaStreamSynchronize(t->st));
+    // bf16 pools with head_dim 128: tensor maps over [pool rows][128] for the tensor-core decode attention
+    t->kv_maps_ok = false;
+    const uint64_t pool_rows = (uint64_t)n_pages * page_elems / (size_t)t->hd;
+    if (t->kv_bf16 && !t->kv_q8 && t->hd == 128 && pool_rows < (1ull << 31))
+        t->kv_maps_ok = make_map_bf16_2d(&t->kv_maps.k, t->kpool, pool_rows, 128, 256, 64, 64) &&
+                        make_map_bf16_2d(&t->kv_maps.v, t->vpool, pool_rows, 128, 256, 64, 64);
     t->n_streams = n_streams;
     t->max_seq = max_seq_len;
     t->pps = pps;
@@ -997,15 +1015,15 @@ static talker_status decode_impl(talker *t, const float *emb, const CodeGather *
     if (t->decode_mode == 3 && kind == 0) return TALKER_EINVAL;
     int max_len = 0;
     for (int b = 0; b < B; ++b) max_len = std::max(max_len, t->len[b]);
-    int splits = 0, cluster = 0;
-    attn_config(t, B, max_len, &splits, &cluster);
+    int splits = 0, cluster = 0, mm = 0;
+    attn_config(t, B, max_len, &splits, &cluster, &mm);
     TRY(ensure_capacity(t, B, splits));
     if (kind == 1) TRY(ensure_tc(t, B));
     GraphEntry *ge = nullptr;
     const int32_t *ids = gather ? gather->ids : nullptr;
     const float *overlay = gather ? gather->overlay : nullptr;
     for (auto &g : t->graphs)
-        if (g.kind == kind && g.B == B && g.splits == splits && g.cluster == cluster && g.emb == emb &&
+        if (g.kind == kind && g.B == B && g.splits == splits && g.cluster == cluster && g.mm == mm && g.emb == emb &&
             g.logits == logits && g.hidden == hidden && g.argmax == argmax && g.ids == ids && g.overlay == overlay)
             ge = &g;
     if (!ge) {
@@ -1018,6 +1036,7 @@ static talker_status decode_impl(talker *t, const float *emb, const CodeGather *
         int nk = 0;
         cudaGraph_t graph = nullptr;
         t->attn_cluster = cluster;
+        t->attn_mm = mm;
         TRY_CUDA(cudaStreamBeginCapture(t->cap_st, cudaStreamCaptureModeThreadLocal));
         talker_status s = kind == 1 ? enqueue_tc(t, t->cap_st, B, rm, emb, splits, out, &nk, gather)
                                     : enqueue_forward(t, t->cap_st, B, rm, emb, splits, out, &nk, gather);
@@ -1031,7 +1050,7 @@ static talker_status decode_impl(talker *t, const float *emb, const CodeGather *
         e = cudaGraphInstantiate(&exec, graph, 0);
         cudaGraphDestroy(graph);
         if (e != cudaSuccess) return from_cuda(e);
-        t->graphs.push_back(GraphEntry{kind, B, splits, cluster, emb, logits, hidden, argmax, ids, overlay, exec, nk});
+        t->graphs.push_back(GraphEntry{kind, B, splits, cluster, mm, emb, logits, hidden, argmax, ids, overlay, exec, nk});
         ge = &t->graphs.back();
     }
     TRY_CUDA(cudaGraphLaunch(ge->exec, t->st));
@@ -1236,7 +1255,7 @@ talker_status talker_frame(talker_t *t, const float *emb, int T0, int n_steps, c
             cg.ids_stride = 1;
             const int len = T0 + i;   // cache length before the step
             int splits = 0;
-            attn_config(t, 1, len, &splits, &t->attn_cluster);
+            attn_config(t, 1, len, &splits, &t->attn_cluster, &t->attn_mm);
             RowMap rm{0, 0, 0, t->d_len};
             ForwardOut out{logits ? logits + (size_t)(i + 1) * t->V : t->frame_logits, nullptr, codes + i + 1, false, 1};
             out.head_w = head_of(i + 1);
