@@ -420,12 +420,13 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
         __syncthreads();
         if (flag_s) {
             __threadfence();
-            // the last CTA reduces the per-CTA partials of each row with the whole block:
-            // strided loads (all in flight together), then warp and block argmax (lowest index on ties)
-            for (int r = 0; r < nrows; ++r) {
+            // the last CTA reduces the per-CTA partials: one warp per row (rows spread over the
+            // warps, every lane's loads in flight together), lowest index on ties
+            for (int r = warp; r < nrows; r += kGemvWarps) {
                 float best = -INFINITY;
                 int bi = 0x7fffffff;
-                for (int b = threadIdx.x; b < (int)gridDim.x; b += kGemvThreads) {
+#pragma unroll 4
+                for (int b = lane; b < (int)gridDim.x; b += 32) {
                     const size_t slot = ((size_t)rb * gridDim.x + b) * ROWS + r;
                     const float v = __ldcg(p.part_val + slot);
                     const int i = __ldcg(p.part_idx + slot);
@@ -444,21 +445,11 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p) {
                     }
                 }
                 if (lane == 0) {
-                    hv_s[warp][0] = best;
-                    hi_s[warp][0] = bi;
-                }
-                __syncthreads();
-                if (threadIdx.x == 0) {
-                    for (int w = 1; w < kGemvWarps; ++w)
-                        if (hv_s[w][0] > best || (hv_s[w][0] == best && hi_s[w][0] < bi)) {
-                            best = hv_s[w][0];
-                            bi = hi_s[w][0];
-                        }
                     if (p.argmax_out != nullptr) p.argmax_out[row0 + r] = bi;
                     if (p.inc_len) p.cur_len_rw[row0 + r] += 1;
                 }
-                __syncthreads();
             }
+            __syncthreads();
             if (threadIdx.x == 0) p.head_cnt[rb] = 0;
         }
     }

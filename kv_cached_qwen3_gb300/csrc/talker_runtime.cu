@@ -211,8 +211,9 @@ int decode_splits(const talker *t, int B) {
 // (captured steps are keyed by both). Measured on GB300: one or two short streams run one CTA
 // per KV group up to 2 pages (no combine at all), then a cluster of 8 (one or two pages per
 // split, combined on chip) up to 16 pages; longer or more streams fill the GPU in one wave,
-// combined through L2, and with several ragged streams a split walks about four pages of the
-// longest one, which balances the waves.
+// combined through L2, and with several streams a split walks about eight pages of the longest
+// one (fewer, longer splits keep their copy pipelines busy: measured at 4, 8 and 16 streams
+// against four, six and twelve pages).
 constexpr int kAttnMmMinPages = 3;
 
 void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster, int *mm) {
@@ -225,7 +226,7 @@ void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster,
         *cluster = 1;
     } else {
         *cluster = 0;
-        *splits = B == 1 ? decode_splits(t, B) : std::min(64, std::max(decode_splits(t, B), (pages_max + 3) / 4));
+        *splits = B == 1 ? decode_splits(t, B) : std::min(64, std::max(decode_splits(t, B), (pages_max + 7) / 8));
     }
     // the tensor-core form pays for its fragment setup from three pages per split on
     *mm = t->kv_maps_ok && (pages_max + *splits - 1) / *splits >= kAttnMmMinPages ? 1 : 0;
@@ -741,7 +742,7 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
     h.cur_len_rw = t->d_len;
     h.suppress_tail = t->suppress_tail;
     h.eos_id = t->suppress_eos;
-    TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, st, false));
+    TRY_CUDA(launch_gemv(EPI_HEAD, t->w_bf16, pick_rows(hrows, t->H), h, st, true));
     ++nk;
     *n_kernels = nk;
     return TALKER_OK;
