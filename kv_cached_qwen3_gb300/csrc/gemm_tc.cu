@@ -2,18 +2,22 @@
 //   C[M, N] (+)= A[M, K] * B[N, K]^T,  A = activations, B = weights, both bf16,
 //   K-major ("[out, in]" row-major weights, as ggml_mul_mat reads them), fp32 accumulation.
 //
-// Persistent kernel, one CTA per SM over a list of 128 x BN output tiles (BN = 256 where
-// N allows, else 128), each optionally one K range of a split-K:
-//   warp 0, one lane: TMA producer - 2-D tiled bulk tensor copies of 128x64 (A) and
-//                     BNx64 (B) bf16 tiles with 128-byte swizzle into a STAGES-deep ring;
-//   warp 1:           allocates two TMEM accumulators (128 lanes x BN fp32 columns each);
-//                     one lane issues tcgen05.mma (kind::f16, M=128, N=BN, K=16) from
-//                     shared memory descriptors and commits each stage back to the producer;
+// Three kernels by shape:
+//   k_gemm_tc_pair    tall products (1024 rows or more) with N % 256 == 0: CTA pairs on
+//                     256 x 256 tiles (cta_group::2 MMAs of M = 256), persistent over the tiles;
+//   k_gemm_tc_persist other products above 128 rows: one CTA per SM over 128 x 128 tiles;
+//   k_gemm_tc_swap    at most 128 rows (decode batches, small prefills): the weights as the
+//                     MMA's M operand, the rows as N.
+// Each persistent CTA runs:
+//   warp 0, one lane: TMA producer - 2-D tiled bulk tensor copies of 64-wide K slices with the
+//                     128-byte swizzle into a STAGES-deep ring;
+//   warp 1:           allocates two TMEM accumulators; one lane issues tcgen05.mma (kind::f16,
+//                     K=16) from shared memory descriptors and commits each stage back to the
+//                     producer;
 //   warps 2..5:       epilogue - tcgen05.ld of their 32-lane quadrant (one row per lane),
-//                     staged through a per-warp shared block so that each instruction
-//                     stores or reduce-adds (red.add) whole 128-byte row segments of the fp32
-//                     output, or (gate/up projection) silu(gate) * up of interleaved column
-//                     pairs, stored as bf16.
+//                     staged through per-warp shared blocks so that whole 128-byte row segments
+//                     of the fp32 output are stored or reduce-added, or (gate/up projection)
+//                     silu(gate) * up of interleaved column pairs is stored as bf16.
 // Every mbarrier wait is bounded; a wait that gives up sets the device status word.
 #include <cuda.h>
 
@@ -31,6 +35,63 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BK = 64;                 // 64 bf16 = one 128-byte swizzle row
 constexpr int NTHREADS = 192;
+
+// One 32-column chunk of a warp's 32 accumulator rows (v: this lane's row, global rows row0 ..
+// row0 + 31, columns col0 .. col0 + 31) through the warp's 32 x 32 staging block: with the
+// SwiGLU epilogue, silu(gate) * up of the interleaved column pairs as bf16; else the fp32
+// values stored or reduce-added. The caller syncs the warp before the block is reused.
+__device__ __forceinline__ void epi_chunk32(const GemmParams &p, float *stg, const float (&v)[32], int row0, int col0,
+                                            int lane) {
+    if (p.swiglu_out != nullptr) {
+        // columns (2j, 2j + 1) = (gate_j, up_j): 16 bf16 outputs = 32 bytes of this lane's
+        // row, staged as [32 rows][2 x 16 B] with the halves swapped on every other group of
+        // 4 rows (conflict-free), then written 16 rows x 32 bytes per instruction
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float g0 = v[4 * i], u0 = v[4 * i + 1], g1 = v[4 * i + 2], u1 = v[4 * i + 3];
+            const __nv_bfloat16 lo = __float2bfloat16_rn(g0 / (1.0f + expf(-g0)) * u0);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(g1 / (1.0f + expf(-g1)) * u1);
+            h[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+        }
+        uint4 *w = reinterpret_cast<uint4 *>(stg);
+        const int sw = (lane >> 2) & 1;
+        w[lane * 2 + sw] = make_uint4(h[0], h[1], h[2], h[3]);
+        w[lane * 2 + (sw ^ 1)] = make_uint4(h[4], h[5], h[6], h[7]);
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int r = it * 16 + (lane >> 1), half = lane & 1;
+            const uint4 x = w[r * 2 + (half ^ ((r >> 2) & 1))];
+            const int grow = row0 + r;
+            if (grow < p.M)
+                *reinterpret_cast<uint4 *>(p.swiglu_out + (size_t)grow * p.ld_swiglu + col0 / 2 +
+                                           half * 8) = x;
+        }
+    } else {
+        // this lane's 32 values of its row go to the warp's 32 x 32 block (16-byte chunks
+        // XOR-swizzled by row, conflict-free), then each instruction stores or reduce-adds
+        // 4 rows x 128 contiguous bytes
+        float4 *w = reinterpret_cast<float4 *>(stg);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[lane * 8 + (i ^ (lane & 7))] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int r = it * 4 + (lane >> 3), ch = lane & 7;
+            const float4 x = w[r * 8 + (ch ^ (r & 7))];
+            const int grow = row0 + r;
+            if (grow < p.M) {
+                float *o = p.out + (size_t)grow * p.ld_out + col0 + ch * 4;
+                if (p.accumulate)
+                    red_add_v4(o, x.x, x.y, x.z, x.w);
+                else
+                    *reinterpret_cast<float4 *>(o) = x;
+            }
+        }
+    }
+}
 
 // One CTA per SM walks the tile list; each tile is (row block, column block, K split),
 // and every CTA loads its own A and B boxes. The accumulator is double buffered in TMEM
@@ -180,55 +241,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), v);
-                    if (p.swiglu_out != nullptr) {
-                        // columns (2j, 2j + 1) = (gate_j, up_j): 16 bf16 outputs = 32 bytes of this lane's
-                        // row, staged as [32 rows][2 x 16 B] with the halves swapped on every other group of
-                        // 4 rows (conflict-free), then written 16 rows x 32 bytes per instruction
-                        uint32_t h[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float g0 = v[4 * i], u0 = v[4 * i + 1], g1 = v[4 * i + 2], u1 = v[4 * i + 3];
-                            const __nv_bfloat16 lo = __float2bfloat16_rn(g0 / (1.0f + expf(-g0)) * u0);
-                            const __nv_bfloat16 hi = __float2bfloat16_rn(g1 / (1.0f + expf(-g1)) * u1);
-                            h[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-                        }
-                        uint4 *w = reinterpret_cast<uint4 *>(stg);
-                        const int sw = (lane >> 2) & 1;
-                        w[lane * 2 + sw] = make_uint4(h[0], h[1], h[2], h[3]);
-                        w[lane * 2 + (sw ^ 1)] = make_uint4(h[4], h[5], h[6], h[7]);
-                        __syncwarp();
-#pragma unroll
-                        for (int it = 0; it < 2; ++it) {
-                            const int r = it * 16 + (lane >> 1), half = lane & 1;
-                            const uint4 x = w[r * 2 + (half ^ ((r >> 2) & 1))];
-                            const int grow = m0 + q * 32 + r;
-                            if (grow < p.M)
-                                *reinterpret_cast<uint4 *>(p.swiglu_out + (size_t)grow * p.ld_swiglu + (n0 + c * 32) / 2 +
-                                                           half * 8) = x;
-                        }
-                    } else {
-                        // this lane's 32 values of its row go to the warp's 32 x 32 block (16-byte chunks
-                        // XOR-swizzled by row, conflict-free), then each instruction stores or reduce-adds
-                        // 4 rows x 128 contiguous bytes
-                        float4 *w = reinterpret_cast<float4 *>(stg);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            w[lane * 8 + (i ^ (lane & 7))] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                        __syncwarp();
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {
-                            const int r = it * 4 + (lane >> 3), ch = lane & 7;
-                            const float4 x = w[r * 8 + (ch ^ (r & 7))];
-                            const int grow = m0 + q * 32 + r;
-                            if (grow < p.M) {
-                                float *o = p.out + (size_t)grow * p.ld_out + n0 + c * 32 + ch * 4;
-                                if (p.accumulate)
-                                    red_add_v4(o, x.x, x.y, x.z, x.w);
-                                else
-                                    *reinterpret_cast<float4 *>(o) = x;
-                            }
-                        }
-                    }
+                    epi_chunk32(p, stg, v, m0 + q * 32, n0 + c * 32, lane);
                     __syncwarp();   // the block is rewritten by the next chunk
                 }
             }
@@ -246,6 +259,218 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+
+// Tall products on CTA pairs (a cluster of 2): tiles of 256 x 256, CTA r of the pair holding rows
+// 128 r .. 128 r + 127 of A and columns 128 r .. 128 r + 127 of B in its own 6-stage ring; the
+// even CTA issues M = 256, N = 256 MMAs (cta_group::2) that read both CTAs' shared memory and
+// accumulate each CTA's 128 rows x 256 columns in its own TMEM (two buffers of 256 columns).
+// Per CTA and K block 32 KB of operands feed 2 x 128 x 256 x 64 FLOP, 1.5 times the single-CTA
+// 128 x 256 tile, and the deeper ring covers twice its copy latency. Both CTAs' copies count on
+// the even CTA's full barriers; its commits arrive on both CTAs' empty and TMEM-full barriers, and
+// all eight epilogue warps release a TMEM buffer on the even CTA's barrier. The fp32 epilogue
+// stages each 32 x 32 chunk in the swizzled layout of the output's tensor map and hands it to the
+// TMA (a bulk store, or an element-wise reduce-add for the residual stream and split-K), with two
+// staging blocks per warp so that the next chunk is written while the previous one drains.
+constexpr int kPairStages = 6;
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_gemm_tc_pair(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ CUtensorMap map_o, const GemmParams p, int splits) {
+    constexpr int STAGES = kPairStages;
+    constexpr int BN = 256;                                // pair tile: 256 x 256
+    constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = (BN / 2) * BK * 2;
+    constexpr uint32_t IDESC = instr_desc(2 * BM, BN);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *sA = smem;
+    unsigned char *sB = smem + STAGES * A_BYTES;
+    __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int fail_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    const int tiles_n = p.N / BN;
+    const int tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
+    const int n_tiles = tiles_m * tiles_n * splits;
+    const int nk_total = p.K / BK;
+    const int per = (nk_total + splits - 1) / splits;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 8);   // the four epilogue warps of both CTAs
+        }
+        fail_s = 0;
+        fence_barrier_init();
+    }
+    // both CTAs' barriers are initialised before either signals the other's
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_s)),
+                     "r"((uint32_t)(2 * BN))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    auto lead = [&](const void *local) {   // the even CTA's copy of a barrier (shared::cluster address)
+        uint32_t a;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(0u));
+        return a;
+    };
+
+    // tile t -> (256-row block, 256-column block, split); column blocks vary fastest
+    auto tile_of = [&](int t, int &m0, int &n0, int &kb0, int &nk) {
+        const int sp = t / (tiles_m * tiles_n), rem = t - sp * tiles_m * tiles_n;
+        m0 = (rem / tiles_n) * 2 * BM;
+        n0 = (rem % tiles_n) * BN;
+        kb0 = sp * per;
+        nk = max(0, min(per, nk_total - kb0));
+    };
+
+    pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer of this CTA's halves; the even CTA arms each stage for both
+        const int ra = (int)rank * BM, rb = (int)rank * (BN / 2);
+        uint32_t pre = 0;
+        for (int t = pair; t < n_tiles && pre < (uint32_t)STAGES; t += n_pairs) {
+            int m0, n0, kb0, nk;
+            tile_of(t, m0, n0, kb0, nk);
+            for (int i = 0; i < nk && pre < (uint32_t)STAGES; ++i, ++pre) {
+                if (rank == 0) mbar_arrive_expect_tx(&full[pre], 2 * (A_BYTES + B_BYTES));
+                tma_load_2d_pair(sB + pre * B_BYTES, &map_b, (kb0 + i) * BK, n0 + rb, lead(&full[pre]));
+            }
+        }
+        pdl_wait();
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = pair; t < n_tiles && ok; t += n_pairs) {
+            int m0, n0, kb0, nk;
+            tile_of(t, m0, n0, kb0, nk);
+            for (int i = 0; i < nk; ++i, ++it) {
+                const int s = it % STAGES;
+                if (it < pre) {   // weights already requested
+                    tma_load_2d_pair(sA + s * A_BYTES, &map_a, (kb0 + i) * BK, m0 + ra, lead(&full[s]));
+                    continue;
+                }
+                if (it >= (uint32_t)STAGES && !mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, p.status)) {
+                    fail_s = 1;
+                    ok = false;
+                    break;
+                }
+                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (A_BYTES + B_BYTES));
+                tma_load_2d_pair(sA + s * A_BYTES, &map_a, (kb0 + i) * BK, m0 + ra, lead(&full[s]));
+                tma_load_2d_pair(sB + s * B_BYTES, &map_b, (kb0 + i) * BK, n0 + rb, lead(&full[s]));
+            }
+        }
+        for (uint32_t j = (it > (uint32_t)STAGES ? it - STAGES : 0); j < it; ++j)
+            mbar_wait(&empty[j % STAGES], (j / STAGES) & 1, p.status);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---- MMA issuer (even CTA)
+        uint32_t it = 0;
+        int j = 0;
+        bool ok = true;
+        for (int t = pair; t < n_tiles && ok; t += n_pairs, ++j) {
+            int m0, n0, kb0, nk;
+            tile_of(t, m0, n0, kb0, nk);
+            const int b = j & 1;
+            if (j >= 2 && !mbar_wait(&tempty[b], ((j >> 1) - 1) & 1, p.status)) {
+                fail_s = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc = tmem + (uint32_t)(b * BN);
+            for (int i = 0; i < nk; ++i, ++it) {
+                const int s = it % STAGES;
+                if (!mbar_wait(&full[s], (it / STAGES) & 1, p.status)) {
+                    fail_s = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + s * A_BYTES), b0 = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_bf16_pair(acc, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), IDESC,
+                                   (i > 0 || k > 0) ? 1u : 0u);
+                umma_commit_pair(&empty[s], 0x3);
+            }
+            umma_commit_pair(&tfull[b], 0x3);
+        }
+    } else if (warp >= 2) {
+        // ---- epilogue: this CTA's 128 rows of the tile, TMEM lane quadrant (warp % 4)
+        pdl_wait();
+        const int q = warp & 3;
+        float *stg = reinterpret_cast<float *>(sB + STAGES * B_BYTES) + q * 2 * 32 * 32;   // two 4 KB blocks
+        int nst = 0;   // chunks this warp has handed to the TMA
+        int j = 0;
+        for (int t = pair; t < n_tiles; t += n_pairs, ++j) {
+            int m0, n0, kb0, nk;
+            tile_of(t, m0, n0, kb0, nk);
+            const int b = j & 1;
+            const bool ok = mbar_wait(&tfull[b], (j >> 1) & 1, p.status);
+            tc_fence_after();
+            if (!ok) break;
+            if (nk > 0) {
+                const int row0 = m0 + (int)rank * BM + q * 32;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), v);
+                    if (p.swiglu_out != nullptr) {
+                        epi_chunk32(p, stg, v, row0, n0 + c * 32, lane);
+                    } else {
+                        float4 *w = reinterpret_cast<float4 *>(stg + (nst & 1) * 32 * 32);
+                        if (nst >= 2) {   // the block's previous store has been read out
+                            if (lane == 0) bulk_wait_read_1();
+                            __syncwarp();
+                        }
+                        // row = lane, 16-byte chunk i at i ^ (row % 8): the tensor map's 128-byte swizzle
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[lane * 8 + (i ^ (lane & 7))] =
+                                make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {   // rows past M are clipped by the copy (a block wholly past M is skipped)
+                            if (row0 < p.M) {
+                                if (p.accumulate) tma_reduce_add_2d(&map_o, n0 + c * 32, row0, w);
+                                else tma_store_2d(&map_o, n0 + c * 32, row0, w);
+                            }
+                            bulk_commit();
+                        }
+                        ++nst;
+                    }
+                    __syncwarp();   // the block is rewritten by the next chunk
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)   // this warp's quadrant of buffer b is free (on the even CTA's barrier)
+                asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(lead(&tempty[b]))
+                             : "memory");
+        }
+        if (lane == 0) bulk_wait_all();   // every store has landed before the CTA moves on
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    // neither CTA releases TMEM (or leaves) while the other may still use the pair's resources
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)(2 * BN))
+                     : "memory");
+    }
+}
 
 
 // Short products (M <= 128 activation rows: decode batches, small prefills) with the weights as
@@ -466,16 +691,30 @@ bool make_map_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t c
 
 namespace {
 
+// fp32 matrix [rows][cols] (row stride in bytes) in boxes of 32 x 32 with the 128-byte swizzle:
+// the destination of the bulk tensor stores and reduce-adds of an epilogue.
+bool make_map_f32_2d(CUtensorMap *m, void *ptr, uint64_t rows, uint64_t cols, uint64_t row_stride_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_stride_bytes};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // row-major [rows, K] operand, boxes of 64 (K) x box_rows
 bool make_map(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows) {
     return make_map_bf16_2d(m, ptr, (uint64_t)rows, (uint64_t)K, (uint64_t)K * 2, tc::BK, box_rows);
 }
 
-// Two tile widths: 128 x 256 tiles (M=128, N=256 MMAs, 4-stage ring) for tall products
-// where N allows, which halves the operand bytes per FLOP, and 128 x 128 tiles (6-stage
-// ring) otherwise. TMEM holds two accumulators of BN columns either way.
+// Two tile widths: 256 x 256 pair tiles for tall products where N allows (per CTA and K block
+// 32 KB of operands for 128 x 256 outputs), and 128 x 128 single-CTA tiles (6-stage ring)
+// otherwise. TMEM holds two accumulators either way.
 constexpr int kBNNarrow = 128, kStagesNarrow = 6;
-constexpr int kBNWide = 256, kStagesWide = 4;
+constexpr int kBNWide = 256;
 // ring + the epilogue's staging blocks (4 warps x 32 x 32 f32) + alignment slack
 constexpr size_t smem_for(int bn, int stages) {
     return (size_t)stages * (tc::BM + bn) * tc::BK * 2 + 4 * 32 * 32 * 4 + 1024;
@@ -528,9 +767,13 @@ size_t smem_swap(int M) {
 constexpr int kSwapMaxRows = 128;
 }  // namespace
 
+// CTA pair kernel: 6 stages of 16 KB (A) + 16 KB (half of B) per CTA, two staging blocks per
+// epilogue warp, slack.
+constexpr size_t kPairSmem = (size_t)tc::kPairStages * 2 * tc::BM * tc::BK * 2 + 4 * 2 * 32 * 32 * 4 + 1024;
+
 cudaError_t prepare_gemm_tc() {
     cudaError_t e = raise_smem<kBNNarrow, kStagesNarrow>();
-    e = e ? e : raise_smem<kBNWide, kStagesWide>();
+    e = e ? e : cudaFuncSetAttribute(tc::k_gemm_tc_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem);
     return e ? e : cudaFuncSetAttribute(tc::k_gemm_tc_swap, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)smem_swap(kSwapMaxRows));
 }
@@ -613,16 +856,46 @@ cudaError_t launch_cfg(const CUtensorMap &ma, const CUtensorMap &mb, const GemmP
     return cudaLaunchKernelEx(&cfg, tc::k_gemm_tc_persist<BN, STAGES>, ma, mb, p, splits);
 }
 
+// Tall products with N % 256 == 0 on CTA pairs: 256 x 256 tiles, one pair per two SMs.
+cudaError_t launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mo, const GemmParams &p,
+                        int splits, int n_sm, cudaStream_t st) {
+    const int tiles = ((p.M + 2 * tc::BM - 1) / (2 * tc::BM)) * (p.N / kBNWide) * splits;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(tc::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = kPairSmem;
+    cfg.stream = st;
+    cfg.gridDim = dim3(2 * std::min(tiles, std::max(1, n_sm / 2)), 1, 1);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, tc::k_gemm_tc_pair, ma, mb, mo, p, splits);
+}
+
 cudaError_t launch_persist(const void *A, const void *B, GemmParams &p, int splits, cudaStream_t st) {
     const int M = p.M, N = p.N, K = p.K;
     if (!gemm_tc_supported(N, K) || M < 1) return cudaErrorInvalidValue;
     const int bn = tile_n_for(M, N);
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, A, M, K, tc::BM) || !make_map(&mb, B, N, K, bn)) return cudaErrorInvalidValue;
     const int s = std::max(1, splits);
     const int n_sm = sm_count_current();
     if (n_sm <= 0) return cudaErrorInvalidDevice;
-    if (bn == kBNWide) return launch_cfg<kBNWide, kStagesWide>(ma, mb, p, s, n_sm, st);
+    CUtensorMap ma, mb;
+    if (bn == kBNWide) {   // CTA pairs: each CTA loads its 128 rows of A and 128 rows (half) of B
+        if (!make_map(&ma, A, M, K, tc::BM) || !make_map(&mb, B, N, K, kBNWide / 2)) return cudaErrorInvalidValue;
+        CUtensorMap mo{};
+        if (p.swiglu_out == nullptr) {   // fp32 output [M][N], row stride ld_out: 32 x 32 boxes, 128-byte swizzle
+            if (p.out == nullptr || p.ld_out % 4 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15u) != 0 ||
+                !make_map_f32_2d(&mo, p.out, (uint64_t)M, (uint64_t)N, (uint64_t)p.ld_out * 4))
+                return cudaErrorInvalidValue;
+        }
+        return launch_pair(ma, mb, mo, p, s, n_sm, st);
+    }
+    if (!make_map(&ma, A, M, K, tc::BM) || !make_map(&mb, B, N, K, bn)) return cudaErrorInvalidValue;
     return launch_cfg<kBNNarrow, kStagesNarrow>(ma, mb, p, s, n_sm, st);
 }
 }  // namespace

@@ -1,6 +1,7 @@
 // Element-wise stages of the tensor-core prefill path (the projections run on
 // the tcgen05 GEMM):
-//   k_rmsnorm_bf16: x / sqrt(mean(x^2) + eps) * w, rounded to bf16 as the next
+//   k_rmsnorm_bf16 (tall inputs: k_rmsnorm_bf16_rows, a warp per row):
+//                   x / sqrt(mean(x^2) + eps) * w, rounded to bf16 as the next
 //                   GEMM's A operand ("talker-forward.h", talker_layer_forward
 //                   pre-norm and MLP pre-norm); it also clears the split-K
 //                   accumulator of the GEMM that follows, when there is one;
@@ -80,6 +81,55 @@ __global__ void k_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int 
             const float4 g = *reinterpret_cast<const float4 *>(w + k);
             *reinterpret_cast<__nv_bfloat162 *>(o + k) = __floats2bfloat162_rn(v[i].x * inv * g.x, v[i].y * inv * g.y);
             *reinterpret_cast<__nv_bfloat162 *>(o + k + 2) = __floats2bfloat162_rn(v[i].z * inv * g.z, v[i].w * inv * g.w);
+        }
+    }
+}
+
+// Tall inputs: one warp per row (4 rows per CTA), the row held in registers (H <= 1024).
+__global__ void k_rmsnorm_bf16_rows(float *x, int ld, const float *w, float eps, int rows, int H,
+                                    __nv_bfloat16 *out, CodeGather gather, int *status, float4 *zero, size_t zero_n4) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 4 + warp;
+    pdl_launch_dependents();
+    pdl_wait();
+    if (zero != nullptr) {
+        const size_t per = (zero_n4 + gridDim.x - 1) / gridDim.x;
+        const size_t b = (size_t)blockIdx.x * per, e = b + per < zero_n4 ? b + per : zero_n4;
+        for (size_t i = b + threadIdx.x; i < e; i += blockDim.x) zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (row >= rows) return;
+    constexpr int MAXV = 8;   // float4s per lane
+    float4 v[MAXV];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+        const int k = (lane + 32 * i) * 4;
+        if (k < H) {
+            if (gather.n > 0) {
+                v[i] = gather_row4(gather, row, k, H, status);
+                *reinterpret_cast<float4 *>(x + (size_t)row * ld + k) = v[i];
+            } else {
+                v[i] = *reinterpret_cast<const float4 *>(x + (size_t)row * ld + k);
+            }
+        } else {
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+    __nv_bfloat16 *o = out + (size_t)row * H;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+        const int k = (lane + 32 * i) * 4;
+        if (k < H) {
+            const float4 g = *reinterpret_cast<const float4 *>(w + k);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v[i].x * inv * g.x, v[i].y * inv * g.y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(v[i].z * inv * g.z, v[i].w * inv * g.w);
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t *>(&lo);
+            u.y = *reinterpret_cast<const uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(o + k) = u;
         }
     }
 }
@@ -200,6 +250,9 @@ __global__ void k_swiglu_bf16(float *gu, int rows, int I, __nv_bfloat16 *out) {
     }
 }
 
+// from this many rows on, the one-warp-per-row form (below it, a CTA per row spreads the work wider)
+constexpr int kRmsRowsMin = 2048;
+
 cudaError_t launch_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int rows, int H, void *out,
                                 cudaStream_t st, const CodeGather *gather, int *status, float *zero, size_t zero_n) {
     const int threads = 256;
@@ -208,6 +261,10 @@ cudaError_t launch_rmsnorm_bf16(float *x, int ld, const float *w, float eps, int
     if (zero != nullptr && (zero_n % 4 != 0 || (reinterpret_cast<uintptr_t>(zero) & 15u) != 0))
         return cudaErrorInvalidValue;
     const CodeGather none{};
+    if (rows >= kRmsRowsMin && H <= 1024)   // tall: a warp per row
+        return launch_pdl(k_rmsnorm_bf16_rows, dim3((rows + 3) / 4), dim3(128), st, x, ld, w, eps, rows, H,
+                          static_cast<__nv_bfloat16 *>(out), gather ? *gather : none, status,
+                          reinterpret_cast<float4 *>(zero), zero != nullptr ? zero_n / 4 : (size_t)0);
     return launch_pdl(k_rmsnorm_bf16, dim3(rows), dim3(threads), st, x, ld, w, eps, rows, H,
                       static_cast<__nv_bfloat16 *>(out), gather ? *gather : none, status,
                       reinterpret_cast<float4 *>(zero), zero != nullptr ? zero_n / 4 : (size_t)0);
