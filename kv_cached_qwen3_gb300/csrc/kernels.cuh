@@ -35,8 +35,6 @@ __device__ __forceinline__ int rowmap_pos(const RowMap &m, int r) {
     return m.mode == 0 ? m.cur_len[r] : m.pos0 + (m.rows_per_stream > 0 ? r % m.rows_per_stream : r);
 }
 
-// The paged KV cache. Page = [n_layers][n_kv][kPage][head_dim] elements; the
-// position p of stream s lives in page page_table[s * pages_per_stream + p / kPage].
 // Tensor maps of a bf16 K and V pool with head_dim 128, viewed as [pool rows][128] (a
 // (page, layer, head) tile is 64 consecutive rows): boxes of 64 rows x 64 dims, 128-byte swizzle.
 struct KvMaps {
@@ -48,6 +46,8 @@ struct KvMaps {
 bool make_map_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint64_t row_stride_bytes,
                       int box_cols, int box_rows);
 
+// The paged KV cache. Page = [n_layers][n_kv][kPage][head_dim] elements; the
+// position p of stream s lives in page page_table[s * pages_per_stream + p / kPage].
 struct CacheView {
     const KvMaps *maps;   // host copy of the pool's tensor maps (bf16 storage, head_dim 128), else null
     void *k;

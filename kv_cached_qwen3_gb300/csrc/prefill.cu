@@ -5,7 +5,8 @@
 //                   GEMM's A operand ("talker-forward.h", talker_layer_forward
 //                   pre-norm and MLP pre-norm); it also clears the split-K
 //                   accumulator of the GEMM that follows, when there is one;
-//   k_qkv_post:     per (row, head) of the raw projections: QK-RMSNorm with the
+//   k_qkv_post (k_qkv_post_v: head_dim 128 without Q8_0, 16-byte accesses):
+//                   per (row, head) of the raw projections: QK-RMSNorm with the
 //                   [hd] gain and NEOX RoPE at the row's position for q and k,
 //                   k and v appended to the cache at that position (set_rows),
 //                   q kept in f32 for attention;
@@ -237,6 +238,62 @@ __global__ void k_qkv_post(const float *raw, int rows, int n_q, int n_kv, int hd
     }
 }
 
+// head_dim 128, bf16 or f32 storage: the same per (row, head) steps with 16-byte accesses. Lane l
+// holds dims 64 (l / 16) + 4 (l % 16) .. +3; the RoPE partner (dim +- 64) is lane l ^ 16.
+__global__ void k_qkv_post_v(const float *raw, int rows, int n_q, int n_kv, const float *q_norm, const float *k_norm,
+                             const float2 *rope, float eps, float *q_out, CacheView cache, int layer, RowMap rm,
+                             int *status) {
+    constexpr int HD = 128, HALF = 64;
+    const int n_heads = n_q + 2 * n_kv;
+    const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
+    if (item >= rows * n_heads) return;
+    const int r = item / n_heads, h = item - r * n_heads;
+    const int part = lane >> 4, i0 = (lane & 15) * 4, d0 = part * HALF + i0;
+    const float4 x = *reinterpret_cast<const float4 *>(raw + ((size_t)r * n_heads + h) * HD + d0);
+    const int pos = rowmap_pos(rm, r);
+    const int stream = rowmap_stream(rm, r);
+    if (pos < 0 || pos >= cache.max_seq) {
+        if (lane == 0) atomicOr(status, ST_BAD_POSITION);
+        return;
+    }
+    const bool is_q = h < n_q, is_k = !is_q && h < n_q + n_kv;
+    float y[4] = {x.x, x.y, x.z, x.w};
+    if (is_q || is_k) {
+        const float *gain = is_q ? q_norm : k_norm;
+        const float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + eps);
+        const float4 g = *reinterpret_cast<const float4 *>(gain + d0);
+        const float n[4] = {x.x * inv * g.x, x.y * inv * g.y, x.z * inv * g.z, x.w * inv * g.w};
+        const float4 cs01 = *reinterpret_cast<const float4 *>(rope + (size_t)pos * HALF + i0);
+        const float4 cs23 = *reinterpret_cast<const float4 *>(rope + (size_t)pos * HALF + i0 + 2);
+        const float c[4] = {cs01.x, cs01.z, cs23.x, cs23.z}, sn[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float o = __shfl_xor_sync(0xffffffffu, n[e], 16);
+            y[e] = part == 0 ? n[e] * c[e] - o * sn[e] : n[e] * c[e] + o * sn[e];
+        }
+    }
+    if (is_q) {
+        *reinterpret_cast<float4 *>(q_out + ((size_t)r * n_q + h) * HD + d0) = make_float4(y[0], y[1], y[2], y[3]);
+        return;
+    }
+    const int kvh = is_k ? h - n_q : h - n_q - n_kv;
+    const int page = cache.page_table[(size_t)stream * cache.pages_per_stream + pos / kPage];
+    const size_t off = (size_t)page * cache.page_elems + ((size_t)(layer * n_kv + kvh) * kPage + pos % kPage) * HD + d0;
+    void *base = is_k ? cache.k : cache.v;
+    if (cache.kv_bf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]), hi = __floats2bfloat162_rn(y[2], y[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t *>(&lo);
+        u.y = *reinterpret_cast<const uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(base) + off) = u;
+    } else {
+        *reinterpret_cast<float4 *>(static_cast<float *>(base) + off) = make_float4(y[0], y[1], y[2], y[3]);
+    }
+}
+
 __global__ void k_swiglu_bf16(float *gu, int rows, int I, __nv_bfloat16 *out) {
     const size_t n = (size_t)rows * I;
     pdl_launch_dependents();
@@ -276,6 +333,9 @@ cudaError_t launch_qkv_post(const float *raw, int rows, int n_q, int n_kv, int h
     if (cache.kv_q8 && dense_kv == nullptr) return cudaErrorInvalidValue;
     const long long items = (long long)rows * (n_q + 2 * n_kv);
     const int per_block = 8;
+    if (!cache.kv_q8 && hd == 128)
+        return launch_pdl(k_qkv_post_v, dim3((unsigned)((items + per_block - 1) / per_block)), dim3(per_block * 32), st,
+                          raw, rows, n_q, n_kv, q_norm, k_norm, rope, eps, q_out, cache, layer, rm, status);
     return launch_pdl(k_qkv_post, dim3((unsigned)((items + per_block - 1) / per_block)), dim3(per_block * 32), st,
                       raw, rows, n_q, n_kv, hd, q_norm, k_norm, rope, eps, q_out, cache, layer, rm, status, dense_kv);
 }
