@@ -321,11 +321,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
-    auto lead = [&](const void *local) {   // the even CTA's copy of a barrier (shared::cluster address)
+    auto at_rank = [&](const void *local, uint32_t r) {   // a barrier's copy in CTA r (shared::cluster address)
         uint32_t a;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(0u));
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(r));
         return a;
     };
+    auto lead = [&](const void *local) { return at_rank(local, 0u); };
 
     // tile t -> (256-row block, 256-column block, split); column blocks vary fastest
     auto tile_of = [&](int t, int &m0, int &n0, int &kb0, int &nk) {
@@ -401,9 +402,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int k = 0; k < BK / 16; ++k)
                     umma_bf16_pair(acc, smem_desc(a0 + k * 32), smem_desc(b0 + k * 32), IDESC,
                                    (i > 0 || k > 0) ? 1u : 0u);
-                umma_commit_pair(&empty[s], 0x3);
+                umma_commit_pair(at_rank(&empty[s], 0u));   // the stage is free in both CTAs
+                umma_commit_pair(at_rank(&empty[s], 1u));
             }
-            umma_commit_pair(&tfull[b], 0x3);
+            umma_commit_pair(at_rank(&tfull[b], 0u));   // both CTAs' accumulator halves are complete
+            umma_commit_pair(at_rank(&tfull[b], 1u));
         }
     } else if (warp >= 2) {
         // ---- epilogue: this CTA's 128 rows of the tile, TMEM lane quadrant (warp % 4)

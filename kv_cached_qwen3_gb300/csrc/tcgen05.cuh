@@ -77,13 +77,10 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t tmem_d, uint64_t adesc, 
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// Arrive on the mbarrier at this offset in every CTA of cta_mask once the pair's earlier MMAs complete.
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
+// Arrive on an mbarrier of either CTA of the pair (bar: a shared::cluster address) once the
+// pair's earlier MMAs issued by this thread complete.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // ---- bulk tensor stores from shared memory (async proxy), tracked in this thread's bulk groups
