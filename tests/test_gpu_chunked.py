@@ -91,6 +91,14 @@ def test_chunked_prefill_long_chunks(cuda, mode):
     run_chunks(g, inputs.make_weights(g, 56), [300, 260, 40], 1, 58, bf16=True, prefill_mode=mode)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "f32"])
+def test_chunked_prefill_tall_chunk(cuda, kv):
+    """A 1000-row chunk appended after 300 cached rows: tall products on the CTA-pair GEMM, QK-norm,
+    RoPE and the KV append at positions 300..1299 (bf16 and f32 caches)."""
+    g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 2, "kv_dtype": kv})
+    run_chunks(g, inputs.make_weights(g, 61), [300, 1000], 1, 62, bf16=True)
+
+
 def test_append_overflow_changes_nothing(cuda):
     from kv_cached_qwen3_gb300.talker import Talker, TalkerError
     g = inputs.TINY
@@ -110,14 +118,14 @@ def test_append_overflow_changes_nothing(cuda):
 
 
 @pytest.mark.parametrize("mode", [pytest.param(3, id="mma-sync-attention"), pytest.param(4, id="tcgen05-attention")])
-@pytest.mark.parametrize("kv", ["bf16", "q8_0"])
-def test_batched_prefill_streams(cuda, kv, mode):
+@pytest.mark.parametrize("kv,B,T", [("bf16", 3, 70), ("q8_0", 3, 70), ("bf16", 4, 240)])
+def test_batched_prefill_streams(cuda, kv, B, T, mode):
     """Streams 0..B-1 prefilled in one call (T rows each, across page boundaries), then a decode
-    step; the causal attention pinned to either kernel (tcgen05: one launch pair per stream)."""
+    step; the causal attention pinned to either kernel (tcgen05: one launch pair per stream). With
+    4 x 240 rows the projections run on the CTA-pair GEMM and each row maps to its stream's position."""
     from kv_cached_qwen3_gb300.talker import Talker
     g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 2, "kv_dtype": kv})
     w = inputs.make_weights(g, 57)
-    B, T = 3, 70
     emb = np.stack([inputs.make_embeddings(g, 57, 0, T + 1, stream=s) for s in range(B)])   # [B, T+1, H]
     tk = Talker(g, w)
     tk.set_prefill_mode(mode)
