@@ -97,6 +97,10 @@ __global__ void __launch_bounds__(kWarpsPerHead * HPC * 32) k_attn_prefill(const
     const int kvh = (blockIdx.y * HPC) / group;
     const int qd = n_q * HD;
     const int row0 = qt * kBM + (warp % kWarpsPerHead) * 16;   // this warp's first query row
+    // launched with programmatic dependent launch: q and the call's K/V rows come from the
+    // previous kernel
+    pdl_launch_dependents();
+    pdl_wait();
 
     // Q fragments (A operand, row-major 16 x HD), scaled for base-2 exponentials
     uint32_t qa[NKS][4];
@@ -282,10 +286,20 @@ static cudaError_t launch_ap(const AttnParams &a, int T, cudaStream_t st) {
     const int ns = T / rps;
     const dim3 grid(ns * ((rps + kBM - 1) / kBM), a.n_q / HPC);
     const float scale_log2 = a.scale * 1.4426950408889634f;
-    k_attn_prefill<HD, HPC><<<grid, kWarpsPerHead * HPC * 32, ap_smem<HD>(), st>>>(
-        a.q, static_cast<__nv_bfloat16 *>(a.out), rps, a.rowmap.pos0, a.rowmap.stream0, a.n_q, a.group, a.layer,
-        scale_log2, a.cache, a.dense_k, a.dense_v, ns);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kWarpsPerHead * HPC * 32, 1, 1);
+    cfg.dynamicSmemBytes = ap_smem<HD>();
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_attn_prefill<HD, HPC>, a.q, static_cast<__nv_bfloat16 *>(a.out), rps,
+                              a.rowmap.pos0, a.rowmap.stream0, a.n_q, a.group, a.layer, scale_log2, a.cache,
+                              static_cast<const __nv_bfloat16 *>(a.dense_k), static_cast<const __nv_bfloat16 *>(a.dense_v),
+                              ns);
 }
 
 template <int HD, int HPC>
