@@ -213,7 +213,9 @@ int decode_splits(const talker *t, int B) {
 // split, combined on chip) up to 16 pages; longer or more streams fill the GPU in one wave,
 // combined through L2, and with several streams a split walks about eight pages of the longest
 // one (fewer, longer splits keep their copy pipelines busy: measured at 4, 8 and 16 streams
-// against four, six and twelve pages).
+// against four, six and twelve pages). A single stream past 16 pages takes 16 splits, or one
+// per six pages, up to one wave (B=1 at 2000 / 4096 / 8192 rows: 0.66 / 0.73 / 0.82 ms against
+// 0.71 / 0.78 / 0.83 ms with a full wave of splits).
 constexpr int kAttnMmMinPages = 3;
 
 void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster, int *mm) {
@@ -226,7 +228,8 @@ void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster,
         *cluster = 1;
     } else {
         *cluster = 0;
-        *splits = B == 1 ? decode_splits(t, B) : std::min(64, std::max(decode_splits(t, B), (pages_max + 7) / 8));
+        *splits = B == 1 ? std::min(decode_splits(t, B), std::max(16, (pages_max + 5) / 6))
+                         : std::min(64, std::max(decode_splits(t, B), (pages_max + 7) / 8));
     }
     // the tensor-core form pays for its fragment setup from three pages per split on
     *mm = t->kv_maps_ok && (pages_max + *splits - 1) / *splits >= kAttnMmMinPages ? 1 : 0;
