@@ -209,8 +209,8 @@ int decode_splits(const talker *t, int B) {
 // Attention splits of a decode step (CTAs per (row, KV group) along the cache) and whether they
 // combine inside a thread-block cluster, from the longest stream's length before the step
 // (captured steps are keyed by both). Measured on GB300: one or two short streams run one CTA
-// per KV group up to 2 pages (no combine at all), then a cluster of 8 (one or two pages per
-// split, combined on chip) up to 16 pages; longer or more streams fill the GPU in one wave,
+// per KV group up to 3 pages (no combine at all), then a cluster of 8 (one or two pages per
+// split, combined on chip; 4 and 6 measured slower) up to 16 pages; longer or more streams fill the GPU in one wave,
 // combined through L2, and with several streams a split walks about eight pages of the longest
 // one (fewer, longer splits keep their copy pipelines busy: measured at 4, 8 and 16 streams
 // against four, six and twelve pages). A single stream past 16 pages takes 16 splits, or one
@@ -220,7 +220,7 @@ constexpr int kAttnMmMinPages = 3;
 
 void attn_config(const talker *t, int B, int max_len, int *splits, int *cluster, int *mm) {
     const int pages_max = (max_len + 1 + kPageRows - 1) / kPageRows;
-    if (B <= 2 && pages_max <= 2) {
+    if (B <= 2 && pages_max <= 3) {
         *splits = 1;
         *cluster = 0;
     } else if (B <= 2 && pages_max <= 2 * kAttnClusterMax) {
