@@ -236,7 +236,7 @@ const char *talker_status_str(talker_status s);
  * ENOMEM (static thread-local buffer; empty if none). */
 const char *talker_last_error(void);
 
-/* Choose how talker_decode runs a step: 0 = automatic (B >= 4 with bf16
+/* Choose how talker_decode runs a step: 0 = automatic (B >= 2 with bf16
  * weights: the CUDA graph of tensor-core GEMMs; otherwise the CUDA graph of
  * GEMV kernels), 2 = always the GEMV graph, 3 = always the tensor-core graph
  * (talker_decode returns EINVAL where the chosen path cannot run).
@@ -245,8 +245,9 @@ talker_status talker_set_decode_mode(talker_t *t, int mode);
 
 /* Choose how prefill runs: 0 = automatic (tensor-core GEMMs when the weights
  * are bf16, T >= 16 and every projection shape is a multiple of the GEMM tile;
- * otherwise the GEMV kernels; the causal attention of a head_dim-128 prefill of
- * T >= 256 rows from position 0 of one stream on tcgen05, else on mma.sync),
+ * otherwise the GEMV kernels; the causal attention of a head_dim-128 prefill with
+ * at least 256 rows per stream on tcgen05 (bf16 storage from any start
+ * position, Q8_0 storage from position 0), else on mma.sync),
  * 2 = always the GEMV kernels, 3 / 4 = as 0 but the attention on mma.sync /
  * on tcgen05 (where supported) at any T (comparison and test support).
  * Errors: EINVAL. */
@@ -254,9 +255,11 @@ talker_status talker_set_prefill_mode(talker_t *t, int mode);
 
 /* Test support: the tensor-core GEMM of the prefill path on its own,
  * out[M, N] (+)= A[M, K] B[N, K]^T with bf16 A and B and f32 out (device
- * pointers; N % 128 == 0, K % 64 == 0). With accumulate or splits > 1 the
- * product is added to out. Synchronises the stream. Errors: EINVAL, ECUDA,
- * EDEVICE (a wait in the kernel gave up). */
+ * pointers; N % 128 == 0, K % 64 == 0), in the form the runtime picks for M
+ * (weights as the MMA's M operand up to 128 rows, CTA pairs for 1024 rows or
+ * more with N % 256 == 0, single-CTA tiles otherwise). With accumulate or
+ * splits > 1 the product is added to out. Synchronises the stream. Errors:
+ * EINVAL, ECUDA, EDEVICE (a wait in the kernel gave up). */
 talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, int N, float *out, int accumulate,
                                     int splits, void *cuda_stream);
 
@@ -264,8 +267,12 @@ talker_status talker_test_gemm_bf16(const void *A, int M, int K, const void *B, 
  * talker-forward.h", talker_layer_forward MLP: silu(gate) * up). B [N, K] bf16 holds the
  * gate and up rows interleaved (row 2j = gate_j, row 2j + 1 = up_j); out_bf16 [M, N/2]
  * receives bf16(silu(A B[2j]^T) * (A B[2j+1]^T)), silu(z) = z / (1 + exp(-z)). Device
- * pointers; N % 128 == 0, K % 64 == 0, out 16-byte aligned. Synchronises the stream.
- * Errors: EINVAL, ECUDA, EDEVICE (a wait in the kernel gave up). */
+ * pointers; N % 128 == 0, K % 64 == 0, out 16-byte aligned. Where the runtime would split K
+ * (at most 128 rows), the call does the same: the splits reduce into a zeroed scratch
+ * accumulator and the last split of each tile writes the SwiGLU outputs; the call then checks
+ * that the accumulator and the tile counters are zeros again. Synchronises the stream.
+ * Errors: EINVAL, ECUDA, EDEVICE (a wait in the kernel gave up, or the scratch was left
+ * non-zero). */
 talker_status talker_test_gemm_swiglu_bf16(const void *A, int M, int K, const void *B, int N, void *out_bf16,
                                            void *cuda_stream);
 
