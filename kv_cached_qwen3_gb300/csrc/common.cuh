@@ -66,31 +66,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Non-blocking test of a phase (never suspends the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// try_wait with a suspend-time hint: the thread sleeps until the phase completes
-// or about `hint_ns` passes, instead of spinning on the issue slots.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
 
 // Wait for the phase with the given parity to complete, giving up after
 // kWaitLimitNs. Returns false (and sets ST_WAIT_TIMEOUT) on timeout.
@@ -129,16 +104,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
 __device__ __forceinline__ uint4 lds_u4(uint32_t a) {
     uint4 v;
     asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ float4 lds_f4(uint32_t a) {
-    float4 v;
-    asm("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ float lds_f(uint32_t a) {
-    float v;
-    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
     return v;
 }
 __device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
