@@ -12,17 +12,19 @@
 // k_attn_prefill_tc: one CTA per 128 query rows of one q head (longest tiles first),
 // walking key blocks of 128:
 //   warp 0, one lane: TMA producer of K and V^T blocks (double buffered);
-//   warp 1:           allocates TMEM (S[2] and O_j[2], 128 columns each); one lane issues
-//                     S_j = Q K_j^T (tcgen05.mma M=128 N=128, K=16 steps over head_dim) and
-//                     O_j = P_j V_j (over the 128 keys), S_{j+1} ahead of O_j;
+//   warp 1:           allocates TMEM (S[2], 128 columns each, and one O of 128 columns); one
+//                     lane issues S_j = Q K_j^T (tcgen05.mma M=128 N=128, K=16 steps over
+//                     head_dim) and O += P_j V_j (over the 128 keys), S_{j+1} ahead of P_j V_j;
 //   warps 2..9:       two threads per query row (its TMEM lane), each owning half of the
 //                     head dimension and half of each key block: stage the row of q (scaled by
 //                     log2(e)/sqrt(head_dim), bf16) as the A operand, then per block read S_j
 //                     twice from TMEM (the row max, exchanged between the two halves through
 //                     shared memory; then p = 2^(s - m), partial row sums, P_j as bf16 into
-//                     shared memory for the second MMA) and fold O_{j-1} into f32 registers
-//                     rescaled to the running max; at the end divide by the row sum and store
-//                     bf16 rows through shared memory.
+//                     shared memory for the second MMA). m is the exponent reference: it moves
+//                     to the new row maximum only when that exceeds it by more than 8 (p stays
+//                     below 2^8, exact enough in bf16 and f32), and then the threads rescale
+//                     their half of O in TMEM before P_j is released; at the end O is read once,
+//                     divided by the row sum and stored as bf16 rows through shared memory.
 // Every mbarrier wait is bounded; a wait that gives up sets the device status word.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *sQ = smem, *sK = smem + TILE, *sV = sK + 2 * TILE, *sP = sV + 2 * TILE;
-    __shared__ __align__(8) uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], o_full[2], o_free[2];
+    __shared__ __align__(8) uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], o_full;
     __shared__ __align__(8) uint64_t p_full, q_full, mma_done;
     __shared__ uint32_t tmem_base_s;
     __shared__ __align__(8) uint64_t pair_bar[4];   // the two softmax warps of a lane quadrant
@@ -99,9 +101,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&kv_empty[b], 1);
             mbar_init(&s_full[b], 1);
             mbar_init(&s_free[b], 8);   // one arrival per softmax warp
-            mbar_init(&o_full[b], 1);
-            mbar_init(&o_free[b], 8);
         }
+        mbar_init(&o_full, 1);
         mbar_init(&p_full, 8);
         mbar_init(&q_full, 8);
         mbar_init(&mma_done, 1);
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = tmem_base_s;   // columns [0,256): S[2]; [256,512): O_j[2]
+    const uint32_t tmem = tmem_base_s;   // columns [0,256): S[2]; [256,384): O
 
     if (warp == 0 && lane == 0) {
         // ---- producer
@@ -154,17 +155,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int j = 0; j < nb && ok; ++j) {
             if (j + 1 < nb && !issue_s(j + 1)) break;
             const int b = j & 1;
+            // P_j is staged and O rescaled (when the reference moved): O += P_j V_j
             if (!mbar_wait(&p_full, j & 1, p.status)) break;
-            if (j >= 2 && !mbar_wait(&o_free[b], ((j >> 1) - 1) & 1, p.status)) break;
             tc::tc_fence_after();
             const uint32_t pa = smem_u32(sP), vb = smem_u32(sV + b * TILE);
 #pragma unroll
             for (int k = 0; k < BN / 16; ++k) {
                 const uint32_t off = (uint32_t)(k >> 2) * CB + (uint32_t)(k & 3) * 32;
-                tc::umma_bf16(tmem + 256u + (uint32_t)(b * 128), tc::smem_desc(pa + off), tc::smem_desc(vb + off),
-                              IDESC, k > 0 ? 1u : 0u);
+                tc::umma_bf16(tmem + 256u, tc::smem_desc(pa + off), tc::smem_desc(vb + off), IDESC,
+                              (j > 0 || k > 0) ? 1u : 0u);
             }
-            tc::umma_commit(&o_full[b]);
+            tc::umma_commit(&o_full);
             tc::umma_commit(&kv_empty[b]);
         }
         tc::umma_commit(&mma_done);   // arrives once every MMA issued above has completed
@@ -207,28 +208,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) mbar_arrive(&q_full);
         }
 
-        float o[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) o[i] = 0.f;
-        float m = -INFINITY, l = 0.f, m_fold = -INFINITY;   // l: this half's share of the row sum
+        float m = -INFINITY, l = 0.f;   // exponent reference; this half's share of the row sum
         bool ok = true;
-        // o <- o * 2^(m_fold - m_i) + O_i (this half's 64 columns), O_i = P_i V_i formed with max m_i
-        auto fold = [&](int i, float m_i) {
-            const int b = i & 1;
-            tc::tc_fence_after();
-            const float sc = fast_exp2(m_fold - m_i);
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tc::tmem_ld32(lane_base + 256u + (uint32_t)(b * 128 + half * 64 + c * 32), v);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) o[c * 32 + t] = fmaf(o[c * 32 + t], sc, v[t]);
-            }
-            m_fold = m_i;
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[b]);
-        };
+        const uint32_t o_base = lane_base + 256u + (uint32_t)(half * 64);   // this half's 64 O columns
         for (int j = 0; j < nb; ++j) {
             const int b = j & 1;
             if (!mbar_wait(&s_full[b], (j >> 1) & 1, p.status)) {
@@ -259,14 +241,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ok = false;
                 break;
             }
-            const float m_old = m;
-            m = fmaxf(m, fmaxf(mx_s[b][0][r], mx_s[b][1][r]));
-            // P's buffer is free once O_{j-1} = P_{j-1} V_{j-1} has completed
-            if (j >= 1 && !mbar_wait(&o_full[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status)) {
+            // both halves see the same maxima: they move the reference together
+            const float m_blk = fmaxf(mx_s[b][0][r], mx_s[b][1][r]);
+            const bool move = m == -INFINITY || m_blk > m + 8.0f;
+            // P's buffer is free, and O settled, once P_{j-1} V_{j-1} has completed
+            if (j >= 1 && !mbar_wait(&o_full, (j - 1) & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc::tc_fence_after();
+            if (move) {
+                const float m_new = fmaxf(m, m_blk);
+                if (j >= 1) {   // O and l were formed against the old reference
+                    const float sc = fast_exp2(m - m_new);
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        float v[32];
+                        tc::tmem_ld32(o_base + (uint32_t)(c * 32), v);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) v[t] *= sc;
+                        tc::tmem_st32(o_base + (uint32_t)(c * 32), v);
+                    }
+                    l *= sc;
+                }
+                m = m_new;
+            }
             // pass 2: p = 2^(s - m) (0 past the position), this half's row sum, P_j as bf16
             float ps = 0.f;
 #pragma unroll
@@ -290,7 +289,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     *reinterpret_cast<uint4 *>(sP + op_off(r, half * 8 + c * 4 + t)) =
                         make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
             }
-            l = l * fast_exp2(m_old - m) + ps;
+            l += ps;
             tc::tc_fence_before();
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -298,10 +297,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mbar_arrive(&s_free[b]);
                 mbar_arrive(&p_full);
             }
-            if (j >= 1) fold(j - 1, m_old);
         }
-        if (ok && mbar_wait(&o_full[(nb - 1) & 1], ((nb - 1) >> 1) & 1, p.status)) {
-            fold(nb - 1, m);
+        if (ok && mbar_wait(&o_full, (nb - 1) & 1, p.status)) {
+            tc::tc_fence_after();
+            float o[64];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+                tc::tmem_ld32(o_base + (uint32_t)(c * 32), v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) o[c * 32 + t] = v[t];
+            }
             // row sum = both halves' shares; rows go out through shared memory (P's buffer: no
             // MMA reads it any more)
             l_s[half][r] = l;
