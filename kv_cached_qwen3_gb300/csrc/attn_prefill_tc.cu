@@ -17,10 +17,10 @@
 //                     head_dim) and O += P_j V_j (over the 128 keys), S_{j+1} ahead of P_j V_j;
 //   warps 2..9:       two threads per query row (its TMEM lane), each owning half of the
 //                     head dimension and half of each key block: stage the row of q (scaled by
-//                     log2(e)/sqrt(head_dim), bf16) as the A operand, then per block read S_j
-//                     twice from TMEM (the row max, exchanged between the two halves through
-//                     shared memory; then p = 2^(s - m), partial row sums, P_j as bf16 into
-//                     shared memory for the second MMA). m is the exponent reference: it moves
+//                     log2(e)/sqrt(head_dim), bf16) as the A operand, then per block read its
+//                     64 scores of S_j once from TMEM (the row max, exchanged between the two
+//                     halves through shared memory; then p = 2^(s - m), partial row sums, P_j
+//                     as bf16 into shared memory for the second MMA). m is the exponent reference: it moves
 //                     to the new row maximum only when that exceeds it by more than 8 (p stays
 //                     below 2^8, exact enough in bf16 and f32), and then the threads rescale
 //                     their half of O in TMEM before P_j is released; at the end O is read once,
@@ -221,19 +221,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int key0 = j * BN + half * 64;                 // first key of this half
             const bool masked = j * BN + BN - 1 > p.pos0 + qt * BM;   // the block reaches past the tile's first row
             const uint32_t sb = lane_base + (uint32_t)(b * 128 + half * 64);
-            // pass 1: this half's row max over the keys this row may see (key <= position)
+            // pass 1: this half's 64 scores of the block (kept in registers) and their max over
+            // the keys this row may see (key <= position)
+            float sv[2][32];
+            tc::tmem_ld32(sb, sv[0]);
+            tc::tmem_ld32(sb + 32u, sv[1]);
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[b]);   // S_j is in registers: its buffer may take S_{j+2}
             float mx = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tc::tmem_ld32(sb + (uint32_t)(c * 32), v);
                 if (masked) {
 #pragma unroll
                     for (int t = 0; t < 32; ++t)
-                        if (key0 + c * 32 + t <= qpos) mx = fmaxf(mx, v[t]);
+                        if (key0 + c * 32 + t <= qpos) mx = fmaxf(mx, sv[c][t]);
                 } else {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) mx = fmaxf(mx, v[t]);
+                    for (int t = 0; t < 32; ++t) mx = fmaxf(mx, sv[c][t]);
                 }
             }
             mx_s[b][half][r] = mx;
@@ -270,8 +275,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float ps = 0.f;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tc::tmem_ld32(sb + (uint32_t)(c * 32), v);
+                const float(&v)[32] = sv[c];
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
@@ -293,10 +297,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::tc_fence_before();
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&s_free[b]);
-                mbar_arrive(&p_full);
-            }
+            if (lane == 0) mbar_arrive(&p_full);
         }
         if (ok && mbar_wait(&o_full, (nb - 1) & 1, p.status)) {
             tc::tc_fence_after();
