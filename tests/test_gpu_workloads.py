@@ -146,7 +146,7 @@ def test_long_context_prefill_4096_tensor_cores(cuda, talker_long):
     rh, rl = o.forward_full(emb)
     check_rows(hid, rh, bf16=True, what="prefill 4096 hidden")
     check_rows(lg, rl, bf16=True, what="prefill 4096 logits")
-    assert top1_agreement(lg, rl) >= TOL_TOP1
+    assert_top1(lg, rl, what="prefill 4096 rows")
 
 
 def stream_cache(g, seed, s, L):
