@@ -55,8 +55,8 @@ typedef enum {
 /* TALKER_DTYPE_Q8_0 is a KV-cache storage type only ("qwen3-tts" talker TurboQuantQ8_0,
  * ggml Q8_0 blocks): per head row, blocks of 32 int8 codes with an fp16 scale max|x|/127.
  * A call attends the rows cached by earlier calls dequantized and its own rows exactly.
- * It needs bf16 weights and head_dim 64 or 128; talker_prefill_append is not available
- * with it. */
+ * It needs bf16 weights and head_dim 64 or 128; talker_prefill_append with it needs
+ * head_dim 128 (EINVAL otherwise). */
 typedef enum { TALKER_DTYPE_F32 = 0, TALKER_DTYPE_BF16 = 1, TALKER_DTYPE_Q8_0 = 2 } talker_dtype;
 
 /* Geometry and storage formats (names as in the rightkit-qts TtsTransformerConfig).

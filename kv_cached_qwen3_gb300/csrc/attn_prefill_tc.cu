@@ -7,7 +7,8 @@
 //
 // Per layer, k_kv_dense_tc first writes the KV group's keys densely, K [n_kv][L][128], and
 // its values transposed, V^T [n_kv][128][L] (L = pos0 + T keys rounded up to 128, zero rows
-// past them), so that both products read K-major operands.
+// past them), so that both products read K-major operands; with Q8_0 storage the earlier
+// rows are dequantized there and the call's own rows come from their exact bf16 copy.
 //
 // k_attn_prefill_tc: one CTA per 128 query rows of one q head (longest tiles first),
 // walking key blocks of 128:
@@ -342,30 +343,51 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// 8 dims (16-byte chunk ch) of row `row` of a Q8_0 tile ([64][HD] int8 codes, then [64][HD/32]
+// fp16 scales), dequantized (code x scale, exact in f32) and rounded to bf16.
+__device__ __forceinline__ uint4 q8_chunk_bf16(const unsigned char *tile, int row, int ch) {
+    const uint2 cw = *reinterpret_cast<const uint2 *>(tile + row * HD + ch * 8);
+    const float sc = __half2float(*reinterpret_cast<const __half *>(tile + kPage * HD + (row * (HD / 32) + ch / 4) * 2));
+    const uint32_t w[2] = {cw.x, cw.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int b0 = (int)(signed char)((w[i >> 1] >> (16 * (i & 1))) & 0xffu);
+        const int b1 = (int)(signed char)((w[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu);
+        o[i] = pack2((float)b0 * sc, (float)b1 * sc);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Dense K rows and transposed V rows of one (64-key block, KV head); keys at or past
-// nkeys are written as zeros. Sources: the paged bf16 cache of `stream`, or the dense bf16
-// copy of the call's rows [rows][n_kv][HD] (Q8_0 storage).
+// nkeys are written as zeros. Sources: the paged bf16 cache of `stream`; with Q8_0 storage,
+// the dense bf16 copy of the call's rows [rows][n_kv][HD] for keys >= pos0 and the cache's
+// Q8_0 tiles, dequantized, for the earlier keys.
 __global__ void __launch_bounds__(256) k_kv_dense_tc(const CacheView c, int layer, int stream, int nkeys, int Lpad,
-                                                     const __nv_bfloat16 *dense_k, const __nv_bfloat16 *dense_v,
-                                                     __nv_bfloat16 *kd, __nv_bfloat16 *vt) {
+                                                     int pos0, const __nv_bfloat16 *dense_k,
+                                                     const __nv_bfloat16 *dense_v, __nv_bfloat16 *kd,
+                                                     __nv_bfloat16 *vt) {
     __shared__ __align__(16) __nv_bfloat16 vs[64][HD + 8];
     const int j0 = blockIdx.x * 64, kvh = blockIdx.y;
     for (int idx = threadIdx.x; idx < 64 * 16; idx += 256) {
         const int r = idx >> 4, ch = idx & 15, key = j0 + r;
         uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
         if (key < nkeys) {
-            const __nv_bfloat16 *ks, *vsrc;
-            if (dense_k != nullptr) {
-                ks = dense_k + ((size_t)key * c.n_kv + kvh) * HD;
-                vsrc = dense_v + ((size_t)key * c.n_kv + kvh) * HD;
+            if (dense_k != nullptr && key >= pos0) {   // the call's own rows, exact up to bf16
+                kx = *reinterpret_cast<const uint4 *>(dense_k + ((size_t)(key - pos0) * c.n_kv + kvh) * HD + ch * 8);
+                vx = *reinterpret_cast<const uint4 *>(dense_v + ((size_t)(key - pos0) * c.n_kv + kvh) * HD + ch * 8);
+            } else if (c.kv_q8) {   // a row of an earlier call, as stored
+                const size_t tile = (size_t)kPage * HD + (size_t)kPage * (HD / 32) * 2;
+                const size_t off = (size_t)c.page_table[stream * c.pages_per_stream + key / kPage] * c.page_elems +
+                                   (size_t)(layer * c.n_kv + kvh) * tile;
+                kx = q8_chunk_bf16(static_cast<const unsigned char *>(c.k) + off, key % kPage, ch);
+                vx = q8_chunk_bf16(static_cast<const unsigned char *>(c.v) + off, key % kPage, ch);
             } else {
                 const size_t off = (size_t)c.page_table[stream * c.pages_per_stream + key / kPage] * c.page_elems +
                                    ((size_t)(layer * c.n_kv + kvh) * kPage + key % kPage) * HD;
-                ks = static_cast<const __nv_bfloat16 *>(c.k) + off;
-                vsrc = static_cast<const __nv_bfloat16 *>(c.v) + off;
+                kx = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(c.k) + off + ch * 8);
+                vx = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(c.v) + off + ch * 8);
             }
-            kx = *reinterpret_cast<const uint4 *>(ks + ch * 8);
-            vx = *reinterpret_cast<const uint4 *>(vsrc + ch * 8);
         }
         *reinterpret_cast<uint4 *>(kd + ((size_t)kvh * Lpad + key) * HD + ch * 8) = kx;
         *reinterpret_cast<uint4 *>(&vs[r][ch * 8]) = vx;
@@ -389,10 +411,10 @@ int attn_prefill_tc_lpad(int nkeys) { return (nkeys + atc::BN - 1) / atc::BN * a
 
 bool attn_prefill_tc_supported(const AttnParams &a, int T) {
     const bool one_stream = a.rowmap.rows_per_stream == 0 || a.rowmap.rows_per_stream == T;
-    // bf16 cache: any start position (the dense copy reads every key from the pages); Q8_0: the
-    // call's own rows from position 0 only (the dense bf16 copy of the call)
+    // bf16 cache: the dense copy reads every key from the pages; Q8_0: the call's own rows from
+    // their dense bf16 copy, earlier rows dequantized from the cache (any start position)
     return a.rowmap.mode == 1 && one_stream && a.out_bf16 && a.cache.head_dim == atc::HD && T >= 1 &&
-           (a.cache.kv_bf16 || (a.cache.kv_q8 && a.dense_k != nullptr && a.rowmap.pos0 == 0));
+           (a.cache.kv_bf16 || (a.cache.kv_q8 && a.dense_k != nullptr));
 }
 
 cudaError_t prepare_attn_prefill_tc() {
@@ -405,7 +427,7 @@ cudaError_t launch_attn_prefill_tc(const AttnParams &a, int T, __nv_bfloat16 *kd
     const int nkeys = a.rowmap.pos0 + T, Lpad = attn_prefill_tc_lpad(nkeys);
     const int n_kv = a.cache.n_kv;
     atc::k_kv_dense_tc<<<dim3(Lpad / 64, n_kv), 256, 0, st>>>(a.cache, a.layer, a.rowmap.stream0, nkeys, Lpad,
-                                                               a.dense_k, a.dense_v, kd, vt);
+                                                               a.rowmap.pos0, a.dense_k, a.dense_v, kd, vt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap mk, mv;

@@ -668,14 +668,16 @@ talker_status enqueue_tc(talker *t, cudaStream_t st, int T, const RowMap &rm, co
         a.cnt = t->attn_cnt;
         a.status = t->d_status;
         if (rm.mode == 0) set_raw_heads(t, d, a);
-        if (rm.mode == 1 && t->kv_q8) {   // the call's rows from the dense copy (prefill from position 0)
+        if (rm.mode == 1 && t->kv_q8) {   // the call's own rows from their dense copy, exact up to bf16
             a.dense_k = t->kv_dense;
             a.dense_v = t->kv_dense + (size_t)T * t->nkv * t->hd;
         }
         // rows of one stream: all T, or T / B in a batched prefill (B streams of rows_per_stream rows)
         const int Ts = rm.rows_per_stream > 0 ? rm.rows_per_stream : T;
         const int n_str = T / Ts;
-        const bool attn_tc = t->prefill_mode == 4 || (t->prefill_mode != 3 && Ts >= kAttnTcMinRows);
+        // (an appended chunk over Q8_0 storage attends earlier rows dequantized: tcgen05 only)
+        const bool attn_tc = t->prefill_mode == 4 || (t->prefill_mode != 3 && Ts >= kAttnTcMinRows) ||
+                             (t->kv_q8 && rm.pos0 > 0);
         AttnParams a1 = a;   // the first stream's rows as a one-stream call
         a1.rowmap.rows_per_stream = 0;
         if (rm.mode == 1 && attn_tc && t->kd_tc != nullptr && rm.pos0 + Ts <= t->cap_kd_keys &&
@@ -799,7 +801,7 @@ talker_status prefill_impl(talker *t, int stream, const float *emb, int T, float
                            int32_t *argmax, bool all_rows, bool append) {
     TRY(check_stream(t, stream));
     if (!emb || !logits || T < 1) return TALKER_EINVAL;
-    if (append && t->kv_q8) return TALKER_EINVAL;   // Q8_0: the prefill attends only its own rows
+    if (append && t->kv_q8 && t->hd != 128) return TALKER_EINVAL;   // Q8_0 appends: the tcgen05 attention
     const int pos0 = append ? t->len[stream] : 0;
     if (T > t->max_seq - pos0) return TALKER_EOVERFLOW;
     TRY_CUDA(cudaSetDevice(t->dev));

@@ -3,7 +3,8 @@
 The oracle appends the same chunks with n_past = cur_len (talker_forward_core); chunk
 sizes cross page boundaries and switch between the GEMV path (T < 16) and the
 tensor-core path (T >= 16, bf16 weights). Decode steps after the chunks read the cache
-the chunks wrote.
+the chunks wrote. With Q8_0 storage every chunk takes the tensor-core path and attends the
+earlier chunks' rows dequantized.
 """
 import numpy as np
 import pytest
@@ -40,7 +41,7 @@ def run_chunks(g, w, chunks, n_dec, seed, bf16, prefill_mode=0):
     tk = Talker(g, w)
     tk.set_prefill_mode(prefill_mode)
     tk.kv_init_batched(1, total + 3)
-    oc = OracleCache(Oracle(g, w), 1, total + 3)
+    oc = OracleCache(Oracle(g, w), 1, total + 3, kv_q8=(g.kv_dtype == "q8_0"))
     at = 0
     for i, T in enumerate(chunks):
         part = emb[at:at + T]
@@ -81,6 +82,16 @@ def test_chunked_prefill_bf16_both_paths(cuda, mode):
     earlier keys of the stream through its dense copy and masks on positions pos0 + r)."""
     g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 4})
     run_chunks(g, inputs.make_weights(g, 53), [100, 70, 5, 16, 64], 2, 54, bf16=True, prefill_mode=mode)
+
+
+@pytest.mark.parametrize("chunks", [pytest.param([100, 70, 5, 16, 64], id="short"),
+                                    pytest.param([300, 260, 40], id="long")])
+def test_chunked_prefill_q8_0(cuda, chunks):
+    """Chunks over Q8_0 storage: each chunk attends the rows of the earlier chunks dequantized
+    from the cache and its own rows exactly (the oracle's reading), on the tcgen05 attention
+    whatever the chunk size, then decode steps over the quantized rows."""
+    g = inputs.Geometry(**{**inputs.TALKER.__dict__, "n_layers": 2, "kv_dtype": "q8_0"})
+    run_chunks(g, inputs.make_weights(g, 63), chunks, 2, 64, bf16=True)
 
 
 @pytest.mark.parametrize("mode", [pytest.param(0, id="auto"), pytest.param(4, id="tcgen05-attention")])

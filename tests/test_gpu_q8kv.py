@@ -124,15 +124,6 @@ def test_q8_long_context_decode(cuda, L):
 def test_q8_refusals(cuda):
     from kv_cached_qwen3_gb300.talker import Talker, TalkerError
     g = q8_geom(1)
-    w = inputs.make_weights(g, 73)
-    tk = Talker(g, w)
-    tk.kv_init_batched(1, 64)
-    emb = inputs.make_embeddings(g, 73, 0, 10)
-    tk.prefill(0, dev(emb[:5]))
-    with pytest.raises(TalkerError) as ei:
-        tk.prefill_append(0, dev(emb[5:10]))   # not available with Q8_0 storage
-    assert ei.value.status == 1 and tk.cur_len(0) == 5
-    tk.close()
     for bad in ({"weight_dtype": "f32"}, {"head_dim": 32, "intermediate": 384}):
         gb = inputs.Geometry(**{**g.__dict__, **bad})
         with pytest.raises(TalkerError):
