@@ -571,6 +571,32 @@ def test_q8_cache_attends_own_row_exactly(tiny):
     assert not np.array_equal(kp[:, :, L], kq[:, :, L])   # the plain cache keeps it exact
 
 
+def test_q8_cache_chunk_attends_own_rows_exactly(tiny):
+    """Q8_0 storage, an appended chunk of several rows: the earlier rows enter dequantized, the
+    chunk's own rows (each other's keys included) exactly, and they are stored quantized. Same
+    outputs as a plain cache whose earlier rows hold the Q8_0 round trip."""
+    from oracle import q8_0_roundtrip
+    _, o = tiny
+    g = TINY
+    L, T = 20, 9
+    layers = [inputs.make_kv_layer(g, 9, l, L) for l in range(g.n_layers)]
+    K = np.stack([k for k, _ in layers])
+    V = np.stack([v for _, v in layers])
+    x = inputs.make_embeddings(g, 9, 0, T)
+    cq = OracleCache(o, 1, 64, kv_q8=True)
+    cq.kv_import(0, K, V, L)
+    cp = OracleCache(o, 1, 64)
+    cp.kv_import(0, q8_0_roundtrip(K), q8_0_roundtrip(V), L)
+    hq, lq = cq.append_rows(0, x)
+    hp, lp = cp.append_rows(0, x)
+    np.testing.assert_array_equal(lq, lp)
+    np.testing.assert_array_equal(hq, hp)
+    kq, vq = cq.kv_export(0, L + T)
+    kp, vp = cp.kv_export(0, L + T)
+    np.testing.assert_array_equal(kq[:, :, L:], q8_0_roundtrip(kp[:, :, L:]))
+    np.testing.assert_array_equal(vq[:, :, L:], q8_0_roundtrip(vp[:, :, L:]))
+
+
 def test_q8_0_rounding_just_below_half():
     """x * (1/d) = 0.5 - 2^-25 must round to 0 (adding 0.5 in f32 would give 1.0)."""
     from oracle import q8_0_quantize
