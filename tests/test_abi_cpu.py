@@ -38,6 +38,33 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def declared_arity():
+    """Function name -> number of parameters, from the prototypes in include/*.h."""
+    arity = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            for name, params in re.findall(r"\b(talker_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+                params = params.strip()
+                arity[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return arity
+
+
+def test_binding_signatures_match_header(lib):
+    """Every prototype the ctypes binding sets has as many arguments as the header declares."""
+    arity = declared_arity()
+    checked = 0
+    for name in declared_functions():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        assert name in arity, name
+        assert len(fn.argtypes) == arity[name], (name, len(fn.argtypes), arity[name])
+        checked += 1
+    assert checked >= 20
+
+
 def test_status_strings(lib):
     assert lib.talker_status_str(0) == b"ok"
     assert lib.talker_status_str(2) == b"KV cache overflow"
